@@ -1,0 +1,150 @@
+"""CPU oracle for MXFP8 block-scaled quantization (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it, and the two share no code.
+
+The arithmetic lives in ``mxfp8_oracle.c`` (plain scalar C, exact double
+evaluation); this module compiles it with gcc and wraps it with numpy arrays.
+See the header of ``mxfp8_oracle.c`` for what each function computes and which
+page passage it follows.  NaN/Inf inputs are outside the contract (parity
+unpinned for them).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3 = 0
+E5M2 = 1
+BLOCK = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxfp8_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, -O2, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u8, u16p, u8p = ctypes.c_uint8, ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_uint8)
+            i64, i64p, f32p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_float)
+            lib.mxo_bf16_to_double.restype = ctypes.c_double
+            lib.mxo_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.mxo_fp8_decode.restype = ctypes.c_double
+            lib.mxo_fp8_decode.argtypes = [u8, ctypes.c_int]
+            lib.mxo_fp8_encode.restype = u8
+            lib.mxo_fp8_encode.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.mxo_fp8_max.restype = ctypes.c_double
+            lib.mxo_fp8_max.argtypes = [ctypes.c_int]
+            lib.mxo_block_exponent.restype = ctypes.c_int
+            lib.mxo_block_exponent.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.mxo_e8m0_decode.restype = ctypes.c_double
+            lib.mxo_e8m0_decode.argtypes = [u8]
+            lib.mxo_quantize.restype = ctypes.c_int
+            lib.mxo_quantize.argtypes = [u16p, i64, i64, ctypes.c_int, u8p, u8p, u8p, u8p, f32p]
+            lib.mxo_quantize_grouped.restype = ctypes.c_int
+            lib.mxo_quantize_grouped.argtypes = [u16p, i64, i64, ctypes.c_int, i64p, ctypes.c_int,
+                                                 u8p, u8p, u8p, u8p]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# ---- scalar helpers ---------------------------------------------------------
+
+def bf16_to_float(bits: int) -> float:
+    return _load().mxo_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def fp8_decode(byte: int, fmt: int) -> float:
+    return _load().mxo_fp8_decode(int(byte) & 0xFF, fmt)
+
+
+def fp8_encode(v: float, fmt: int) -> int:
+    return int(_load().mxo_fp8_encode(float(v), fmt))
+
+
+def fp8_max(fmt: int) -> float:
+    return _load().mxo_fp8_max(fmt)
+
+
+def block_exponent(amax: float, fmt: int) -> int:
+    return int(_load().mxo_block_exponent(float(amax), fmt))
+
+
+def e8m0_decode(e: int) -> float:
+    return _load().mxo_e8m0_decode(int(e) & 0xFF)
+
+
+# ---- array entry points -------------------------------------------------------
+
+def quantize(x_bits: np.ndarray, fmt: int, rowwise: bool = True, colwise: bool = True,
+             with_dbias: bool = False):
+    """Quantize BF16 bits ``x_bits`` (uint16 [M,N], row-major).
+
+    Returns ``(out_row, scale_row, out_col, scale_col, dbias)``; entries for a
+    direction that was not requested are None.  Shapes: out_* [M,N] uint8,
+    scale_row [M,N/32], scale_col [M/32,N] uint8, dbias [N] float32.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N = x.shape
+    out_row = np.empty((M, N), np.uint8) if rowwise else None
+    scale_row = np.empty((M, N // BLOCK), np.uint8) if rowwise else None
+    out_col = np.empty((M, N), np.uint8) if colwise else None
+    scale_col = np.empty((M // BLOCK, N), np.uint8) if colwise else None
+    dbias = np.empty((N,), np.float32) if with_dbias else None
+    rc = _load().mxo_quantize(_ptr(x, ctypes.c_uint16), M, N, fmt,
+                              _ptr(out_row, ctypes.c_uint8), _ptr(scale_row, ctypes.c_uint8),
+                              _ptr(out_col, ctypes.c_uint8), _ptr(scale_col, ctypes.c_uint8),
+                              _ptr(dbias, ctypes.c_float))
+    if rc != 0:
+        raise ValueError(f"oracle: M={M}, N={N} must be non-negative multiples of {BLOCK}")
+    return out_row, scale_row, out_col, scale_col, dbias
+
+
+def quantize_grouped(x_bits: np.ndarray, offsets: np.ndarray, fmt: int):
+    """Grouped quantize: rows [offsets[g], offsets[g+1]) are group g.
+
+    Returns ``(out_row, scale_row, out_col, scale_col)`` laid out as for the flat
+    call on the concatenated rows.  Raises ValueError on invalid offsets.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    total, N = x.shape
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    G = off.shape[0] - 1
+    out_row = np.zeros((total, N), np.uint8)
+    scale_row = np.zeros((total, N // BLOCK), np.uint8)
+    out_col = np.zeros((total, N), np.uint8)
+    scale_col = np.zeros((total // BLOCK, N), np.uint8)
+    rc = _load().mxo_quantize_grouped(_ptr(x, ctypes.c_uint16), total, N, G, _ptr(off, ctypes.c_int64), fmt,
+                                      _ptr(out_row, ctypes.c_uint8), _ptr(scale_row, ctypes.c_uint8),
+                                      _ptr(out_col, ctypes.c_uint8), _ptr(scale_col, ctypes.c_uint8))
+    if rc != 0:
+        raise ValueError("oracle: invalid group offsets")
+    return out_row, scale_row, out_col, scale_col

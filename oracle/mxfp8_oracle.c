@@ -1,0 +1,256 @@
+/*
+ * MXFP8 block-scaled quantization: plain scalar CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * CPU-baseline leg of the benchmark may load this file's library.  The CUDA
+ * path never calls it and shares no code with it.
+ *
+ * What it computes (the MXFP8 quantize operation of "[Common] Experimental
+ * CuTeDSL MXFP8 backends in C++ via TVM-FFI", TransformerEngine PR #3137,
+ * sections "Description" and the quantization-config review of `to_key()`,
+ * whose fields name dtype, fp8_dtype, rowwise, colwise, with_dbias and
+ * with_noop; 32-element blocks per the review "Why are the non-32-divisible
+ * shapes omitted?"):
+ *
+ *   A BF16 matrix x[M,N] (row-major) is cut into blocks of 32 elements,
+ *   1x32 along a row (rowwise) and 32x1 down a column (colwise).  For every
+ *   block with amax = max |x| over its 32 elements the block gets an E8M0
+ *   scale byte
+ *         e = clamp(k + 127, 0, 254),   k = smallest integer with
+ *                                          amax <= Fmax * 2^k,
+ *   i.e. k = ceil(log2(amax / Fmax)); an all-zero block gets e = 127.
+ *   Each element becomes q = RNE-saturate_F(x * 2^(127 - e)), F = E4M3
+ *   (Fmax 448) or E5M2 (Fmax 57344).  The optional dbias is the fp32 column
+ *   sum of the unquantized input.
+ *
+ * Everything is evaluated exactly in double precision: a BF16 value has 8
+ * significant bits, the scale is a power of two, so x * 2^(127-e) is exact
+ * and the only rounding is the single FP8 rounding.  FP8 layouts follow the
+ * bit layouts quoted on the cudnn-frontend PR #593 page ("frost" block-scale
+ * GEMMs, FP8 data-type discussion): E4M3 = 1 sign, 4 exponent (bias 7),
+ * 3 mantissa bits, no infinity, S.1111.111 = NaN; E5M2 = 1 sign, 5 exponent
+ * (bias 15), 2 mantissa bits, IEEE-style infinities and NaNs.
+ *
+ * NaN / Inf inputs are outside the contract: parity unpinned for them.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#define MXO_E4M3 0
+#define MXO_E5M2 1
+#define MXO_BLOCK 32
+
+/* Per-format constants, written from the bit layouts above. */
+static int mxo_mbits(int fmt) { return fmt == MXO_E4M3 ? 3 : 2; }
+static int mxo_ebits(int fmt) { return fmt == MXO_E4M3 ? 4 : 5; }
+static int mxo_bias(int fmt) { return fmt == MXO_E4M3 ? 7 : 15; }
+/* Largest finite magnitude: E4M3 0.1111.110 = 1.75 * 2^8; E5M2 0.11110.11 = 1.75 * 2^15. */
+double mxo_fp8_max(int fmt) { return fmt == MXO_E4M3 ? 448.0 : 57344.0; }
+
+/* BF16 bit pattern -> exact value: 1 sign, 8 exponent (bias 127), 7 mantissa. */
+double mxo_bf16_to_double(uint16_t u)
+{
+    int sign = (u >> 15) & 1;
+    int ef = (u >> 7) & 0xFF;
+    int m = u & 0x7F;
+    double mag;
+    if (ef == 0xFF)
+        mag = m ? NAN : INFINITY;
+    else if (ef == 0)
+        mag = ldexp((double)m, 1 - 127 - 7);            /* subnormal */
+    else
+        mag = ldexp((double)(128 + m), ef - 127 - 7);   /* (1 + m/128) * 2^(ef-127) */
+    return sign ? -mag : mag;
+}
+
+/* FP8 byte -> exact value. */
+double mxo_fp8_decode(uint8_t b, int fmt)
+{
+    const int mbits = mxo_mbits(fmt), ebits = mxo_ebits(fmt), bias = mxo_bias(fmt);
+    const int sign = b >> 7;
+    const int ef = (b >> mbits) & ((1 << ebits) - 1);
+    const int m = b & ((1 << mbits) - 1);
+    double mag;
+    if (fmt == MXO_E4M3 && ef == 15 && m == 7)
+        return NAN;
+    if (fmt == MXO_E5M2 && ef == 31) {
+        if (m)
+            return NAN;
+        mag = INFINITY;
+    } else if (ef == 0) {
+        mag = ldexp((double)m, 1 - bias - mbits);
+    } else {
+        mag = ldexp((double)((1 << mbits) + m), ef - bias - mbits);
+    }
+    return sign ? -mag : mag;
+}
+
+/*
+ * Exact value -> FP8 byte, round to nearest with ties to even mantissa,
+ * saturating every finite overflow (and +-Inf) to +-Fmax.  The sign of a
+ * result that rounds to zero is kept (-tiny -> 0x80).
+ */
+uint8_t mxo_fp8_encode(double v, int fmt)
+{
+    const int mbits = mxo_mbits(fmt), bias = mxo_bias(fmt);
+    const int emin = 1 - bias;                /* exponent of the smallest normal */
+    const double fmax = mxo_fp8_max(fmt);
+    const int sign = signbit(v) ? 1 : 0;
+    double a = fabs(v), r;
+    int ex, e2, ef, m;
+
+    if (isnan(a))
+        return (uint8_t)((sign << 7) | 0x7F);  /* S.1111.111 / S.11111.11 */
+    if (a == 0.0)
+        return (uint8_t)(sign << 7);
+    if (isinf(a)) {
+        r = fmax;
+    } else {
+        /* Spacing of representable values around a: 2^(max(floor(log2 a), emin) - mbits). */
+        frexp(a, &e2);                         /* a = f * 2^e2, f in [0.5, 1) */
+        ex = e2 - 1;                           /* floor(log2 a) */
+        if (ex < emin)
+            ex = emin;
+        const double quantum = ldexp(1.0, ex - mbits);
+        r = nearbyint(a / quantum) * quantum;  /* default mode: ties to even */
+        if (r > fmax)
+            r = fmax;
+    }
+    if (r == 0.0)
+        return (uint8_t)(sign << 7);
+    frexp(r, &e2);
+    ex = e2 - 1;
+    if (ex < emin) {
+        ef = 0;
+        m = (int)(r / ldexp(1.0, emin - mbits));
+    } else {
+        ef = ex + bias;
+        m = (int)(r / ldexp(1.0, ex - mbits)) - (1 << mbits);
+    }
+    return (uint8_t)((sign << 7) | (ef << mbits) | m);
+}
+
+/* E8M0 block exponent e for a block whose largest magnitude is amax. */
+int mxo_block_exponent(double amax, int fmt)
+{
+    const double fmax = mxo_fp8_max(fmt);
+    int k, e;
+    if (amax == 0.0)
+        return 127;
+    /* smallest integer k with amax <= fmax * 2^k, found by search from a guess */
+    k = ilogb(amax) - ilogb(fmax);
+    while (amax > ldexp(fmax, k))
+        k++;
+    while (amax <= ldexp(fmax, k - 1))
+        k--;
+    e = k + 127;
+    if (e < 0)
+        e = 0;
+    if (e > 254)
+        e = 254;
+    return e;
+}
+
+/* E8M0 byte -> scale value 2^(e-127) (255 is NaN). */
+double mxo_e8m0_decode(uint8_t e)
+{
+    return e == 255 ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/*
+ * Flat quantize of x[M,N] (BF16 bits, row-major).  Any of the four output
+ * pairs may be NULL to skip that direction; dbias may be NULL.
+ *   out_row[i*N + j], scale_row[i*(N/32) + j/32]   (1x32 blocks along a row)
+ *   out_col[i*N + j], scale_col[(i/32)*N + j]      (32x1 blocks down a column)
+ * Returns 0, or -1 if M or N is not a non-negative multiple of 32.
+ */
+int mxo_quantize(const uint16_t *x, int64_t M, int64_t N, int fmt,
+                 uint8_t *out_row, uint8_t *scale_row,
+                 uint8_t *out_col, uint8_t *scale_col, float *dbias)
+{
+    int64_t i, j, c, r, k;
+    if (M < 0 || N < 0 || M % MXO_BLOCK || N % MXO_BLOCK)
+        return -1;
+
+    if (out_row && scale_row) {
+        for (i = 0; i < M; i++) {
+            for (c = 0; c < N / MXO_BLOCK; c++) {
+                const uint16_t *blk = x + i * N + c * MXO_BLOCK;
+                double amax = 0.0;
+                for (k = 0; k < MXO_BLOCK; k++) {
+                    double a = fabs(mxo_bf16_to_double(blk[k]));
+                    if (a > amax)
+                        amax = a;
+                }
+                const int e = mxo_block_exponent(amax, fmt);
+                const double s = ldexp(1.0, 127 - e);
+                scale_row[i * (N / MXO_BLOCK) + c] = (uint8_t)e;
+                for (k = 0; k < MXO_BLOCK; k++)
+                    out_row[i * N + c * MXO_BLOCK + k] = mxo_fp8_encode(mxo_bf16_to_double(blk[k]) * s, fmt);
+            }
+        }
+    }
+
+    if (out_col && scale_col) {
+        for (r = 0; r < M / MXO_BLOCK; r++) {
+            for (j = 0; j < N; j++) {
+                double amax = 0.0;
+                for (k = 0; k < MXO_BLOCK; k++) {
+                    double a = fabs(mxo_bf16_to_double(x[(r * MXO_BLOCK + k) * N + j]));
+                    if (a > amax)
+                        amax = a;
+                }
+                const int e = mxo_block_exponent(amax, fmt);
+                const double s = ldexp(1.0, 127 - e);
+                scale_col[r * N + j] = (uint8_t)e;
+                for (k = 0; k < MXO_BLOCK; k++) {
+                    const int64_t idx = (r * MXO_BLOCK + k) * N + j;
+                    out_col[idx] = mxo_fp8_encode(mxo_bf16_to_double(x[idx]) * s, fmt);
+                }
+            }
+        }
+    }
+
+    if (dbias) {
+        for (j = 0; j < N; j++) {
+            double acc = 0.0;
+            for (i = 0; i < M; i++)
+                acc += mxo_bf16_to_double(x[i * N + j]);
+            dbias[j] = (float)acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Grouped quantize: rows [offsets[g], offsets[g+1]) form group g; each
+ * group is quantized as its own flat problem and written at its own row
+ * offset in the same output buffers.  offsets has num_groups+1 entries.
+ * Returns 0, or -1 when the offsets are not a prefix-sum vector starting at
+ * 0, ending at total_rows, non-decreasing, with every entry a multiple of 32.
+ */
+int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int num_groups,
+                         const int64_t *offsets, int fmt,
+                         uint8_t *out_row, uint8_t *scale_row,
+                         uint8_t *out_col, uint8_t *scale_col)
+{
+    int g;
+    if (num_groups < 0 || total_rows < 0 || N < 0 || N % MXO_BLOCK)
+        return -1;
+    if (offsets[0] != 0 || offsets[num_groups] != total_rows)
+        return -1;
+    for (g = 0; g < num_groups; g++)
+        if (offsets[g + 1] < offsets[g] || offsets[g + 1] % MXO_BLOCK)
+            return -1;
+    for (g = 0; g < num_groups; g++) {
+        const int64_t r0 = offsets[g], rows = offsets[g + 1] - offsets[g];
+        if (rows == 0)
+            continue;
+        mxo_quantize(x + r0 * N, rows, N, fmt,
+                     out_row ? out_row + r0 * N : 0, scale_row ? scale_row + r0 * (N / MXO_BLOCK) : 0,
+                     out_col ? out_col + r0 * N : 0, scale_col ? scale_col + (r0 / MXO_BLOCK) * N : 0,
+                     0);
+    }
+    return 0;
+}

@@ -1,0 +1,316 @@
+"""Pins for the CPU oracle, against things other than the oracle itself.
+
+* FP8 decode of all 256 codes against torch's float8 dtypes (a library routine).
+* FP8 encode against torch's float32 -> float8 cast on in-range values, plus
+  brute-force properties: round-trip of every finite code, ties-to-even at every
+  midpoint, monotonicity, saturation.
+* The block exponent against its defining inequality and against an integer
+  closed form on the BF16 bits, for every finite positive BF16 value.
+* Hand-worked blocks (tests/golden/hand_blocks.txt).
+* Whole-matrix quantize against a brute-force nearest-code search on small
+  matrices with M != N (catches a transposed operand or a wrong index).
+* The round-trip error bound, the dbias column sum against math.fsum, and the
+  grouped == flat invariant.
+"""
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+E4M3, E5M2 = 0, 1
+FMAX = {E4M3: 448.0, E5M2: 57344.0}
+MBITS = {E4M3: 3, E5M2: 2}
+EMIN = {E4M3: -6, E5M2: -14}
+TORCH_DT = {E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_blocks.txt")
+
+
+def torch_decode_table(fmt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(TORCH_DT[fmt]).to(torch.float64).numpy()
+
+
+def is_finite_code(b, fmt):
+    return math.isfinite(torch_decode_table(fmt)[b])
+
+
+# ---- FP8 codec ----------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_decode_every_code_matches_torch(oracle_mod, fmt):
+    table = torch_decode_table(fmt)
+    for b in range(256):
+        got = oracle_mod.fp8_decode(b, fmt)
+        want = table[b]
+        if math.isnan(want):
+            assert math.isnan(got), (fmt, b)
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), (fmt, b, got, want)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_encode_roundtrips_every_finite_code(oracle_mod, fmt):
+    table = torch_decode_table(fmt)
+    for b in range(256):
+        if math.isfinite(table[b]):
+            assert oracle_mod.fp8_encode(table[b], fmt) == b, (fmt, b)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_encode_midpoints_tie_to_even(oracle_mod, fmt):
+    table = torch_decode_table(fmt)
+    for sign in (0x00, 0x80):
+        for c in range(0, 127):
+            lo, hi = sign | c, sign | (c + 1)
+            if not (math.isfinite(table[lo]) and math.isfinite(table[hi])):
+                continue
+            mid = (table[lo] + table[hi]) / 2
+            even = lo if (c % 2 == 0) else hi   # codes differ only in the mantissa LSB chain
+            assert oracle_mod.fp8_encode(mid, fmt) == even, (fmt, hex(lo), hex(hi))
+            toward_hi = math.nextafter(mid, math.copysign(math.inf, mid))
+            toward_lo = math.nextafter(mid, 0.0)
+            assert oracle_mod.fp8_encode(toward_hi, fmt) == hi
+            assert oracle_mod.fp8_encode(toward_lo, fmt) == lo
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_encode_matches_torch_on_random_inrange(oracle_mod, fmt):
+    rng = np.random.Generator(np.random.PCG64(123 + fmt))
+    n = 40000
+    mag = np.exp2(rng.uniform(math.log2(FMAX[fmt]) - 30, math.log2(FMAX[fmt]), n))
+    v = (rng.choice([-1.0, 1.0], n) * mag).astype(np.float32)
+    want = torch.from_numpy(v).to(TORCH_DT[fmt]).view(torch.uint8).numpy()
+    got = np.array([oracle_mod.fp8_encode(float(t), fmt) for t in v], dtype=np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(v[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_encode_saturates_and_is_monotone(oracle_mod, fmt):
+    top = 0x7E if fmt == E4M3 else 0x7B
+    for v in (FMAX[fmt] * 1.0001, FMAX[fmt] * 1.07, 1e30, math.inf):
+        assert oracle_mod.fp8_encode(v, fmt) == top
+        assert oracle_mod.fp8_encode(-v, fmt) == top | 0x80
+    rng = np.random.Generator(np.random.PCG64(7))
+    v = np.sort(np.exp2(rng.uniform(-30, 20, 3000)))
+    table = torch_decode_table(fmt)
+    dec = [table[oracle_mod.fp8_encode(t, fmt)] for t in v]
+    assert all(a <= b for a, b in zip(dec, dec[1:]))
+
+
+# ---- block exponent ---------------------------------------------------------------
+
+def all_positive_finite_bf16():
+    bits = np.arange(1, 0x7F80, dtype=np.uint16)    # 0x0001 .. 0x7F7F
+    vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    return bits, vals
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_block_exponent_defining_inequality(oracle_mod, fmt):
+    bits, vals = all_positive_finite_bf16()
+    fmax = FMAX[fmt]
+    for a in vals:
+        e = oracle_mod.block_exponent(a, fmt)
+        assert 0 <= e <= 254
+        k = e - 127
+        assert a <= fmax * 2.0 ** k, (a, e)            # scaled amax never exceeds Fmax
+        if e > 0:
+            assert a > fmax * 2.0 ** (k - 1), (a, e)   # and k is the smallest such integer
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_block_exponent_integer_form_on_bf16_bits(oracle_mod, fmt):
+    # For a normal BF16 a = (1 + m/128) 2^(E-127): a <= 1.75 2^(emax+k) iff
+    # k >= E-127-emax + [m/128 > 0.75]; a subnormal amax always clamps to 0.
+    emax = 8 if fmt == E4M3 else 15
+    bits, vals = all_positive_finite_bf16()
+    for b, a in zip(bits.tolist(), vals):
+        E, m = b >> 7, b & 0x7F
+        want = max(0, E - emax + (1 if m > 0x60 else 0)) if E > 0 else 0
+        assert oracle_mod.block_exponent(a, fmt) == want, (hex(b), a)
+    assert oracle_mod.block_exponent(0.0, fmt) == 127
+
+
+def test_e8m0_decode(oracle_mod):
+    assert oracle_mod.e8m0_decode(127) == 1.0
+    assert oracle_mod.e8m0_decode(0) == 2.0 ** -127
+    assert oracle_mod.e8m0_decode(254) == 2.0 ** 127
+    assert math.isnan(oracle_mod.e8m0_decode(255))
+
+
+# ---- hand-worked blocks ---------------------------------------------------------
+
+def parse_value(tok):
+    """'1.0', '-0.0', '2**-130', '3*2**-133', '-2**-10' -> float."""
+    m = re.fullmatch(r"(-?)(?:(\d+)\*)?2\*\*(-?\d+)", tok)
+    if m:
+        v = float(m.group(2) or 1) * 2.0 ** int(m.group(3))
+        return -v if m.group(1) else v
+    return float(tok)
+
+
+def parse_golden():
+    cases = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            fmt_s, elems_s, e_s, bytes_s = [p.strip() for p in line.split("|")]
+            elems, out = [], []
+            for tok in elems_s.split(","):
+                tok = tok.strip()
+                if "**" in tok:
+                    elems.append(parse_value(tok))
+                else:
+                    v, _, n = tok.partition("*")
+                    elems += [parse_value(v)] * (int(n) if n else 1)
+            for tok in bytes_s.split(","):
+                h, _, n = tok.strip().partition("*")
+                out += [int(h, 16)] * (int(n) if n else 1)
+            assert len(elems) == 32 and len(out) == 32, line
+            cases.append((E4M3 if fmt_s == "E4M3" else E5M2, elems, int(e_s), out))
+    return cases
+
+
+GOLDEN_CASES = parse_golden()
+
+
+@pytest.mark.parametrize("case", range(len(GOLDEN_CASES)))
+def test_hand_worked_blocks(oracle_mod, case):
+    fmt, elems, e, want = GOLDEN_CASES[case]
+    bits = wl.to_bf16_bits(np.array(elems, np.float64).reshape(1, 32))
+    back = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(back.ravel(), np.array(elems)), "fixture value is not an exact BF16"
+    # Rowwise: the block is one row.  Colwise: the same block as one column.
+    out_row, scale_row, _, _, _ = oracle_mod.quantize(np.tile(bits, (32, 1)), fmt)
+    assert scale_row[0, 0] == e
+    assert out_row[0].tolist() == want
+    _, _, out_col, scale_col, _ = oracle_mod.quantize(np.tile(bits.reshape(32, 1), (1, 32)), fmt)
+    assert scale_col[0, 0] == e
+    assert out_col[:, 0].tolist() == want
+
+
+# ---- whole matrices against a brute-force nearest-code search -------------------
+
+def brute_force(x_bits, fmt):
+    """Rowwise/colwise quantize by exhaustive search; independent of the oracle's code."""
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    table = torch_decode_table(fmt)
+    finite = np.array([b for b in range(256) if math.isfinite(table[b])])
+    tv = table[finite]
+    fmax = FMAX[fmt]
+
+    def scale_of(amax):
+        if amax == 0:
+            return 127
+        k = next(k for k in range(-300, 300) if amax <= fmax * 2.0 ** k)
+        return min(max(k + 127, 0), 254)
+
+    def encode(v):
+        d = np.abs(tv - v)
+        cand = finite[d == d.min()]
+        same_sign = [b for b in cand if (b >> 7) == (1 if math.copysign(1, v) < 0 else 0)]
+        cand = same_sign or list(cand)
+        even = [b for b in cand if b % 2 == 0]
+        return (even or cand)[0]
+
+    M, N = x.shape
+    out_row = np.zeros((M, N), np.uint8)
+    scale_row = np.zeros((M, N // 32), np.uint8)
+    out_col = np.zeros((M, N), np.uint8)
+    scale_col = np.zeros((M // 32, N), np.uint8)
+    for i in range(M):
+        for c in range(N // 32):
+            blk = x[i, 32 * c:32 * c + 32]
+            e = scale_of(np.abs(blk).max())
+            scale_row[i, c] = e
+            out_row[i, 32 * c:32 * c + 32] = [encode(v * 2.0 ** (127 - e)) for v in blk]
+    for r in range(M // 32):
+        for j in range(N):
+            blk = x[32 * r:32 * r + 32, j]
+            e = scale_of(np.abs(blk).max())
+            scale_col[r, j] = e
+            out_col[32 * r:32 * r + 32, j] = [encode(v * 2.0 ** (127 - e)) for v in blk]
+    return out_row, scale_row, out_col, scale_col
+
+
+def structured_input(M, N, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal((M, N)) * np.exp2(rng.integers(-12, 12, (M, 1)))   # row scales differ
+    a *= np.exp2(rng.integers(-6, 6, (1, N)))                                  # column scales differ
+    a[0, :32] = 0.0
+    a[:32, 0] = 0.0
+    a[1, 32:64] = rng.standard_normal(32) * 1e-39                               # subnormal block
+    a[5, 7] = 3000.0
+    return wl.to_bf16_bits(a)
+
+
+@pytest.mark.parametrize("fmt,M,N", [(E4M3, 64, 96), (E5M2, 96, 64)])
+def test_quantize_matches_brute_force(oracle_mod, fmt, M, N):
+    x = structured_input(M, N, seed=M + N + fmt)
+    got = oracle_mod.quantize(x, fmt)[:4]
+    want = brute_force(x, fmt)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got, want):
+        assert np.array_equal(g, w), name
+
+
+# ---- bounds, dbias, grouped -----------------------------------------------------
+
+@pytest.mark.parametrize("name", ["small_128x256"])
+def test_roundtrip_error_bound(oracle_mod, name):
+    w = wl.make(name)
+    fmt = w["fmt"]
+    x = torch.from_numpy(w["x"].view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    out_row, scale_row, out_col, scale_col, _ = oracle_mod.quantize(w["x"], fmt)
+    table = torch_decode_table(fmt)
+    for q, s in ((out_row, np.repeat(scale_row, 32, axis=1)), (out_col, np.repeat(scale_col, 32, axis=0))):
+        sc = np.exp2(s.astype(np.float64) - 127)
+        v = np.abs(x) / sc
+        ex = np.maximum(np.floor(np.log2(np.where(v > 0, v, 1.0))), EMIN[fmt])
+        half_ulp = np.exp2(ex - MBITS[fmt]) / 2
+        assert np.all(np.abs(table[q] * sc - x) <= half_ulp * sc)
+        assert np.all(v <= FMAX[fmt])
+
+
+def test_dbias_matches_fsum(oracle_mod):
+    rng = np.random.Generator(np.random.PCG64(5))
+    M, N = 96, 64
+    a = rng.standard_normal((M, N))
+    a[:, 0] = rng.integers(-50, 50, M)                 # exact small integers
+    a[:, 1] = np.exp2(rng.integers(-10, 10, M))         # exact powers of two
+    a[:, 2] = 1.0                                        # an fp32 running sum loses these ones
+    a[0, 2] = 2.0 ** 24                                  # behind 2^24; the exact sum keeps them
+    a[:, 3] *= np.exp2(rng.integers(-20, 20, M))         # wide exponent spread
+    x = wl.to_bf16_bits(a)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    dbias = oracle_mod.quantize(x, E5M2, with_dbias=True)[4]
+    want = np.array([math.fsum(xv[:, j]) for j in range(N)], np.float32)
+    assert np.array_equal(dbias, want)
+    assert dbias[0] == float(np.sum(xv[:, 0]))
+    assert dbias[2] == np.float32(2.0 ** 24 + 95)
+
+
+def test_grouped_equals_flat_and_rejects_bad_offsets(oracle_mod):
+    sizes = wl.moe_group_sizes(8, 512, seed=3, forced_empty=2)
+    off = wl.offsets_from_sizes(sizes)
+    x = wl.moe_bf16(sizes, 96, seed=3)
+    flat = oracle_mod.quantize(x, E4M3)[:4]
+    grouped = oracle_mod.quantize_grouped(x, off, E4M3)
+    for f, g in zip(flat, grouped):
+        assert np.array_equal(f, g)
+    for bad in ([0, 16, 512], [0, 256, 128, 512], [0, 256, 480], [32, 512]):
+        with pytest.raises(ValueError):
+            oracle_mod.quantize_grouped(x, np.array(bad), E4M3)
+
+
+def test_moe_sizes_recipe():
+    sizes = wl.moe_group_sizes(64, 65536, seed=4)
+    assert sizes.sum() == 65536 and np.all(sizes % 32 == 0)
+    assert (sizes == 0).sum() >= 4
