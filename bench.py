@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""MXFP8 quantize benchmark: prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload fc1_8192x28672|act_4096x4096|grad_16384x8192|moe_64x65536x7168]
+
+A step is one bidirectional (rowwise + colwise) quantize of the whole
+workload, inputs already resident in device memory.  The metric is effective
+bandwidth: (2 + 1 + 1 + 1/16) * M * N bytes per step (read BF16, write two FP8
+planes and two E8M0 scale planes; + 4N for dbias) over the device-timed step.
+
+Under torchrun (N > 1) every rank quantizes its own copy of the workload
+(weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the max over ranks is reported.
+
+--impl reference times the CPU oracle (the only other implementation there
+is) on a bounded 32-row sample of the same workload per step, on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 quantize effective GB/s and % of GB300 HBM peak (rowwise+colwise)"
+BYTES_PER_ELEM = 2 + 1 + 1 + 1 / 16
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["mxfp8_block_scaled_04_gb300/csrc/quantize.cuh", "mxfp8_block_scaled_04_gb300/csrc/ptx.cuh",
+                  "mxfp8_block_scaled_04_gb300/csrc/api.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="fc1_8192x28672")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"quantize_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_sha and m_b) or m_sha.group(1) != kernel_source_sha():
+        return None
+    return int(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in a background process."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid=None):
+        self.samples = []   # (host time, sm, max, power, reasons)
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_uuid:
+            cmd += ["-i", gpu_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx, pw = float(parts[0]), float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(names, parts[3:7]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, mx, pw, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
+        window = "timed"
+        if not inside:
+            inside, window = self.samples, "whole run (timed region shorter than the 100 ms sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in inside for r in s[4]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(s[3] for s in inside)}
+
+
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def cpu_baseline(wl_x, N, fmt, target_s):
+    """Time the oracle on the first R rows of the workload (R adaptive for ~target_s of CPU work)."""
+    import numpy as np
+    import oracle
+
+    oracle.build()
+    stripe = np.ascontiguousarray(wl_x[:32])
+    t = time.perf_counter()
+    oracle.quantize(stripe, fmt)
+    per_stripe = max(time.perf_counter() - t, 1e-6)
+    stripes = int(max(1, min(wl_x.shape[0] // 32, target_s / per_stripe)))
+    sample = np.ascontiguousarray(wl_x[: 32 * stripes])
+    t = time.perf_counter()
+    oracle.quantize(sample, fmt)
+    dt = time.perf_counter() - t
+    return {"value": BYTES_PER_ELEM * sample.size / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {32 * stripes} rows x {N} columns ({sample.size} elements) of the workload, "
+                      f"single-threaded scalar C oracle, {dt:.2f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, rank 0 only, bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+    oracle.build()
+    spec = wl.WORKLOADS[args.workload]
+    M, N, fmt = spec[0], spec[1], spec[2]
+    # sample: rows 0..31 of a workload-shaped input, C columns (C adaptive: whole run within ~2 minutes)
+    full = wl.make(args.workload) if M * N <= 300_000_000 else None
+    if full is None:
+        raise SystemExit("workload too large for the reference arm")
+    x = full["x"]
+    probe = np.ascontiguousarray(x[:32, : min(N, 1024)])
+    t = time.perf_counter()
+    oracle.quantize(probe, fmt)
+    per_elem = (time.perf_counter() - t) / probe.size
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    C = int(max(32, min(N, (budget / per_elem / 32) // 32 * 32)))
+    sample = np.ascontiguousarray(x[:32, :C])
+    for _ in range(args.warmup):
+        oracle.quantize(sample, fmt)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.quantize(sample, fmt)
+    dt = time.perf_counter() - t
+    value = BYTES_PER_ELEM * sample.size * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
+                   "sample_per_step": f"rows 0..31 x columns 0..{C - 1}"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"32 x {C} elements of the workload per step, single-threaded scalar C oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import mxfp8_block_scaled_04_gb300 as mx
+    from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    spec = wl.WORKLOADS[args.workload]
+    w = wl.make(args.workload)
+    x_bits, fmt, with_dbias, offsets = w["x"], w["fmt"], w["with_dbias"], w["offsets"]
+    M, N = x_bits.shape
+    grouped = offsets is not None
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    out_row = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    scale_row = torch.empty((M, N // 32), dtype=torch.uint8, device="cuda")
+    out_col = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    scale_col = torch.empty((M // 32, N), dtype=torch.uint8, device="cuda")
+    dbias = torch.empty((N,), dtype=torch.float32, device="cuda") if with_dbias else None
+    ws = (torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
+          if with_dbias else None)
+    off_dev = torch.from_numpy(offsets).cuda() if grouped else None
+    stream = torch.cuda.current_stream()
+
+    def step(xin=x):
+        if grouped:
+            st = mx.mxfp8_quantize_grouped(xin, M, N, off_dev.numel() - 1, off_dev, fmt, out_row, scale_row,
+                                           out_col, scale_col, None, None, None, stream)
+        else:
+            st = mx.mxfp8_quantize(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
+                                   stream)
+        if st != 0:
+            raise mx.MXFP8Error(st, "bench step")
+
+    algo_bytes = BYTES_PER_ELEM * M * N + (4 * N if with_dbias else 0)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    def timed():
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        launches0 = mx.mxfp8_kernel_launch_count()
+        barrier()
+        torch.cuda.synchronize()
+        h0 = time.time()
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.time()
+        barrier()
+        launches = mx.mxfp8_kernel_launch_count() - launches0
+        total_ms = t_begin.elapsed_time(t_end)
+        per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return total_ms, per_launch, launches, h0, h1
+
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    total_ms, per_launch, launches, h0, h1 = timed()
+    clocks = sampler.summary(h0, h1)
+    if BAD_REASONS & set(clocks.get("reasons", [])):
+        total_ms, per_launch, launches, h0, h1 = timed()     # re-measure once
+        clocks = sampler.summary(h0, h1)
+        clocks["remeasured"] = True
+    sampler.stop()
+
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    ms_per_step = total_ms / args.steps
+    value = algo_bytes * args.steps * world / (total_ms / 1e3) / 1e9
+    kernel_ms = statistics.mean(per_launch)
+    peak, peak_src = measured_peak()
+    achieved = algo_bytes / (kernel_ms / 1e3) / 1e9
+
+    # ---- end to end through the public API: pinned host in, pinned host out ----
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        outs_dev = [out_row, scale_row, out_col, scale_col] + ([dbias] if with_dbias else [])
+        outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
+        x_stage = torch.empty_like(x)
+        h2d = x_host.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in outs_host)
+
+        def e2e_step():
+            x_stage.copy_(x_host, non_blocking=True)
+            step(x_stage)
+            for hd, dd in zip(outs_host, outs_dev):
+                hd.copy_(dd, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.e2e_steps)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        if dist is not None:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": algo_bytes * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "pinned host -> device copy, mxfp8 C-ABI call, device -> pinned host copy of every output"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x_bits, N, fmt, args.cpu_seconds)
+
+    fault = mx.mxfp8_device_fault_word()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
+                       "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
+                       "bytes_per_step": algo_bytes,
+                       "l2": f"inputs larger than L2: {M * N * 2 / 1e6:.0f} MB bf16 read per step vs "
+                             f"{L2_BYTES / 2 ** 20:.0f} MiB L2, no flush",
+                       "parallelism": f"{world} independent replica(s)" if world > 1 else "single GPU"},
+            "pct_of_8tbs": 100 * value / world / 8000.0,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
+                         "traffic": profiled_traffic(args.workload),
+                         "kernel": "quantize_kernel" + (" + dbias_reduce_kernel" if with_dbias else ""),
+                         "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": algo_bytes},
+            "clocks": clocks,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "device_fault_word": fault,
+            "kernel_source_sha": kernel_source_sha(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        from mxfp8_block_scaled_04_gb300 import build
+
+        if build.needs_build():
+            build.build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * mxfp8.h -- C ABI of the GB300 (sm_103a) MXFP8 block-scaled quantize library.
+ *
+ * The operation is the MXFP8 cast of "[Common] Experimental CuTeDSL MXFP8
+ * backends in C++ via TVM-FFI" (TransformerEngine PR #3137): a BF16 matrix
+ * becomes FP8 data plus one E8M0 power-of-two scale per 32-element block.
+ * The quantization-config review on that page (`to_key()`) names the options
+ * this ABI exposes: fp8_dtype, rowwise, colwise, with_dbias and with_noop;
+ * the "non-32-divisible shapes" review fixes the 32-element block and the
+ * requirement that M and N be multiples of 32.
+ *
+ * Arithmetic, per 32-element block with amax = max |x| over the block:
+ *     e = clamp(ceil(log2(amax / Fmax)) + 127, 0, 254)   (amax == 0 -> e = 127)
+ *     q = round-to-nearest-even, saturate-finite (x * 2^(127 - e))
+ * with Fmax = 448 (E4M3) or 57344 (E5M2).  Results are bit-exact with that
+ * definition for every finite BF16 input.
+ *
+ * Layouts (all row-major, all buffers device memory owned by the caller):
+ *     x          bf16  [M, N]
+ *     out_row    uint8 [M, N]     FP8 codes, block = 1x32 along a row
+ *     scale_row  uint8 [M, N/32]  E8M0 of block (i, j/32)
+ *     out_col    uint8 [M, N]     FP8 codes, block = 32x1 down a column;
+ *                                 element (i, j) uses scale_col[i/32, j]
+ *     scale_col  uint8 [M/32, N]  E8M0 of block (i/32, j)
+ *     dbias      fp32  [N]        column sums of x (unquantized)
+ *
+ * Conventions shared by every call:
+ *   - The library allocates nothing.  It keeps per-device cached attributes
+ *     and a launch counter, nothing else.
+ *   - All validation happens on the host before any launch; every rejection
+ *     is a status code, nothing throws or aborts across this boundary.
+ *   - Work is stream-ordered on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call synchronizes the host or reads device memory
+ *     from the host, except mxfp8_device_fault_word().
+ *   - The device is the calling thread's current device; x must live on it.
+ *   - noop: optional device fp32 scalar.  When *noop == 1.0f every kernel of
+ *     the call returns without writing anything (the "Perform noop tensor
+ *     check on device" change on the PR #3137 page), dbias included.
+ */
+#ifndef MXFP8_GB300_H
+#define MXFP8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* FP8 element format (the `fp8_dtype` field of the PR #3137 config key). */
+typedef enum {
+    MXFP8_E4M3 = 0, /* 1 sign, 4 exponent (bias 7), 3 mantissa; max 448   */
+    MXFP8_E5M2 = 1  /* 1 sign, 5 exponent (bias 15), 2 mantissa; max 57344 */
+} mxfp8_fmt_t;
+
+typedef enum {
+    MXFP8_OK = 0,
+    MXFP8_ERR_NULL = 1,      /* required pointer NULL, a data/scale pair half set, or no direction */
+    MXFP8_ERR_SHAPE = 2,     /* M or N negative or not a multiple of 32, or too large */
+    MXFP8_ERR_ALIGN = 3,     /* x/out/workspace not 16-byte aligned, scale_col/dbias not 4-byte */
+    MXFP8_ERR_FORMAT = 4,    /* fp8_fmt not MXFP8_E4M3 / MXFP8_E5M2 */
+    MXFP8_ERR_WORKSPACE = 5, /* dbias requested and workspace NULL */
+    MXFP8_ERR_DEVICE = 6,    /* no usable CUDA device, or a buffer not on the current device */
+    MXFP8_ERR_LAUNCH = 7,    /* a CUDA call of this library failed (driver/launch error) */
+    MXFP8_ERR_GROUPS = 8     /* num_groups < 1 or above MXFP8_MAX_GROUPS, or offsets NULL */
+} mxfp8_status_t;
+
+/* Largest num_groups mxfp8_quantize_grouped accepts. */
+#define MXFP8_MAX_GROUPS 512
+
+/*
+ * Bytes of device workspace mxfp8_quantize needs for (M, N, with_dbias).
+ * 0 when with_dbias == 0.  With dbias it holds one fp32 partial column sum
+ * per 128-row tile: ceil(M/128) * N * 4 bytes.  Returns 0 for invalid shapes.
+ * (The workspace query precedes any launch, as on the PR #3137 page.)
+ */
+size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias);
+
+/*
+ * Quantize x[M,N] rowwise and/or columnwise (PR #3137: rowwise / colwise /
+ * with_dbias / with_noop config fields).
+ *
+ *   x           device, bf16 [M,N], 16-byte aligned.
+ *   M, N        multiples of 32, >= 0.  M == 0 or N == 0: nothing to quantize,
+ *               x and the output pointers may then be NULL (dbias, if
+ *               requested, is set to zeros unless noop).
+ *   fp8_fmt     MXFP8_E4M3 or MXFP8_E5M2.
+ *   out_row, scale_row   rowwise outputs; both NULL skips the rowwise direction.
+ *   out_col, scale_col   columnwise outputs; both NULL skips that direction.
+ *               Setting only one pointer of a pair is MXFP8_ERR_NULL, and so
+ *               is skipping both directions.  out_* 16-byte aligned,
+ *               scale_col 4-byte aligned.
+ *   dbias       device fp32 [N] or NULL.  Written with the column sums of x,
+ *               accumulated deterministically (fixed order, no atomics):
+ *               per-tile fp32 partials, then an fp64 sum over tiles.
+ *   workspace   device, >= mxfp8_quantize_workspace_bytes(M, N, dbias != NULL)
+ *               bytes, 16-byte aligned; may be NULL when dbias is NULL.
+ *   noop        device fp32 scalar or NULL (see above).
+ *   stream      cudaStream_t.
+ *
+ * Returns MXFP8_OK once the work is enqueued.  The outputs must not overlap x
+ * or each other.
+ */
+mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt,
+                              void *out_row, void *scale_row,
+                              void *out_col, void *scale_col,
+                              float *dbias, void *workspace, const float *noop,
+                              void *stream);
+
+/*
+ * Workspace bytes for mxfp8_quantize_grouped: currently always 0 (the grouped
+ * call keeps its schedule in shared memory); reserved so callers can size it.
+ */
+size_t mxfp8_quantize_grouped_workspace_bytes(int64_t total_rows, int64_t N, int num_groups);
+
+/*
+ * Grouped (MoE) quantize in one launch: rows [offsets[g], offsets[g+1]) of x
+ * belong to expert g.  The ragged-offset convention follows the grouped
+ * expert routing of "Lightning W4A16 grouped NVFP4 GEMM" (cudnn-frontend
+ * PR #811, API section: per-expert offsets read on the device, one kernel,
+ * zero workspace, no host copy of the offsets), here as a full prefix vector.
+ *
+ *   x            device bf16 [total_rows, N], 16-byte aligned.
+ *   num_groups   1 .. MXFP8_MAX_GROUPS.
+ *   offsets      device int64 [num_groups + 1]: offsets[0] == 0,
+ *                offsets[num_groups] == total_rows, non-decreasing, every
+ *                entry a multiple of 32.  Read only on the device.  Empty
+ *                groups produce no work.  No tile straddles two groups.
+ *   outputs      as for mxfp8_quantize on the concatenated rows (so the
+ *                result equals the flat call on x); no dbias.
+ *   workspace    may be NULL (see mxfp8_quantize_grouped_workspace_bytes).
+ *   err_flag     device int or NULL.  If the offsets break a rule above, the
+ *                kernel writes nothing and sets *err_flag = 1.  It is never
+ *                cleared by the library.
+ *
+ * total_rows and N must be multiples of 32.
+ */
+mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t N,
+                                      int num_groups, const int64_t *offsets, int fp8_fmt,
+                                      void *out_row, void *scale_row,
+                                      void *out_col, void *scale_col,
+                                      void *workspace, const float *noop, int *err_flag,
+                                      void *stream);
+
+/* Static, human-readable text for a status code. */
+const char *mxfp8_status_string(int status);
+
+/* Number of kernels this library has launched in this process (diagnostic). */
+uint64_t mxfp8_kernel_launch_count(void);
+
+/*
+ * Read (and, if clear != 0, reset) the library's device fault word on the
+ * current device.  Bit 0 is set when a kernel gave up waiting for its own
+ * tile copies (a bounded wait expired) and returned early.  Synchronizes the
+ * device.  Returns MXFP8_OK or MXFP8_ERR_DEVICE / MXFP8_ERR_LAUNCH.
+ */
+mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_GB300_H */

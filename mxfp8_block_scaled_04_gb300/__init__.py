@@ -1,0 +1,14 @@
+"""GB300-native (sm_103a) MXFP8 block-scaled quantize engine.
+
+BF16 [M, N] -> FP8 (E4M3 / E5M2) with one E8M0 scale per 32-element block,
+rowwise (1x32) and columnwise (32x1) in one pass, with optional fused dbias
+and a device noop flag, plus a grouped (MoE, ragged row offsets) variant.
+The compute runs in the CUDA library built from ``csrc/``; this package is its
+ctypes binding.
+"""
+from .binding import (  # noqa: F401
+    BLOCK, E4M3, E5M2, MAX_GROUPS, MXFP8Error, MXFP8Tensor, STATUS_NAMES,
+    lib, mxfp8_device_fault_word, mxfp8_kernel_launch_count, mxfp8_quantize,
+    mxfp8_quantize_grouped, mxfp8_quantize_grouped_workspace_bytes,
+    mxfp8_quantize_workspace_bytes, mxfp8_status_string, quantize, quantize_grouped,
+)

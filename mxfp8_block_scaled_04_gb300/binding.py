@@ -1,0 +1,188 @@
+"""Python binding of the C ABI in include/mxfp8.h (ctypes; marshalling only).
+
+The functions named ``mxfp8_*`` mirror the C entry points one for one: they
+take torch tensors (or raw integer device addresses, or None for NULL) and
+return the C status code.  ``quantize`` / ``quantize_grouped`` allocate the
+outputs with torch and raise :class:`MXFP8Error` on a non-OK status.  Every
+step of the computation runs in the CUDA library; there is no fallback, and
+the first call fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+E4M3 = 0
+E5M2 = 1
+BLOCK = 32
+MAX_GROUPS = 512
+
+STATUS_NAMES = {
+    0: "MXFP8_OK", 1: "MXFP8_ERR_NULL", 2: "MXFP8_ERR_SHAPE", 3: "MXFP8_ERR_ALIGN",
+    4: "MXFP8_ERR_FORMAT", 5: "MXFP8_ERR_WORKSPACE", 6: "MXFP8_ERR_DEVICE",
+    7: "MXFP8_ERR_LAUNCH", 8: "MXFP8_ERR_GROUPS",
+}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmxfp8.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class MXFP8Error(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({mxfp8_status_string(status)})")
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"MXFP8 CUDA library not found at {LIB_PATH}; build it with "
+                    "`python -m mxfp8_block_scaled_04_gb300.build` (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.mxfp8_quantize_workspace_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_workspace_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize.restype = i32
+            L.mxfp8_quantize.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_grouped_workspace_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_grouped_workspace_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_grouped.restype = i32
+            L.mxfp8_quantize_grouped.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_status_string.restype = ctypes.c_char_p
+            L.mxfp8_status_string.argtypes = [i32]
+            L.mxfp8_kernel_launch_count.restype = ctypes.c_uint64
+            L.mxfp8_kernel_launch_count.argtypes = []
+            L.mxfp8_device_fault_word.restype = i32
+            L.mxfp8_device_fault_word.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+            _lib = L
+    return _lib
+
+
+def _addr(a) -> Optional[int]:
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        return a.data_ptr() if a.numel() > 0 or a.data_ptr() else None
+    return int(a)
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream
+    return int(s)
+
+
+# ---- one-for-one C entry points --------------------------------------------------
+
+def mxfp8_quantize_workspace_bytes(M: int, N: int, with_dbias: bool) -> int:
+    return int(lib().mxfp8_quantize_workspace_bytes(M, N, int(bool(with_dbias))))
+
+
+def mxfp8_quantize(x, M, N, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                   dbias=None, workspace=None, noop=None, stream=None) -> int:
+    return int(lib().mxfp8_quantize(_addr(x), M, N, fp8_fmt, _addr(out_row), _addr(scale_row),
+                                    _addr(out_col), _addr(scale_col), _addr(dbias), _addr(workspace),
+                                    _addr(noop), _stream(stream)))
+
+
+def mxfp8_quantize_grouped_workspace_bytes(total_rows: int, N: int, num_groups: int) -> int:
+    return int(lib().mxfp8_quantize_grouped_workspace_bytes(total_rows, N, num_groups))
+
+
+def mxfp8_quantize_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row,
+                           out_col, scale_col, workspace=None, noop=None, err_flag=None, stream=None) -> int:
+    return int(lib().mxfp8_quantize_grouped(_addr(x), total_rows, N, num_groups, _addr(offsets), fp8_fmt,
+                                            _addr(out_row), _addr(scale_row), _addr(out_col),
+                                            _addr(scale_col), _addr(workspace), _addr(noop),
+                                            _addr(err_flag), _stream(stream)))
+
+
+def mxfp8_status_string(status: int) -> str:
+    return lib().mxfp8_status_string(int(status)).decode()
+
+
+def mxfp8_kernel_launch_count() -> int:
+    return int(lib().mxfp8_kernel_launch_count())
+
+
+def mxfp8_device_fault_word(clear: bool = False) -> int:
+    out = ctypes.c_uint(0)
+    st = lib().mxfp8_device_fault_word(ctypes.byref(out), int(bool(clear)))
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_device_fault_word")
+    return int(out.value)
+
+
+# ---- torch conveniences ----------------------------------------------------------
+
+class MXFP8Tensor(NamedTuple):
+    """Quantized outputs; a direction that was not requested is None."""
+    out_row: Optional[torch.Tensor]     # uint8 [M, N]
+    scale_row: Optional[torch.Tensor]   # uint8 [M, N/32] (E8M0)
+    out_col: Optional[torch.Tensor]     # uint8 [M, N]
+    scale_col: Optional[torch.Tensor]   # uint8 [M/32, N] (E8M0)
+    dbias: Optional[torch.Tensor]       # float32 [N]
+
+
+def _fmt(fmt) -> int:
+    if isinstance(fmt, str):
+        return {"e4m3": E4M3, "e5m2": E5M2}[fmt.lower()]
+    return int(fmt)
+
+
+def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool):
+    M, N = x.shape
+    dev = x.device
+    u8 = torch.uint8
+    return (torch.empty((M, N), dtype=u8, device=dev) if rowwise else None,
+            torch.empty((M, N // BLOCK), dtype=u8, device=dev) if rowwise else None,
+            torch.empty((M, N), dtype=u8, device=dev) if colwise else None,
+            torch.empty((M // BLOCK, N), dtype=u8, device=dev) if colwise else None)
+
+
+def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
+             with_dbias: bool = False, noop: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (M, N multiples of 32)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
+    M, N = x.shape
+    f = _fmt(fmt)
+    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
+    dbias = torch.empty((N,), dtype=torch.float32, device=x.device) if with_dbias else None
+    if with_dbias and workspace is None:
+        nbytes = mxfp8_quantize_workspace_bytes(M, N, True)
+        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
+    st = mxfp8_quantize(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,
+                        workspace if with_dbias else None, noop, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+
+
+def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,
+                     colwise: bool = True, noop: Optional[torch.Tensor] = None,
+                     err_flag: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
+    if offsets.dtype != torch.int64 or offsets.dim() != 1 or not offsets.is_contiguous():
+        raise ValueError("offsets must be a contiguous 1-D torch.int64 tensor")
+    total, N = x.shape
+    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
+    st = mxfp8_quantize_grouped(x, total, N, offsets.numel() - 1, offsets, _fmt(fmt), out_row, scale_row,
+                                out_col, scale_col, None, noop, err_flag, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_grouped")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)

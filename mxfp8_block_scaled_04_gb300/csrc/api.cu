@@ -1,0 +1,340 @@
+// C ABI of the MXFP8 quantize library (declarations and contract in
+// include/mxfp8.h).  Host-side validation, TMA descriptor encoding and
+// kernel launches; the device code is in quantize.cuh.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/mxfp8.h"
+#include "quantize.cuh"
+
+namespace {
+
+using namespace mxfp8;
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<uint64_t> g_launches{0};
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int ctas_per_sm[8] = {};  // indexed by kernel variant
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Is p device (or managed) memory of `device`?  NULL passes.
+bool on_device(const void *p, int device)
+{
+    if (p == nullptr)
+        return true;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged)
+        return true;
+    return a.type == cudaMemoryTypeDevice && a.device == device;
+}
+
+template <int FMT, bool DBIAS, bool GROUPED>
+int variant_index()
+{
+    return FMT + 2 * (DBIAS ? 1 : 0) + 4 * (GROUPED ? 1 : 0);
+}
+
+// One-time per (device, variant) set-up: opt in to the large shared-memory
+// carve-out and record how many CTAs fit per SM.
+template <int FMT, bool DBIAS, bool GROUPED>
+mxfp8_status_t prepare(int device, int *grid_cap)
+{
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (device < 0 || device >= kMaxDevices)
+        return MXFP8_ERR_DEVICE;
+    DeviceInfo &d = g_dev[device];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            return MXFP8_ERR_DEVICE;
+        d.ready = true;
+    }
+    const int v = variant_index<FMT, DBIAS, GROUPED>();
+    if (d.ctas_per_sm[v] == 0) {
+        const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
+        auto kern = quantize_kernel<FMT, DBIAS, GROUPED>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1)
+            return MXFP8_ERR_LAUNCH;
+        d.ctas_per_sm[v] = n;
+    }
+    *grid_cap = d.ctas_per_sm[v] * d.sm_count;
+    return MXFP8_OK;
+}
+
+mxfp8_status_t make_tensor_map(CUtensorMap *map, const void *x, int64_t rows, int64_t N)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr)
+        return MXFP8_ERR_DEVICE;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint32_t box[2] = {kBoxCols, kBM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+// dbias[j] = sum over row tiles t (in order) of ws[t][j], accumulated in fp64.
+__global__ void dbias_reduce_kernel(const float *__restrict__ ws, int64_t row_tiles, int64_t N,
+                                    float *__restrict__ dbias, const float *noop)
+{
+    if (noop != nullptr && *noop == 1.0f)
+        return;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= N)
+        return;
+    double acc = 0.0;
+    for (int64_t t = 0; t < row_tiles; ++t)
+        acc += static_cast<double>(ws[t * N + j]);
+    dbias[j] = static_cast<float>(acc);
+}
+
+// Shared host-side checks of the direction pointers.
+mxfp8_status_t check_outputs(void *out_row, void *scale_row, void *out_col, void *scale_col)
+{
+    if ((out_row == nullptr) != (scale_row == nullptr) || (out_col == nullptr) != (scale_col == nullptr))
+        return MXFP8_ERR_NULL;
+    if (out_row == nullptr && out_col == nullptr)
+        return MXFP8_ERR_NULL;
+    if (!aligned(out_row, 16) || !aligned(out_col, 16) || !aligned(scale_col, 4))
+        return MXFP8_ERR_ALIGN;
+    return MXFP8_OK;
+}
+
+mxfp8_status_t current_device(int *device)
+{
+    if (cudaGetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return MXFP8_ERR_DEVICE;
+    }
+    return MXFP8_OK;
+}
+
+template <bool DBIAS, bool GROUPED>
+mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, const QuantParams &p,
+                               int64_t tile_bound, cudaStream_t stream)
+{
+    int cap = 0;
+    mxfp8_status_t st = fmt == MXFP8_E4M3 ? prepare<0, DBIAS, GROUPED>(device, &cap)
+                                          : prepare<1, DBIAS, GROUPED>(device, &cap);
+    if (st != MXFP8_OK)
+        return st;
+    const int grid = static_cast<int>(tile_bound < cap ? tile_bound : cap);
+    const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
+    if (fmt == MXFP8_E4M3)
+        quantize_kernel<0, DBIAS, GROUPED><<<grid, kThreads, smem, stream>>>(map, p);
+    else
+        quantize_kernel<1, DBIAS, GROUPED><<<grid, kThreads, smem, stream>>>(map, p);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias)
+{
+    if (!with_dbias || M < 0 || N < 0 || M % 32 || N % 32)
+        return 0;
+    return static_cast<size_t>((M + kBM - 1) / kBM) * static_cast<size_t>(N) * sizeof(float);
+}
+
+size_t mxfp8_quantize_grouped_workspace_bytes(int64_t, int64_t, int) { return 0; }
+
+mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, void *out_row, void *scale_row,
+                              void *out_col, void *scale_col, float *dbias, void *workspace, const float *noop,
+                              void *stream_)
+{
+    // ---- host-only checks, in a fixed order, before touching the device ----
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    const bool empty = M == 0 || N == 0;  // nothing to read or write: data pointers may be NULL
+    mxfp8_status_t st;
+    if (!empty) {
+        if (x == nullptr)
+            return MXFP8_ERR_NULL;
+        if ((st = check_outputs(out_row, scale_row, out_col, scale_col)) != MXFP8_OK)
+            return st;
+    }
+    if (!aligned(x, 16) || !aligned(dbias, 4) || !aligned(workspace, 16))
+        return MXFP8_ERR_ALIGN;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kBN - 1) / kBN;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (dbias != nullptr && workspace == nullptr && M > 0)
+        return MXFP8_ERR_WORKSPACE;
+
+    // ---- device checks ----
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(out_row, device) || !on_device(scale_row, device) ||
+        !on_device(out_col, device) || !on_device(scale_col, device) || !on_device(dbias, device) ||
+        !on_device(workspace, device) || !on_device(noop, device))
+        return MXFP8_ERR_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    if (!empty) {
+        CUtensorMap map;
+        if ((st = make_tensor_map(&map, x, M, N)) != MXFP8_OK)
+            return st;
+        QuantParams p{};
+        p.out_row = static_cast<uint8_t *>(out_row);
+        p.scale_row = static_cast<uint8_t *>(scale_row);
+        p.out_col = static_cast<uint8_t *>(out_col);
+        p.scale_col = static_cast<uint8_t *>(scale_col);
+        p.ws = dbias != nullptr ? static_cast<float *>(workspace) : nullptr;
+        p.noop = noop;
+        p.M = M;
+        p.N = N;
+        p.row_tiles = static_cast<int>(row_tiles);
+        p.col_tiles = static_cast<int>(col_tiles);
+        st = dbias != nullptr ? launch_quantize<true, false>(fp8_fmt, device, map, p, row_tiles * col_tiles, stream)
+                              : launch_quantize<false, false>(fp8_fmt, device, map, p, row_tiles * col_tiles, stream);
+        if (st != MXFP8_OK)
+            return st;
+    }
+    if (dbias != nullptr && N > 0) {
+        const int threads = 256;
+        const int64_t blocks = (N + threads - 1) / threads;
+        dbias_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+            static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (cudaGetLastError() != cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+    }
+    return MXFP8_OK;
+}
+
+mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                      const int64_t *offsets, int fp8_fmt, void *out_row, void *scale_row,
+                                      void *out_col, void *scale_col, void *workspace, const float *noop,
+                                      int *err_flag, void *stream_)
+{
+    (void)workspace;
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 32 || total_rows >= (int64_t{1} << 31) ||
+        N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
+        return MXFP8_ERR_GROUPS;
+    if (x == nullptr)
+        return MXFP8_ERR_NULL;
+    mxfp8_status_t st = check_outputs(out_row, scale_row, out_col, scale_col);
+    if (st != MXFP8_OK)
+        return st;
+    if (!aligned(x, 16) || !aligned(offsets, 8) || !aligned(err_flag, 4))
+        return MXFP8_ERR_ALIGN;
+    const int64_t col_tiles = (N + kBN - 1) / kBN;
+    // Upper bound on the tile count: every non-empty group adds at most one partial row tile.
+    const int64_t tile_bound = (total_rows / kBM + num_groups) * col_tiles;
+    if (tile_bound >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(offsets, device) || !on_device(out_row, device) ||
+        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
+        !on_device(noop, device) || !on_device(err_flag, device))
+        return MXFP8_ERR_DEVICE;
+    if (total_rows == 0 || N == 0)
+        return MXFP8_OK;
+
+    CUtensorMap map;
+    if ((st = make_tensor_map(&map, x, total_rows, N)) != MXFP8_OK)
+        return st;
+    QuantParams p{};
+    p.out_row = static_cast<uint8_t *>(out_row);
+    p.scale_row = static_cast<uint8_t *>(scale_row);
+    p.out_col = static_cast<uint8_t *>(out_col);
+    p.scale_col = static_cast<uint8_t *>(scale_col);
+    p.noop = noop;
+    p.offsets = offsets;
+    p.err_flag = err_flag;
+    p.M = total_rows;
+    p.N = N;
+    p.num_groups = num_groups;
+    p.col_tiles = static_cast<int>(col_tiles);
+    return launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, static_cast<cudaStream_t>(stream_));
+}
+
+const char *mxfp8_status_string(int status)
+{
+    switch (status) {
+    case MXFP8_OK: return "ok";
+    case MXFP8_ERR_NULL: return "required pointer is NULL, a data/scale pair is half set, or no direction requested";
+    case MXFP8_ERR_SHAPE: return "M/N must be non-negative multiples of 32 and below 2^31";
+    case MXFP8_ERR_ALIGN: return "x/out/workspace must be 16-byte aligned, scale_col/dbias 4-byte aligned";
+    case MXFP8_ERR_FORMAT: return "fp8_fmt must be MXFP8_E4M3 (0) or MXFP8_E5M2 (1)";
+    case MXFP8_ERR_WORKSPACE: return "dbias requested without a workspace";
+    case MXFP8_ERR_DEVICE: return "no usable CUDA device, or a buffer is not on the current device";
+    case MXFP8_ERR_LAUNCH: return "a CUDA call failed while preparing or launching a kernel";
+    case MXFP8_ERR_GROUPS: return "num_groups out of range or offsets NULL";
+    default: return "unknown status";
+    }
+}
+
+uint64_t mxfp8_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear)
+{
+    if (out == nullptr)
+        return MXFP8_ERR_NULL;
+    int device = 0;
+    mxfp8_status_t st = current_device(&device);
+    if (st != MXFP8_OK)
+        return st;
+    if (cudaMemcpyFromSymbol(out, g_fault_word, sizeof(unsigned int)) != cudaSuccess)
+        return MXFP8_ERR_LAUNCH;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned int)) != cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+    }
+    return MXFP8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,406 @@
+// MXFP8 block-scaled quantize kernels for sm_103a (GB300).
+//
+// One pass over HBM: every BF16 element is read once (TMA, 128x128 tiles)
+// and produces a rowwise FP8 byte (1x32 block along the row) and a
+// columnwise FP8 byte (32x1 block down the column), plus the two E8M0 scale
+// planes and, optionally, fp32 per-tile column partials for dbias.
+//
+// The operation is the MXFP8 cast of "[Common] Experimental CuTeDSL MXFP8
+// backends in C++ via TVM-FFI" (TransformerEngine PR #3137): rowwise /
+// colwise / with_dbias / with_noop config fields, 32-element blocks.
+//
+// Per block, amax is taken on the BF16 bit patterns (|x| ordering equals the
+// integer ordering of bits & 0x7FFF for finite values) and the E8M0 exponent
+//     e = clamp(ceil(log2(amax / Fmax)) + 127, 0, 254),  amax == 0 -> 127
+// is computed exactly in integers: for a normal amax = (1 + m/128) 2^(E-127)
+// with Fmax = 1.75 * 2^emax, ceil(log2(amax/Fmax)) = E - 127 - emax + [m > 96];
+// a subnormal amax always clamps to e = 0.  Each element is then multiplied
+// by 2^(127 - e) in fp32 (exact: BF16 has 8 significant bits, the factor is a
+// power of two and subnormals are kept) and converted with
+// cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32.
+//
+// Tile pipeline (per CTA, persistent over a static round-robin tile list):
+//   - thread 0 keeps STAGES tiles in flight: two 64-column TMA boxes per
+//     128x128 tile, 128B-swizzled, completion on one mbarrier per stage;
+//   - phase 1 (all 8 warps): column amax of the four 32-row blocks, read as
+//     conflict-free 8-byte shared loads; writes scale_col and the fp32 column
+//     multipliers (and dbias partial sums) to shared memory;
+//   - phase 2 (all 8 warps): each thread takes 16 consecutive columns of one
+//     row (two 16-byte shared loads), does the rowwise amax with one shuffle,
+//     converts the 16 values twice (row multiplier, 16 column multipliers)
+//     and writes two 16-byte global stores.
+// Every wait on an mbarrier is bounded; on expiry the CTA records a fault,
+// drains its own copies (again bounded) and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace mxfp8 {
+
+constexpr int kBM = 128;                      // tile rows
+constexpr int kBN = 128;                      // tile columns
+constexpr int kBoxCols = 64;                  // TMA box width (128 bytes of BF16)
+constexpr int kBoxBytes = kBM * kBoxCols * 2; // 16 KiB
+constexpr int kStageBytes = 2 * kBoxBytes;    // 32 KiB
+constexpr int kStages = 3;
+constexpr int kThreads = 256;
+constexpr int kMaxGroups = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
+
+// Shared-memory layout (bytes from a 1024-aligned base).
+constexpr int kOffColMul = kStages * kStageBytes;      // float [4][128]
+constexpr int kOffDSum = kOffColMul + 4 * kBN * 4;     // float [4][128]
+constexpr int kOffBars = kOffDSum + 4 * kBN * 4;       // uint64 [kStages]
+constexpr int kOffScan = kOffBars + 8 * kStages;       // int [kThreads / 32]
+constexpr int kOffGOff = kOffScan + 4 * (kThreads / 32);   // int64 [kMaxGroups + 1]
+constexpr int kOffGPre = kOffGOff + 8 * (kMaxGroups + 1);  // int [kMaxGroups + 1]
+constexpr int kSmemFlat = kOffGOff + 1024;                 // + alignment slack
+constexpr int kSmemGrouped = kOffGPre + 4 * (kMaxGroups + 1) + 1024;
+
+struct QuantParams {
+    uint8_t *out_row;
+    uint8_t *scale_row;
+    uint8_t *out_col;
+    uint8_t *scale_col;
+    float *ws;               // dbias partials [row_tiles][N], or nullptr
+    const float *noop;       // device scalar or nullptr
+    const int64_t *offsets;  // grouped: [num_groups + 1]
+    int *err_flag;           // grouped: device flag or nullptr
+    int64_t M;               // rows (total rows when grouped)
+    int64_t N;
+    int num_groups;
+    int col_tiles;
+    int row_tiles;           // flat only
+};
+
+// Library-wide device fault word (bit 0: a bounded wait expired).
+__device__ unsigned int g_fault_word;
+
+template <int FMT>
+__device__ __forceinline__ int block_exponent(uint32_t amax_bits)
+{
+    constexpr int kEmax = FMT == 0 ? 8 : 15;
+    int e = static_cast<int>(amax_bits >> 7) - kEmax + ((amax_bits & 0x7Fu) > 0x60u ? 1 : 0);
+    e = e < 0 ? 0 : e;
+    return amax_bits == 0 ? 127 : e;
+}
+
+// 2^(127 - e) as fp32, for 0 <= e <= 253.
+__device__ __forceinline__ float scale_multiplier(int e)
+{
+    return __uint_as_float(static_cast<uint32_t>(254 - e) << 23);
+}
+
+struct TileCoord {
+    int64_t row0;     // first row of the tile
+    int64_t row_end;  // one past the last row that belongs to the tile
+    int col0;
+    int rt;           // flat row-tile index (dbias partial row)
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, const int64_t *goff,
+                                                const int *gpre)
+{
+    TileCoord c;
+    if constexpr (GROUPED) {
+        int lo = 0, hi = p.num_groups;  // gpre[lo] <= t < gpre[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (gpre[mid] <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int local = t - gpre[lo];
+        const int rtl = local / p.col_tiles;
+        const int ct = local - rtl * p.col_tiles;
+        c.row0 = goff[lo] + static_cast<int64_t>(rtl) * kBM;
+        c.row_end = min(c.row0 + kBM, goff[lo + 1]);
+        c.col0 = ct * kBN;
+        c.rt = 0;
+    } else {
+        const int rt = t / p.col_tiles;
+        const int ct = t - rt * p.col_tiles;
+        c.row0 = static_cast<int64_t>(rt) * kBM;
+        c.row_end = min(c.row0 + kBM, p.M);
+        c.col0 = ct * kBN;
+        c.rt = rt;
+    }
+    return c;
+}
+
+// Grouped set-up: load and check the offsets, build the per-group tile
+// prefix in shared memory.  Returns the tile count, or -1 for bad offsets.
+__device__ __forceinline__ int grouped_setup(const QuantParams &p, int64_t *goff, int *gpre, int *scan)
+{
+    const int tid = threadIdx.x;
+    const int G = p.num_groups;
+    for (int g = tid; g <= G; g += kThreads)
+        goff[g] = p.offsets[g];
+    __syncthreads();
+    int bad = 0;
+    for (int g = tid; g < G; g += kThreads) {
+        const int64_t a = goff[g], b = goff[g + 1];
+        if (b < a || (b & 31))
+            bad = 1;
+    }
+    if (tid == 0 && (goff[0] != 0 || goff[G] != p.M))
+        bad = 1;
+    if (__syncthreads_or(bad))
+        return -1;
+
+    // tiles of group g = ceil(rows_g / 128) * col_tiles; exclusive scan over g.
+    // Thread t owns groups 2t and 2t+1 (kMaxGroups == 2 * kThreads).
+    int c[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int g = 2 * tid + k;
+        c[k] = 0;
+        if (g < G) {
+            const int64_t rows = goff[g + 1] - goff[g];
+            c[k] = static_cast<int>((rows + kBM - 1) / kBM) * p.col_tiles;
+        }
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = c[0] + c[1];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d)
+            incl += v;
+    }
+    if (lane == 31)
+        scan[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w)
+        base += scan[w];
+    const int excl = base + incl - (c[0] + c[1]);
+    if (2 * tid < G)
+        gpre[2 * tid] = excl;
+    if (2 * tid + 1 < G)
+        gpre[2 * tid + 1] = excl + c[0];
+    int total = 0;
+    for (int w = 0; w < kThreads / 32; ++w)
+        total += scan[w];
+    if (tid == 0)
+        gpre[G] = total;
+    __syncthreads();
+    return total;
+}
+
+template <int FMT, bool DBIAS, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *colmul = reinterpret_cast<float *>(smem + kOffColMul);
+    float *dsum = reinterpret_cast<float *>(smem + kOffDSum);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+    int *scan = reinterpret_cast<int *>(smem + kOffScan);
+    int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
+    int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
+
+    if (p.noop != nullptr && *p.noop == 1.0f)
+        return;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t N = p.N;
+
+    int num_tiles;
+    if constexpr (GROUPED) {
+        num_tiles = grouped_setup(p, goff, gpre, scan);
+        if (num_tiles < 0) {
+            if (blockIdx.x == 0 && tid == 0 && p.err_flag != nullptr)
+                atomicOr(p.err_flag, 1);
+            return;
+        }
+    } else {
+        num_tiles = p.row_tiles * p.col_tiles;
+    }
+    const int first = blockIdx.x, stride = gridDim.x;
+    const int my_count = first < num_tiles ? (num_tiles - 1 - first) / stride + 1 : 0;
+    if (my_count == 0)
+        return;
+
+    const bool do_row = p.out_row != nullptr;
+    const bool do_col = p.out_col != nullptr;
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmap);
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(smem_u32(&bars[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int slot, int t) {
+        const TileCoord c = tile_coord<GROUPED>(t, p, goff, gpre);
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t dst = smem_u32(smem + slot * kStageBytes);
+        const bool second = c.col0 + kBoxCols < N;  // skip a box that lies wholly past column N
+        mbar_arrive_expect_tx(bar, second ? kStageBytes : kBoxBytes);
+        tma_load_2d(dst, &tmap, bar, c.col0, static_cast<int32_t>(c.row0));
+        if (second)
+            tma_load_2d(dst + kBoxBytes, &tmap, bar, c.col0 + kBoxCols, static_cast<int32_t>(c.row0));
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages && s < my_count; ++s)
+            issue(s, first + s * stride);
+    }
+
+    for (int it = 0; it < my_count; ++it) {
+        const int slot = it % kStages;
+        const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
+        const TileCoord tc = tile_coord<GROUPED>(first + it * stride, p, goff, gpre);
+        const unsigned char *stage = smem + slot * kStageBytes;
+
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
+
+        // ---- phase 1: column blocks (rb = 32-row block, box = 64-column half) ----
+        if (ok && (do_col || DBIAS)) {
+            const int rb = warp >> 1, box = warp & 1;
+            const int cq = lane & 15, half = lane >> 4;   // 4-column group, 16-row half
+            const unsigned char *base = stage + box * kBoxBytes + (rb * 32 + half * 16) * 128 + (cq & 1) * 8;
+            uint32_t mx0 = 0, mx1 = 0;
+            float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                // row r = rb*32 + half*16 + i has (r & 7) == (i & 7): 128B swizzle
+                const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
+                mx0 = max_u16x2(mx0, v.x & 0x7FFF7FFFu);
+                mx1 = max_u16x2(mx1, v.y & 0x7FFF7FFFu);
+                if constexpr (DBIAS) {
+                    d0 += bf16_lo(v.x);
+                    d1 += bf16_hi(v.x);
+                    d2 += bf16_lo(v.y);
+                    d3 += bf16_hi(v.y);
+                }
+            }
+            mx0 = max_u16x2(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+            mx1 = max_u16x2(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+            if constexpr (DBIAS) {
+                // 32-row column sums; a + b == b + a, so both halves agree bit for bit
+                d0 += __shfl_xor_sync(0xffffffffu, d0, 16);
+                d1 += __shfl_xor_sync(0xffffffffu, d1, 16);
+                d2 += __shfl_xor_sync(0xffffffffu, d2, 16);
+                d3 += __shfl_xor_sync(0xffffffffu, d3, 16);
+            }
+            const int e0 = block_exponent<FMT>(mx0 & 0xFFFFu), e1 = block_exponent<FMT>(mx0 >> 16);
+            const int e2 = block_exponent<FMT>(mx1 & 0xFFFFu), e3 = block_exponent<FMT>(mx1 >> 16);
+            const int64_t gcol = tc.col0 + box * kBoxCols + cq * 4;
+            const int64_t grow = tc.row0 + rb * 32;
+            if (half == 0) {
+                if (do_col && gcol < N && grow < tc.row_end)
+                    *reinterpret_cast<uint32_t *>(p.scale_col + (grow >> 5) * N + gcol) =
+                        static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
+                        (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
+                if constexpr (DBIAS)
+                    *reinterpret_cast<float4 *>(dsum + rb * kBN + box * kBoxCols + cq * 4) =
+                        make_float4(d0, d1, d2, d3);
+            } else {
+                // column multipliers for phase 2: 4-column group q of segment sp is
+                // stored at chunk 4*sp + ((q + (sp >> 1)) & 3) (bank-conflict free reads)
+                const int sp = cq >> 2, q = cq & 3;
+                const int chunk = 4 * sp + ((q + (sp >> 1)) & 3);
+                *reinterpret_cast<float4 *>(colmul + rb * kBN + box * kBoxCols + chunk * 4) =
+                    make_float4(scale_multiplier(e0), scale_multiplier(e1), scale_multiplier(e2),
+                                scale_multiplier(e3));
+            }
+        }
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_fault_word, 1u);
+                if (GROUPED && p.err_flag != nullptr)
+                    atomicOr(p.err_flag, 2);
+                for (int j = it; j < my_count && j < it + kStages; ++j)
+                    mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
+                                      kDrainLimitNs);
+            }
+            return;
+        }
+
+        // dbias partial of this tile: the four 32-row block sums, in a fixed order
+        if constexpr (DBIAS) {
+            if (tid < kBN) {
+                const int64_t gcol = tc.col0 + tid;
+                if (gcol < N)
+                    p.ws[static_cast<int64_t>(tc.rt) * N + gcol] =
+                        ((dsum[tid] + dsum[kBN + tid]) + dsum[2 * kBN + tid]) + dsum[3 * kBN + tid];
+            }
+        }
+
+        // ---- phase 2: row segments of 16 columns ----
+        {
+            const int rr = lane >> 2, sp = lane & 3;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int task = warp + 8 * k;
+                const int box = task & 1, rg = task >> 1;
+                const int r = rg * 8 + rr;  // (r & 7) == rr
+                const unsigned char *rowp = stage + box * kBoxBytes + r * 128;
+                const int p0 = (2 * sp) ^ rr;
+                const uint4 A = lds128(rowp + p0 * 16);        // columns 16sp + 0..7
+                const uint4 B = lds128(rowp + (p0 ^ 1) * 16);  // columns 16sp + 8..15
+                const uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+                const int64_t grow = tc.row0 + r;
+                const int64_t gcol = tc.col0 + box * kBoxCols + sp * 16;
+                const bool in = grow < tc.row_end && gcol < N;
+                if (do_row) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
+                    uint32_t a = max(m & 0xFFFFu, m >> 16);
+                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                    const int er = block_exponent<FMT>(a);
+                    const float rm = scale_multiplier(er);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t lo = cvt_fp8x2<FMT>(bf16_lo(w[2 * j]) * rm, bf16_hi(w[2 * j]) * rm);
+                        const uint32_t hi =
+                            cvt_fp8x2<FMT>(bf16_lo(w[2 * j + 1]) * rm, bf16_hi(w[2 * j + 1]) * rm);
+                        o[j] = lo | (hi << 16);
+                    }
+                    if (in) {
+                        stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        if ((sp & 1) == 0)
+                            p.scale_row[grow * (N >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                    }
+                }
+                if (do_col) {
+                    const float *cm = colmul + (r >> 5) * kBN + box * kBoxCols + sp * 16;
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
+                        const uint32_t lo = cvt_fp8x2<FMT>(bf16_lo(w[2 * j]) * c.x, bf16_hi(w[2 * j]) * c.y);
+                        const uint32_t hi =
+                            cvt_fp8x2<FMT>(bf16_lo(w[2 * j + 1]) * c.z, bf16_hi(w[2 * j + 1]) * c.w);
+                        o[j] = lo | (hi << 16);
+                    }
+                    if (in)
+                        stg128(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                }
+            }
+        }
+        __syncthreads();  // stage `slot` and colmul are free again
+
+        if (tid == 0 && it + kStages < my_count) {
+            fence_proxy_async_smem();
+            issue(slot, first + (it + kStages) * stride);
+        }
+    }
+}
+
+}  // namespace mxfp8

@@ -18,3 +18,12 @@ def oracle_mod():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The built CUDA library (built in-tree with nvcc if missing or stale)."""
+    from mxfp8_block_scaled_04_gb300 import build, binding
+
+    build.build()
+    return binding.lib()

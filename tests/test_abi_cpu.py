@@ -1,0 +1,97 @@
+"""Host-side checks of the C ABI; no GPU needed (no compute calls are made).
+
+Every rejection below is decided on the host before the library touches the
+device, so these run on a machine without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp8_block_scaled_04_gb300 as mx
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mxfp8.h")
+
+OK, NULL, SHAPE, ALIGN, FORMAT, WORKSPACE, DEVICE, LAUNCH, GROUPS = range(9)
+A = 1 << 20     # a fake, 16-byte aligned address: never dereferenced by these calls
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(mxfp8_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mxfp8_quantize", "mxfp8_quantize_grouped", "mxfp8_quantize_workspace_bytes",
+              "mxfp8_quantize_grouped_workspace_bytes", "mxfp8_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    for name in declared_functions():
+        assert hasattr(cuda_lib, name), name
+        assert ctypes.cast(getattr(cuda_lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(cuda_lib):
+    for s in range(9):
+        assert mx.mxfp8_status_string(s)
+    assert mx.mxfp8_status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(cuda_lib):
+    assert mx.mxfp8_quantize_workspace_bytes(16384, 8192, False) == 0
+    assert mx.mxfp8_quantize_workspace_bytes(16384, 8192, True) == 128 * 8192 * 4
+    assert mx.mxfp8_quantize_workspace_bytes(96, 64, True) == 1 * 64 * 4
+    assert mx.mxfp8_quantize_workspace_bytes(160, 64, True) == 2 * 64 * 4
+    assert mx.mxfp8_quantize_workspace_bytes(100, 64, True) == 0          # invalid shape
+    assert mx.mxfp8_quantize_grouped_workspace_bytes(65536, 7168, 64) == 0
+
+
+def q(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, ws=None, noop=None):
+    return mx.mxfp8_quantize(x, M, N, fmt, orow, srow, ocol, scol, dbias, ws, noop, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=2), FORMAT), (dict(fmt=-1), FORMAT),
+    (dict(M=48), SHAPE), (dict(N=100), SHAPE), (dict(M=-32), SHAPE), (dict(N=1 << 31), SHAPE),
+    (dict(x=None), NULL), (dict(orow=None), NULL), (dict(scol=None), NULL),
+    (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
+    (dict(x=A + 8), ALIGN), (dict(orow=A + 4), ALIGN), (dict(ocol=A + 8), ALIGN), (dict(scol=A + 2), ALIGN),
+    (dict(dbias=A + 2, ws=A), ALIGN), (dict(dbias=A, ws=A + 4), ALIGN),
+    (dict(dbias=A), WORKSPACE),
+])
+def test_quantize_rejections(cuda_lib, kw, status):
+    assert q(**kw) == status
+
+
+def test_scale_row_needs_no_alignment_and_unaligned_pair_checks_pass_host_stage(cuda_lib):
+    # scale_row is written byte by byte: any address passes the host checks, so
+    # the call proceeds to the device stage, which fails without a usable GPU
+    # (or with a fake pointer) and reports MXFP8_ERR_DEVICE.
+    assert q(srow=A + 1) == DEVICE
+
+
+def g(x=A, total=128, N=64, G=2, off=A, fmt=0, orow=A, srow=A, ocol=A, scol=A, err=None):
+    return mx.mxfp8_quantize_grouped(x, total, N, G, off, fmt, orow, srow, ocol, scol, None, None, err, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=48), SHAPE),
+    (dict(G=0), GROUPS), (dict(G=mx.MAX_GROUPS + 1), GROUPS), (dict(off=None), GROUPS),
+    (dict(x=None), NULL), (dict(orow=None), NULL), (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
+    (dict(x=A + 2), ALIGN), (dict(off=A + 4), ALIGN), (dict(err=A + 2), ALIGN),
+])
+def test_grouped_rejections(cuda_lib, kw, status):
+    assert g(**kw) == status
+
+
+def test_binding_wrappers_reject_bad_tensors(cuda_lib):
+    import torch
+    with pytest.raises(ValueError):
+        mx.quantize(torch.zeros(64, 64, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        mx.quantize(torch.zeros(64, 64, dtype=torch.bfloat16).t())

@@ -1,0 +1,335 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+FP8 and E8M0 bytes must be bit-exact.  dbias must satisfy
+|gpu - oracle| <= 1e-5 * sum_i |x[i, j]| per column (fp32 partial sums over
+at most 32 rows, combined over 4 blocks and then summed in fp64: the fp32
+part contributes at most ~37 ulps of sum|x|, about 2.2e-6 relative).
+
+Small and medium shapes are compared element by element.  The full-size
+workloads (8192x28672, 16384x8192, 65536x7168 grouped) are compared on
+sampled 32-row stripes and 32-column slices, which the oracle computes on
+their own (a stripe of 32 rows holds complete rowwise and columnwise blocks).
+Every output sits between 4 KiB canary bands that must stay untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_block_scaled_04_gb300 as mx
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+E4M3, E5M2 = 0, 1
+GUARD = 4096
+CANARY = 0xA5
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+class Guarded:
+    """A device buffer with canary bands on both sides."""
+
+    def __init__(self, shape, dtype=torch.uint8, fill=CANARY):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        self.raw = torch.full((n + 2 * GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+        self.raw[GUARD:GUARD + n].fill_(fill)
+        self.t = self.raw[GUARD:GUARD + n].view(dtype).view(shape)
+
+    def guards_intact(self):
+        return bool((self.raw[:GUARD] == CANARY).all() and (self.raw[-GUARD:] == CANARY).all())
+
+
+def run_quantize(x_bits, fmt, rowwise=True, colwise=True, with_dbias=False, noop=None, prefill=CANARY):
+    M, N = x_bits.shape
+    x = dev_bf16(x_bits)
+    bufs = dict(
+        out_row=Guarded((M, N), fill=prefill) if rowwise else None,
+        scale_row=Guarded((M, N // 32), fill=prefill) if rowwise else None,
+        out_col=Guarded((M, N), fill=prefill) if colwise else None,
+        scale_col=Guarded((M // 32, N), fill=prefill) if colwise else None,
+        dbias=Guarded((N,), torch.float32, fill=prefill) if with_dbias else None,
+    )
+    ws = None
+    if with_dbias:
+        ws = torch.empty(max(mx.mxfp8_quantize_workspace_bytes(M, N, True), 16), dtype=torch.uint8, device="cuda")
+    t = {k: (v.t if v is not None else None) for k, v in bufs.items()}
+    before = mx.mxfp8_kernel_launch_count()
+    st = mx.mxfp8_quantize(x, M, N, fmt, t["out_row"], t["scale_row"], t["out_col"], t["scale_col"],
+                           t["dbias"], ws, noop, None)
+    assert st == 0, mx.mxfp8_status_string(st)
+    torch.cuda.synchronize()
+    if M > 0 and N > 0:
+        assert mx.mxfp8_kernel_launch_count() > before     # the CUDA kernel really ran
+    for k, v in bufs.items():
+        if v is not None:
+            assert v.guards_intact(), f"{k}: canary band overwritten"
+    host = {k: (v.t.cpu().numpy() if v is not None else None) for k, v in bufs.items()}
+    return host
+
+
+def assert_bytes_equal(got, want, name):
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{name}: {len(bad)} mismatches; first at {i}: gpu {got[i]:#04x} oracle {want[i]:#04x}")
+
+
+def check_against_oracle(oracle_mod, x_bits, fmt, host, rowwise=True, colwise=True):
+    o_row, s_row, o_col, s_col, _ = oracle_mod.quantize(x_bits, fmt, rowwise, colwise)
+    if rowwise:
+        assert_bytes_equal(host["scale_row"], s_row, "scale_row")
+        assert_bytes_equal(host["out_row"], o_row, "out_row")
+    if colwise:
+        assert_bytes_equal(host["scale_col"], s_col, "scale_col")
+        assert_bytes_equal(host["out_col"], o_col, "out_col")
+
+
+def dbias_tolerance(x_bits):
+    xv = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double()
+    return 1e-5 * xv.abs().sum(dim=0).numpy()
+
+
+def mixed_input(M, N, seed):
+    """N(0,1) with per-row exponent spread, zeros, subnormals, outliers, powers of two."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal((M, N)) * np.exp2(rng.integers(-20, 20, (M, 1)))
+    flat = a.reshape(-1)
+    n = flat.size
+    flat[rng.integers(0, n, n // 50)] = rng.standard_normal(n // 50) * 1e-39
+    flat[rng.integers(0, n, n // 100)] = np.exp2(rng.integers(-30, 30, n // 100)) * rng.choice([-1, 1], n // 100)
+    flat[rng.integers(0, n, n // 200)] = 0.0
+    flat[rng.integers(0, n, n // 500)] = -0.0
+    a[:32, :32] = 0.0
+    if M >= 64 and N >= 64:
+        a[32:64, 32:64] = rng.standard_normal((32, 32)) * 1e-39
+    return wl.to_bf16_bits(a)
+
+
+SHAPES = [(32, 32), (64, 96), (96, 160), (160, 96), (128, 256), (256, 384), (384, 224),
+          (128, 8192), (544, 1056), (1024, 64)]
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_parity_shapes(oracle_mod, shape, fmt):
+    M, N = shape
+    x = mixed_input(M, N, seed=M * 7 + N + fmt)
+    host = run_quantize(x, fmt)
+    check_against_oracle(oracle_mod, x, fmt, host)
+
+
+def test_parity_small_workload(oracle_mod):
+    w = wl.make("small_128x256")
+    host = run_quantize(w["x"], w["fmt"])
+    check_against_oracle(oracle_mod, w["x"], w["fmt"], host)
+
+
+@pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
+def test_parity_single_direction(oracle_mod, rowwise, colwise):
+    x = mixed_input(160, 288, seed=11)
+    host = run_quantize(x, E4M3, rowwise=rowwise, colwise=colwise)
+    check_against_oracle(oracle_mod, x, E4M3, host, rowwise, colwise)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", [(32, 32), (96, 160), (384, 224), (1056, 288)])
+def test_parity_dbias(oracle_mod, shape, fmt):
+    M, N = shape
+    x = mixed_input(M, N, seed=3 * M + N)
+    host = run_quantize(x, fmt, with_dbias=True)
+    check_against_oracle(oracle_mod, x, fmt, host)
+    want = oracle_mod.quantize(x, fmt, False, False, with_dbias=True)[4]
+    assert np.all(np.abs(host["dbias"].astype(np.float64) - want) <= dbias_tolerance(x))
+
+
+def test_dbias_exact_columns(oracle_mod):
+    rng = np.random.Generator(np.random.PCG64(9))
+    M, N = 512, 64
+    a = rng.integers(-64, 64, (M, N)).astype(np.float64)      # sums are exact in fp32
+    a[:, 1] = np.exp2(rng.integers(-8, 8, M))
+    x = wl.to_bf16_bits(a)
+    host = run_quantize(x, E5M2, with_dbias=True)
+    want = oracle_mod.quantize(x, E5M2, False, False, with_dbias=True)[4]
+    assert np.array_equal(host["dbias"], want)
+
+
+@pytest.mark.parametrize("with_dbias", [False, True])
+def test_noop_flag(oracle_mod, with_dbias):
+    x = mixed_input(256, 384, seed=5)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    zero = torch.zeros(1, dtype=torch.float32, device="cuda")
+    host = run_quantize(x, E5M2, with_dbias=with_dbias, noop=one, prefill=0x3C)
+    for k, v in host.items():
+        if v is not None:
+            assert np.all(v.view(np.uint8) == 0x3C), f"{k} written despite noop"
+    host = run_quantize(x, E5M2, with_dbias=with_dbias, noop=zero, prefill=0x3C)
+    check_against_oracle(oracle_mod, x, E5M2, host)
+
+
+def test_empty_rows_dbias_zero():
+    x = np.zeros((0, 64), np.uint16)
+    host = run_quantize(x, E4M3, with_dbias=True, prefill=0x3C)
+    assert np.all(host["dbias"] == 0.0)
+
+
+# ---- grouped -------------------------------------------------------------------
+
+def run_grouped(x_bits, offsets, fmt, noop=None, prefill=CANARY):
+    total, N = x_bits.shape
+    x = dev_bf16(x_bits)
+    off = torch.from_numpy(np.asarray(offsets, np.int64)).cuda()
+    bufs = dict(out_row=Guarded((total, N), fill=prefill), scale_row=Guarded((total, N // 32), fill=prefill),
+                out_col=Guarded((total, N), fill=prefill), scale_col=Guarded((total // 32, N), fill=prefill))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = mx.mxfp8_quantize_grouped(x, total, N, off.numel() - 1, off, fmt, bufs["out_row"].t,
+                                   bufs["scale_row"].t, bufs["out_col"].t, bufs["scale_col"].t,
+                                   None, noop, err, None)
+    assert st == 0, mx.mxfp8_status_string(st)
+    torch.cuda.synchronize()
+    for k, v in bufs.items():
+        assert v.guards_intact(), k
+    return {k: v.t.cpu().numpy() for k, v in bufs.items()}, int(err.item())
+
+
+@pytest.mark.parametrize("N", [96, 160, 512])
+def test_parity_grouped(oracle_mod, N):
+    sizes = np.array([64, 0, 32, 416, 0, 0, 128, 96, 160, 32], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    x = wl.moe_bf16(sizes, N, seed=N)
+    host, err = run_grouped(x, off, E4M3)
+    assert err == 0
+    o = oracle_mod.quantize_grouped(x, off, E4M3)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"),
+                          (host["out_row"], host["scale_row"], host["out_col"], host["scale_col"]), o):
+        assert_bytes_equal(g, w, name)
+
+
+@pytest.mark.parametrize("offsets,valid", [
+    ([0, 16, 928], False),          # 16 is not a multiple of 32
+    ([0, 512, 256, 928], False),    # decreasing
+    ([0, 512, 896], False),         # last entry != total rows
+    ([32, 928], False),             # first entry != 0
+    ([0, 480, 928], True),          # valid: 480 and 448 rows
+])
+def test_grouped_offsets_validation(offsets, valid):
+    x = wl.normal_bf16(928, 96, seed=1)
+    host, err = run_grouped(x, offsets, E4M3, prefill=0x3C)
+    if valid:
+        assert err == 0
+        return
+    assert err == 1
+    for k, v in host.items():
+        assert np.all(v == 0x3C), f"{k} written despite invalid offsets"
+
+
+def test_grouped_noop():
+    sizes = np.array([64, 96], np.int64)
+    x = wl.moe_bf16(sizes, 128, seed=2)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    host, err = run_grouped(x, wl.offsets_from_sizes(sizes), E4M3, noop=one, prefill=0x3C)
+    assert err == 0
+    for k, v in host.items():
+        assert np.all(v == 0x3C), k
+
+
+def test_no_device_fault_recorded():
+    assert mx.mxfp8_device_fault_word() == 0
+
+
+# ---- full-size workloads: full compare (4096^2) and sampled stripes -------------
+
+def test_parity_act_4096_full(oracle_mod):
+    w = wl.make("act_4096x4096")
+    host = run_quantize(w["x"], w["fmt"])
+    check_against_oracle(oracle_mod, w["x"], w["fmt"], host)
+
+
+def stripes_to_check(M, rng, must=()):
+    n = M // 32
+    picks = {0, n - 1, *must}
+    picks |= set(rng.integers(0, n, 6).tolist())
+    return sorted(p for p in picks if 0 <= p < n)
+
+
+def check_stripes(oracle_mod, x_bits, fmt, out, stripes):
+    N = x_bits.shape[1]
+    for s in stripes:
+        r0 = 32 * s
+        xs = np.ascontiguousarray(x_bits[r0:r0 + 32])
+        o_row, s_row, o_col, s_col, _ = oracle_mod.quantize(xs, fmt)
+        assert_bytes_equal(out["out_row"][r0:r0 + 32].cpu().numpy(), o_row, f"out_row stripe {s}")
+        assert_bytes_equal(out["scale_row"][r0:r0 + 32].cpu().numpy(), s_row, f"scale_row stripe {s}")
+        assert_bytes_equal(out["out_col"][r0:r0 + 32].cpu().numpy(), o_col, f"out_col stripe {s}")
+        assert_bytes_equal(out["scale_col"][s:s + 1].cpu().numpy(), s_col, f"scale_col stripe {s}")
+    assert N % 32 == 0
+
+
+def quantize_device(x_bits, fmt, with_dbias=False, noop=None):
+    x = dev_bf16(x_bits)
+    return x, mx.quantize(x, fmt, with_dbias=with_dbias, noop=noop)
+
+
+def test_parity_fc1_8192x28672_sampled(oracle_mod):
+    w = wl.make("fc1_8192x28672")
+    x, r = quantize_device(w["x"], w["fmt"])
+    torch.cuda.synchronize()
+    out = r._asdict()
+    rng = np.random.Generator(np.random.PCG64(21))
+    check_stripes(oracle_mod, w["x"], w["fmt"], out, stripes_to_check(w["M"], rng))
+    # every scale byte is a valid finite-input exponent
+    assert int(r.scale_row.max()) <= 254 and int(r.scale_col.max()) <= 254
+    del x, r
+    torch.cuda.empty_cache()
+
+
+def test_parity_grad_16384x8192_sampled_with_dbias(oracle_mod):
+    w = wl.make("grad_16384x8192")
+    x_bits, fmt = w["x"], w["fmt"]
+    M, N = x_bits.shape
+    x, r = quantize_device(x_bits, fmt, with_dbias=True)
+    torch.cuda.synchronize()
+    rng = np.random.Generator(np.random.PCG64(22))
+    check_stripes(oracle_mod, x_bits, fmt, r._asdict(), stripes_to_check(M, rng, must=(0, 1)))
+    # full columns: dbias and the columnwise bytes of sampled 32-column slices
+    dbias = r.dbias.cpu().numpy()
+    for j0 in sorted({0, 32, N - 32, *(32 * rng.integers(0, N // 32, 3)).tolist()}):
+        xs = np.ascontiguousarray(x_bits[:, j0:j0 + 32])
+        _, _, o_col, s_col, db = oracle_mod.quantize(xs, fmt, rowwise=False, colwise=True, with_dbias=True)
+        assert_bytes_equal(r.out_col[:, j0:j0 + 32].cpu().numpy(), o_col, f"out_col cols {j0}")
+        assert_bytes_equal(r.scale_col[:, j0:j0 + 32].cpu().numpy(), s_col, f"scale_col cols {j0}")
+        tol = dbias_tolerance(xs)
+        assert np.all(np.abs(dbias[j0:j0 + 32].astype(np.float64) - db) <= tol), j0
+    # noop = 1 at full size: nothing changes
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    before = [t.clone() for t in (r.out_row, r.scale_row, r.out_col, r.scale_col, r.dbias)]
+    ws = torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
+    xin = torch.zeros_like(x)
+    st = mx.mxfp8_quantize(xin, M, N, fmt, r.out_row, r.scale_row, r.out_col, r.scale_col, r.dbias, ws, one, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    for a, b in zip(before, (r.out_row, r.scale_row, r.out_col, r.scale_col, r.dbias)):
+        assert torch.equal(a, b)
+    del x, r, before, xin, ws
+    torch.cuda.empty_cache()
+
+
+def test_parity_moe_64x65536x7168_sampled(oracle_mod):
+    w = wl.make("moe_64x65536x7168")
+    x_bits, off = w["x"], w["offsets"]
+    x = dev_bf16(x_bits)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mx.quantize_grouped(x, torch.from_numpy(off).cuda(), w["fmt"], err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rng = np.random.Generator(np.random.PCG64(23))
+    edges = set()
+    for g in range(len(off) - 1):
+        if off[g + 1] > off[g]:
+            edges |= {off[g] // 32, off[g + 1] // 32 - 1}
+    must = sorted(edges)[:: max(1, len(edges) // 12)]
+    check_stripes(oracle_mod, x_bits, w["fmt"], r._asdict(), stripes_to_check(w["M"], rng, must=must))
+    del x, r
+    torch.cuda.empty_cache()
