@@ -47,11 +47,19 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="fc1_8192x28672")
+    ap.add_argument("--shape", default=None, help="MxN: the workload's value recipe at another shape")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
+
+
+def parse_shape(s):
+    if not s:
+        return None
+    m, n = s.lower().split("x")
+    return int(m), int(n)
 
 
 def dist_env():
@@ -234,8 +242,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    spec = wl.WORKLOADS[args.workload]
-    w = wl.make(args.workload)
+    w = wl.make(args.workload, shape=parse_shape(args.shape))
     x_bits, fmt, with_dbias, offsets = w["x"], w["fmt"], w["with_dbias"], w["offsets"]
     M, N = x_bits.shape
     grouped = offsets is not None
@@ -364,7 +371,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
+            "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "bytes_per_step": algo_bytes,
                        "l2": f"inputs larger than L2: {M * N * 2 / 1e6:.0f} MB bf16 read per step vs "

@@ -152,9 +152,14 @@ WORKLOADS = {
 }
 
 
-def make(name: str, seed: int | None = None):
-    """Return ``dict(x=uint16 bits [M,N], fmt, with_dbias, offsets or None)`` for a named workload."""
+def make(name: str, seed: int | None = None, shape: tuple[int, int] | None = None):
+    """Return ``dict(x=uint16 bits [M,N], fmt, with_dbias, offsets or None)`` for a named workload.
+
+    ``shape`` draws the same value recipe at another (M, N) (total rows for the grouped one).
+    """
     M, N, fmt, dbias, grouped, s0 = WORKLOADS[name]
+    if shape is not None:
+        M, N = shape
     seed = s0 if seed is None else seed
     offsets = None
     if name == "small_128x256":
