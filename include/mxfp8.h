@@ -156,6 +156,39 @@ uint64_t mxfp8_kernel_launch_count(void);
  */
 mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear);
 
+/* Size of the static scratch array used by mxfp8_quantize_dbias_noalloc. */
+#define MXFP8_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * mxfp8_quantize with dbias, for callers that cannot allocate device memory.
+ * (The pages have no counterpart to this call.)
+ *
+ * Some callers have no way to allocate: a plugin or callback that is handed
+ * only its input and output tensors, with no allocator or workspace to draw
+ * from, or code that must not allocate once it is running.  This call takes
+ * the same arguments as mxfp8_quantize minus the workspace, and keeps the
+ * dbias workspace in a file-scope device array of MXFP8_NOALLOC_SCRATCH_BYTES
+ * (8 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits.  It calls no cudaMalloc or cudaFree.
+ *
+ *   dbias      required (device fp32 [N]); NULL is MXFP8_ERR_NULL.
+ *   M, N       as for mxfp8_quantize; shapes whose workspace
+ *              (mxfp8_quantize_workspace_bytes(M, N, 1) = ceil(M/128)*N*4
+ *              bytes) exceeds 8 MiB are rejected with MXFP8_ERR_SHAPE, e.g.
+ *              16384 x 8192 fits (4 MiB), 32768 x 16384 does not.
+ *   others     as for mxfp8_quantize.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the one array, and each call writes every
+ * workspace entry it reads, so nothing carries over between calls; calls that
+ * overlap on the GPU (other streams, other host threads) race on the array.
+ */
+mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N, int fp8_fmt,
+                                            void *out_row, void *scale_row,
+                                            void *out_col, void *scale_col,
+                                            float *dbias, const float *noop, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

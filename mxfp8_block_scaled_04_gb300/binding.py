@@ -186,3 +186,19 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: 
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_grouped")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
+
+
+def mxfp8_quantize_dbias_noalloc(x, M, N, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                                 dbias, noop=None, stream=None) -> int:
+    """mxfp8_quantize with dbias and no workspace argument (for callers that cannot allocate).
+
+    The C entry point keeps the dbias workspace in an 8 MiB static device array;
+    see include/mxfp8.h for its limits and its sharing rule.
+    """
+    f = lib().mxfp8_quantize_dbias_noalloc
+    if f.argtypes is None:
+        vp = ctypes.c_void_p
+        f.restype = ctypes.c_int
+        f.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp]
+    return int(f(_addr(x), M, N, fp8_fmt, _addr(out_row), _addr(scale_row), _addr(out_col), _addr(scale_col),
+                 _addr(dbias), _addr(noop), _stream(stream)))

@@ -338,3 +338,60 @@ mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear)
 }
 
 }  // extern "C"
+
+// ---- dbias quantize without any allocation ------------------------------------
+//
+// For callers that cannot allocate device memory themselves: a plugin or callback
+// that is handed only its input and output tensors and has no allocator or
+// workspace to draw from, or code that must not allocate once it is running.
+// The dbias workspace such a caller cannot provide lives in this file-scope device
+// array instead: 8 MiB, held on every GPU that loads the library until the process
+// exits.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MXFP8_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+// Device address of g_noalloc_scratch per device (host code only holds a stand-in
+// for the symbol, so the address is looked up once per device with it current).
+void *g_noalloc_addr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+extern "C" {
+
+mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N, int fp8_fmt, void *out_row,
+                                            void *scale_row, void *out_col, void *scale_col, float *dbias,
+                                            const float *noop, void *stream)
+{
+    if (dbias == nullptr)
+        return MXFP8_ERR_NULL;
+    if (M < 0 || N < 0 || M % 32 || N % 32)
+        return MXFP8_ERR_SHAPE;
+    if (mxfp8_quantize_workspace_bytes(M, N, 1) > MXFP8_NOALLOC_SCRATCH_BYTES)
+        return MXFP8_ERR_SHAPE;  // needs more than the static scratch array holds
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        cudaGetLastError();
+        return MXFP8_ERR_DEVICE;
+    }
+    if (device < 0 || device >= kMaxDevices)
+        return MXFP8_ERR_DEVICE;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (g_noalloc_addr[device] == nullptr) {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+                cudaGetLastError();
+                return MXFP8_ERR_DEVICE;
+            }
+            g_noalloc_addr[device] = addr;
+        }
+        scratch = g_noalloc_addr[device];
+    }
+    // Every (row tile, column) entry of the workspace the call uses is written
+    // before it is read, so nothing needs clearing between calls.
+    return mxfp8_quantize(x, M, N, fp8_fmt, out_row, scale_row, out_col, scale_col, dbias, scratch, noop, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+"""mxfp8_quantize_dbias_noalloc: dbias quantize for callers that cannot allocate.
+
+Some callers have no way to allocate device memory (a plugin or callback that
+is handed only its input and output tensors, or code that must not allocate
+once it is running), so they cannot supply the dbias workspace.  This entry
+point keeps that workspace in a static 8 MiB device array inside the library.
+The test calls it through the C ABI twice in a row, on different inputs and
+shapes, and checks that every output matches the regular entry point given an
+explicit workspace: FP8 and scale bytes identical, dbias within
+1e-5 * sum|x| per column (the same tolerance as the other dbias tests).
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_block_scaled_04_gb300 as mx
+from mxfp8_block_scaled_04_gb300 import binding
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def outputs(M, N):
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    return [torch.full((M, N), 0x11, **u8), torch.full((M, N // 32), 0x11, **u8),
+            torch.full((M, N), 0x11, **u8), torch.full((M // 32, N), 0x11, **u8),
+            torch.full((N,), 7.0, dtype=torch.float32, device="cuda")]
+
+
+@pytest.mark.parametrize("fmt", [mx.E5M2, mx.E4M3])
+def test_noalloc_matches_workspace_entry_point_two_calls(fmt):
+    for call, (M, N) in enumerate([(1056, 288), (4096, 1024)]):
+        x_bits = wl.grad_bf16(M, N, seed=100 + call)
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        ref = outputs(M, N)
+        ws = torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
+        assert mx.mxfp8_quantize(x, M, N, fmt, *ref[:4], ref[4], ws, None, None) == 0
+        got = outputs(M, N)
+        assert binding.mxfp8_quantize_dbias_noalloc(x, M, N, fmt, *got[:4], got[4], None, None) == 0
+        torch.cuda.synchronize()
+        for name, a, b in zip(("out_row", "scale_row", "out_col", "scale_col"), ref[:4], got[:4]):
+            assert torch.equal(a, b), f"call {call}: {name} differs"
+        tol = 1e-5 * torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().abs().sum(0)
+        diff = (ref[4].double().cpu() - got[4].double().cpu()).abs()
+        assert bool((diff <= tol).all()), f"call {call}: dbias differs"
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # 32768 x 16384 needs 256 * 16384 * 4 = 16 MiB of workspace > 8 MiB; rejected
+    # on the host before any pointer is touched.
+    A = 1 << 20
+    st = binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, mx.E4M3, A, A, A, A, A, None, None)
+    assert st == 2      # MXFP8_ERR_SHAPE
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, mx.E4M3, A, A, A, A, None, None, None) == 1
