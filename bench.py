@@ -36,8 +36,9 @@ METRIC = "MXFP8 quantize effective GB/s and % of GB300 HBM peak (rowwise+colwise
 BYTES_PER_ELEM = 2 + 1 + 1 + 1 / 16
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["mxfp8_block_scaled_04_gb300/csrc/quantize.cuh", "mxfp8_block_scaled_04_gb300/csrc/ptx.cuh",
-                  "mxfp8_block_scaled_04_gb300/csrc/api.cu"]
+# Sources that define the dominant (quantize) kernel: a committed ncu traffic figure is only
+# reported while these are unchanged since it was taken.
+KERNEL_SOURCES = ["mxfp8_block_scaled_04_gb300/csrc/quantize.cuh", "mxfp8_block_scaled_04_gb300/csrc/ptx.cuh"]
 
 
 def parse_args():
@@ -279,6 +280,11 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
+    # Inputs that fit in L2 would be re-read from L2 on the next step:
+    # flush L2 (write a 256 MiB buffer) before every timed step and time only the steps.
+    flush = M * N * 2 <= L2_BYTES
+    flush_buf = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda") if flush else None
+
     def timed():
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -290,6 +296,8 @@ def run_ours(args):
         h0 = time.time()
         t_begin.record(stream)
         for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -298,8 +306,8 @@ def run_ours(args):
         h1 = time.time()
         barrier()
         launches = mx.mxfp8_kernel_launch_count() - launches0
-        total_ms = t_begin.elapsed_time(t_end)
         per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total_ms = sum(per_launch) if flush else t_begin.elapsed_time(t_end)
         return total_ms, per_launch, launches, h0, h1
 
     sampler = ClockSampler(uuid)
@@ -374,8 +382,10 @@ def run_ours(args):
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "bytes_per_step": algo_bytes,
-                       "l2": f"inputs larger than L2: {M * N * 2 / 1e6:.0f} MB bf16 read per step vs "
-                             f"{L2_BYTES / 2 ** 20:.0f} MiB L2, no flush",
+                       "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
+                              f"bf16 input; time = sum of the per-step event intervals" if flush else
+                              f"inputs larger than L2: {M * N * 2 / 1e6:.0f} MB bf16 read per step vs "
+                              f"{L2_BYTES / 2 ** 20:.0f} MiB L2, no flush"),
                        "parallelism": f"{world} independent replica(s)" if world > 1 else "single GPU"},
             "pct_of_8tbs": 100 * value / world / 8000.0,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/mxfp8.h"
+#include "dbias_reduce.cuh"
 #include "quantize.cuh"
 
 namespace {
@@ -110,21 +111,6 @@ mxfp8_status_t make_tensor_map(CUtensorMap *map, const void *x, int64_t rows, in
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXFP8_OK : MXFP8_ERR_LAUNCH;
-}
-
-// dbias[j] = sum over row tiles t (in order) of ws[t][j], accumulated in fp64.
-__global__ void dbias_reduce_kernel(const float *__restrict__ ws, int64_t row_tiles, int64_t N,
-                                    float *__restrict__ dbias, const float *noop)
-{
-    if (noop != nullptr && *noop == 1.0f)
-        return;
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (j >= N)
-        return;
-    double acc = 0.0;
-    for (int64_t t = 0; t < row_tiles; ++t)
-        acc += static_cast<double>(ws[t * N + j]);
-    dbias[j] = static_cast<float>(acc);
 }
 
 // Shared host-side checks of the direction pointers.
@@ -236,9 +222,8 @@ mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, 
             return st;
     }
     if (dbias != nullptr && N > 0) {
-        const int threads = 256;
-        const int64_t blocks = (N + threads - 1) / threads;
-        dbias_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        const int64_t blocks = (N + kReduceCols - 1) / kReduceCols;
+        dbias_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceCols * kReduceWarps, 0, stream>>>(
             static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (cudaGetLastError() != cudaSuccess)

@@ -55,7 +55,8 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
 constexpr int kOffColMul = kStages * kStageBytes;      // float [4][128]
 constexpr int kOffDSum = kOffColMul + 4 * kBN * 4;     // float [4][128]
 constexpr int kOffBars = kOffDSum + 4 * kBN * 4;       // uint64 [kStages]
-constexpr int kOffScan = kOffBars + 8 * kStages;       // int [kThreads / 32]
+constexpr int kOffCoord = kOffBars + 8 * kStages;      // TileCoord [kStages]
+constexpr int kOffScan = kOffCoord + 32 * kStages;     // int [kThreads / 32]
 constexpr int kOffGOff = kOffScan + 4 * (kThreads / 32);   // int64 [kMaxGroups + 1]
 constexpr int kOffGPre = kOffGOff + 8 * (kMaxGroups + 1);  // int [kMaxGroups + 1]
 constexpr int kSmemFlat = kOffGOff + 1024;                 // + alignment slack
@@ -101,6 +102,7 @@ struct TileCoord {
     int col0;
     int rt;           // flat row-tile index (dbias partial row)
 };
+static_assert(sizeof(TileCoord) <= 32, "coordinate slot");
 
 template <bool GROUPED>
 __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, const int64_t *goff,
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *colmul = reinterpret_cast<float *>(smem + kOffColMul);
     float *dsum = reinterpret_cast<float *>(smem + kOffDSum);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+    TileCoord *coords = reinterpret_cast<TileCoord *>(smem + kOffCoord);
     int *scan = reinterpret_cast<int *>(smem + kOffScan);
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     auto issue = [&](int slot, int t) {
         const TileCoord c = tile_coord<GROUPED>(t, p, goff, gpre);
+        coords[slot] = c;  // published to the consumers by the arrive below
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * kStageBytes);
         const bool second = c.col0 + kBoxCols < N;  // skip a box that lies wholly past column N
@@ -261,13 +265,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int it = 0; it < my_count; ++it) {
         const int slot = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
-        const TileCoord tc = tile_coord<GROUPED>(first + it * stride, p, goff, gpre);
         const unsigned char *stage = smem + slot * kStageBytes;
 
         const bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
+        const TileCoord tc = coords[slot];
 
         // ---- phase 1: column blocks (rb = 32-row block, box = 64-column half) ----
-        if (ok && (do_col || DBIAS)) {
+        const bool rb_live = tc.row0 + (warp >> 1) * 32 < tc.row_end;  // this warp's 32-row block exists
+        if (ok && (do_col || DBIAS) && !rb_live) {
+            if constexpr (DBIAS) {  // an absent row block adds nothing to the column sums
+                const int rb = warp >> 1, box = warp & 1;
+                if (lane < 16)
+                    *reinterpret_cast<float4 *>(dsum + rb * kBN + box * kBoxCols + lane * 4) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (ok && (do_col || DBIAS) && rb_live) {
             const int rb = warp >> 1, box = warp & 1;
             const int cq = lane & 15, half = lane >> 4;   // 4-column group, 16-row half
             const unsigned char *base = stage + box * kBoxBytes + (rb * 32 + half * 16) * 128 + (cq & 1) * 8;
@@ -346,6 +359,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int k = 0; k < 4; ++k) {
                 const int task = warp + 8 * k;
                 const int box = task & 1, rg = task >> 1;
+                if (tc.row0 + rg * 8 >= tc.row_end)
+                    continue;               // warp-uniform: the whole 8-row group is past the tile end
                 const int r = rg * 8 + rr;  // (r & 7) == rr
                 const unsigned char *rowp = stage + box * kBoxBytes + r * 128;
                 const int p0 = (2 * sp) ^ rr;
