@@ -142,6 +142,45 @@ mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t
                                       void *workspace, const float *noop, int *err_flag,
                                       void *stream);
 
+/*
+ * Device staging bytes mxfp8_quantize_host needs for (M, N, with_dbias):
+ * three chunk slots (input chunk plus its outputs) and, with dbias, the dbias
+ * workspace of the whole matrix and an fp32 [N] vector.  0 for invalid or
+ * empty shapes.
+ */
+size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias);
+
+/*
+ * The same quantize with x and every output in HOST memory: the call moves
+ * x to the device, quantizes it and moves the outputs back, pipelined over
+ * row chunks (at most about 32 MiB of BF16 each, smaller at both ends) so
+ * that the host-to-device copies,
+ * the kernels and the device-to-host copies overlap.  Results are identical
+ * to mxfp8_quantize on the same data (dbias included: the chunks write the
+ * per-tile partials of one workspace and one reduce follows).
+ *
+ *   x_host, out_*_host, dbias_host   host buffers in the layouts of
+ *               mxfp8_quantize; a direction is skipped as there.  Pinned
+ *               memory (cudaHostAlloc / cudaHostRegister) lets the copies
+ *               overlap; pageable memory works but serialises them.
+ *   M, N        multiples of 32, > 0.
+ *   staging     device buffer, 256-byte aligned, at least
+ *               mxfp8_quantize_host_staging_bytes(M, N, dbias_host != NULL)
+ *               bytes (otherwise MXFP8_ERR_WORKSPACE); owned by the caller.
+ *   stream      the kernels run on it; the copies run on two internal streams
+ *               that wait for `stream` first, and `stream` waits for the last
+ *               copy, so synchronising `stream` means every host output is
+ *               written.  The library creates those two streams and a few
+ *               events once per device, on the first call.
+ * No noop flag: a skipped quantize would still copy stale staging bytes out.
+ * Calls from several host threads are serialised while they enqueue.
+ */
+mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int fp8_fmt,
+                                   void *out_row_host, void *scale_row_host,
+                                   void *out_col_host, void *scale_col_host,
+                                   float *dbias_host, void *staging, size_t staging_bytes,
+                                   void *stream);
+
 /* Static, human-readable text for a status code. */
 const char *mxfp8_status_string(int status);
 

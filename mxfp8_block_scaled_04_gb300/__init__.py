@@ -9,6 +9,7 @@ ctypes binding.
 from .binding import (  # noqa: F401
     BLOCK, E4M3, E5M2, MAX_GROUPS, MXFP8Error, MXFP8Tensor, STATUS_NAMES,
     lib, mxfp8_device_fault_word, mxfp8_kernel_launch_count, mxfp8_quantize,
-    mxfp8_quantize_grouped, mxfp8_quantize_grouped_workspace_bytes,
+    mxfp8_quantize_grouped, mxfp8_quantize_grouped_workspace_bytes, mxfp8_quantize_host,
+    mxfp8_quantize_host_staging_bytes, mxfp8_quantize_dbias_noalloc, quantize_host,
     mxfp8_quantize_workspace_bytes, mxfp8_status_string, quantize, quantize_grouped,
 )

@@ -57,6 +57,10 @@ def lib():
             L.mxfp8_quantize_grouped_workspace_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_grouped.restype = i32
             L.mxfp8_quantize_grouped.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_host.restype = i32
+            L.mxfp8_quantize_host.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
             L.mxfp8_status_string.restype = ctypes.c_char_p
             L.mxfp8_status_string.argtypes = [i32]
             L.mxfp8_kernel_launch_count.restype = ctypes.c_uint64
@@ -106,6 +110,17 @@ def mxfp8_quantize_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, out_r
                                             _addr(out_row), _addr(scale_row), _addr(out_col),
                                             _addr(scale_col), _addr(workspace), _addr(noop),
                                             _addr(err_flag), _stream(stream)))
+
+
+def mxfp8_quantize_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
+    return int(lib().mxfp8_quantize_host_staging_bytes(M, N, int(bool(with_dbias))))
+
+
+def mxfp8_quantize_host(x_host, M, N, fp8_fmt, out_row_host, scale_row_host, out_col_host, scale_col_host,
+                        dbias_host, staging, staging_bytes, stream=None) -> int:
+    return int(lib().mxfp8_quantize_host(_addr(x_host), M, N, fp8_fmt, _addr(out_row_host), _addr(scale_row_host),
+                                         _addr(out_col_host), _addr(scale_col_host), _addr(dbias_host),
+                                         _addr(staging), int(staging_bytes), _stream(stream)))
 
 
 def mxfp8_status_string(status: int) -> str:
@@ -168,6 +183,33 @@ def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = Tr
                         workspace if with_dbias else None, noop, stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+
+
+def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
+                  with_dbias: bool = False, staging: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """Quantize a host (CPU, ideally pinned) bf16 tensor; outputs are pinned host tensors.
+
+    The copies and kernels are pipelined by the library.  The outputs are ready
+    once ``stream`` (default: the current CUDA stream) has been synchronised.
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous() or x.is_cuda:
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 host tensor")
+    M, N = x.shape
+    pin = dict(pin_memory=True)
+    u8 = torch.uint8
+    out_row = torch.empty((M, N), dtype=u8, **pin) if rowwise else None
+    scale_row = torch.empty((M, N // BLOCK), dtype=u8, **pin) if rowwise else None
+    out_col = torch.empty((M, N), dtype=u8, **pin) if colwise else None
+    scale_col = torch.empty((M // BLOCK, N), dtype=u8, **pin) if colwise else None
+    dbias = torch.empty((N,), dtype=torch.float32, **pin) if with_dbias else None
+    need = mxfp8_quantize_host_staging_bytes(M, N, with_dbias)
+    if staging is None:
+        staging = torch.empty((max(need, 256),), dtype=u8, device="cuda")
+    st = mxfp8_quantize_host(x, M, N, _fmt(fmt), out_row, scale_row, out_col, scale_col, dbias,
+                             staging, staging.numel(), stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_host")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
 
 

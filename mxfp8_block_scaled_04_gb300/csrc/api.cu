@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -153,6 +154,44 @@ mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, cons
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
+// Enqueue the flat quantize kernel (no validation: the caller has checked every
+// argument).  ws != nullptr selects the dbias variant, which writes one fp32
+// partial column sum per 128-row tile of this call to ws[tile][N].
+mxfp8_status_t enqueue_flat(int device, int fmt, const void *x, int64_t M, int64_t N, void *out_row,
+                            void *scale_row, void *out_col, void *scale_col, float *ws, const float *noop,
+                            cudaStream_t stream)
+{
+    CUtensorMap map;
+    mxfp8_status_t st = make_tensor_map(&map, x, M, N);
+    if (st != MXFP8_OK)
+        return st;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kBN - 1) / kBN;
+    QuantParams p{};
+    p.out_row = static_cast<uint8_t *>(out_row);
+    p.scale_row = static_cast<uint8_t *>(scale_row);
+    p.out_col = static_cast<uint8_t *>(out_col);
+    p.scale_col = static_cast<uint8_t *>(scale_col);
+    p.ws = ws;
+    p.noop = noop;
+    p.M = M;
+    p.N = N;
+    p.row_tiles = static_cast<int>(row_tiles);
+    p.col_tiles = static_cast<int>(col_tiles);
+    return ws != nullptr ? launch_quantize<true, false>(fmt, device, map, p, row_tiles * col_tiles, stream)
+                         : launch_quantize<false, false>(fmt, device, map, p, row_tiles * col_tiles, stream);
+}
+
+// Enqueue the dbias reduce over row_tiles partial rows of ws.
+mxfp8_status_t enqueue_reduce(const float *ws, int64_t row_tiles, int64_t N, float *dbias, const float *noop,
+                              cudaStream_t stream)
+{
+    const int64_t blocks = (N + kReduceCols - 1) / kReduceCols;
+    dbias_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceCols * kReduceWarps, 0, stream>>>(ws, row_tiles, N,
+                                                                                                   dbias, noop);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,32 +241,15 @@ mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
     if (!empty) {
-        CUtensorMap map;
-        if ((st = make_tensor_map(&map, x, M, N)) != MXFP8_OK)
-            return st;
-        QuantParams p{};
-        p.out_row = static_cast<uint8_t *>(out_row);
-        p.scale_row = static_cast<uint8_t *>(scale_row);
-        p.out_col = static_cast<uint8_t *>(out_col);
-        p.scale_col = static_cast<uint8_t *>(scale_col);
-        p.ws = dbias != nullptr ? static_cast<float *>(workspace) : nullptr;
-        p.noop = noop;
-        p.M = M;
-        p.N = N;
-        p.row_tiles = static_cast<int>(row_tiles);
-        p.col_tiles = static_cast<int>(col_tiles);
-        st = dbias != nullptr ? launch_quantize<true, false>(fp8_fmt, device, map, p, row_tiles * col_tiles, stream)
-                              : launch_quantize<false, false>(fp8_fmt, device, map, p, row_tiles * col_tiles, stream);
+        st = enqueue_flat(device, fp8_fmt, x, M, N, out_row, scale_row, out_col, scale_col,
+                          dbias != nullptr ? static_cast<float *>(workspace) : nullptr, noop, stream);
         if (st != MXFP8_OK)
             return st;
     }
     if (dbias != nullptr && N > 0) {
-        const int64_t blocks = (N + kReduceCols - 1) / kReduceCols;
-        dbias_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceCols * kReduceWarps, 0, stream>>>(
-            static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (cudaGetLastError() != cudaSuccess)
-            return MXFP8_ERR_LAUNCH;
+        st = enqueue_reduce(static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop, stream);
+        if (st != MXFP8_OK)
+            return st;
     }
     return MXFP8_OK;
 }
@@ -377,6 +399,256 @@ mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N,
     // Every (row tile, column) entry of the workspace the call uses is written
     // before it is read, so nothing needs clearing between calls.
     return mxfp8_quantize(x, M, N, fp8_fmt, out_row, scale_row, out_col, scale_col, dbias, scratch, noop, stream);
+}
+
+}  // extern "C"
+
+// ---- quantize from and to host memory, pipelined over row chunks ----------------
+//
+// Rows are cut into chunks of at most R rows (a multiple of 128, about 32 MiB of
+// BF16); the first and last chunks ramp (R/8, R/4, R/2 ... R/2, R/4, R/8) so the
+// copies that cannot overlap (the first upload, the last download) stay short.
+// Chunk c goes through staging slot c % 3: host-to-device copy on an internal
+// copy stream, the quantize kernel on the caller's stream, device-to-host copies
+// of every requested output on a second internal copy stream.  Each arrow is an
+// event wait, so the two copy directions and the kernels overlap.  With dbias,
+// every chunk writes its 128-row tile partials into one workspace for the whole
+// matrix and a single reduce runs after the last chunk, giving exactly the sums
+// of the one-shot call.
+
+namespace {
+
+constexpr int64_t kHostChunkBytes = int64_t{32} << 20;  // BF16 bytes of x per full chunk (target)
+constexpr int kHostSlots = 3;
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+int64_t host_chunk_rows(int64_t M, int64_t N)
+{
+    int64_t r = (kHostChunkBytes / (2 * N)) / kBM * kBM;
+    if (r < kBM)
+        r = kBM;
+    const int64_t m_up = (M + kBM - 1) / kBM * kBM;
+    return r < m_up ? r : m_up;
+}
+
+// Chunk boundaries 0 = b[0] < b[1] < ... < b[k] = M; every b[i] < M is a multiple
+// of 128 (so chunks start on dbias tiles) and no chunk exceeds R rows.
+std::vector<int64_t> chunk_plan(int64_t M, int64_t R)
+{
+    std::vector<int64_t> ramp;
+    for (int64_t d : {8, 4, 2}) {
+        const int64_t r = R / d / kBM * kBM;
+        if (r >= kBM)
+            ramp.push_back(r);
+    }
+    int64_t ramp_rows = 0;
+    for (int64_t r : ramp)
+        ramp_rows += r;
+    std::vector<int64_t> b{0};
+    const int64_t M128 = M / kBM * kBM;  // the last chunk also takes the final M - M128 rows
+    if (M128 <= 2 * ramp_rows + R) {
+        for (int64_t r = R; r < M; r += R)
+            b.push_back(r);
+    } else {
+        int64_t pos = 0;
+        for (int64_t r : ramp)
+            b.push_back(pos += r);
+        const int64_t tail_start = M128 - ramp_rows;
+        while (pos + R < tail_start)
+            b.push_back(pos += R);
+        if (pos < tail_start)
+            b.push_back(pos = tail_start);
+        for (auto it = ramp.rbegin(); it + 1 != ramp.rend(); ++it)
+            b.push_back(pos += *it);
+    }
+    b.push_back(M);
+    return b;
+}
+
+struct SlotLayout {
+    size_t x, out_row, out_col, scale_row, scale_col, bytes;
+};
+
+SlotLayout slot_layout(int64_t R, int64_t N)
+{
+    SlotLayout L;
+    size_t o = 0;
+    L.x = o;
+    o += align256(static_cast<size_t>(R * N * 2));
+    L.out_row = o;
+    o += align256(static_cast<size_t>(R * N));
+    L.out_col = o;
+    o += align256(static_cast<size_t>(R * N));
+    L.scale_row = o;
+    o += align256(static_cast<size_t>(R * N / 32));
+    L.scale_col = o;
+    o += align256(static_cast<size_t>(R / 32 * N));
+    L.bytes = o;
+    return L;
+}
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr, reduced = nullptr;
+    cudaEvent_t h2d_done[kHostSlots] = {}, comp_done[kHostSlots] = {}, d2h_done[kHostSlots] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+// Streams and events of the host pipeline, created once per device (the device is current).
+mxfp8_status_t host_pipe(int device, HostPipe **out)
+{
+    HostPipe &h = g_pipe[device];
+    if (!h.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.start, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.end, ef) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h.reduced, ef) == cudaSuccess;
+        for (int k = 0; ok && k < kHostSlots; ++k)
+            ok = cudaEventCreateWithFlags(&h.h2d_done[k], ef) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.comp_done[k], ef) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h.d2h_done[k], ef) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            return MXFP8_ERR_LAUNCH;
+        }
+        h.ready = true;
+    }
+    *out = &h;
+    return MXFP8_OK;
+}
+
+bool cuda_ok(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return true;
+    cudaGetLastError();
+    return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias)
+{
+    if (M <= 0 || N <= 0 || M % 32 || N % 32)
+        return 0;
+    const SlotLayout L = slot_layout(host_chunk_rows(M, N), N);
+    size_t b = kHostSlots * L.bytes;
+    if (with_dbias)
+        b += align256(mxfp8_quantize_workspace_bytes(M, N, 1)) + align256(static_cast<size_t>(N) * 4);
+    return b;
+}
+
+mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int fp8_fmt, void *out_row_host,
+                                   void *scale_row_host, void *out_col_host, void *scale_col_host,
+                                   float *dbias_host, void *staging, size_t staging_bytes, void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (M <= 0 || N <= 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (x_host == nullptr || staging == nullptr)
+        return MXFP8_ERR_NULL;
+    mxfp8_status_t st = MXFP8_OK;
+    if ((out_row_host == nullptr) != (scale_row_host == nullptr) ||
+        (out_col_host == nullptr) != (scale_col_host == nullptr) ||
+        (out_row_host == nullptr && out_col_host == nullptr))
+        return MXFP8_ERR_NULL;
+    if (!aligned(staging, 256))
+        return MXFP8_ERR_ALIGN;
+    if (staging_bytes < mxfp8_quantize_host_staging_bytes(M, N, dbias_host != nullptr))
+        return MXFP8_ERR_WORKSPACE;
+    const int64_t col_tiles = (N + kBN - 1) / kBN, row_tiles = (M + kBM - 1) / kBM;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(device, &hp)) != MXFP8_OK)
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t R = host_chunk_rows(M, N);
+    const SlotLayout L = slot_layout(R, N);
+    unsigned char *base = static_cast<unsigned char *>(staging);
+    float *ws = nullptr, *dbias_dev = nullptr;
+    if (dbias_host != nullptr) {
+        ws = reinterpret_cast<float *>(base + kHostSlots * L.bytes);
+        dbias_dev = reinterpret_cast<float *>(base + kHostSlots * L.bytes +
+                                              align256(mxfp8_quantize_workspace_bytes(M, N, 1)));
+    }
+    const unsigned char *xh = static_cast<const unsigned char *>(x_host);
+
+    if (!cuda_ok(cudaEventRecord(hp->start, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+        !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+        return MXFP8_ERR_LAUNCH;
+    const std::vector<int64_t> plan = chunk_plan(M, R);
+    const int64_t chunks = static_cast<int64_t>(plan.size()) - 1;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int k = static_cast<int>(c % kHostSlots);
+        const int64_t row0 = plan[c], rows = plan[c + 1] - plan[c];
+        unsigned char *slot = base + k * L.bytes;
+        // host -> device, once the slot's previous outputs have left
+        if (c >= kHostSlots && !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->d2h_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        if (!cuda_ok(cudaMemcpyAsync(slot + L.x, xh + row0 * N * 2, static_cast<size_t>(rows * N * 2),
+                                     cudaMemcpyHostToDevice, hp->h2d)) ||
+            !cuda_ok(cudaEventRecord(hp->h2d_done[k], hp->h2d)) ||
+            !cuda_ok(cudaStreamWaitEvent(stream, hp->h2d_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // quantize the chunk on the caller's stream
+        const bool row = out_row_host != nullptr, col = out_col_host != nullptr;
+        st = enqueue_flat(device, fp8_fmt, slot + L.x, rows, N, row ? slot + L.out_row : nullptr,
+                          row ? slot + L.scale_row : nullptr, col ? slot + L.out_col : nullptr,
+                          col ? slot + L.scale_col : nullptr, ws != nullptr ? ws + (row0 / kBM) * N : nullptr,
+                          nullptr, stream);
+        if (st != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->comp_done[k], stream)) ||
+            !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->comp_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // device -> host of every requested output of the chunk
+        bool ok = true;
+        if (row) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + row0 * N, slot + L.out_row,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * (N / 32),
+                                               slot + L.scale_row, static_cast<size_t>(rows * (N / 32)),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (col) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + row0 * N, slot + L.out_col,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + (row0 / 32) * N,
+                                               slot + L.scale_col, static_cast<size_t>((rows / 32) * N),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    if (dbias_host != nullptr) {
+        if ((st = enqueue_reduce(ws, row_tiles, N, dbias_dev, nullptr, stream)) != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->reduced, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->reduced, 0)) ||
+            !cuda_ok(cudaMemcpyAsync(dbias_host, dbias_dev, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
+                                     hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    // the caller's stream resumes once the last copy to the host is done
+    if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
+        return MXFP8_ERR_LAUNCH;
+    return MXFP8_OK;
 }
 
 }  // extern "C"

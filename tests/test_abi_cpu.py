@@ -95,3 +95,27 @@ def test_binding_wrappers_reject_bad_tensors(cuda_lib):
         mx.quantize(torch.zeros(64, 64, dtype=torch.float32))
     with pytest.raises(ValueError):
         mx.quantize(torch.zeros(64, 64, dtype=torch.bfloat16).t())
+
+
+def h(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, staging=A, nbytes=1 << 30):
+    return mx.mxfp8_quantize_host(x, M, N, fmt, orow, srow, ocol, scol, dbias, staging, nbytes, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=5), FORMAT), (dict(M=0), SHAPE), (dict(N=40), SHAPE),
+    (dict(x=None), NULL), (dict(staging=None), NULL), (dict(orow=None), NULL),
+    (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
+    (dict(staging=A + 16), ALIGN), (dict(nbytes=1024), WORKSPACE),
+])
+def test_host_pipeline_rejections(cuda_lib, kw, status):
+    assert h(**kw) == status
+
+
+def test_host_staging_bytes(cuda_lib):
+    # 8192 x 28672: chunks of at most 512 rows (32 MiB of BF16 rounded down to 128 rows),
+    # three slots of 512 * 28672 * (2 + 1 + 1) bytes plus both scale planes
+    per_slot = 512 * 28672 * 2 + 2 * 512 * 28672 + 512 * 28672 // 32 + 16 * 28672
+    assert mx.mxfp8_quantize_host_staging_bytes(8192, 28672, False) == 3 * per_slot
+    with_db = mx.mxfp8_quantize_host_staging_bytes(8192, 28672, True)
+    assert with_db == 3 * per_slot + 64 * 28672 * 4 + 28672 * 4
+    assert mx.mxfp8_quantize_host_staging_bytes(0, 64, False) == 0

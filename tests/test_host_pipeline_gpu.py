@@ -1,0 +1,58 @@
+"""mxfp8_quantize_host: host buffers in and out, pipelined over row chunks.
+
+Its results must be byte-identical to mxfp8_quantize on the same data (dbias
+too: the chunks fill one workspace and the same reduce runs once).  Shapes
+are chosen so the call cuts the rows into several chunks with a ragged last
+one; pageable host memory must give the same bytes as pinned memory.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_block_scaled_04_gb300 as mx
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def device_reference(x_bits, fmt, with_dbias, rowwise=True, colwise=True):
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    r = mx.quantize(x, fmt, rowwise=rowwise, colwise=colwise, with_dbias=with_dbias)
+    torch.cuda.synchronize()
+    return [t.cpu() if t is not None else None for t in r]
+
+
+@pytest.mark.parametrize("shape,fmt,with_dbias,pinned", [
+    ((4192, 4096), mx.E4M3, False, True),     # 1024-row chunks, last one 96 rows
+    ((1056, 28672), mx.E5M2, True, True),     # 128-row chunks, last one 32 rows
+    ((1056, 28672), mx.E5M2, True, False),    # pageable host memory
+    ((96, 160), mx.E4M3, True, True),         # a single chunk smaller than a tile
+])
+def test_host_pipeline_matches_device_path(shape, fmt, with_dbias, pinned):
+    M, N = shape
+    x_bits = wl.grad_bf16(M, N, seed=M + N)
+    want = device_reference(x_bits, fmt, with_dbias)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16)
+    x_host = x_host.pin_memory() if pinned else x_host.clone()
+    before = mx.mxfp8_kernel_launch_count()
+    got = mx.quantize_host(x_host, fmt, with_dbias=with_dbias)
+    torch.cuda.synchronize()
+    assert mx.mxfp8_kernel_launch_count() > before
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col", "dbias"), got, want):
+        if w is None:
+            assert g is None
+            continue
+        assert torch.equal(g, w), name
+
+
+def test_host_pipeline_single_direction_and_staging_reuse():
+    M, N = 2080, 4096
+    x_bits = wl.fc1_bf16(M, N, seed=3)
+    want = device_reference(x_bits, mx.E4M3, False, rowwise=False, colwise=True)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    staging = torch.empty(mx.mxfp8_quantize_host_staging_bytes(M, N, False), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        got = mx.quantize_host(x_host, mx.E4M3, rowwise=False, colwise=True, staging=staging)
+        torch.cuda.synchronize()
+        assert got.out_row is None
+        assert torch.equal(got.out_col, want[2]) and torch.equal(got.scale_col, want[3])
