@@ -68,6 +68,14 @@ def _load():
             lib.mxo_quantize_grouped.restype = ctypes.c_int
             lib.mxo_quantize_grouped.argtypes = [u16p, i64, i64, ctypes.c_int, i64p, ctypes.c_int,
                                                  u8p, u8p, u8p, u8p]
+            lib.mxo_swizzled_bytes.restype = i64
+            lib.mxo_swizzled_bytes.argtypes = [i64, i64]
+            lib.mxo_swizzle_offset.restype = i64
+            lib.mxo_swizzle_offset.argtypes = [i64, i64, i64]
+            lib.mxo_swizzle_scales.restype = None
+            lib.mxo_swizzle_scales.argtypes = [u8p, i64, i64, u8p]
+            lib.mxo_amax.restype = ctypes.c_float
+            lib.mxo_amax.argtypes = [u16p, i64, i64]
             _lib = lib
     return _lib
 
@@ -148,3 +156,24 @@ def quantize_grouped(x_bits: np.ndarray, offsets: np.ndarray, fmt: int):
     if rc != 0:
         raise ValueError("oracle: invalid group offsets")
     return out_row, scale_row, out_col, scale_col
+
+
+def swizzle_offset(r: int, c: int, C: int) -> int:
+    """Byte offset of scale (r, c) of an R x C scale matrix in the GEMM-ready layout."""
+    return int(_load().mxo_swizzle_offset(r, c, C))
+
+
+def swizzle_scales(plain: np.ndarray) -> np.ndarray:
+    """Plain scales [R, C] (uint8) -> GEMM-ready layout (1-D uint8, zero padded)."""
+    p = np.ascontiguousarray(plain, dtype=np.uint8)
+    R, C = p.shape
+    out = np.empty(int(_load().mxo_swizzled_bytes(R, C)), np.uint8)
+    _load().mxo_swizzle_scales(_ptr(p, ctypes.c_uint8), R, C, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def amax(x_bits: np.ndarray) -> float:
+    """max |x| over a BF16 matrix (uint16 bits), as fp32."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N = x.shape
+    return float(_load().mxo_amax(_ptr(x, ctypes.c_uint16), M, N))

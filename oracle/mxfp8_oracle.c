@@ -254,3 +254,51 @@ int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int n
     }
     return 0;
 }
+
+/*
+ * GEMM-ready ("swizzled") E8M0 scale layout.  The pages name a `swizzled`
+ * config bit (TransformerEngine PR #3137, `to_key()` review) without giving
+ * the layout; the reading used here is the layout block-scaled tensor-core
+ * GEMMs take on Blackwell: a scale matrix of R rows x C scale columns is
+ * padded to multiples of 128 rows and 4 columns and cut into 128x4 tiles of
+ * 512 bytes, tiles stored row-tile major (all column tiles of row tile 0,
+ * then row tile 1, ...); inside a tile, entry (r, c) sits at
+ * (r % 32) * 16 + (r / 32) * 4 + c.  Padding entries are 0.
+ */
+int64_t mxo_swizzled_bytes(int64_t R, int64_t C)
+{
+    return ((R + 127) / 128 * 128) * ((C + 3) / 4 * 4);
+}
+
+int64_t mxo_swizzle_offset(int64_t r, int64_t c, int64_t C)
+{
+    const int64_t col_tiles = (C + 3) / 4;
+    const int64_t tile = (r / 128) * col_tiles + c / 4;
+    const int64_t rr = r % 128, cc = c % 4;
+    return tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc;
+}
+
+/* plain[R][C] (row-major) -> out[mxo_swizzled_bytes(R, C)], padding zeroed. */
+void mxo_swizzle_scales(const uint8_t *plain, int64_t R, int64_t C, uint8_t *out)
+{
+    int64_t r, c;
+    const int64_t n = mxo_swizzled_bytes(R, C);
+    for (r = 0; r < n; r++)
+        out[r] = 0;
+    for (r = 0; r < R; r++)
+        for (c = 0; c < C; c++)
+            out[mxo_swizzle_offset(r, c, C)] = plain[r * C + c];
+}
+
+/* Per-tensor amax: max |x| over the whole BF16 matrix, as fp32 (exact). */
+float mxo_amax(const uint16_t *x, int64_t M, int64_t N)
+{
+    double amax = 0.0;
+    int64_t i;
+    for (i = 0; i < M * N; i++) {
+        const double a = fabs(mxo_bf16_to_double(x[i]));
+        if (a > amax)
+            amax = a;
+    }
+    return (float)amax;
+}

@@ -314,3 +314,42 @@ def test_moe_sizes_recipe():
     sizes = wl.moe_group_sizes(64, 65536, seed=4)
     assert sizes.sum() == 65536 and np.all(sizes % 32 == 0)
     assert (sizes == 0).sum() >= 4
+
+
+# ---- GEMM-ready scale layout and per-tensor amax -----------------------------------
+
+SWZ_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "swizzle_offsets.txt")
+
+
+def test_swizzle_offsets_hand_worked(oracle_mod):
+    for line in open(SWZ_GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        shape, rc, off = [p.strip() for p in line.split("|")]
+        R, C = map(int, shape.split())
+        r, c = map(int, rc.split())
+        assert oracle_mod.swizzle_offset(r, c, C) == int(off), line
+
+
+@pytest.mark.parametrize("R,C", [(128, 4), (256, 8), (100, 5), (300, 13), (32, 1)])
+def test_swizzle_equals_tile_transpose(oracle_mod, R, C):
+    # The same layout written as a reshape/transpose of the zero-padded plain
+    # matrix: [R/128, 4, 32, C/4, 4] (row tile, 32-row group, row in group,
+    # column tile, column) -> order (row tile, column tile, row in group,
+    # 32-row group, column).
+    rng = np.random.Generator(np.random.PCG64(R * 31 + C))
+    plain = rng.integers(1, 255, (R, C)).astype(np.uint8)
+    Rp, Cp = -(-R // 128) * 128, -(-C // 4) * 4
+    padded = np.zeros((Rp, Cp), np.uint8)
+    padded[:R, :C] = plain
+    want = padded.reshape(Rp // 128, 4, 32, Cp // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+    got = oracle_mod.swizzle_scales(plain)
+    assert np.array_equal(got, want)
+
+
+def test_amax_matches_numpy(oracle_mod):
+    x = structured_input(96, 160, seed=17)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert oracle_mod.amax(x) == np.float32(np.abs(xv).max())
+    assert oracle_mod.amax(np.zeros((32, 32), np.uint16)) == 0.0
