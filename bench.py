@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="fc1_8192x28672")
     ap.add_argument("--shape", default=None, help="MxN: the workload's value recipe at another shape")
+    ap.add_argument("--swizzled", action="store_true", help="write GEMM-ready (swizzled) scale planes")
+    ap.add_argument("--amax", action="store_true", help="also write the per-tensor amax")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -265,9 +267,13 @@ def run_ours(args):
     grouped = offsets is not None
     x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
     out_row = torch.empty((M, N), dtype=torch.uint8, device="cuda")
-    scale_row = torch.empty((M, N // 32), dtype=torch.uint8, device="cuda")
+    layout = mx.SCALES_SWIZZLED if args.swizzled else mx.SCALES_PLAIN
+    scale_row = torch.empty((mx.mxfp8_scale_bytes(M, N // 32, layout),), dtype=torch.uint8, device="cuda")
     out_col = torch.empty((M, N), dtype=torch.uint8, device="cuda")
-    scale_col = torch.empty((M // 32, N), dtype=torch.uint8, device="cuda")
+    scale_col = torch.empty((mx.mxfp8_scale_bytes(N, M // 32, layout),), dtype=torch.uint8, device="cuda")
+    amax = torch.empty((1,), dtype=torch.float32, device="cuda") if args.amax else None
+    if (args.swizzled or args.amax) and offsets is not None:
+        raise SystemExit("--swizzled / --amax apply to the flat workloads")
     dbias = torch.empty((N,), dtype=torch.float32, device="cuda") if with_dbias else None
     ws = (torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
           if with_dbias else None)
@@ -278,6 +284,10 @@ def run_ours(args):
         if grouped:
             st = mx.mxfp8_quantize_grouped(xin, M, N, off_dev.numel() - 1, off_dev, fmt, out_row, scale_row,
                                            out_col, scale_col, None, None, None, stream)
+        elif args.swizzled or args.amax:
+            cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
+                                 layout, amax)
+            st = mx.mxfp8_quantize_ex(cfg, stream)
         else:
             st = mx.mxfp8_quantize(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
                                    stream)
@@ -292,8 +302,16 @@ def run_ours(args):
     except Exception:
         uuid = None
 
-    for _ in range(max(3, args.warmup)):
+    # Warm-up: at least W steps, continued until 100 ms have passed so that the
+    # clocks have left their idle state before the timed region (measured: the
+    # first ~50 calls after idle run a few percent slow).
+    warm_t0 = time.perf_counter()
+    warmup_run = 0
+    while warmup_run < max(3, args.warmup) or time.perf_counter() - warm_t0 < 0.1:
         step()
+        warmup_run += 1
+        if warmup_run % 16 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
 
     # Inputs that fit in L2 would be re-read from L2 on the next step:
@@ -302,8 +320,11 @@ def run_ours(args):
     flush_buf = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda") if flush else None
 
     def timed():
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        # Per-step events only when L2 is flushed between steps (the flush must stay outside
+        # the timed intervals); otherwise two events bracket the K back-to-back steps, and a
+        # step's average duration is total / K (gaps between launches included).
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if flush else None
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if flush else None
         t_begin = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         launches0 = mx.mxfp8_kernel_launch_count()
@@ -314,16 +335,21 @@ def run_ours(args):
         for i in range(args.steps):
             if flush:
                 flush_buf.zero_()
-            starts[i].record(stream)
+                starts[i].record(stream)
             step()
-            ends[i].record(stream)
+            if flush:
+                ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         h1 = time.time()
         barrier()
         launches = mx.mxfp8_kernel_launch_count() - launches0
-        per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        total_ms = sum(per_launch) if flush else t_begin.elapsed_time(t_end)
+        if flush:
+            per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+            total_ms = sum(per_launch)
+        else:
+            total_ms = t_begin.elapsed_time(t_end)
+            per_launch = [total_ms / args.steps]
         return total_ms, per_launch, launches, h0, h1
 
     sampler = ClockSampler(uuid)
@@ -351,10 +377,10 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped:
-            # no host-buffer grouped call: copy in, grouped call, copy every output out
+        if grouped or args.swizzled or args.amax:
+            # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
-            path = "pinned host -> device copy, grouped C-ABI call, device -> pinned host copies (one stream)"
+            path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"
 
             def e2e_step():
                 x_stage.copy_(x_host, non_blocking=True)
@@ -399,10 +425,11 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "warmup_steps_run": warmup_run, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
+                       "scales": "swizzled" if args.swizzled else "plain", "amax": bool(args.amax),
                        "bytes_per_step": algo_bytes,
                        "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
                               f"bf16 input; time = sum of the per-step event intervals" if flush else

@@ -182,6 +182,60 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
                                    float *dbias_host, void *staging, size_t staging_bytes,
                                    void *stream);
 
+/* Layout of the E8M0 scale planes (the `swizzled` field of the PR #3137 config key). */
+typedef enum {
+    MXFP8_SCALES_PLAIN = 0,    /* scale_row [M, N/32], scale_col [M/32, N], row-major */
+    MXFP8_SCALES_SWIZZLED = 1  /* GEMM-ready: see mxfp8_scale_bytes */
+} mxfp8_scale_layout_t;
+
+/*
+ * Bytes of one scale plane for a scale matrix of `rows` x `scale_cols`.
+ * MXFP8_SCALES_PLAIN: rows * scale_cols.  MXFP8_SCALES_SWIZZLED: the matrix
+ * padded to multiples of 128 rows and 4 columns and stored as 128x4 tiles of
+ * 512 bytes, tiles in row-tile-major order, entry (r, c) of a tile at byte
+ * 16*(r % 32) + 4*(r / 32) + c; padding entries are written as 0.  This is
+ * the scale-factor arrangement block-scaled tensor-core GEMMs read (the
+ * reading taken for the config key's `swizzled` bit, which the pages leave
+ * undefined).  For the rowwise plane rows = M, scale_cols = N/32; the
+ * columnwise plane serves the transposed operand, rows = N, scale_cols = M/32
+ * (swizzled entry (j, i/32) holds the scale of column j, rows i..i+31).
+ * Returns 0 for an unknown layout or negative sizes.
+ */
+size_t mxfp8_scale_bytes(int64_t rows, int64_t scale_cols, int scale_layout);
+
+/*
+ * Options of mxfp8_quantize_ex: the fields of the quantization config key on
+ * the PR #3137 page (fp8_dtype, rowwise, colwise, swizzled, with_amax,
+ * with_dbias, with_noop) as one struct.  Zero-initialise it and set what is
+ * needed; pointers and sizes mean what they mean for mxfp8_quantize.
+ */
+typedef struct mxfp8_quantize_config {
+    const void *x;         /* device bf16 [M, N] */
+    int64_t M, N;          /* multiples of 32 */
+    int fp8_fmt;           /* MXFP8_E4M3 / MXFP8_E5M2 */
+    void *out_row;         /* uint8 [M, N] or NULL */
+    void *scale_row;       /* mxfp8_scale_bytes(M, N/32, scale_layout) bytes */
+    void *out_col;         /* uint8 [M, N] or NULL */
+    void *scale_col;       /* mxfp8_scale_bytes(N, M/32, scale_layout) bytes (plain: [M/32, N]) */
+    float *dbias;          /* fp32 [N] or NULL */
+    void *workspace;       /* mxfp8_quantize_workspace_bytes(M, N, dbias != NULL) bytes */
+    const float *noop;     /* device fp32 scalar or NULL */
+    int scale_layout;      /* mxfp8_scale_layout_t */
+    float *amax;           /* device fp32 scalar or NULL: receives max |x| over the tensor */
+    int reserved[6];       /* must be 0 */
+} mxfp8_quantize_config_t;
+
+/*
+ * mxfp8_quantize with every option of mxfp8_quantize_config_t.  With
+ * MXFP8_SCALES_SWIZZLED the scale planes are written in the GEMM-ready
+ * layout; swizzled scale pointers need no alignment.  amax, if set, is a
+ * device fp32 written with the largest |x| of the tensor (4-byte aligned;
+ * noop leaves it untouched like every other output).  Returns the status
+ * codes of mxfp8_quantize, plus MXFP8_ERR_FORMAT for an unknown layout or a
+ * non-zero reserved field, and MXFP8_ERR_NULL for cfg == NULL.
+ */
+mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream);
+
 /* Static, human-readable text for a status code. */
 const char *mxfp8_status_string(int status);
 

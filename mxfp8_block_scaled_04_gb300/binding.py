@@ -27,6 +27,19 @@ STATUS_NAMES = {
     7: "MXFP8_ERR_LAUNCH", 8: "MXFP8_ERR_GROUPS",
 }
 
+SCALES_PLAIN = 0
+SCALES_SWIZZLED = 1
+
+
+class QuantizeConfig(ctypes.Structure):
+    """Mirror of mxfp8_quantize_config_t (include/mxfp8.h)."""
+    _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("fp8_fmt", ctypes.c_int),
+                ("out_row", ctypes.c_void_p), ("scale_row", ctypes.c_void_p), ("out_col", ctypes.c_void_p),
+                ("scale_col", ctypes.c_void_p), ("dbias", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("noop", ctypes.c_void_p), ("scale_layout", ctypes.c_int), ("amax", ctypes.c_void_p),
+                ("reserved", ctypes.c_int * 6)]
+
+
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmxfp8.so")
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +74,10 @@ def lib():
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
             L.mxfp8_quantize_host.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.mxfp8_scale_bytes.restype = ctypes.c_size_t
+            L.mxfp8_scale_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_ex.restype = i32
+            L.mxfp8_quantize_ex.argtypes = [ctypes.POINTER(QuantizeConfig), vp]
             L.mxfp8_status_string.restype = ctypes.c_char_p
             L.mxfp8_status_string.argtypes = [i32]
             L.mxfp8_kernel_launch_count.restype = ctypes.c_uint64
@@ -123,6 +140,22 @@ def mxfp8_quantize_host(x_host, M, N, fp8_fmt, out_row_host, scale_row_host, out
                                          _addr(staging), int(staging_bytes), _stream(stream)))
 
 
+def mxfp8_scale_bytes(rows: int, scale_cols: int, scale_layout: int = SCALES_PLAIN) -> int:
+    return int(lib().mxfp8_scale_bytes(rows, scale_cols, scale_layout))
+
+
+def mxfp8_quantize_ex(cfg: QuantizeConfig, stream=None) -> int:
+    return int(lib().mxfp8_quantize_ex(ctypes.byref(cfg) if cfg is not None else None, _stream(stream)))
+
+
+def make_config(x, M, N, fp8_fmt, out_row=None, scale_row=None, out_col=None, scale_col=None, dbias=None,
+                workspace=None, noop=None, scale_layout=SCALES_PLAIN, amax=None) -> QuantizeConfig:
+    """A QuantizeConfig from tensors / addresses / None (marshalling only)."""
+    return QuantizeConfig(_addr(x), M, N, fp8_fmt, _addr(out_row), _addr(scale_row), _addr(out_col),
+                          _addr(scale_col), _addr(dbias), _addr(workspace), _addr(noop), scale_layout,
+                          _addr(amax), (ctypes.c_int * 6)())
+
+
 def mxfp8_status_string(status: int) -> str:
     return lib().mxfp8_status_string(int(status)).decode()
 
@@ -144,10 +177,11 @@ def mxfp8_device_fault_word(clear: bool = False) -> int:
 class MXFP8Tensor(NamedTuple):
     """Quantized outputs; a direction that was not requested is None."""
     out_row: Optional[torch.Tensor]     # uint8 [M, N]
-    scale_row: Optional[torch.Tensor]   # uint8 [M, N/32] (E8M0)
+    scale_row: Optional[torch.Tensor]   # uint8 [M, N/32] (E8M0), or the swizzled plane (1-D)
     out_col: Optional[torch.Tensor]     # uint8 [M, N]
-    scale_col: Optional[torch.Tensor]   # uint8 [M/32, N] (E8M0)
+    scale_col: Optional[torch.Tensor]   # uint8 [M/32, N] (E8M0), or the swizzled plane (1-D)
     dbias: Optional[torch.Tensor]       # float32 [N]
+    amax: Optional[torch.Tensor] = None  # float32 [1]: max |x|
 
 
 def _fmt(fmt) -> int:
@@ -168,22 +202,41 @@ def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool):
 
 def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
              with_dbias: bool = False, noop: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
-    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (M, N multiples of 32)."""
+             workspace: Optional[torch.Tensor] = None, stream=None, swizzled: bool = False,
+             with_amax: bool = False) -> MXFP8Tensor:
+    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (M, N multiples of 32).
+
+    ``swizzled`` writes both scale planes in the GEMM-ready layout (1-D tensors of
+    mxfp8_scale_bytes bytes); ``with_amax`` also returns max |x| as a float32 [1].
+    """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
     M, N = x.shape
     f = _fmt(fmt)
-    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
+    if swizzled:
+        u8 = dict(dtype=torch.uint8, device=x.device)
+        out_row = torch.empty((M, N), **u8) if rowwise else None
+        scale_row = torch.empty((mxfp8_scale_bytes(M, N // BLOCK, SCALES_SWIZZLED),), **u8) if rowwise else None
+        out_col = torch.empty((M, N), **u8) if colwise else None
+        scale_col = torch.empty((mxfp8_scale_bytes(N, M // BLOCK, SCALES_SWIZZLED),), **u8) if colwise else None
+    else:
+        out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
     dbias = torch.empty((N,), dtype=torch.float32, device=x.device) if with_dbias else None
+    amax = torch.empty((1,), dtype=torch.float32, device=x.device) if with_amax else None
     if with_dbias and workspace is None:
         nbytes = mxfp8_quantize_workspace_bytes(M, N, True)
         workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
-    st = mxfp8_quantize(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,
-                        workspace if with_dbias else None, noop, stream)
+    if swizzled or with_amax:
+        cfg = make_config(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,
+                          workspace if with_dbias else None, noop,
+                          SCALES_SWIZZLED if swizzled else SCALES_PLAIN, amax)
+        st = mxfp8_quantize_ex(cfg, stream)
+    else:
+        st = mxfp8_quantize(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,
+                            workspace if with_dbias else None, noop, stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize")
-    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias, amax)
 
 
 def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,

@@ -26,7 +26,7 @@ std::atomic<uint64_t> g_launches{0};
 struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
-    int ctas_per_sm[8] = {};  // indexed by kernel variant
+    int ctas_per_sm[32] = {};  // indexed by kernel variant
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -64,15 +64,15 @@ bool on_device(const void *p, int device)
     return a.type == cudaMemoryTypeDevice && a.device == device;
 }
 
-template <int FMT, bool DBIAS, bool GROUPED>
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
 int variant_index()
 {
-    return FMT + 2 * (DBIAS ? 1 : 0) + 4 * (GROUPED ? 1 : 0);
+    return FMT + 2 * (DBIAS ? 1 : 0) + 4 * (GROUPED ? 1 : 0) + 8 * (SWZ ? 1 : 0) + 16 * (AMAX ? 1 : 0);
 }
 
 // One-time per (device, variant) set-up: opt in to the large shared-memory
 // carve-out and record how many CTAs fit per SM.
-template <int FMT, bool DBIAS, bool GROUPED>
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
 mxfp8_status_t prepare(int device, int *grid_cap)
 {
     std::lock_guard<std::mutex> lock(g_dev_mu);
@@ -84,10 +84,10 @@ mxfp8_status_t prepare(int device, int *grid_cap)
             return MXFP8_ERR_DEVICE;
         d.ready = true;
     }
-    const int v = variant_index<FMT, DBIAS, GROUPED>();
+    const int v = variant_index<FMT, DBIAS, GROUPED, SWZ, AMAX>();
     if (d.ctas_per_sm[v] == 0) {
         const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
-        auto kern = quantize_kernel<FMT, DBIAS, GROUPED>;
+        auto kern = quantize_kernel<FMT, DBIAS, GROUPED, SWZ, AMAX>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return MXFP8_ERR_LAUNCH;
         int n = 0;
@@ -135,23 +135,51 @@ mxfp8_status_t current_device(int *device)
     return MXFP8_OK;
 }
 
-template <bool DBIAS, bool GROUPED>
+template <bool DBIAS, bool GROUPED, bool SWZ = false, bool AMAX = false>
 mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, const QuantParams &p,
                                int64_t tile_bound, cudaStream_t stream)
 {
     int cap = 0;
-    mxfp8_status_t st = fmt == MXFP8_E4M3 ? prepare<0, DBIAS, GROUPED>(device, &cap)
-                                          : prepare<1, DBIAS, GROUPED>(device, &cap);
+    mxfp8_status_t st = fmt == MXFP8_E4M3 ? prepare<0, DBIAS, GROUPED, SWZ, AMAX>(device, &cap)
+                                          : prepare<1, DBIAS, GROUPED, SWZ, AMAX>(device, &cap);
     if (st != MXFP8_OK)
         return st;
     const int grid = static_cast<int>(tile_bound < cap ? tile_bound : cap);
     const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
     if (fmt == MXFP8_E4M3)
-        quantize_kernel<0, DBIAS, GROUPED><<<grid, kThreads, smem, stream>>>(map, p);
+        quantize_kernel<0, DBIAS, GROUPED, SWZ, AMAX><<<grid, kThreads, smem, stream>>>(map, p);
     else
-        quantize_kernel<1, DBIAS, GROUPED><<<grid, kThreads, smem, stream>>>(map, p);
+        quantize_kernel<1, DBIAS, GROUPED, SWZ, AMAX><<<grid, kThreads, smem, stream>>>(map, p);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+// Per-tensor amax output: zero it before the quantize kernel (unless noop).
+__global__ void amax_init_kernel(float *amax, const float *noop)
+{
+    if (noop != nullptr && *noop == 1.0f)
+        return;
+    *amax = 0.0f;
+}
+
+// Zero the padding entries of a GEMM-ready scale plane of R x C real entries
+// (unless noop): the tiles of the last row tile and of the last column tile.
+__global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const float *noop)
+{
+    if (noop != nullptr && *noop == 1.0f)
+        return;
+    const int64_t col_tiles = (C + 3) / 4, row_tiles = (R + 127) / 128;
+    // tile list: row tile row_tiles-1 (all column tiles), then column tile col_tiles-1 of the others
+    const int64_t ntiles = col_tiles + row_tiles - 1;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int64_t rt = t < col_tiles ? row_tiles - 1 : t - col_tiles;
+        const int64_t ct = t < col_tiles ? t : col_tiles - 1;
+        for (int w = threadIdx.x; w < 512; w += blockDim.x) {
+            const int64_t r = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), c = ct * 4 + (w & 3);
+            if (r >= R || c >= C)
+                scales[((rt * col_tiles + ct) << 9) + w] = 0;
+        }
+    }
 }
 
 // Enqueue the flat quantize kernel (no validation: the caller has checked every
@@ -159,7 +187,7 @@ mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, cons
 // partial column sum per 128-row tile of this call to ws[tile][N].
 mxfp8_status_t enqueue_flat(int device, int fmt, const void *x, int64_t M, int64_t N, void *out_row,
                             void *scale_row, void *out_col, void *scale_col, float *ws, const float *noop,
-                            cudaStream_t stream)
+                            cudaStream_t stream, bool swizzled = false, float *amax = nullptr)
 {
     CUtensorMap map;
     mxfp8_status_t st = make_tensor_map(&map, x, M, N);
@@ -177,8 +205,23 @@ mxfp8_status_t enqueue_flat(int device, int fmt, const void *x, int64_t M, int64
     p.N = N;
     p.row_tiles = static_cast<int>(row_tiles);
     p.col_tiles = static_cast<int>(col_tiles);
-    return ws != nullptr ? launch_quantize<true, false>(fmt, device, map, p, row_tiles * col_tiles, stream)
-                         : launch_quantize<false, false>(fmt, device, map, p, row_tiles * col_tiles, stream);
+    p.amax = amax;
+    const int64_t tiles = row_tiles * col_tiles;
+    const int opts = (swizzled ? 1 : 0) + (amax != nullptr ? 2 : 0);
+    if (ws != nullptr) {
+        switch (opts) {
+        case 0: return launch_quantize<true, false, false, false>(fmt, device, map, p, tiles, stream);
+        case 1: return launch_quantize<true, false, true, false>(fmt, device, map, p, tiles, stream);
+        case 2: return launch_quantize<true, false, false, true>(fmt, device, map, p, tiles, stream);
+        default: return launch_quantize<true, false, true, true>(fmt, device, map, p, tiles, stream);
+        }
+    }
+    switch (opts) {
+    case 0: return launch_quantize<false, false, false, false>(fmt, device, map, p, tiles, stream);
+    case 1: return launch_quantize<false, false, true, false>(fmt, device, map, p, tiles, stream);
+    case 2: return launch_quantize<false, false, false, true>(fmt, device, map, p, tiles, stream);
+    default: return launch_quantize<false, false, true, true>(fmt, device, map, p, tiles, stream);
+    }
 }
 
 // Enqueue the dbias reduce over row_tiles partial rows of ws.
@@ -248,6 +291,97 @@ mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, 
     }
     if (dbias != nullptr && N > 0) {
         st = enqueue_reduce(static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop, stream);
+        if (st != MXFP8_OK)
+            return st;
+    }
+    return MXFP8_OK;
+}
+
+size_t mxfp8_scale_bytes(int64_t rows, int64_t scale_cols, int scale_layout)
+{
+    if (rows < 0 || scale_cols < 0)
+        return 0;
+    if (scale_layout == MXFP8_SCALES_PLAIN)
+        return static_cast<size_t>(rows) * static_cast<size_t>(scale_cols);
+    if (scale_layout == MXFP8_SCALES_SWIZZLED)
+        return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>((scale_cols + 3) / 4 * 4);
+    return 0;
+}
+
+mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream_)
+{
+    if (cfg == nullptr)
+        return MXFP8_ERR_NULL;
+    for (int r : cfg->reserved)
+        if (r != 0)
+            return MXFP8_ERR_FORMAT;
+    if (cfg->scale_layout != MXFP8_SCALES_PLAIN && cfg->scale_layout != MXFP8_SCALES_SWIZZLED)
+        return MXFP8_ERR_FORMAT;
+    if (cfg->scale_layout == MXFP8_SCALES_PLAIN && cfg->amax == nullptr)
+        return mxfp8_quantize(cfg->x, cfg->M, cfg->N, cfg->fp8_fmt, cfg->out_row, cfg->scale_row, cfg->out_col,
+                              cfg->scale_col, cfg->dbias, cfg->workspace, cfg->noop, stream_);
+
+    const int64_t M = cfg->M, N = cfg->N;
+    if (cfg->fp8_fmt != MXFP8_E4M3 && cfg->fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    const bool swz = cfg->scale_layout == MXFP8_SCALES_SWIZZLED;
+    const bool empty = M == 0 || N == 0;
+    mxfp8_status_t st;
+    if (!empty) {
+        if (cfg->x == nullptr)
+            return MXFP8_ERR_NULL;
+        if ((cfg->out_row == nullptr) != (cfg->scale_row == nullptr) ||
+            (cfg->out_col == nullptr) != (cfg->scale_col == nullptr) ||
+            (cfg->out_row == nullptr && cfg->out_col == nullptr))
+            return MXFP8_ERR_NULL;
+    }
+    if (!aligned(cfg->x, 16) || !aligned(cfg->out_row, 16) || !aligned(cfg->out_col, 16) ||
+        (!swz && !aligned(cfg->scale_col, 4)) || !aligned(cfg->dbias, 4) || !aligned(cfg->workspace, 16) ||
+        !aligned(cfg->amax, 4))
+        return MXFP8_ERR_ALIGN;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kBN - 1) / kBN;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (cfg->dbias != nullptr && cfg->workspace == nullptr && M > 0)
+        return MXFP8_ERR_WORKSPACE;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(cfg->x, device) || !on_device(cfg->out_row, device) || !on_device(cfg->scale_row, device) ||
+        !on_device(cfg->out_col, device) || !on_device(cfg->scale_col, device) || !on_device(cfg->dbias, device) ||
+        !on_device(cfg->workspace, device) || !on_device(cfg->noop, device) || !on_device(cfg->amax, device))
+        return MXFP8_ERR_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    if (cfg->amax != nullptr) {
+        amax_init_kernel<<<1, 1, 0, stream>>>(cfg->amax, cfg->noop);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (swz && !empty) {
+        // padding exists when a scale plane's rows or columns are not tile multiples
+        auto pad = [&](void *plane, int64_t R, int64_t C) {
+            if (plane != nullptr && (R % 128 != 0 || C % 4 != 0)) {
+                swizzle_pad_kernel<<<64, 128, 0, stream>>>(static_cast<uint8_t *>(plane), R, C, cfg->noop);
+                g_launches.fetch_add(1, std::memory_order_relaxed);
+            }
+        };
+        pad(cfg->scale_row, M, N / 32);
+        pad(cfg->scale_col, N, M / 32);
+    }
+    if (cudaGetLastError() != cudaSuccess)
+        return MXFP8_ERR_LAUNCH;
+    if (!empty) {
+        st = enqueue_flat(device, cfg->fp8_fmt, cfg->x, M, N, cfg->out_row, cfg->scale_row, cfg->out_col,
+                          cfg->scale_col, cfg->dbias != nullptr ? static_cast<float *>(cfg->workspace) : nullptr,
+                          cfg->noop, stream, swz, cfg->amax);
+        if (st != MXFP8_OK)
+            return st;
+    }
+    if (cfg->dbias != nullptr && N > 0) {
+        st = enqueue_reduce(static_cast<const float *>(cfg->workspace), M > 0 ? row_tiles : 0, N, cfg->dbias,
+                            cfg->noop, stream);
         if (st != MXFP8_OK)
             return st;
     }

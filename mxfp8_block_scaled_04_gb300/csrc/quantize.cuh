@@ -76,7 +76,17 @@ struct QuantParams {
     int num_groups;
     int col_tiles;
     int row_tiles;           // flat only
+    float *amax;             // per-tensor max |x| (device fp32, zeroed before the launch), AMAX variant
 };
+
+// Byte offset of scale (r, c) of an R x C scale matrix (C scale columns) in the
+// GEMM-ready layout: 128-row x 4-column tiles of 512 bytes, row-tile major,
+// entry (r, c) of a tile at 16 * (r % 32) + 4 * (r / 32) + c.
+__device__ __forceinline__ int64_t swizzled_offset(int64_t r, int64_t c, int64_t C)
+{
+    const int64_t col_tiles = (C + 3) >> 2;
+    return (((r >> 7) * col_tiles + (c >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3);
+}
 
 // Library-wide device fault word (bit 0: a bounded wait expired).
 __device__ unsigned int g_fault_word;
@@ -196,7 +206,9 @@ __device__ __forceinline__ int grouped_setup(const QuantParams &p, int64_t *goff
     return total;
 }
 
-template <int FMT, bool DBIAS, bool GROUPED>
+// SWZ: scale planes in the GEMM-ready layout; AMAX: also produce max |x|.  Both are
+// template switches so the default variant carries no code for them.
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p)
 {
@@ -262,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             issue(s, first + s * stride);
     }
 
+    uint32_t amax_acc = 0;  // running max |x| as BF16 bits (amax output only)
     for (int it = 0; it < my_count; ++it) {
         const int slot = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
@@ -312,11 +325,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int e2 = block_exponent<FMT>(mx1 & 0xFFFFu), e3 = block_exponent<FMT>(mx1 >> 16);
             const int64_t gcol = tc.col0 + box * kBoxCols + cq * 4;
             const int64_t grow = tc.row0 + rb * 32;
+            if (AMAX && gcol < N)
+                amax_acc = max(amax_acc, max(max(mx0 & 0xFFFFu, mx0 >> 16), max(mx1 & 0xFFFFu, mx1 >> 16)));
             if (half == 0) {
-                if (do_col && gcol < N && grow < tc.row_end)
-                    *reinterpret_cast<uint32_t *>(p.scale_col + (grow >> 5) * N + gcol) =
-                        static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
-                        (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
+                if (do_col && gcol < N && grow < tc.row_end) {
+                    if constexpr (!SWZ) {
+                        *reinterpret_cast<uint32_t *>(p.scale_col + (grow >> 5) * N + gcol) =
+                            static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
+                            (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
+                    } else {
+                        // the columnwise operand's scales, seen as N rows x M/32 scale columns
+                        const int64_t C = p.M >> 5, c = grow >> 5;
+                        p.scale_col[swizzled_offset(gcol, c, C)] = static_cast<uint8_t>(e0);
+                        p.scale_col[swizzled_offset(gcol + 1, c, C)] = static_cast<uint8_t>(e1);
+                        p.scale_col[swizzled_offset(gcol + 2, c, C)] = static_cast<uint8_t>(e2);
+                        p.scale_col[swizzled_offset(gcol + 3, c, C)] = static_cast<uint8_t>(e3);
+                    }
+                }
                 if constexpr (DBIAS)
                     *reinterpret_cast<float4 *>(dsum + rb * kBN + box * kBoxCols + cq * 4) =
                         make_float4(d0, d1, d2, d3);
@@ -390,7 +415,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (in) {
                         stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
                         if ((sp & 1) == 0)
-                            p.scale_row[grow * (N >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                            p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, N >> 5)
+                                            : grow * (N >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                        if (AMAX && !do_col)
+                            amax_acc = max(amax_acc, a);
                     }
                 }
                 if (do_col) {
@@ -415,6 +443,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             fence_proxy_async_smem();
             issue(slot, first + (it + kStages) * stride);
         }
+    }
+    if constexpr (AMAX) {
+        // fp32 bits of a non-negative value order like the value itself
+        const uint32_t m = __reduce_max_sync(0xffffffffu, amax_acc);
+        if (lane == 0 && m != 0)
+            atomicMax(reinterpret_cast<unsigned int *>(p.amax), m << 16);
     }
 }
 

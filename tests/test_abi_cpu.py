@@ -119,3 +119,41 @@ def test_host_staging_bytes(cuda_lib):
     with_db = mx.mxfp8_quantize_host_staging_bytes(8192, 28672, True)
     assert with_db == 3 * per_slot + 64 * 28672 * 4 + 28672 * 4
     assert mx.mxfp8_quantize_host_staging_bytes(0, 64, False) == 0
+
+
+def test_config_struct_layout_matches_the_c_header(tmp_path):
+    # compile a probe against include/mxfp8.h and compare sizeof/offsetof with the ctypes mirror
+    import subprocess
+    src = tmp_path / "probe.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mxfp8.h"\n'
+                   '#define F(f) printf(" %zu", offsetof(mxfp8_quantize_config_t, f));\n'
+                   'int main(void){ printf("%zu", sizeof(mxfp8_quantize_config_t));\n'
+                   'F(x) F(M) F(N) F(fp8_fmt) F(out_row) F(scale_row) F(out_col) F(scale_col) F(dbias) F(workspace)'
+                   ' F(noop) F(scale_layout) F(amax) F(reserved) return 0; }\n')
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    c_vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    C = mx.QuantizeConfig
+    py_vals = [ctypes.sizeof(C)] + [getattr(C, f).offset for f, _ in C._fields_]
+    assert c_vals == py_vals
+
+
+def test_scale_bytes(cuda_lib):
+    assert mx.mxfp8_scale_bytes(8192, 896, mx.SCALES_PLAIN) == 8192 * 896
+    assert mx.mxfp8_scale_bytes(8192, 896, mx.SCALES_SWIZZLED) == 8192 * 896
+    assert mx.mxfp8_scale_bytes(96, 5, mx.SCALES_SWIZZLED) == 128 * 8
+    assert mx.mxfp8_scale_bytes(96, 5, 7) == 0
+
+
+def test_ex_rejections(cuda_lib):
+    assert mx.mxfp8_quantize_ex(None, 0) == NULL
+    cfg = mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=2)
+    assert mx.mxfp8_quantize_ex(cfg, 0) == FORMAT
+    cfg = mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1)
+    cfg.reserved[3] = 1
+    assert mx.mxfp8_quantize_ex(cfg, 0) == FORMAT
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 48, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, None, A, A, A, scale_layout=1), 0) == NULL
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1, amax=A + 2), 0) == ALIGN
+    # swizzled scale planes need no alignment: an odd scale pointer reaches the device stage
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A + 1, A, A + 1, scale_layout=1), 0) == DEVICE
