@@ -76,6 +76,14 @@ def _load():
             lib.mxo_swizzle_scales.argtypes = [u8p, i64, i64, u8p]
             lib.mxo_amax.restype = ctypes.c_float
             lib.mxo_amax.argtypes = [u16p, i64, i64]
+            lib.mxo_activation_f64.restype = ctypes.c_double
+            lib.mxo_activation_f64.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.mxo_activation.restype = ctypes.c_float
+            lib.mxo_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.mxo_quantize_f32.restype = ctypes.c_int
+            lib.mxo_quantize_f32.argtypes = [f32p, i64, i64, ctypes.c_int, u8p, u8p, u8p, u8p, f32p]
+            lib.mxo_activate.restype = None
+            lib.mxo_activate.argtypes = [u16p, i64, ctypes.c_int, f32p]
             _lib = lib
     return _lib
 
@@ -177,3 +185,42 @@ def amax(x_bits: np.ndarray) -> float:
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     M, N = x.shape
     return float(_load().mxo_amax(_ptr(x, ctypes.c_uint16), M, N))
+
+
+ACT_NONE, ACT_RELU, ACT_SRELU, ACT_GELU, ACT_SILU, ACT_QGELU = range(6)
+
+
+def activate(x_bits: np.ndarray, act: int) -> np.ndarray:
+    """fp32 activation of a BF16 matrix (see mxo_activation for the formulas)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    y = np.empty(x.shape, np.float32)
+    _load().mxo_activate(_ptr(x, ctypes.c_uint16), x.size, act, _ptr(y, ctypes.c_float))
+    return y
+
+
+def quantize_f32(y: np.ndarray, fmt: int, rowwise: bool = True, colwise: bool = True, with_dbias: bool = False):
+    """Quantize fp32 values [M,N]; returns (out_row, scale_row, out_col, scale_col, dbias) as quantize()."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    M, N = y.shape
+    out_row = np.empty((M, N), np.uint8) if rowwise else None
+    scale_row = np.empty((M, N // BLOCK), np.uint8) if rowwise else None
+    out_col = np.empty((M, N), np.uint8) if colwise else None
+    scale_col = np.empty((M // BLOCK, N), np.uint8) if colwise else None
+    dbias = np.empty((N,), np.float32) if with_dbias else None
+    rc = _load().mxo_quantize_f32(_ptr(y, ctypes.c_float), M, N, fmt, _ptr(out_row, ctypes.c_uint8),
+                                  _ptr(scale_row, ctypes.c_uint8), _ptr(out_col, ctypes.c_uint8),
+                                  _ptr(scale_col, ctypes.c_uint8), _ptr(dbias, ctypes.c_float))
+    if rc != 0:
+        raise ValueError("oracle: M, N must be non-negative multiples of 32")
+    return out_row, scale_row, out_col, scale_col, dbias
+
+
+def quantize_act(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True, colwise: bool = True,
+                 with_dbias: bool = False):
+    """Activation in fp32, then the MXFP8 cast of the fp32 values."""
+    return quantize_f32(activate(x_bits, act), fmt, rowwise, colwise, with_dbias)
+
+
+def activation_f64(v: float, act: int) -> float:
+    """Exact-as-double activation of one value (no fp32 rounding)."""
+    return float(_load().mxo_activation_f64(float(v), act))

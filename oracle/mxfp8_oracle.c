@@ -302,3 +302,113 @@ float mxo_amax(const uint16_t *x, int64_t M, int64_t N)
     }
     return (float)amax;
 }
+
+/*
+ * Fused activation before the cast (the `with_act` / `activation` fields of the
+ * config key on the PR #3137 page).  The pages do not give the formulas; the
+ * reading used: the activation is evaluated in fp32 (the value the cast then
+ * quantizes, and whose block amax sets the scale) from the BF16 input:
+ *   1 ReLU      x > 0 ? x : +0
+ *   2 SReLU     x > 0 ? x*x : +0            (squared ReLU, the FC1 epilogue of
+ *                                            the Lightning W4A16 page)
+ *   3 GeLU      x * sigmoid(2 sqrt(2/pi) (x + 0.044715 x^3))
+ *               (= 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), the tanh
+ *               form, written without the cancellation of 1 + tanh for x << 0)
+ *   4 SiLU      x * sigmoid(x)
+ *   5 QGeLU     x * sigmoid(1.702 x)
+ * with sigmoid(t) = 1 / (1 + e^-t) for t >= 0 and e^t / (1 + e^t) for t < 0
+ * (no overflow, no cancellation).  mxo_activation_f64 is the exact-as-double
+ * value; mxo_activation rounds it once to fp32: exact for ReLU and SReLU (a
+ * BF16 square has 16 significant bits), within an ulp or so of the GPU's fp32
+ * evaluation for the others.
+ */
+static double mxo_sigmoid(double t)
+{
+    if (t >= 0)
+        return 1.0 / (1.0 + exp(-t));
+    const double e = exp(t);
+    return e / (1.0 + e);
+}
+
+double mxo_activation_f64(double x, int act)
+{
+    switch (act) {
+    case 1: return x > 0 ? x : 0.0;
+    case 2: return x > 0 ? x * x : 0.0;
+    case 3: return x * mxo_sigmoid(2.0 * 0.7978845608028654 * (x + 0.044715 * x * x * x));
+    case 4: return x * mxo_sigmoid(x);
+    case 5: return x * mxo_sigmoid(1.702 * x);
+    default: return x;
+    }
+}
+
+float mxo_activation(double x, int act)
+{
+    return (float)mxo_activation_f64(x, act);
+}
+
+/*
+ * Quantize fp32 values y[M,N] (already activated): same blocks, scale rule
+ * and rounding as mxo_quantize, evaluated exactly on the fp32 values; dbias
+ * (if requested) is the column sum of y.
+ */
+int mxo_quantize_f32(const float *y, int64_t M, int64_t N, int fmt,
+                     uint8_t *out_row, uint8_t *scale_row,
+                     uint8_t *out_col, uint8_t *scale_col, float *dbias)
+{
+    int64_t i, j, c, r, k;
+    if (M < 0 || N < 0 || M % MXO_BLOCK || N % MXO_BLOCK)
+        return -1;
+    if (out_row && scale_row) {
+        for (i = 0; i < M; i++) {
+            for (c = 0; c < N / MXO_BLOCK; c++) {
+                const float *blk = y + i * N + c * MXO_BLOCK;
+                double amax = 0.0;
+                for (k = 0; k < MXO_BLOCK; k++)
+                    if (fabs((double)blk[k]) > amax)
+                        amax = fabs((double)blk[k]);
+                const int e = mxo_block_exponent(amax, fmt);
+                const double s = ldexp(1.0, 127 - e);
+                scale_row[i * (N / MXO_BLOCK) + c] = (uint8_t)e;
+                for (k = 0; k < MXO_BLOCK; k++)
+                    out_row[i * N + c * MXO_BLOCK + k] = mxo_fp8_encode((double)blk[k] * s, fmt);
+            }
+        }
+    }
+    if (out_col && scale_col) {
+        for (r = 0; r < M / MXO_BLOCK; r++) {
+            for (j = 0; j < N; j++) {
+                double amax = 0.0;
+                for (k = 0; k < MXO_BLOCK; k++) {
+                    const double a = fabs((double)y[(r * MXO_BLOCK + k) * N + j]);
+                    if (a > amax)
+                        amax = a;
+                }
+                const int e = mxo_block_exponent(amax, fmt);
+                const double s = ldexp(1.0, 127 - e);
+                scale_col[r * N + j] = (uint8_t)e;
+                for (k = 0; k < MXO_BLOCK; k++) {
+                    const int64_t idx = (r * MXO_BLOCK + k) * N + j;
+                    out_col[idx] = mxo_fp8_encode((double)y[idx] * s, fmt);
+                }
+            }
+        }
+    }
+    if (dbias) {
+        for (j = 0; j < N; j++) {
+            double acc = 0.0;
+            for (i = 0; i < M; i++)
+                acc += (double)y[i * N + j];
+            dbias[j] = (float)acc;
+        }
+    }
+    return 0;
+}
+
+/* y[i] = activation(x[i]) for a BF16 matrix, as fp32. */
+void mxo_activate(const uint16_t *x, int64_t n, int act, float *y)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        y[i] = mxo_activation(mxo_bf16_to_double(x[i]), act);
+}

@@ -353,3 +353,51 @@ def test_amax_matches_numpy(oracle_mod):
     xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
     assert oracle_mod.amax(x) == np.float32(np.abs(xv).max())
     assert oracle_mod.amax(np.zeros((32, 32), np.uint16)) == 0.0
+
+
+# ---- fused activation -----------------------------------------------------------
+
+def torch_act64(x64, act):
+    import torch.nn.functional as F
+    t = torch.from_numpy(x64)
+    if act == 1:
+        return torch.relu(t).numpy()
+    if act == 2:
+        return (torch.relu(t) ** 2).numpy()
+    if act == 3:
+        return F.gelu(t, approximate="tanh").numpy()
+    if act == 4:
+        return F.silu(t).numpy()
+    return (t * torch.sigmoid(1.702 * t)).numpy()
+
+
+@pytest.mark.parametrize("act", [1, 2, 3, 4, 5])
+def test_activation_matches_torch_float64(oracle_mod, act):
+    x = structured_input(64, 96, seed=act)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    want = torch_act64(xv, act).astype(np.float32)       # library routine in fp64, rounded once
+    got = oracle_mod.activate(x, act)
+    if act in (1, 2):
+        assert np.array_equal(got, want)                 # exact for ReLU and squared ReLU
+    else:
+        # torch evaluates GeLU as 0.5 x (1 + tanh(.)), which cancels for x << 0; the slack
+        # 1e-15 |x| covers that and still catches any wrong constant or formula
+        assert np.all(np.abs(got.astype(np.float64) - want) <= 2 ** -22 * np.abs(want) + 1e-15 * np.abs(xv) + 1e-38)
+    assert np.all(got[xv < 0] >= (-0.3 if act > 2 else 0.0))
+
+
+def test_act_none_quantize_f32_equals_bf16_path(oracle_mod):
+    x = structured_input(96, 64, seed=11)
+    y = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float().numpy()
+    a = oracle_mod.quantize(x, 0, with_dbias=True)
+    b = oracle_mod.quantize_f32(y, 0, with_dbias=True)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_relu_quantize_hand_checks(oracle_mod):
+    # a row block of -1 and +2 with ReLU: values 0 and 2, amax 2 -> e = ceil(log2(2/448)) + 127 = 120;
+    # 2 * 2^7 = 256 -> 0x78, zeros -> 0x00 (ReLU gives +0)
+    x = wl.to_bf16_bits(np.tile(np.array([-1.0, 2.0] * 16), (32, 1)))
+    o_row, s_row, _, _, _ = oracle_mod.quantize_act(x, 0, 1)
+    assert s_row[0, 0] == 120 and o_row[0, :2].tolist() == [0x00, 0x78]
