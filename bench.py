@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--shape", default=None, help="MxN: the workload's value recipe at another shape")
     ap.add_argument("--swizzled", action="store_true", help="write GEMM-ready (swizzled) scale planes")
     ap.add_argument("--amax", action="store_true", help="also write the per-tensor amax")
+    ap.add_argument("--act", default="none", help="activation before the cast: relu, srelu, gelu, silu, qgelu")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -272,8 +273,11 @@ def run_ours(args):
     out_col = torch.empty((M, N), dtype=torch.uint8, device="cuda")
     scale_col = torch.empty((mx.mxfp8_scale_bytes(N, M // 32, layout),), dtype=torch.uint8, device="cuda")
     amax = torch.empty((1,), dtype=torch.float32, device="cuda") if args.amax else None
-    if (args.swizzled or args.amax) and offsets is not None:
-        raise SystemExit("--swizzled / --amax apply to the flat workloads")
+    act = mx.binding.ACTIVATIONS[args.act.lower()]
+    if (args.swizzled or args.amax or act) and offsets is not None:
+        raise SystemExit("--swizzled / --amax / --act apply to the flat workloads")
+    if act and with_dbias:
+        raise SystemExit("--act does not combine with the dbias workload")
     dbias = torch.empty((N,), dtype=torch.float32, device="cuda") if with_dbias else None
     ws = (torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
           if with_dbias else None)
@@ -284,9 +288,9 @@ def run_ours(args):
         if grouped:
             st = mx.mxfp8_quantize_grouped(xin, M, N, off_dev.numel() - 1, off_dev, fmt, out_row, scale_row,
                                            out_col, scale_col, None, None, None, stream)
-        elif args.swizzled or args.amax:
+        elif args.swizzled or args.amax or act:
             cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
-                                 layout, amax)
+                                 layout, amax, act)
             st = mx.mxfp8_quantize_ex(cfg, stream)
         else:
             st = mx.mxfp8_quantize(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
@@ -377,7 +381,7 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped or args.swizzled or args.amax:
+        if grouped or args.swizzled or args.amax or act:
             # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
             path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"
@@ -430,6 +434,7 @@ def run_ours(args):
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "scales": "swizzled" if args.swizzled else "plain", "amax": bool(args.amax),
+                       "activation": args.act.lower(),
                        "bytes_per_step": algo_bytes,
                        "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
                               f"bf16 input; time = sum of the per-step event intervals" if flush else

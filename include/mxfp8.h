@@ -204,6 +204,27 @@ typedef enum {
 size_t mxfp8_scale_bytes(int64_t rows, int64_t scale_cols, int scale_layout);
 
 /*
+ * Activation applied to every element before the cast (the `with_act` /
+ * `activation` fields of the PR #3137 config key).  It is evaluated in fp32
+ * from the BF16 input; the block amax, the scales and the FP8 codes are those
+ * of the fp32 activations, and amax (if requested) is max |act(x)|.
+ *   RELU   x > 0 ? x : +0          SRELU  x > 0 ? x*x : +0   (squared ReLU)
+ *   GELU   x * sigmoid(2 sqrt(2/pi) (x + 0.044715 x^3))      (tanh form)
+ *   SILU   x * sigmoid(x)          QGELU  x * sigmoid(1.702 x)
+ * sigmoid(t) is computed as 1/(1+e) or e/(1+e), e = exp(-|t|).  ReLU and SReLU
+ * are exact; the others are within a few fp32 ulps of the exact function.
+ * Not combinable with dbias (MXFP8_ERR_FORMAT).
+ */
+typedef enum {
+    MXFP8_ACT_NONE = 0,
+    MXFP8_ACT_RELU = 1,
+    MXFP8_ACT_SRELU = 2,
+    MXFP8_ACT_GELU = 3,
+    MXFP8_ACT_SILU = 4,
+    MXFP8_ACT_QGELU = 5
+} mxfp8_activation_t;
+
+/*
  * Options of mxfp8_quantize_ex: the fields of the quantization config key on
  * the PR #3137 page (fp8_dtype, rowwise, colwise, swizzled, with_amax,
  * with_dbias, with_noop) as one struct.  Zero-initialise it and set what is
@@ -222,7 +243,8 @@ typedef struct mxfp8_quantize_config {
     const float *noop;     /* device fp32 scalar or NULL */
     int scale_layout;      /* mxfp8_scale_layout_t */
     float *amax;           /* device fp32 scalar or NULL: receives max |x| over the tensor */
-    int reserved[6];       /* must be 0 */
+    int activation;        /* mxfp8_activation_t applied to x before the cast */
+    int reserved[5];       /* must be 0 */
 } mxfp8_quantize_config_t;
 
 /*
@@ -230,9 +252,11 @@ typedef struct mxfp8_quantize_config {
  * MXFP8_SCALES_SWIZZLED the scale planes are written in the GEMM-ready
  * layout; swizzled scale pointers need no alignment.  amax, if set, is a
  * device fp32 written with the largest |x| of the tensor (4-byte aligned;
- * noop leaves it untouched like every other output).  Returns the status
- * codes of mxfp8_quantize, plus MXFP8_ERR_FORMAT for an unknown layout or a
- * non-zero reserved field, and MXFP8_ERR_NULL for cfg == NULL.
+ * noop leaves it untouched like every other output).  activation applies an
+ * mxfp8_activation_t before the cast.  Returns the status codes of
+ * mxfp8_quantize, plus MXFP8_ERR_FORMAT for an unknown layout or activation,
+ * an activation with dbias, or a non-zero reserved field, and MXFP8_ERR_NULL
+ * for cfg == NULL.
  */
 mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream);
 

@@ -37,7 +37,10 @@ class QuantizeConfig(ctypes.Structure):
                 ("out_row", ctypes.c_void_p), ("scale_row", ctypes.c_void_p), ("out_col", ctypes.c_void_p),
                 ("scale_col", ctypes.c_void_p), ("dbias", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("noop", ctypes.c_void_p), ("scale_layout", ctypes.c_int), ("amax", ctypes.c_void_p),
-                ("reserved", ctypes.c_int * 6)]
+                ("activation", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "srelu": 2, "gelu": 3, "silu": 4, "qgelu": 5}
 
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libmxfp8.so")
@@ -149,11 +152,13 @@ def mxfp8_quantize_ex(cfg: QuantizeConfig, stream=None) -> int:
 
 
 def make_config(x, M, N, fp8_fmt, out_row=None, scale_row=None, out_col=None, scale_col=None, dbias=None,
-                workspace=None, noop=None, scale_layout=SCALES_PLAIN, amax=None) -> QuantizeConfig:
+                workspace=None, noop=None, scale_layout=SCALES_PLAIN, amax=None, activation=0) -> QuantizeConfig:
     """A QuantizeConfig from tensors / addresses / None (marshalling only)."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
     return QuantizeConfig(_addr(x), M, N, fp8_fmt, _addr(out_row), _addr(scale_row), _addr(out_col),
                           _addr(scale_col), _addr(dbias), _addr(workspace), _addr(noop), scale_layout,
-                          _addr(amax), (ctypes.c_int * 6)())
+                          _addr(amax), int(activation), (ctypes.c_int * 5)())
 
 
 def mxfp8_status_string(status: int) -> str:
@@ -203,12 +208,14 @@ def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool):
 def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
              with_dbias: bool = False, noop: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, stream=None, swizzled: bool = False,
-             with_amax: bool = False) -> MXFP8Tensor:
+             with_amax: bool = False, activation="none") -> MXFP8Tensor:
     """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (M, N multiples of 32).
 
     ``swizzled`` writes both scale planes in the GEMM-ready layout (1-D tensors of
-    mxfp8_scale_bytes bytes); ``with_amax`` also returns max |x| as a float32 [1].
+    mxfp8_scale_bytes bytes); ``with_amax`` also returns max |x| as a float32 [1];
+    ``activation`` ("relu", "srelu", "gelu", "silu", "qgelu") is applied before the cast.
     """
+    act = ACTIVATIONS[activation.lower()] if isinstance(activation, str) else int(activation)
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
     M, N = x.shape
@@ -226,10 +233,10 @@ def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = Tr
     if with_dbias and workspace is None:
         nbytes = mxfp8_quantize_workspace_bytes(M, N, True)
         workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
-    if swizzled or with_amax:
+    if swizzled or with_amax or act:
         cfg = make_config(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,
                           workspace if with_dbias else None, noop,
-                          SCALES_SWIZZLED if swizzled else SCALES_PLAIN, amax)
+                          SCALES_SWIZZLED if swizzled else SCALES_PLAIN, amax, act)
         st = mxfp8_quantize_ex(cfg, stream)
     else:
         st = mxfp8_quantize(x, M, N, f, out_row, scale_row, out_col, scale_col, dbias,

@@ -26,7 +26,7 @@ std::atomic<uint64_t> g_launches{0};
 struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
-    int ctas_per_sm[32] = {};  // indexed by kernel variant
+    int ctas_per_sm[192] = {};  // indexed by kernel variant
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -64,15 +64,15 @@ bool on_device(const void *p, int device)
     return a.type == cudaMemoryTypeDevice && a.device == device;
 }
 
-template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX, int ACT>
 int variant_index()
 {
-    return FMT + 2 * (DBIAS ? 1 : 0) + 4 * (GROUPED ? 1 : 0) + 8 * (SWZ ? 1 : 0) + 16 * (AMAX ? 1 : 0);
+    return FMT + 2 * (DBIAS ? 1 : 0) + 4 * (GROUPED ? 1 : 0) + 8 * (SWZ ? 1 : 0) + 16 * (AMAX ? 1 : 0) + 32 * ACT;
 }
 
 // One-time per (device, variant) set-up: opt in to the large shared-memory
 // carve-out and record how many CTAs fit per SM.
-template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX, int ACT>
 mxfp8_status_t prepare(int device, int *grid_cap)
 {
     std::lock_guard<std::mutex> lock(g_dev_mu);
@@ -84,10 +84,10 @@ mxfp8_status_t prepare(int device, int *grid_cap)
             return MXFP8_ERR_DEVICE;
         d.ready = true;
     }
-    const int v = variant_index<FMT, DBIAS, GROUPED, SWZ, AMAX>();
+    const int v = variant_index<FMT, DBIAS, GROUPED, SWZ, AMAX, ACT>();
     if (d.ctas_per_sm[v] == 0) {
         const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
-        auto kern = quantize_kernel<FMT, DBIAS, GROUPED, SWZ, AMAX>;
+        auto kern = quantize_kernel<FMT, DBIAS, GROUPED, SWZ, AMAX, ACT>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return MXFP8_ERR_LAUNCH;
         int n = 0;
@@ -135,21 +135,21 @@ mxfp8_status_t current_device(int *device)
     return MXFP8_OK;
 }
 
-template <bool DBIAS, bool GROUPED, bool SWZ = false, bool AMAX = false>
+template <bool DBIAS, bool GROUPED, bool SWZ = false, bool AMAX = false, int ACT = 0>
 mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, const QuantParams &p,
                                int64_t tile_bound, cudaStream_t stream)
 {
     int cap = 0;
-    mxfp8_status_t st = fmt == MXFP8_E4M3 ? prepare<0, DBIAS, GROUPED, SWZ, AMAX>(device, &cap)
-                                          : prepare<1, DBIAS, GROUPED, SWZ, AMAX>(device, &cap);
+    mxfp8_status_t st = fmt == MXFP8_E4M3 ? prepare<0, DBIAS, GROUPED, SWZ, AMAX, ACT>(device, &cap)
+                                          : prepare<1, DBIAS, GROUPED, SWZ, AMAX, ACT>(device, &cap);
     if (st != MXFP8_OK)
         return st;
     const int grid = static_cast<int>(tile_bound < cap ? tile_bound : cap);
     const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
     if (fmt == MXFP8_E4M3)
-        quantize_kernel<0, DBIAS, GROUPED, SWZ, AMAX><<<grid, kThreads, smem, stream>>>(map, p);
+        quantize_kernel<0, DBIAS, GROUPED, SWZ, AMAX, ACT><<<grid, kThreads, smem, stream>>>(map, p);
     else
-        quantize_kernel<1, DBIAS, GROUPED, SWZ, AMAX><<<grid, kThreads, smem, stream>>>(map, p);
+        quantize_kernel<1, DBIAS, GROUPED, SWZ, AMAX, ACT><<<grid, kThreads, smem, stream>>>(map, p);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
@@ -185,9 +185,22 @@ __global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const 
 // Enqueue the flat quantize kernel (no validation: the caller has checked every
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
+// Activated (ACT != 0) variants: flat, no dbias; swizzle and amax as template switches.
+template <int ACT>
+mxfp8_status_t launch_activated(int opts, int fmt, int device, const CUtensorMap &map, const QuantParams &p,
+                                int64_t tiles, cudaStream_t stream)
+{
+    switch (opts) {
+    case 0: return launch_quantize<false, false, false, false, ACT>(fmt, device, map, p, tiles, stream);
+    case 1: return launch_quantize<false, false, true, false, ACT>(fmt, device, map, p, tiles, stream);
+    case 2: return launch_quantize<false, false, false, true, ACT>(fmt, device, map, p, tiles, stream);
+    default: return launch_quantize<false, false, true, true, ACT>(fmt, device, map, p, tiles, stream);
+    }
+}
+
 mxfp8_status_t enqueue_flat(int device, int fmt, const void *x, int64_t M, int64_t N, void *out_row,
                             void *scale_row, void *out_col, void *scale_col, float *ws, const float *noop,
-                            cudaStream_t stream, bool swizzled = false, float *amax = nullptr)
+                            cudaStream_t stream, bool swizzled = false, float *amax = nullptr, int act = 0)
 {
     CUtensorMap map;
     mxfp8_status_t st = make_tensor_map(&map, x, M, N);
@@ -208,6 +221,18 @@ mxfp8_status_t enqueue_flat(int device, int fmt, const void *x, int64_t M, int64
     p.amax = amax;
     const int64_t tiles = row_tiles * col_tiles;
     const int opts = (swizzled ? 1 : 0) + (amax != nullptr ? 2 : 0);
+    if (act != MXFP8_ACT_NONE) {
+        if (ws != nullptr)
+            return MXFP8_ERR_FORMAT;
+        switch (act) {
+        case MXFP8_ACT_RELU: return launch_activated<1>(opts, fmt, device, map, p, tiles, stream);
+        case MXFP8_ACT_SRELU: return launch_activated<2>(opts, fmt, device, map, p, tiles, stream);
+        case MXFP8_ACT_GELU: return launch_activated<3>(opts, fmt, device, map, p, tiles, stream);
+        case MXFP8_ACT_SILU: return launch_activated<4>(opts, fmt, device, map, p, tiles, stream);
+        case MXFP8_ACT_QGELU: return launch_activated<5>(opts, fmt, device, map, p, tiles, stream);
+        default: return MXFP8_ERR_FORMAT;
+        }
+    }
     if (ws != nullptr) {
         switch (opts) {
         case 0: return launch_quantize<true, false, false, false>(fmt, device, map, p, tiles, stream);
@@ -317,7 +342,10 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
             return MXFP8_ERR_FORMAT;
     if (cfg->scale_layout != MXFP8_SCALES_PLAIN && cfg->scale_layout != MXFP8_SCALES_SWIZZLED)
         return MXFP8_ERR_FORMAT;
-    if (cfg->scale_layout == MXFP8_SCALES_PLAIN && cfg->amax == nullptr)
+    if (cfg->activation < MXFP8_ACT_NONE || cfg->activation > MXFP8_ACT_QGELU ||
+        (cfg->activation != MXFP8_ACT_NONE && cfg->dbias != nullptr))
+        return MXFP8_ERR_FORMAT;
+    if (cfg->scale_layout == MXFP8_SCALES_PLAIN && cfg->amax == nullptr && cfg->activation == MXFP8_ACT_NONE)
         return mxfp8_quantize(cfg->x, cfg->M, cfg->N, cfg->fp8_fmt, cfg->out_row, cfg->scale_row, cfg->out_col,
                               cfg->scale_col, cfg->dbias, cfg->workspace, cfg->noop, stream_);
 
@@ -375,7 +403,7 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
     if (!empty) {
         st = enqueue_flat(device, cfg->fp8_fmt, cfg->x, M, N, cfg->out_row, cfg->scale_row, cfg->out_col,
                           cfg->scale_col, cfg->dbias != nullptr ? static_cast<float *>(cfg->workspace) : nullptr,
-                          cfg->noop, stream, swz, cfg->amax);
+                          cfg->noop, stream, swz, cfg->amax, cfg->activation);
         if (st != MXFP8_OK)
             return st;
     }

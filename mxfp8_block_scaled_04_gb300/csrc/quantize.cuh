@@ -100,6 +100,67 @@ __device__ __forceinline__ int block_exponent(uint32_t amax_bits)
     return amax_bits == 0 ? 127 : e;
 }
 
+// Same rule for an fp32 amax (the activated path): amax = (1 + m/2^23) 2^(E-127),
+// ceil(log2(amax/Fmax)) = E - 127 - emax + [m > 0.75 * 2^23]; subnormal -> 0.
+template <int FMT>
+__device__ __forceinline__ int block_exponent_f32(uint32_t amax_bits)
+{
+    constexpr int kEmax = FMT == 0 ? 8 : 15;
+    int e = static_cast<int>(amax_bits >> 23) - kEmax + ((amax_bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = e < 0 ? 0 : e;
+    return amax_bits == 0 ? 127 : e;
+}
+
+// Activation applied to each input before the cast (fp32): 1 ReLU, 2 squared
+// ReLU, 3 GeLU (tanh form, as x * sigmoid(2 sqrt(2/pi) (x + 0.044715 x^3))),
+// 4 SiLU, 5 QGeLU (x * sigmoid(1.702 x)).  The sigmoid is 1 / (1 + e) or
+// e / (1 + e) with e = 2^(-|t| log2 e): no overflow and no cancellation for
+// large |t|.  It uses the hardware ex2 / rcp approximations (a few ulps; no
+// flush to zero), which the parity tests allow for at decision boundaries.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int ACT>
+__device__ __forceinline__ float activation(float x)
+{
+    if constexpr (ACT == 1) {
+        return x > 0.f ? x : 0.f;
+    } else if constexpr (ACT == 2) {
+        return x > 0.f ? x * x : 0.f;
+    } else {
+        float t;
+        if constexpr (ACT == 3)
+            t = 1.5957691216057308f * (x + 0.044715f * x * x * x);
+        else if constexpr (ACT == 4)
+            t = x;
+        else
+            t = 1.702f * x;
+        const float e = ex2_approx(-1.4426950408889634f * fabsf(t));
+        const float r = rcp_approx(1.f + e);
+        return x * (t >= 0.f ? r : e * r);
+    }
+}
+
+// Largest |act(x)| over x <= 0 (the activations above are monotone increasing for
+// x > 0, and bounded in magnitude by this for x <= 0): SiLU's minimum is
+// -0.2785 at x = -1.278; GeLU's and QGeLU's are smaller; ReLU's is 0.
+template <int ACT>
+__device__ __forceinline__ float negative_side_bound()
+{
+    return ACT <= 2 ? 0.f : 0.2785f * 1.01f;
+}
+
 // 2^(127 - e) as fp32, for 0 <= e <= 253.
 __device__ __forceinline__ float scale_multiplier(int e)
 {
@@ -206,9 +267,10 @@ __device__ __forceinline__ int grouped_setup(const QuantParams &p, int64_t *goff
     return total;
 }
 
-// SWZ: scale planes in the GEMM-ready layout; AMAX: also produce max |x|.  Both are
-// template switches so the default variant carries no code for them.
-template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX>
+// SWZ: scale planes in the GEMM-ready layout; AMAX: also produce max |x|; ACT: an
+// activation applied before the cast (0 = none).  All are template switches so the
+// default variant carries no code for them.
+template <int FMT, bool DBIAS, bool GROUPED, bool SWZ, bool AMAX, int ACT = 0>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p)
 {
@@ -274,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             issue(s, first + s * stride);
     }
 
-    uint32_t amax_acc = 0;  // running max |x| as BF16 bits (amax output only)
+    uint32_t amax_acc = 0;  // running max |value| as fp32 bits (amax output only)
     for (int it = 0; it < my_count; ++it) {
         const int slot = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
@@ -297,23 +359,73 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int rb = warp >> 1, box = warp & 1;
             const int cq = lane & 15, half = lane >> 4;   // 4-column group, 16-row half
             const unsigned char *base = stage + box * kBoxBytes + (rb * 32 + half * 16) * 128 + (cq & 1) * 8;
-            uint32_t mx0 = 0, mx1 = 0;
             float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+            int e0, e1, e2, e3;
+            uint32_t amax_bits;  // fp32 bits of the largest of the four column amaxes
+            if constexpr (ACT == 0) {
+                uint32_t mx0 = 0, mx1 = 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                // row r = rb*32 + half*16 + i has (r & 7) == (i & 7): 128B swizzle
-                const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
-                mx0 = max_u16x2(mx0, v.x & 0x7FFF7FFFu);
-                mx1 = max_u16x2(mx1, v.y & 0x7FFF7FFFu);
-                if constexpr (DBIAS) {
-                    d0 += bf16_lo(v.x);
-                    d1 += bf16_hi(v.x);
-                    d2 += bf16_lo(v.y);
-                    d3 += bf16_hi(v.y);
+                for (int i = 0; i < 16; ++i) {
+                    // row r = rb*32 + half*16 + i has (r & 7) == (i & 7): 128B swizzle
+                    const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
+                    mx0 = max_u16x2(mx0, v.x & 0x7FFF7FFFu);
+                    mx1 = max_u16x2(mx1, v.y & 0x7FFF7FFFu);
+                    if constexpr (DBIAS) {
+                        d0 += bf16_lo(v.x);
+                        d1 += bf16_hi(v.x);
+                        d2 += bf16_lo(v.y);
+                        d3 += bf16_hi(v.y);
+                    }
                 }
+                mx0 = max_u16x2(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
+                mx1 = max_u16x2(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
+                e0 = block_exponent<FMT>(mx0 & 0xFFFFu);
+                e1 = block_exponent<FMT>(mx0 >> 16);
+                e2 = block_exponent<FMT>(mx1 & 0xFFFFu);
+                e3 = block_exponent<FMT>(mx1 >> 16);
+                amax_bits = max(max(mx0 & 0xFFFFu, mx0 >> 16), max(mx1 & 0xFFFFu, mx1 >> 16)) << 16;
+            } else {
+                // On x > 0 every activation here is increasing, so a column's amax is
+                // act(max x) whenever that exceeds anything x <= 0 can give; ReLU and
+                // squared ReLU give 0 for x <= 0, so for them this is always exact.
+                float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
+                    xm[0] = fmaxf(xm[0], bf16_lo(v.x));
+                    xm[1] = fmaxf(xm[1], bf16_hi(v.x));
+                    xm[2] = fmaxf(xm[2], bf16_lo(v.y));
+                    xm[3] = fmaxf(xm[3], bf16_hi(v.y));
+                }
+                float f[4];
+                bool slow = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    xm[k] = fmaxf(xm[k], __shfl_xor_sync(0xffffffffu, xm[k], 16));
+                    f[k] = xm[k] > 0.f ? activation<ACT>(xm[k]) : 0.f;
+                    slow |= ACT > 2 && f[k] < negative_side_bound<ACT>();
+                }
+                if (__any_sync(0xffffffffu, slow)) {
+                    // some column's amax may come from its negative entries: evaluate them all
+                    float g[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
+                        g[0] = fmaxf(g[0], fabsf(activation<ACT>(bf16_lo(v.x))));
+                        g[1] = fmaxf(g[1], fabsf(activation<ACT>(bf16_hi(v.x))));
+                        g[2] = fmaxf(g[2], fabsf(activation<ACT>(bf16_lo(v.y))));
+                        g[3] = fmaxf(g[3], fabsf(activation<ACT>(bf16_hi(v.y))));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        f[k] = fmaxf(g[k], __shfl_xor_sync(0xffffffffu, g[k], 16));
+                }
+                e0 = block_exponent_f32<FMT>(__float_as_uint(f[0]));
+                e1 = block_exponent_f32<FMT>(__float_as_uint(f[1]));
+                e2 = block_exponent_f32<FMT>(__float_as_uint(f[2]));
+                e3 = block_exponent_f32<FMT>(__float_as_uint(f[3]));
+                amax_bits = __float_as_uint(fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3])));
             }
-            mx0 = max_u16x2(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
-            mx1 = max_u16x2(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
             if constexpr (DBIAS) {
                 // 32-row column sums; a + b == b + a, so both halves agree bit for bit
                 d0 += __shfl_xor_sync(0xffffffffu, d0, 16);
@@ -321,12 +433,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 d2 += __shfl_xor_sync(0xffffffffu, d2, 16);
                 d3 += __shfl_xor_sync(0xffffffffu, d3, 16);
             }
-            const int e0 = block_exponent<FMT>(mx0 & 0xFFFFu), e1 = block_exponent<FMT>(mx0 >> 16);
-            const int e2 = block_exponent<FMT>(mx1 & 0xFFFFu), e3 = block_exponent<FMT>(mx1 >> 16);
             const int64_t gcol = tc.col0 + box * kBoxCols + cq * 4;
             const int64_t grow = tc.row0 + rb * 32;
             if (AMAX && gcol < N)
-                amax_acc = max(amax_acc, max(max(mx0 & 0xFFFFu, mx0 >> 16), max(mx1 & 0xFFFFu, mx1 >> 16)));
+                amax_acc = max(amax_acc, amax_bits);
             if (half == 0) {
                 if (do_col && gcol < N && grow < tc.row_end) {
                     if constexpr (!SWZ) {
@@ -395,21 +505,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int64_t grow = tc.row0 + r;
                 const int64_t gcol = tc.col0 + box * kBoxCols + sp * 16;
                 const bool in = grow < tc.row_end && gcol < N;
-                if (do_row) {
-                    uint32_t m = 0;
+                // the 16 values of the segment: the BF16 inputs, or their fp32 activations
+                float y[16];
+                if constexpr (ACT != 0) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
-                    uint32_t a = max(m & 0xFFFFu, m >> 16);
-                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-                    const int er = block_exponent<FMT>(a);
+                    for (int j = 0; j < 8; ++j) {
+                        y[2 * j] = activation<ACT>(bf16_lo(w[j]));
+                        y[2 * j + 1] = activation<ACT>(bf16_hi(w[j]));
+                    }
+                }
+                auto val = [&](int i) -> float {
+                    if constexpr (ACT == 0)
+                        return (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+                    else
+                        return y[i];
+                };
+                if (do_row) {
+                    int er;
+                    uint32_t row_amax_bits;  // fp32 bits
+                    if constexpr (ACT == 0) {
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
+                        uint32_t a = max(m & 0xFFFFu, m >> 16);
+                        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                        er = block_exponent<FMT>(a);
+                        row_amax_bits = a << 16;
+                    } else {
+                        float fm = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            fm = fmaxf(fm, fabsf(y[i]));
+                        fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, 1));
+                        er = block_exponent_f32<FMT>(__float_as_uint(fm));
+                        row_amax_bits = __float_as_uint(fm);
+                    }
                     const float rm = scale_multiplier(er);
                     uint32_t o[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t lo = cvt_fp8x2<FMT>(bf16_lo(w[2 * j]) * rm, bf16_hi(w[2 * j]) * rm);
-                        const uint32_t hi =
-                            cvt_fp8x2<FMT>(bf16_lo(w[2 * j + 1]) * rm, bf16_hi(w[2 * j + 1]) * rm);
+                        const uint32_t lo = cvt_fp8x2<FMT>(val(4 * j) * rm, val(4 * j + 1) * rm);
+                        const uint32_t hi = cvt_fp8x2<FMT>(val(4 * j + 2) * rm, val(4 * j + 3) * rm);
                         o[j] = lo | (hi << 16);
                     }
                     if (in) {
@@ -418,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, N >> 5)
                                             : grow * (N >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
                         if (AMAX && !do_col)
-                            amax_acc = max(amax_acc, a);
+                            amax_acc = max(amax_acc, row_amax_bits);
                     }
                 }
                 if (do_col) {
@@ -427,9 +564,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
-                        const uint32_t lo = cvt_fp8x2<FMT>(bf16_lo(w[2 * j]) * c.x, bf16_hi(w[2 * j]) * c.y);
-                        const uint32_t hi =
-                            cvt_fp8x2<FMT>(bf16_lo(w[2 * j + 1]) * c.z, bf16_hi(w[2 * j + 1]) * c.w);
+                        const uint32_t lo = cvt_fp8x2<FMT>(val(4 * j) * c.x, val(4 * j + 1) * c.y);
+                        const uint32_t hi = cvt_fp8x2<FMT>(val(4 * j + 2) * c.z, val(4 * j + 3) * c.w);
                         o[j] = lo | (hi << 16);
                     }
                     if (in)
@@ -448,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // fp32 bits of a non-negative value order like the value itself
         const uint32_t m = __reduce_max_sync(0xffffffffu, amax_acc);
         if (lane == 0 && m != 0)
-            atomicMax(reinterpret_cast<unsigned int *>(p.amax), m << 16);
+            atomicMax(reinterpret_cast<unsigned int *>(p.amax), m);
     }
 }
 

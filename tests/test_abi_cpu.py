@@ -129,7 +129,7 @@ def test_config_struct_layout_matches_the_c_header(tmp_path):
                    '#define F(f) printf(" %zu", offsetof(mxfp8_quantize_config_t, f));\n'
                    'int main(void){ printf("%zu", sizeof(mxfp8_quantize_config_t));\n'
                    'F(x) F(M) F(N) F(fp8_fmt) F(out_row) F(scale_row) F(out_col) F(scale_col) F(dbias) F(workspace)'
-                   ' F(noop) F(scale_layout) F(amax) F(reserved) return 0; }\n')
+                   ' F(noop) F(scale_layout) F(amax) F(activation) F(reserved) return 0; }\n')
     exe = tmp_path / "probe"
     subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
     c_vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
@@ -155,5 +155,8 @@ def test_ex_rejections(cuda_lib):
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 48, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, None, A, A, A, scale_layout=1), 0) == NULL
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1, amax=A + 2), 0) == ALIGN
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, activation=6), 0) == FORMAT
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, dbias=A, workspace=A,
+                                               activation="gelu"), 0) == FORMAT
     # swizzled scale planes need no alignment: an odd scale pointer reaches the device stage
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A + 1, A, A + 1, scale_layout=1), 0) == DEVICE

@@ -1,0 +1,135 @@
+"""Fused activation before the cast (mxfp8_quantize_ex with `activation`), on the GPU.
+
+ReLU and squared ReLU are exact in fp32, so FP8 codes and scales must be
+bit-exact with the oracle.  GeLU, SiLU and QGeLU involve exp: the kernel's
+fp32 value and the oracle's (the double value rounded once to fp32) can differ
+by a few fp32 ulps, so where the exact value sits on a decision boundary the
+two sides may legitimately decide differently.  A code may differ from the
+oracle's only if the exact (double) scaled value lies within 2^-20 (relative)
+of the midpoint between the two codes, or the fp32 value is subnormal (fewer
+significant bits on both sides); a scale byte may differ by one only if the
+block's exact amax lies within 2^-20 of the power-of-two boundary between the
+two exponents, and then the block's codes are checked against the oracle's
+rounding at the GPU's exponent.  At most 1e-4 of the codes may use the rule.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_block_scaled_04_gb300 as mx
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+FMAX = {0: 448.0, 1: 57344.0}
+TOL = 2.0 ** -20
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def act_input(M, N, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal((M, N)) * np.exp2(rng.integers(-6, 6, (M, 1)))
+    a[0, :32] = -np.abs(a[0, :32]) * 8          # a block that the activations squash to tiny values
+    a[1, :64] = 0.0
+    a[2, 32:64] = rng.standard_normal(32) * 1e-39
+    a[5, 7] = 60.0
+    return wl.to_bf16_bits(a)
+
+
+def x_values(x_bits):
+    return torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, x_bits, act, fmt, colwise):
+    """Compare one direction; returns how many codes needed the boundary rule."""
+    M, N = x_bits.shape
+    xv = x_values(x_bits)
+    y32 = oracle_mod.activate(x_bits, act)
+    exact = act in (1, 2)
+    if exact:
+        assert np.array_equal(gpu_scales, ref_scales)
+        assert np.array_equal(gpu_codes, ref_codes)
+        return 0
+
+    def block_of(i, j):   # element indices of the block holding (i, j)
+        if colwise:
+            r0 = (i // 32) * 32
+            return [(r, j) for r in range(r0, r0 + 32)]
+        c0 = (j // 32) * 32
+        return [(i, c) for c in range(c0, c0 + 32)]
+
+    used = 0
+    expected = ref_codes.copy()
+    # scale bytes that differ: exact amax must sit on the boundary between the two exponents
+    for s_idx in np.argwhere(gpu_scales != ref_scales):
+        s_idx = tuple(s_idx)
+        eg, eo = int(gpu_scales[s_idx]), int(ref_scales[s_idx])
+        assert abs(eg - eo) == 1, (s_idx, eg, eo)
+        i, j = (s_idx[0] * 32, s_idx[1]) if colwise else (s_idx[0], s_idx[1] * 32)
+        elems = block_of(i, j)
+        amax64 = max(abs(oracle_mod.activation_f64(xv[e], act)) for e in elems)
+        boundary = FMAX[fmt] * 2.0 ** (min(eg, eo) - 127)
+        assert abs(amax64 - boundary) <= TOL * boundary, (s_idx, amax64, boundary)
+        for e in elems:   # this block's codes at the GPU's exponent
+            expected[e] = oracle_mod.fp8_encode(float(y32[e]) * 2.0 ** (127 - eg), fmt)
+        used += 32
+    for e in np.argwhere(gpu_codes != expected):
+        e = tuple(e)
+        i, j = e
+        sc = int(gpu_scales[i // 32, j] if colwise else gpu_scales[i, j // 32])
+        v64 = oracle_mod.activation_f64(xv[e], act) * 2.0 ** (127 - sc)
+        dg = oracle_mod.fp8_decode(int(gpu_codes[e]), fmt)
+        do = oracle_mod.fp8_decode(int(expected[e]), fmt)
+        mid = (dg + do) / 2
+        subnormal_y = abs(float(y32[e])) < 2.0 ** -126
+        assert subnormal_y or abs(v64 - mid) <= TOL * max(abs(v64), 2.0 ** -20), (e, v64, dg, do)
+        used += 1
+    assert used <= max(1e-4 * M * N, 64), used
+    return used
+
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_activation_parity(oracle_mod, act, fmt):
+    M, N = 544, 1056
+    x_bits = act_input(M, N, seed=len(act) * 7 + fmt)
+    a = mx.binding.ACTIVATIONS[act]
+    r = mx.quantize(dev(x_bits), fmt, activation=act, with_amax=True)
+    torch.cuda.synchronize()
+    o = oracle_mod.quantize_act(x_bits, fmt, a)
+    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], x_bits, a, fmt, False)
+    check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], x_bits, a, fmt, True)
+    amax_ref = float(np.abs(oracle_mod.activate(x_bits, a)).max())
+    if a in (1, 2):
+        assert float(r.amax.item()) == amax_ref
+    else:
+        assert math.isclose(float(r.amax.item()), amax_ref, rel_tol=2 ** -20)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+def test_activation_swizzled_single_direction(oracle_mod, act):
+    M, N = 256, 160
+    x_bits = act_input(M, N, seed=99)
+    a = mx.binding.ACTIVATIONS[act]
+    r = mx.quantize(dev(x_bits), 0, rowwise=True, colwise=False, activation=act, swizzled=True)
+    torch.cuda.synchronize()
+    o = oracle_mod.quantize_act(x_bits, 0, a, rowwise=True, colwise=False)
+    plain = r.scale_row.cpu().numpy()
+    # unswizzle through the oracle's layout to compare with the plain scales
+    want_swz = oracle_mod.swizzle_scales(o[1])
+    if a == 1:
+        assert np.array_equal(plain, want_swz) and np.array_equal(r.out_row.cpu().numpy(), o[0])
+    else:
+        assert np.mean(plain == want_swz) > 0.999
+        assert np.mean(r.out_row.cpu().numpy() == o[0]) > 0.999
+
+
+def test_activation_with_dbias_is_rejected():
+    x = dev(act_input(64, 64, seed=1))
+    with pytest.raises(mx.MXFP8Error):
+        mx.quantize(x, 0, with_dbias=True, activation="relu")
