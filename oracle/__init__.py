@@ -126,21 +126,22 @@ def quantize(x_bits: np.ndarray, fmt: int, rowwise: bool = True, colwise: bool =
 
     Returns ``(out_row, scale_row, out_col, scale_col, dbias)``; entries for a
     direction that was not requested are None.  Shapes: out_* [M,N] uint8,
-    scale_row [M,N/32], scale_col [M/32,N] uint8, dbias [N] float32.
+    scale_row [M,ceil(N/32)], scale_col [ceil(M/32),N] uint8, dbias [N] float32
+    (a last, partial block takes its amax over the elements it has).
     """
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     M, N = x.shape
     out_row = np.empty((M, N), np.uint8) if rowwise else None
-    scale_row = np.empty((M, N // BLOCK), np.uint8) if rowwise else None
+    scale_row = np.empty((M, -(-N // BLOCK)), np.uint8) if rowwise else None
     out_col = np.empty((M, N), np.uint8) if colwise else None
-    scale_col = np.empty((M // BLOCK, N), np.uint8) if colwise else None
+    scale_col = np.empty((-(-M // BLOCK), N), np.uint8) if colwise else None
     dbias = np.empty((N,), np.float32) if with_dbias else None
     rc = _load().mxo_quantize(_ptr(x, ctypes.c_uint16), M, N, fmt,
                               _ptr(out_row, ctypes.c_uint8), _ptr(scale_row, ctypes.c_uint8),
                               _ptr(out_col, ctypes.c_uint8), _ptr(scale_col, ctypes.c_uint8),
                               _ptr(dbias, ctypes.c_float))
     if rc != 0:
-        raise ValueError(f"oracle: M={M}, N={N} must be non-negative multiples of {BLOCK}")
+        raise ValueError(f"oracle: M={M}, N={N} must be non-negative")
     return out_row, scale_row, out_col, scale_col, dbias
 
 

@@ -160,52 +160,62 @@ double mxo_e8m0_decode(uint8_t e)
 
 /*
  * Flat quantize of x[M,N] (BF16 bits, row-major).  Any of the four output
- * pairs may be NULL to skip that direction; dbias may be NULL.
- *   out_row[i*N + j], scale_row[i*(N/32) + j/32]   (1x32 blocks along a row)
- *   out_col[i*N + j], scale_col[(i/32)*N + j]      (32x1 blocks down a column)
- * Returns 0, or -1 if M or N is not a non-negative multiple of 32.
+ * pairs may be NULL to skip that direction; dbias may be NULL.  With
+ * Cr = ceil(N/32) and Rc = ceil(M/32):
+ *   out_row[i*N + j], scale_row[i*Cr + j/32]   (1x32 blocks along a row)
+ *   out_col[i*N + j], scale_col[(i/32)*N + j]  (32x1 blocks down a column)
+ * When N (or M) is not a multiple of 32 the last block of each row (column)
+ * holds the remaining N % 32 (M % 32) elements, and its amax is taken over
+ * those elements only (the reading adopted for shapes the source page's
+ * kernels leave out: "Why are the non-32-divisible shapes omitted?").
+ * Returns 0, or -1 if M or N is negative.
  */
 int mxo_quantize(const uint16_t *x, int64_t M, int64_t N, int fmt,
                  uint8_t *out_row, uint8_t *scale_row,
                  uint8_t *out_col, uint8_t *scale_col, float *dbias)
 {
     int64_t i, j, c, r, k;
-    if (M < 0 || N < 0 || M % MXO_BLOCK || N % MXO_BLOCK)
+    if (M < 0 || N < 0)
         return -1;
+    const int64_t Cr = (N + MXO_BLOCK - 1) / MXO_BLOCK, Rc = (M + MXO_BLOCK - 1) / MXO_BLOCK;
 
     if (out_row && scale_row) {
         for (i = 0; i < M; i++) {
-            for (c = 0; c < N / MXO_BLOCK; c++) {
-                const uint16_t *blk = x + i * N + c * MXO_BLOCK;
+            for (c = 0; c < Cr; c++) {
+                const int64_t j0 = c * MXO_BLOCK;
+                const int64_t len = N - j0 < MXO_BLOCK ? N - j0 : MXO_BLOCK;
+                const uint16_t *blk = x + i * N + j0;
                 double amax = 0.0;
-                for (k = 0; k < MXO_BLOCK; k++) {
+                for (k = 0; k < len; k++) {
                     double a = fabs(mxo_bf16_to_double(blk[k]));
                     if (a > amax)
                         amax = a;
                 }
                 const int e = mxo_block_exponent(amax, fmt);
                 const double s = ldexp(1.0, 127 - e);
-                scale_row[i * (N / MXO_BLOCK) + c] = (uint8_t)e;
-                for (k = 0; k < MXO_BLOCK; k++)
-                    out_row[i * N + c * MXO_BLOCK + k] = mxo_fp8_encode(mxo_bf16_to_double(blk[k]) * s, fmt);
+                scale_row[i * Cr + c] = (uint8_t)e;
+                for (k = 0; k < len; k++)
+                    out_row[i * N + j0 + k] = mxo_fp8_encode(mxo_bf16_to_double(blk[k]) * s, fmt);
             }
         }
     }
 
     if (out_col && scale_col) {
-        for (r = 0; r < M / MXO_BLOCK; r++) {
+        for (r = 0; r < Rc; r++) {
+            const int64_t i0 = r * MXO_BLOCK;
+            const int64_t len = M - i0 < MXO_BLOCK ? M - i0 : MXO_BLOCK;
             for (j = 0; j < N; j++) {
                 double amax = 0.0;
-                for (k = 0; k < MXO_BLOCK; k++) {
-                    double a = fabs(mxo_bf16_to_double(x[(r * MXO_BLOCK + k) * N + j]));
+                for (k = 0; k < len; k++) {
+                    double a = fabs(mxo_bf16_to_double(x[(i0 + k) * N + j]));
                     if (a > amax)
                         amax = a;
                 }
                 const int e = mxo_block_exponent(amax, fmt);
                 const double s = ldexp(1.0, 127 - e);
                 scale_col[r * N + j] = (uint8_t)e;
-                for (k = 0; k < MXO_BLOCK; k++) {
-                    const int64_t idx = (r * MXO_BLOCK + k) * N + j;
+                for (k = 0; k < len; k++) {
+                    const int64_t idx = (i0 + k) * N + j;
                     out_col[idx] = mxo_fp8_encode(mxo_bf16_to_double(x[idx]) * s, fmt);
                 }
             }
@@ -236,7 +246,7 @@ int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int n
                          uint8_t *out_col, uint8_t *scale_col)
 {
     int g;
-    if (num_groups < 0 || total_rows < 0 || N < 0 || N % MXO_BLOCK)
+    if (num_groups < 0 || total_rows < 0 || N < 0)
         return -1;
     if (offsets[0] != 0 || offsets[num_groups] != total_rows)
         return -1;
@@ -248,7 +258,8 @@ int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int n
         if (rows == 0)
             continue;
         mxo_quantize(x + r0 * N, rows, N, fmt,
-                     out_row ? out_row + r0 * N : 0, scale_row ? scale_row + r0 * (N / MXO_BLOCK) : 0,
+                     out_row ? out_row + r0 * N : 0,
+                     scale_row ? scale_row + r0 * ((N + MXO_BLOCK - 1) / MXO_BLOCK) : 0,
                      out_col ? out_col + r0 * N : 0, scale_col ? scale_col + (r0 / MXO_BLOCK) * N : 0,
                      0);
     }

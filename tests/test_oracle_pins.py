@@ -223,21 +223,21 @@ def brute_force(x_bits, fmt):
 
     M, N = x.shape
     out_row = np.zeros((M, N), np.uint8)
-    scale_row = np.zeros((M, N // 32), np.uint8)
+    scale_row = np.zeros((M, -(-N // 32)), np.uint8)
     out_col = np.zeros((M, N), np.uint8)
-    scale_col = np.zeros((M // 32, N), np.uint8)
+    scale_col = np.zeros((-(-M // 32), N), np.uint8)
     for i in range(M):
-        for c in range(N // 32):
-            blk = x[i, 32 * c:32 * c + 32]
+        for c in range(-(-N // 32)):
+            blk = x[i, 32 * c:32 * c + 32]           # the last block may be shorter
             e = scale_of(np.abs(blk).max())
             scale_row[i, c] = e
-            out_row[i, 32 * c:32 * c + 32] = [encode(v * 2.0 ** (127 - e)) for v in blk]
-    for r in range(M // 32):
+            out_row[i, 32 * c:32 * c + len(blk)] = [encode(v * 2.0 ** (127 - e)) for v in blk]
+    for r in range(-(-M // 32)):
         for j in range(N):
             blk = x[32 * r:32 * r + 32, j]
             e = scale_of(np.abs(blk).max())
             scale_col[r, j] = e
-            out_col[32 * r:32 * r + 32, j] = [encode(v * 2.0 ** (127 - e)) for v in blk]
+            out_col[32 * r:32 * r + len(blk), j] = [encode(v * 2.0 ** (127 - e)) for v in blk]
     return out_row, scale_row, out_col, scale_col
 
 
@@ -247,12 +247,17 @@ def structured_input(M, N, seed):
     a *= np.exp2(rng.integers(-6, 6, (1, N)))                                  # column scales differ
     a[0, :32] = 0.0
     a[:32, 0] = 0.0
-    a[1, 32:64] = rng.standard_normal(32) * 1e-39                               # subnormal block
-    a[5, 7] = 3000.0
+    if M > 1:
+        a[1, 32:64] = rng.standard_normal(a[1, 32:64].shape) * 1e-39          # subnormal block
+    if M > 5 and N > 7:
+        a[5, 7] = 3000.0
+    if M % 32:   # the last, partial column blocks get their own outlier
+        a[-1, -1] = -1500.0
     return wl.to_bf16_bits(a)
 
 
-@pytest.mark.parametrize("fmt,M,N", [(E4M3, 64, 96), (E5M2, 96, 64)])
+@pytest.mark.parametrize("fmt,M,N", [(E4M3, 64, 96), (E5M2, 96, 64), (E4M3, 45, 80), (E5M2, 71, 48),
+                                     (E4M3, 7, 16), (E4M3, 33, 33)])
 def test_quantize_matches_brute_force(oracle_mod, fmt, M, N):
     x = structured_input(M, N, seed=M + N + fmt)
     got = oracle_mod.quantize(x, fmt)[:4]
