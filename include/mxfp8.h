@@ -6,8 +6,10 @@
  * becomes FP8 data plus one E8M0 power-of-two scale per 32-element block.
  * The quantization-config review on that page (`to_key()`) names the options
  * this ABI exposes: fp8_dtype, rowwise, colwise, with_dbias and with_noop;
- * the "non-32-divisible shapes" review fixes the 32-element block and the
- * requirement that M and N be multiples of 32.
+ * the "non-32-divisible shapes" review fixes the 32-element block.  Shapes
+ * that are not multiples of 32 are accepted here: M may be any size and N
+ * any multiple of 16; a row's (column's) last block then holds the
+ * remaining N % 32 (M % 32) elements and takes its amax over those only.
  *
  * Arithmetic, per 32-element block with amax = max |x| over the block:
  *     e = clamp(ceil(log2(amax / Fmax)) + 127, 0, 254)   (amax == 0 -> e = 127)
@@ -17,11 +19,11 @@
  *
  * Layouts (all row-major, all buffers device memory owned by the caller):
  *     x          bf16  [M, N]
- *     out_row    uint8 [M, N]     FP8 codes, block = 1x32 along a row
- *     scale_row  uint8 [M, N/32]  E8M0 of block (i, j/32)
- *     out_col    uint8 [M, N]     FP8 codes, block = 32x1 down a column;
- *                                 element (i, j) uses scale_col[i/32, j]
- *     scale_col  uint8 [M/32, N]  E8M0 of block (i/32, j)
+ *     out_row    uint8 [M, N]            FP8 codes, block = 1x32 along a row
+ *     scale_row  uint8 [M, ceil(N/32)]   E8M0 of block (i, j/32)
+ *     out_col    uint8 [M, N]            FP8 codes, block = 32x1 down a column;
+ *                                        element (i, j) uses scale_col[i/32, j]
+ *     scale_col  uint8 [ceil(M/32), N]   E8M0 of block (i/32, j)
  *     dbias      fp32  [N]        column sums of x (unquantized)
  *
  * Conventions shared by every call:
@@ -56,7 +58,7 @@ typedef enum {
 typedef enum {
     MXFP8_OK = 0,
     MXFP8_ERR_NULL = 1,      /* required pointer NULL, a data/scale pair half set, or no direction */
-    MXFP8_ERR_SHAPE = 2,     /* M or N negative or not a multiple of 32, or too large */
+    MXFP8_ERR_SHAPE = 2,     /* M or N negative, N not a multiple of 16, or too large */
     MXFP8_ERR_ALIGN = 3,     /* x/out/workspace not 16-byte aligned, scale_col/dbias not 4-byte */
     MXFP8_ERR_FORMAT = 4,    /* fp8_fmt not MXFP8_E4M3 / MXFP8_E5M2 */
     MXFP8_ERR_WORKSPACE = 5, /* dbias requested and workspace NULL */
@@ -81,7 +83,8 @@ size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias);
  * with_dbias / with_noop config fields).
  *
  *   x           device, bf16 [M,N], 16-byte aligned.
- *   M, N        multiples of 32, >= 0.  M == 0 or N == 0: nothing to quantize,
+ *   M, N        M >= 0, N >= 0 a multiple of 16 (the TMA row pitch and the
+ *               16-byte stores need 16-byte rows).  M == 0 or N == 0: nothing to quantize,
  *               x and the output pointers may then be NULL (dbias, if
  *               requested, is set to zeros unless noop).
  *   fp8_fmt     MXFP8_E4M3 or MXFP8_E5M2.
@@ -134,7 +137,7 @@ size_t mxfp8_quantize_grouped_workspace_bytes(int64_t total_rows, int64_t N, int
  *                kernel writes nothing and sets *err_flag = 1.  It is never
  *                cleared by the library.
  *
- * total_rows and N must be multiples of 32.
+ * total_rows must be a multiple of 32 (as every group is) and N of 16.
  */
 mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t N,
                                       int num_groups, const int64_t *offsets, int fp8_fmt,
@@ -164,7 +167,7 @@ size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias);
  *               mxfp8_quantize; a direction is skipped as there.  Pinned
  *               memory (cudaHostAlloc / cudaHostRegister) lets the copies
  *               overlap; pageable memory works but serialises them.
- *   M, N        multiples of 32, > 0.
+ *   M, N        M > 0, N > 0 a multiple of 16.
  *   staging     device buffer, 256-byte aligned, at least
  *               mxfp8_quantize_host_staging_bytes(M, N, dbias_host != NULL)
  *               bytes (otherwise MXFP8_ERR_WORKSPACE); owned by the caller.
@@ -196,9 +199,10 @@ typedef enum {
  * 16*(r % 32) + 4*(r / 32) + c; padding entries are written as 0.  This is
  * the scale-factor arrangement block-scaled tensor-core GEMMs read (the
  * reading taken for the config key's `swizzled` bit, which the pages leave
- * undefined).  For the rowwise plane rows = M, scale_cols = N/32; the
- * columnwise plane serves the transposed operand, rows = N, scale_cols = M/32
- * (swizzled entry (j, i/32) holds the scale of column j, rows i..i+31).
+ * undefined).  For the rowwise plane rows = M, scale_cols = ceil(N/32); the
+ * columnwise plane serves the transposed operand, rows = N, scale_cols =
+ * ceil(M/32) (swizzled entry (j, i/32) holds the scale of column j, rows
+ * i..i+31).
  * Returns 0 for an unknown layout or negative sizes.
  */
 size_t mxfp8_scale_bytes(int64_t rows, int64_t scale_cols, int scale_layout);
@@ -232,12 +236,12 @@ typedef enum {
  */
 typedef struct mxfp8_quantize_config {
     const void *x;         /* device bf16 [M, N] */
-    int64_t M, N;          /* multiples of 32 */
+    int64_t M, N;          /* M >= 0, N >= 0 a multiple of 16 */
     int fp8_fmt;           /* MXFP8_E4M3 / MXFP8_E5M2 */
     void *out_row;         /* uint8 [M, N] or NULL */
-    void *scale_row;       /* mxfp8_scale_bytes(M, N/32, scale_layout) bytes */
+    void *scale_row;       /* mxfp8_scale_bytes(M, ceil(N/32), scale_layout) bytes */
     void *out_col;         /* uint8 [M, N] or NULL */
-    void *scale_col;       /* mxfp8_scale_bytes(N, M/32, scale_layout) bytes (plain: [M/32, N]) */
+    void *scale_col;       /* mxfp8_scale_bytes(N, ceil(M/32), scale_layout) bytes (plain: [ceil(M/32), N]) */
     float *dbias;          /* fp32 [N] or NULL */
     void *workspace;       /* mxfp8_quantize_workspace_bytes(M, N, dbias != NULL) bytes */
     const float *noop;     /* device fp32 scalar or NULL */

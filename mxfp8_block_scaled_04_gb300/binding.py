@@ -200,16 +200,16 @@ def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool):
     dev = x.device
     u8 = torch.uint8
     return (torch.empty((M, N), dtype=u8, device=dev) if rowwise else None,
-            torch.empty((M, N // BLOCK), dtype=u8, device=dev) if rowwise else None,
+            torch.empty((M, -(-N // BLOCK)), dtype=u8, device=dev) if rowwise else None,
             torch.empty((M, N), dtype=u8, device=dev) if colwise else None,
-            torch.empty((M // BLOCK, N), dtype=u8, device=dev) if colwise else None)
+            torch.empty((-(-M // BLOCK), N), dtype=u8, device=dev) if colwise else None)
 
 
 def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
              with_dbias: bool = False, noop: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, stream=None, swizzled: bool = False,
              with_amax: bool = False, activation="none") -> MXFP8Tensor:
-    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (M, N multiples of 32).
+    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (any M, N a multiple of 16).
 
     ``swizzled`` writes both scale planes in the GEMM-ready layout (1-D tensors of
     mxfp8_scale_bytes bytes); ``with_amax`` also returns max |x| as a float32 [1];
@@ -223,9 +223,9 @@ def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = Tr
     if swizzled:
         u8 = dict(dtype=torch.uint8, device=x.device)
         out_row = torch.empty((M, N), **u8) if rowwise else None
-        scale_row = torch.empty((mxfp8_scale_bytes(M, N // BLOCK, SCALES_SWIZZLED),), **u8) if rowwise else None
+        scale_row = torch.empty((mxfp8_scale_bytes(M, -(-N // BLOCK), SCALES_SWIZZLED),), **u8) if rowwise else None
         out_col = torch.empty((M, N), **u8) if colwise else None
-        scale_col = torch.empty((mxfp8_scale_bytes(N, M // BLOCK, SCALES_SWIZZLED),), **u8) if colwise else None
+        scale_col = torch.empty((mxfp8_scale_bytes(N, -(-M // BLOCK), SCALES_SWIZZLED),), **u8) if colwise else None
     else:
         out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
     dbias = torch.empty((N,), dtype=torch.float32, device=x.device) if with_dbias else None
@@ -259,9 +259,9 @@ def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool
     pin = dict(pin_memory=True)
     u8 = torch.uint8
     out_row = torch.empty((M, N), dtype=u8, **pin) if rowwise else None
-    scale_row = torch.empty((M, N // BLOCK), dtype=u8, **pin) if rowwise else None
+    scale_row = torch.empty((M, -(-N // BLOCK)), dtype=u8, **pin) if rowwise else None
     out_col = torch.empty((M, N), dtype=u8, **pin) if colwise else None
-    scale_col = torch.empty((M // BLOCK, N), dtype=u8, **pin) if colwise else None
+    scale_col = torch.empty((-(-M // BLOCK), N), dtype=u8, **pin) if colwise else None
     dbias = torch.empty((N,), dtype=torch.float32, **pin) if with_dbias else None
     need = mxfp8_quantize_host_staging_bytes(M, N, with_dbias)
     if staging is None:

@@ -266,7 +266,7 @@ extern "C" {
 
 size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias)
 {
-    if (!with_dbias || M < 0 || N < 0 || M % 32 || N % 32)
+    if (!with_dbias || M < 0 || N < 0 || N % 16)
         return 0;
     return static_cast<size_t>((M + kBM - 1) / kBM) * static_cast<size_t>(N) * sizeof(float);
 }
@@ -280,7 +280,7 @@ mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, 
     // ---- host-only checks, in a fixed order, before touching the device ----
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     const bool empty = M == 0 || N == 0;  // nothing to read or write: data pointers may be NULL
     mxfp8_status_t st;
@@ -352,7 +352,7 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
     const int64_t M = cfg->M, N = cfg->N;
     if (cfg->fp8_fmt != MXFP8_E4M3 && cfg->fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     const bool swz = cfg->scale_layout == MXFP8_SCALES_SWIZZLED;
     const bool empty = M == 0 || N == 0;
@@ -395,8 +395,8 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
                 g_launches.fetch_add(1, std::memory_order_relaxed);
             }
         };
-        pad(cfg->scale_row, M, N / 32);
-        pad(cfg->scale_col, N, M / 32);
+        pad(cfg->scale_row, M, (N + 31) / 32);
+        pad(cfg->scale_col, N, (M + 31) / 32);
     }
     if (cudaGetLastError() != cudaSuccess)
         return MXFP8_ERR_LAUNCH;
@@ -424,7 +424,7 @@ mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t
     (void)workspace;
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 32 || total_rows >= (int64_t{1} << 31) ||
+    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 16 || total_rows >= (int64_t{1} << 31) ||
         N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
@@ -475,7 +475,7 @@ const char *mxfp8_status_string(int status)
     switch (status) {
     case MXFP8_OK: return "ok";
     case MXFP8_ERR_NULL: return "required pointer is NULL, a data/scale pair is half set, or no direction requested";
-    case MXFP8_ERR_SHAPE: return "M/N must be non-negative multiples of 32 and below 2^31";
+    case MXFP8_ERR_SHAPE: return "M must be >= 0, N a non-negative multiple of 16, both below 2^31 (grouped: rows in multiples of 32)";
     case MXFP8_ERR_ALIGN: return "x/out/workspace must be 16-byte aligned, scale_col/dbias 4-byte aligned";
     case MXFP8_ERR_FORMAT: return "fp8_fmt must be MXFP8_E4M3 (0) or MXFP8_E5M2 (1)";
     case MXFP8_ERR_WORKSPACE: return "dbias requested without a workspace";
@@ -534,7 +534,7 @@ mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N,
 {
     if (dbias == nullptr)
         return MXFP8_ERR_NULL;
-    if (M < 0 || N < 0 || M % 32 || N % 32)
+    if (M < 0 || N < 0 || N % 16)
         return MXFP8_ERR_SHAPE;
     if (mxfp8_quantize_workspace_bytes(M, N, 1) > MXFP8_NOALLOC_SCRATCH_BYTES)
         return MXFP8_ERR_SHAPE;  // needs more than the static scratch array holds
@@ -643,7 +643,7 @@ SlotLayout slot_layout(int64_t R, int64_t N)
     L.out_col = o;
     o += align256(static_cast<size_t>(R * N));
     L.scale_row = o;
-    o += align256(static_cast<size_t>(R * N / 32));
+    o += align256(static_cast<size_t>(R * ((N + 31) / 32)));
     L.scale_col = o;
     o += align256(static_cast<size_t>(R / 32 * N));
     L.bytes = o;
@@ -698,7 +698,7 @@ extern "C" {
 
 size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias)
 {
-    if (M <= 0 || N <= 0 || M % 32 || N % 32)
+    if (M <= 0 || N <= 0 || N % 16)
         return 0;
     const SlotLayout L = slot_layout(host_chunk_rows(M, N), N);
     size_t b = kHostSlots * L.bytes;
@@ -713,7 +713,7 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M <= 0 || N <= 0 || M % 32 || N % 32 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M <= 0 || N <= 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (x_host == nullptr || staging == nullptr)
         return MXFP8_ERR_NULL;
@@ -785,15 +785,16 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
         if (row) {
             ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + row0 * N, slot + L.out_row,
                                                static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
-            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * (N / 32),
-                                               slot + L.scale_row, static_cast<size_t>(rows * (N / 32)),
+            const int64_t cr = (N + 31) / 32;
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * cr,
+                                               slot + L.scale_row, static_cast<size_t>(rows * cr),
                                                cudaMemcpyDeviceToHost, hp->d2h));
         }
         if (col) {
             ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + row0 * N, slot + L.out_col,
                                                static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
             ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + (row0 / 32) * N,
-                                               slot + L.scale_col, static_cast<size_t>((rows / 32) * N),
+                                               slot + L.scale_col, static_cast<size_t>(((rows + 31) / 32) * N),
                                                cudaMemcpyDeviceToHost, hp->d2h));
         }
         if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))

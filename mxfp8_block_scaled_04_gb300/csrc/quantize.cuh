@@ -444,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                             static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
                             (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
                     } else {
-                        // the columnwise operand's scales, seen as N rows x M/32 scale columns
-                        const int64_t C = p.M >> 5, c = grow >> 5;
+                        // the columnwise operand's scales, seen as N rows x ceil(M/32) scale columns
+                        const int64_t C = (p.M + 31) >> 5, c = grow >> 5;
                         p.scale_col[swizzled_offset(gcol, c, C)] = static_cast<uint8_t>(e0);
                         p.scale_col[swizzled_offset(gcol + 1, c, C)] = static_cast<uint8_t>(e1);
                         p.scale_col[swizzled_offset(gcol + 2, c, C)] = static_cast<uint8_t>(e2);
@@ -552,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (in) {
                         stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
                         if ((sp & 1) == 0)
-                            p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, N >> 5)
-                                            : grow * (N >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                            p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, (N + 31) >> 5)
+                                            : grow * ((N + 31) >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
                         if (AMAX && !do_col)
                             amax_acc = max(amax_acc, row_amax_bits);
                     }

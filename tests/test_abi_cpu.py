@@ -47,7 +47,8 @@ def test_workspace_bytes(cuda_lib):
     assert mx.mxfp8_quantize_workspace_bytes(16384, 8192, True) == 128 * 8192 * 4
     assert mx.mxfp8_quantize_workspace_bytes(96, 64, True) == 1 * 64 * 4
     assert mx.mxfp8_quantize_workspace_bytes(160, 64, True) == 2 * 64 * 4
-    assert mx.mxfp8_quantize_workspace_bytes(100, 64, True) == 0          # invalid shape
+    assert mx.mxfp8_quantize_workspace_bytes(100, 64, True) == 1 * 64 * 4  # any M
+    assert mx.mxfp8_quantize_workspace_bytes(100, 72, True) == 0          # N not a multiple of 16
     assert mx.mxfp8_quantize_grouped_workspace_bytes(65536, 7168, 64) == 0
 
 
@@ -57,7 +58,7 @@ def q(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, ws=Non
 
 @pytest.mark.parametrize("kw,status", [
     (dict(fmt=2), FORMAT), (dict(fmt=-1), FORMAT),
-    (dict(M=48), SHAPE), (dict(N=100), SHAPE), (dict(M=-32), SHAPE), (dict(N=1 << 31), SHAPE),
+    (dict(N=100), SHAPE), (dict(N=40), SHAPE), (dict(M=-32), SHAPE), (dict(N=1 << 31), SHAPE),
     (dict(x=None), NULL), (dict(orow=None), NULL), (dict(scol=None), NULL),
     (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(x=A + 8), ALIGN), (dict(orow=A + 4), ALIGN), (dict(ocol=A + 8), ALIGN), (dict(scol=A + 2), ALIGN),
@@ -80,7 +81,7 @@ def g(x=A, total=128, N=64, G=2, off=A, fmt=0, orow=A, srow=A, ocol=A, scol=A, e
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=48), SHAPE),
+    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=40), SHAPE),
     (dict(G=0), GROUPS), (dict(G=mx.MAX_GROUPS + 1), GROUPS), (dict(off=None), GROUPS),
     (dict(x=None), NULL), (dict(orow=None), NULL), (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(x=A + 2), ALIGN), (dict(off=A + 4), ALIGN), (dict(err=A + 2), ALIGN),
@@ -152,7 +153,7 @@ def test_ex_rejections(cuda_lib):
     cfg = mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1)
     cfg.reserved[3] = 1
     assert mx.mxfp8_quantize_ex(cfg, 0) == FORMAT
-    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 48, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 40, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, None, A, A, A, scale_layout=1), 0) == NULL
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1, amax=A + 2), 0) == ALIGN
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, activation=6), 0) == FORMAT
@@ -160,3 +161,10 @@ def test_ex_rejections(cuda_lib):
                                                activation="gelu"), 0) == FORMAT
     # swizzled scale planes need no alignment: an odd scale pointer reaches the device stage
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A + 1, A, A + 1, scale_layout=1), 0) == DEVICE
+
+
+def test_ragged_shapes_pass_host_checks(cuda_lib):
+    # M not a multiple of 32 and N a multiple of 16 are valid shapes: with fake
+    # pointers the call gets past every host check and stops at the device stage
+    assert q(M=45, N=80) == DEVICE
+    assert q(M=1, N=16) == DEVICE

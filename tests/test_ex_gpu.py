@@ -75,3 +75,16 @@ def test_ex_noop_leaves_amax_and_padding_untouched():
     assert mx.mxfp8_quantize_ex(cfg, None) == 0
     torch.cuda.synchronize()
     assert bool((srow == 0x3C).all()) and bool((orow == 0x3C).all()) and float(amax.item()) == 7.0
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (130, 144), (257, 4112)])
+def test_swizzled_ragged_shapes(oracle_mod, shape):
+    M, N = shape
+    x_bits = wl.act_bf16(M, N, seed=M + N) if M % 32 == 0 else wl.grad_bf16(M, N, seed=M + N)
+    r = mx.quantize(dev(x_bits), mx.E4M3, swizzled=True, with_amax=True)
+    torch.cuda.synchronize()
+    o_row, s_row, o_col, s_col, _ = oracle_mod.quantize(x_bits, mx.E4M3)
+    assert np.array_equal(r.out_row.cpu().numpy(), o_row) and np.array_equal(r.out_col.cpu().numpy(), o_col)
+    assert np.array_equal(r.scale_row.cpu().numpy(), oracle_mod.swizzle_scales(s_row))
+    assert np.array_equal(r.scale_col.cpu().numpy(), oracle_mod.swizzle_scales(np.ascontiguousarray(s_col.T)))
+    assert float(r.amax.item()) == oracle_mod.amax(x_bits)

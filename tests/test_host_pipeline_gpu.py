@@ -27,6 +27,8 @@ def device_reference(x_bits, fmt, with_dbias, rowwise=True, colwise=True):
     ((1056, 28672), mx.E5M2, True, True),     # 128-row chunks, last one 32 rows
     ((1056, 28672), mx.E5M2, True, False),    # pageable host memory
     ((96, 160), mx.E4M3, True, True),         # a single chunk smaller than a tile
+    ((4195, 4096), mx.E5M2, True, True),      # M not a multiple of 32: last chunk 99 rows
+    ((1000, 1040), mx.E4M3, False, True),     # N = 16 mod 32
 ])
 def test_host_pipeline_matches_device_path(shape, fmt, with_dbias, pinned):
     M, N = shape

@@ -48,9 +48,9 @@ def run_quantize(x_bits, fmt, rowwise=True, colwise=True, with_dbias=False, noop
     x = dev_bf16(x_bits)
     bufs = dict(
         out_row=Guarded((M, N), fill=prefill) if rowwise else None,
-        scale_row=Guarded((M, N // 32), fill=prefill) if rowwise else None,
+        scale_row=Guarded((M, -(-N // 32)), fill=prefill) if rowwise else None,
         out_col=Guarded((M, N), fill=prefill) if colwise else None,
-        scale_col=Guarded((M // 32, N), fill=prefill) if colwise else None,
+        scale_col=Guarded((-(-M // 32), N), fill=prefill) if colwise else None,
         dbias=Guarded((N,), torch.float32, fill=prefill) if with_dbias else None,
     )
     ws = None
@@ -334,3 +334,27 @@ def test_parity_moe_64x65536x7168_sampled(oracle_mod):
     check_stripes(oracle_mod, x_bits, w["fmt"], r._asdict(), stripes_to_check(w["M"], rng, must=must))
     del x, r
     torch.cuda.empty_cache()
+
+
+# ---- shapes that are not multiples of 32 ------------------------------------------
+
+RAGGED = [(45, 80), (71, 48), (1, 16), (33, 16), (130, 144), (1000, 1040), (257, 4112), (31, 4096)]
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", RAGGED)
+def test_parity_ragged_shapes(oracle_mod, shape, fmt):
+    M, N = shape
+    x = mixed_input(M, N, seed=M * 13 + N + fmt)
+    host = run_quantize(x, fmt)
+    check_against_oracle(oracle_mod, x, fmt, host)
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (1000, 1040)])
+def test_parity_ragged_dbias(oracle_mod, shape):
+    M, N = shape
+    x = mixed_input(M, N, seed=M + 3 * N)
+    host = run_quantize(x, E5M2, with_dbias=True)
+    check_against_oracle(oracle_mod, x, E5M2, host)
+    want = oracle_mod.quantize(x, E5M2, False, False, with_dbias=True)[4]
+    assert np.all(np.abs(host["dbias"].astype(np.float64) - want) <= dbias_tolerance(x))
