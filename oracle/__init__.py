@@ -76,6 +76,8 @@ def _load():
             lib.mxo_swizzle_scales.argtypes = [u8p, i64, i64, u8p]
             lib.mxo_amax.restype = ctypes.c_float
             lib.mxo_amax.argtypes = [u16p, i64, i64]
+            lib.mxo_grouped_dbias.restype = ctypes.c_int
+            lib.mxo_grouped_dbias.argtypes = [u16p, i64, i64, ctypes.c_int, i64p, f32p]
             lib.mxo_activation_f64.restype = ctypes.c_double
             lib.mxo_activation_f64.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.mxo_activation.restype = ctypes.c_float
@@ -225,3 +227,16 @@ def quantize_act(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True, c
 def activation_f64(v: float, act: int) -> float:
     """Exact-as-double activation of one value (no fp32 rounding)."""
     return float(_load().mxo_activation_f64(float(v), act))
+
+
+def grouped_dbias(x_bits: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+    """Per-group column sums [G, N] float32 of a grouped input; ValueError on invalid offsets."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    total, N = x.shape
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    G = off.shape[0] - 1
+    out = np.empty((G, N), np.float32)
+    if _load().mxo_grouped_dbias(_ptr(x, ctypes.c_uint16), total, N, G, _ptr(off, ctypes.c_int64),
+                                 _ptr(out, ctypes.c_float)) != 0:
+        raise ValueError("oracle: invalid group offsets")
+    return out

@@ -423,3 +423,29 @@ void mxo_activate(const uint16_t *x, int64_t n, int act, float *y)
     for (i = 0; i < n; i++)
         y[i] = mxo_activation(mxo_bf16_to_double(x[i]), act);
 }
+
+/*
+ * Per-expert dbias of a grouped call (the survey's "grouped-call dbias per
+ * expert"): dbias[g][j] = sum of x[i][j] over the rows i of group g, in
+ * double, rounded once to fp32; an empty group gets zeros.  Returns -1 for
+ * offsets the grouped call rejects.
+ */
+int mxo_grouped_dbias(const uint16_t *x, int64_t total_rows, int64_t N, int num_groups,
+                      const int64_t *offsets, float *dbias)
+{
+    int g;
+    int64_t i, j;
+    if (num_groups < 0 || total_rows < 0 || N < 0 || offsets[0] != 0 || offsets[num_groups] != total_rows)
+        return -1;
+    for (g = 0; g < num_groups; g++)
+        if (offsets[g + 1] < offsets[g] || offsets[g + 1] % MXO_BLOCK)
+            return -1;
+    for (g = 0; g < num_groups; g++)
+        for (j = 0; j < N; j++) {
+            double acc = 0.0;
+            for (i = offsets[g]; i < offsets[g + 1]; i++)
+                acc += mxo_bf16_to_double(x[i * N + j]);
+            dbias[(int64_t)g * N + j] = (float)acc;
+        }
+    return 0;
+}

@@ -406,3 +406,21 @@ def test_relu_quantize_hand_checks(oracle_mod):
     x = wl.to_bf16_bits(np.tile(np.array([-1.0, 2.0] * 16), (32, 1)))
     o_row, s_row, _, _, _ = oracle_mod.quantize_act(x, 0, 1)
     assert s_row[0, 0] == 120 and o_row[0, :2].tolist() == [0x00, 0x78]
+
+
+def test_grouped_dbias_is_per_group_fsum(oracle_mod):
+    sizes = np.array([64, 0, 96, 32], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    x = wl.moe_bf16(sizes, 48, seed=6)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle_mod.grouped_dbias(x, off)
+    for g in range(len(sizes)):
+        rows = xv[off[g]:off[g + 1]]
+        want = np.array([math.fsum(rows[:, j]) for j in range(48)], np.float32)
+        assert np.array_equal(got[g], want)
+    assert np.all(got[1] == 0.0)
+    # the groups' sums add up to the flat dbias (up to fp32 rounding of each)
+    flat = oracle_mod.quantize(x, 0, False, False, with_dbias=True)[4]
+    assert np.allclose(got.astype(np.float64).sum(0), flat, rtol=1e-6, atol=1e-30)
+    with pytest.raises(ValueError):
+        oracle_mod.grouped_dbias(x, np.array([0, 64, 100, 192]))
