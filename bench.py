@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--shape", default=None, help="MxN: the workload's value recipe at another shape")
     ap.add_argument("--swizzled", action="store_true", help="write GEMM-ready (swizzled) scale planes")
     ap.add_argument("--amax", action="store_true", help="also write the per-tensor amax")
+    ap.add_argument("--dbias", action="store_true", help="fused dbias (per expert for the grouped workload)")
     ap.add_argument("--act", default="none", help="activation before the cast: relu, srelu, gelu, silu, qgelu")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -263,7 +264,7 @@ def run_ours(args):
             dist.barrier()
 
     w = wl.make(args.workload, shape=parse_shape(args.shape))
-    x_bits, fmt, with_dbias, offsets = w["x"], w["fmt"], w["with_dbias"], w["offsets"]
+    x_bits, fmt, with_dbias, offsets = w["x"], w["fmt"], w["with_dbias"] or args.dbias, w["offsets"]
     M, N = x_bits.shape
     grouped = offsets is not None
     x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
@@ -278,15 +279,20 @@ def run_ours(args):
         raise SystemExit("--swizzled / --amax / --act apply to the flat workloads")
     if act and with_dbias:
         raise SystemExit("--act does not combine with the dbias workload")
-    dbias = torch.empty((N,), dtype=torch.float32, device="cuda") if with_dbias else None
-    ws = (torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
-          if with_dbias else None)
+    G = offsets.size - 1 if grouped else 0
+    dbias = (torch.empty((G, N) if grouped else (N,), dtype=torch.float32, device="cuda") if with_dbias else None)
+    ws_bytes = (mx.mxfp8_quantize_grouped_dbias_workspace_bytes(M, N, G) if grouped
+                else mx.mxfp8_quantize_workspace_bytes(M, N, True))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if with_dbias else None
     off_dev = torch.from_numpy(offsets).cuda() if grouped else None
     stream = torch.cuda.current_stream()
 
     def step(xin=x):
-        if grouped:
-            st = mx.mxfp8_quantize_grouped(xin, M, N, off_dev.numel() - 1, off_dev, fmt, out_row, scale_row,
+        if grouped and with_dbias:
+            st = mx.mxfp8_quantize_grouped_dbias(xin, M, N, G, off_dev, fmt, out_row, scale_row, out_col,
+                                                 scale_col, dbias, ws, None, None, stream)
+        elif grouped:
+            st = mx.mxfp8_quantize_grouped(xin, M, N, G, off_dev, fmt, out_row, scale_row,
                                            out_col, scale_col, None, None, None, stream)
         elif args.swizzled or args.amax or act:
             cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
@@ -298,7 +304,7 @@ def run_ours(args):
         if st != 0:
             raise mx.MXFP8Error(st, "bench step")
 
-    algo_bytes = BYTES_PER_ELEM * M * N + (4 * N if with_dbias else 0)
+    algo_bytes = BYTES_PER_ELEM * M * N + (4 * N * max(G, 1) if with_dbias else 0)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(local).uuid)

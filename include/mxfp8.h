@@ -264,6 +264,31 @@ typedef struct mxfp8_quantize_config {
  */
 mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream);
 
+/*
+ * Workspace bytes for mxfp8_quantize_grouped_dbias: one fp32 partial row per
+ * 128-row tile, tiles never spanning two groups, so at most
+ * (ceil(total_rows/128) + num_groups) * N * 4 bytes.  0 for invalid sizes.
+ */
+size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups);
+
+/*
+ * mxfp8_quantize_grouped plus a per-expert dbias (the "grouped-call dbias per
+ * expert" next to with_amax in the config fields of the PR #3137 page):
+ *   dbias      device fp32 [num_groups, N]: row g = column sums of the rows of
+ *              group g (zeros for an empty group), accumulated in a fixed
+ *              order as in mxfp8_quantize.
+ *   workspace  device, >= mxfp8_quantize_grouped_dbias_workspace_bytes(...)
+ *              bytes, 16-byte aligned.
+ * Everything else as for mxfp8_quantize_grouped; with invalid offsets nothing
+ * is written, dbias included, and *err_flag is set.
+ */
+mxfp8_status_t mxfp8_quantize_grouped_dbias(const void *x, int64_t total_rows, int64_t N,
+                                            int num_groups, const int64_t *offsets, int fp8_fmt,
+                                            void *out_row, void *scale_row,
+                                            void *out_col, void *scale_col,
+                                            float *dbias, void *workspace, const float *noop,
+                                            int *err_flag, void *stream);
+
 /* Static, human-readable text for a status code. */
 const char *mxfp8_status_string(int status);
 

@@ -73,6 +73,10 @@ def lib():
             L.mxfp8_quantize_grouped_workspace_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_grouped.restype = i32
             L.mxfp8_quantize_grouped.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_grouped_dbias_workspace_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_grouped_dbias_workspace_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_grouped_dbias.restype = i32
+            L.mxfp8_quantize_grouped_dbias.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
@@ -130,6 +134,18 @@ def mxfp8_quantize_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, out_r
                                             _addr(out_row), _addr(scale_row), _addr(out_col),
                                             _addr(scale_col), _addr(workspace), _addr(noop),
                                             _addr(err_flag), _stream(stream)))
+
+
+def mxfp8_quantize_grouped_dbias_workspace_bytes(total_rows: int, N: int, num_groups: int) -> int:
+    return int(lib().mxfp8_quantize_grouped_dbias_workspace_bytes(total_rows, N, num_groups))
+
+
+def mxfp8_quantize_grouped_dbias(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col,
+                                 scale_col, dbias, workspace, noop=None, err_flag=None, stream=None) -> int:
+    return int(lib().mxfp8_quantize_grouped_dbias(_addr(x), total_rows, N, num_groups, _addr(offsets), fp8_fmt,
+                                                  _addr(out_row), _addr(scale_row), _addr(out_col),
+                                                  _addr(scale_col), _addr(dbias), _addr(workspace), _addr(noop),
+                                                  _addr(err_flag), _stream(stream)))
 
 
 def mxfp8_quantize_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
@@ -275,19 +291,31 @@ def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool
 
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,
                      colwise: bool = True, noop: Optional[torch.Tensor] = None,
-                     err_flag: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
-    """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device)."""
+                     err_flag: Optional[torch.Tensor] = None, stream=None, with_dbias: bool = False) -> MXFP8Tensor:
+    """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device).
+
+    ``with_dbias`` also returns the per-group column sums as float32 [G, N].
+    """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
     if offsets.dtype != torch.int64 or offsets.dim() != 1 or not offsets.is_contiguous():
         raise ValueError("offsets must be a contiguous 1-D torch.int64 tensor")
     total, N = x.shape
+    G = offsets.numel() - 1
     out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
-    st = mxfp8_quantize_grouped(x, total, N, offsets.numel() - 1, offsets, _fmt(fmt), out_row, scale_row,
-                                out_col, scale_col, None, noop, err_flag, stream)
+    if with_dbias:
+        dbias = torch.empty((G, N), dtype=torch.float32, device=x.device)
+        ws = torch.empty((max(mxfp8_quantize_grouped_dbias_workspace_bytes(total, N, G), 16),), dtype=torch.uint8,
+                         device=x.device)
+        st = mxfp8_quantize_grouped_dbias(x, total, N, G, offsets, _fmt(fmt), out_row, scale_row, out_col,
+                                          scale_col, dbias, ws, noop, err_flag, stream)
+    else:
+        dbias = None
+        st = mxfp8_quantize_grouped(x, total, N, G, offsets, _fmt(fmt), out_row, scale_row,
+                                    out_col, scale_col, None, noop, err_flag, stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_grouped")
-    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
 
 
 def mxfp8_quantize_dbias_noalloc(x, M, N, fp8_fmt, out_row, scale_row, out_col, scale_col,

@@ -260,6 +260,72 @@ mxfp8_status_t enqueue_reduce(const float *ws, int64_t row_tiles, int64_t N, flo
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
+// The grouped call, with or without per-group dbias (ws and dbias both set).
+mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int num_groups, const int64_t *offsets,
+                            int fp8_fmt, void *out_row, void *scale_row, void *out_col, void *scale_col,
+                            float *dbias, float *ws, const float *noop, int *err_flag, cudaStream_t stream)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 16 || total_rows >= (int64_t{1} << 31) ||
+        N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
+        return MXFP8_ERR_GROUPS;
+    if (x == nullptr)
+        return MXFP8_ERR_NULL;
+    mxfp8_status_t st = check_outputs(out_row, scale_row, out_col, scale_col);
+    if (st != MXFP8_OK)
+        return st;
+    if (!aligned(x, 16) || !aligned(offsets, 8) || !aligned(err_flag, 4) || !aligned(dbias, 4) || !aligned(ws, 16))
+        return MXFP8_ERR_ALIGN;
+    const int64_t col_tiles = (N + kBN - 1) / kBN;
+    // Upper bound on the tile count: every non-empty group adds at most one partial row tile.
+    const int64_t tile_bound = (total_rows / kBM + num_groups) * col_tiles;
+    if (tile_bound >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(offsets, device) || !on_device(out_row, device) ||
+        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
+        !on_device(noop, device) || !on_device(err_flag, device) || !on_device(dbias, device) ||
+        !on_device(ws, device))
+        return MXFP8_ERR_DEVICE;
+    if (total_rows > 0 && N > 0) {
+        CUtensorMap map;
+        if ((st = make_tensor_map(&map, x, total_rows, N)) != MXFP8_OK)
+            return st;
+        QuantParams p{};
+        p.out_row = static_cast<uint8_t *>(out_row);
+        p.scale_row = static_cast<uint8_t *>(scale_row);
+        p.out_col = static_cast<uint8_t *>(out_col);
+        p.scale_col = static_cast<uint8_t *>(scale_col);
+        p.ws = ws;
+        p.noop = noop;
+        p.offsets = offsets;
+        p.err_flag = err_flag;
+        p.M = total_rows;
+        p.N = N;
+        p.num_groups = num_groups;
+        p.col_tiles = static_cast<int>(col_tiles);
+        st = dbias != nullptr ? launch_quantize<true, true>(fp8_fmt, device, map, p, tile_bound, stream)
+                              : launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, stream);
+        if (st != MXFP8_OK)
+            return st;
+    }
+    if (dbias != nullptr && N > 0) {
+        const dim3 grid(static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols), static_cast<unsigned>(num_groups));
+        dbias_reduce_grouped_kernel<<<grid, kReduceCols * kReduceWarps, 0, stream>>>(ws, offsets, num_groups,
+                                                                                      total_rows, N, dbias, noop);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (cudaGetLastError() != cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+    }
+    return MXFP8_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -422,52 +488,28 @@ mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t
                                       int *err_flag, void *stream_)
 {
     (void)workspace;
-    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
-        return MXFP8_ERR_FORMAT;
-    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 16 || total_rows >= (int64_t{1} << 31) ||
-        N >= (int64_t{1} << 31))
-        return MXFP8_ERR_SHAPE;
-    if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
-        return MXFP8_ERR_GROUPS;
-    if (x == nullptr)
+    return grouped_impl(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                        nullptr, nullptr, noop, err_flag, static_cast<cudaStream_t>(stream_));
+}
+
+size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups)
+{
+    if (total_rows < 0 || N < 0 || num_groups < 1 || total_rows % 32 || N % 16)
+        return 0;
+    return static_cast<size_t>((total_rows + kBM - 1) / kBM + num_groups) * static_cast<size_t>(N) * sizeof(float);
+}
+
+mxfp8_status_t mxfp8_quantize_grouped_dbias(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                            const int64_t *offsets, int fp8_fmt, void *out_row, void *scale_row,
+                                            void *out_col, void *scale_col, float *dbias, void *workspace,
+                                            const float *noop, int *err_flag, void *stream_)
+{
+    if (dbias == nullptr)
         return MXFP8_ERR_NULL;
-    mxfp8_status_t st = check_outputs(out_row, scale_row, out_col, scale_col);
-    if (st != MXFP8_OK)
-        return st;
-    if (!aligned(x, 16) || !aligned(offsets, 8) || !aligned(err_flag, 4))
-        return MXFP8_ERR_ALIGN;
-    const int64_t col_tiles = (N + kBN - 1) / kBN;
-    // Upper bound on the tile count: every non-empty group adds at most one partial row tile.
-    const int64_t tile_bound = (total_rows / kBM + num_groups) * col_tiles;
-    if (tile_bound >= (int64_t{1} << 31))
-        return MXFP8_ERR_SHAPE;
-
-    int device = 0;
-    if ((st = current_device(&device)) != MXFP8_OK)
-        return st;
-    if (!on_device(x, device) || !on_device(offsets, device) || !on_device(out_row, device) ||
-        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
-        !on_device(noop, device) || !on_device(err_flag, device))
-        return MXFP8_ERR_DEVICE;
-    if (total_rows == 0 || N == 0)
-        return MXFP8_OK;
-
-    CUtensorMap map;
-    if ((st = make_tensor_map(&map, x, total_rows, N)) != MXFP8_OK)
-        return st;
-    QuantParams p{};
-    p.out_row = static_cast<uint8_t *>(out_row);
-    p.scale_row = static_cast<uint8_t *>(scale_row);
-    p.out_col = static_cast<uint8_t *>(out_col);
-    p.scale_col = static_cast<uint8_t *>(scale_col);
-    p.noop = noop;
-    p.offsets = offsets;
-    p.err_flag = err_flag;
-    p.M = total_rows;
-    p.N = N;
-    p.num_groups = num_groups;
-    p.col_tiles = static_cast<int>(col_tiles);
-    return launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, static_cast<cudaStream_t>(stream_));
+    if (workspace == nullptr && total_rows > 0)
+        return MXFP8_ERR_WORKSPACE;
+    return grouped_impl(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                        dbias, static_cast<float *>(workspace), noop, err_flag, static_cast<cudaStream_t>(stream_));
 }
 
 const char *mxfp8_status_string(int status)

@@ -195,7 +195,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         c.row0 = goff[lo] + static_cast<int64_t>(rtl) * kBM;
         c.row_end = min(c.row0 + kBM, goff[lo + 1]);
         c.col0 = ct * kBN;
-        c.rt = 0;
+        c.rt = gpre[lo] / p.col_tiles + rtl;  // global row-tile index (per-group dbias partial row)
     } else {
         const int rt = t / p.col_tiles;
         const int ct = t - rt * p.col_tiles;

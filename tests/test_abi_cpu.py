@@ -168,3 +168,19 @@ def test_ragged_shapes_pass_host_checks(cuda_lib):
     # pointers the call gets past every host check and stops at the device stage
     assert q(M=45, N=80) == DEVICE
     assert q(M=1, N=16) == DEVICE
+
+
+def test_grouped_dbias_host_checks(cuda_lib):
+    def gd(dbias=A, ws=A, **kw):
+        args = dict(x=A, total=128, N=64, G=2, off=A, fmt=0)
+        args.update(kw)
+        return mx.mxfp8_quantize_grouped_dbias(args["x"], args["total"], args["N"], args["G"], args["off"],
+                                               args["fmt"], A, A, A, A, dbias, ws, None, None, 0)
+    assert gd(dbias=None) == NULL
+    assert gd(ws=None) == WORKSPACE
+    assert gd(total=40) == SHAPE
+    assert gd(G=0) == GROUPS
+    assert gd(dbias=A + 2) == ALIGN
+    assert gd() == DEVICE
+    assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 64) == (512 + 64) * 7168 * 4
+    assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 0) == 0

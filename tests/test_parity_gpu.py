@@ -358,3 +358,60 @@ def test_parity_ragged_dbias(oracle_mod, shape):
     check_against_oracle(oracle_mod, x, E5M2, host)
     want = oracle_mod.quantize(x, E5M2, False, False, with_dbias=True)[4]
     assert np.all(np.abs(host["dbias"].astype(np.float64) - want) <= dbias_tolerance(x))
+
+
+
+# ---- grouped dbias ------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [96, 160, 512])
+def test_grouped_dbias(oracle_mod, N):
+    sizes = np.array([64, 0, 32, 416, 0, 0, 128, 96, 160, 32], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = wl.moe_bf16(sizes, N, seed=N + 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mx.quantize_grouped(dev_bf16(x_bits), torch.from_numpy(off).cuda(), E5M2, err_flag=err, with_dbias=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o = oracle_mod.quantize_grouped(x_bits, off, E5M2)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), r[:4], o):
+        assert_bytes_equal(g.cpu().numpy(), w, name)
+    want = oracle_mod.grouped_dbias(x_bits, off)
+    xv = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().abs().numpy()
+    got = r.dbias.cpu().numpy()
+    for g in range(len(sizes)):
+        tol = 1e-5 * xv[off[g]:off[g + 1]].sum(0)
+        assert np.all(np.abs(got[g].astype(np.float64) - want[g]) <= tol), g
+    assert np.all(got[1] == 0.0) and np.all(got[4] == 0.0)
+
+
+def test_grouped_dbias_bad_offsets_write_nothing():
+    x = dev_bf16(wl.normal_bf16(928, 96, seed=1))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    off = torch.tensor([0, 16, 928], dtype=torch.int64, device="cuda")
+    dbias = torch.full((2, 96), 3.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.mxfp8_quantize_grouped_dbias_workspace_bytes(928, 96, 2), dtype=torch.uint8, device="cuda")
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    outs = [torch.full((928, 96), 0x3C, **u8), torch.full((928, 3), 0x3C, **u8),
+            torch.full((928, 96), 0x3C, **u8), torch.full((29, 96), 0x3C, **u8)]
+    st = mx.mxfp8_quantize_grouped_dbias(x, 928, 96, 2, off, E4M3, *outs, dbias, ws, None, err, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert bool((dbias == 3.0).all()) and all(bool((t == 0x3C).all()) for t in outs)
+
+
+def test_grouped_dbias_moe_64x65536x7168_full(oracle_mod):
+    w = wl.make("moe_64x65536x7168")
+    x_bits, off = w["x"], w["offsets"]
+    r = mx.quantize_grouped(dev_bf16(x_bits), torch.from_numpy(off).cuda(), E4M3, with_dbias=True)
+    torch.cuda.synchronize()
+    want = oracle_mod.grouped_dbias(x_bits, off)
+    got = r.dbias.cpu().numpy().astype(np.float64)
+    xv = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).float().abs()
+    for g in range(len(off) - 1):
+        tol = 1e-5 * xv[off[g]:off[g + 1]].double().sum(0).numpy()
+        assert np.all(np.abs(got[g] - want[g]) <= tol), g
+    rng = np.random.Generator(np.random.PCG64(24))
+    check_stripes(oracle_mod, x_bits, E4M3, r._asdict(), stripes_to_check(w["M"], rng))
+    del r
+    torch.cuda.empty_cache()
