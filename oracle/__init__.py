@@ -78,6 +78,10 @@ def _load():
             lib.mxo_amax.argtypes = [u16p, i64, i64]
             lib.mxo_grouped_dbias.restype = ctypes.c_int
             lib.mxo_grouped_dbias.argtypes = [u16p, i64, i64, ctypes.c_int, i64p, f32p]
+            lib.mxo_dactivation_f64.restype = ctypes.c_double
+            lib.mxo_dactivation_f64.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.mxo_dactivate.restype = None
+            lib.mxo_dactivate.argtypes = [u16p, u16p, i64, ctypes.c_int, f32p]
             lib.mxo_activation_f64.restype = ctypes.c_double
             lib.mxo_activation_f64.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.mxo_activation.restype = ctypes.c_float
@@ -240,3 +244,24 @@ def grouped_dbias(x_bits: np.ndarray, offsets: np.ndarray) -> np.ndarray:
                                  _ptr(out, ctypes.c_float)) != 0:
         raise ValueError("oracle: invalid group offsets")
     return out
+
+
+def dactivation_f64(v: float, act: int) -> float:
+    """Exact-as-double derivative act'(v) (see mxo_dactivation_f64)."""
+    return float(_load().mxo_dactivation_f64(float(v), act))
+
+
+def dactivate(dy_bits: np.ndarray, x_bits: np.ndarray, act: int) -> np.ndarray:
+    """fp32 dY * act'(X) for BF16 matrices of equal shape."""
+    dy = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    assert dy.shape == x.shape
+    y = np.empty(x.shape, np.float32)
+    _load().mxo_dactivate(_ptr(dy, ctypes.c_uint16), _ptr(x, ctypes.c_uint16), x.size, act, _ptr(y, ctypes.c_float))
+    return y
+
+
+def quantize_dact(dy_bits: np.ndarray, x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True,
+                  colwise: bool = True, with_dbias: bool = False):
+    """The MXFP8 cast of dY * act'(X) (and its column sums as dbias)."""
+    return quantize_f32(dactivate(dy_bits, x_bits, act), fmt, rowwise, colwise, with_dbias)

@@ -449,3 +449,58 @@ int mxo_grouped_dbias(const uint16_t *x, int64_t total_rows, int64_t N, int num_
         }
     return 0;
 }
+
+/*
+ * Backward fusion (the `with_dact` field of the config key on the PR #3137
+ * page): the cast quantizes dY * act'(X) for a gradient dY and the
+ * activation's input X, both BF16.  The pages give no formulas; the reading
+ * used is the derivative of each activation of mxo_activation, evaluated in
+ * fp32 and multiplied by dY in fp32:
+ *   1 dReLU    X > 0 ? 1 : 0
+ *   2 dSReLU   X > 0 ? 2X : 0
+ *   3 dGeLU    s + X s (1-s) t',  s = sigmoid(t), t = 2 sqrt(2/pi) (X + 0.044715 X^3),
+ *                                 t' = 2 sqrt(2/pi) (1 + 3 * 0.044715 X^2)
+ *   4 dSiLU    s (1 + X (1-s)),   s = sigmoid(X)
+ *   5 dQGeLU   s (1 + 1.702 X (1-s)), s = sigmoid(1.702 X)
+ * with s and 1-s both taken from e = exp(-|t|) (no cancellation).  Here the
+ * derivative is evaluated in double and the product dY * act'(X) rounded once
+ * to fp32: exact for dReLU and dSReLU (a product of BF16 values and 2), within
+ * a few fp32 ulps of the GPU's evaluation for the others.
+ */
+static void mxo_sigmoid_pair(double t, double *s, double *one_minus_s)
+{
+    const double e = exp(-fabs(t));
+    const double inv = 1.0 / (1.0 + e);
+    *s = t >= 0 ? inv : e * inv;
+    *one_minus_s = t >= 0 ? e * inv : inv;
+}
+
+double mxo_dactivation_f64(double x, int act)
+{
+    double s, oms;
+    switch (act) {
+    case 1: return x > 0 ? 1.0 : 0.0;
+    case 2: return x > 0 ? 2.0 * x : 0.0;
+    case 3: {
+        const double c = 2.0 * 0.7978845608028654;
+        const double t = c * (x + 0.044715 * x * x * x), dt = c * (1.0 + 3.0 * 0.044715 * x * x);
+        mxo_sigmoid_pair(t, &s, &oms);
+        return s + x * s * oms * dt;
+    }
+    case 4:
+        mxo_sigmoid_pair(x, &s, &oms);
+        return s * (1.0 + x * oms);
+    case 5:
+        mxo_sigmoid_pair(1.702 * x, &s, &oms);
+        return s * (1.0 + 1.702 * x * oms);
+    default: return 1.0;
+    }
+}
+
+/* y[i] = dY[i] * act'(X[i]) for BF16 matrices, rounded once to fp32. */
+void mxo_dactivate(const uint16_t *dy, const uint16_t *x, int64_t n, int act, float *y)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        y[i] = (float)(mxo_bf16_to_double(dy[i]) * mxo_dactivation_f64(mxo_bf16_to_double(x[i]), act));
+}

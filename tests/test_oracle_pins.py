@@ -424,3 +424,42 @@ def test_grouped_dbias_is_per_group_fsum(oracle_mod):
     assert np.allclose(got.astype(np.float64).sum(0), flat, rtol=1e-6, atol=1e-30)
     with pytest.raises(ValueError):
         oracle_mod.grouped_dbias(x, np.array([0, 64, 100, 192]))
+
+
+
+@pytest.mark.parametrize("act", [1, 2, 3, 4, 5])
+def test_dactivation_matches_torch_autograd(oracle_mod, act):
+    x = structured_input(32, 96, seed=act + 20)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    t = torch.from_numpy(xv.copy()).requires_grad_(True)
+    import torch.nn.functional as F
+    if act == 1:
+        y = torch.relu(t)
+    elif act == 2:
+        y = torch.relu(t) ** 2
+    elif act == 3:
+        y = F.gelu(t, approximate="tanh")
+    elif act == 4:
+        y = F.silu(t)
+    else:
+        y = t * torch.sigmoid(1.702 * t)
+    y.sum().backward()
+    want = t.grad.numpy()
+    got = np.array([oracle_mod.dactivation_f64(v, act) for v in xv.ravel()]).reshape(xv.shape)
+    if act in (1, 2):
+        want = np.where(xv > 0, want, 0.0)        # torch's relu'(0) = 0 as well
+        assert np.array_equal(got, want)
+    else:
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_dactivate_products_are_rounded_once(oracle_mod):
+    rng = np.random.Generator(np.random.PCG64(31))
+    dy = wl.to_bf16_bits(rng.standard_normal((32, 64)))
+    x = wl.to_bf16_bits(rng.standard_normal((32, 64)))
+    dyv = torch.from_numpy(dy.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle_mod.dactivate(dy, x, 2)                 # squared ReLU: dY * 2X, exact in fp32
+    assert np.array_equal(got.astype(np.float64), np.where(xv > 0, dyv * 2 * xv, 0.0))
+    got = oracle_mod.dactivate(dy, x, 1)
+    assert np.array_equal(got.astype(np.float64), np.where(xv > 0, dyv, 0.0))
