@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--amax", action="store_true", help="also write the per-tensor amax")
     ap.add_argument("--dbias", action="store_true", help="fused dbias (per expert for the grouped workload)")
     ap.add_argument("--act", default="none", help="activation before the cast: relu, srelu, gelu, silu, qgelu")
+    ap.add_argument("--dact", default="none",
+                    help="backward fusion: quantize dY * act'(X), dY = the workload, X = N(0,1) of the same shape")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -275,6 +277,11 @@ def run_ours(args):
     scale_col = torch.empty((mx.mxfp8_scale_bytes(N, M // 32, layout),), dtype=torch.uint8, device="cuda")
     amax = torch.empty((1,), dtype=torch.float32, device="cuda") if args.amax else None
     act = mx.binding.ACTIVATIONS[args.act.lower()]
+    dact = mx.binding.ACTIVATIONS[args.dact.lower()]
+    if dact and (act or args.swizzled or args.amax or grouped):
+        raise SystemExit("--dact takes a flat workload without --act / --swizzled / --amax")
+    x_act = (torch.from_numpy(wl.normal_bf16(M, N, seed=1234).view(np.int16)).view(torch.bfloat16).cuda()
+             if dact else None)
     if (args.swizzled or args.amax or act) and offsets is not None:
         raise SystemExit("--swizzled / --amax / --act apply to the flat workloads")
     if act and with_dbias:
@@ -294,6 +301,9 @@ def run_ours(args):
         elif grouped:
             st = mx.mxfp8_quantize_grouped(xin, M, N, G, off_dev, fmt, out_row, scale_row,
                                            out_col, scale_col, None, None, None, stream)
+        elif dact:
+            st = mx.mxfp8_quantize_dact(xin, x_act, M, N, fmt, dact, out_row, scale_row, out_col, scale_col,
+                                        dbias, ws, None, stream)
         elif args.swizzled or args.amax or act:
             cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
                                  layout, amax, act)
@@ -304,7 +314,7 @@ def run_ours(args):
         if st != 0:
             raise mx.MXFP8Error(st, "bench step")
 
-    algo_bytes = BYTES_PER_ELEM * M * N + (4 * N * max(G, 1) if with_dbias else 0)
+    algo_bytes = (BYTES_PER_ELEM + (2 if dact else 0)) * M * N + (4 * N * max(G, 1) if with_dbias else 0)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(local).uuid)
@@ -387,7 +397,7 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped or args.swizzled or args.amax or act:
+        if grouped or args.swizzled or args.amax or act or dact:
             # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
             path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"
@@ -440,7 +450,7 @@ def run_ours(args):
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "scales": "swizzled" if args.swizzled else "plain", "amax": bool(args.amax),
-                       "activation": args.act.lower(),
+                       "activation": args.act.lower(), "dact": args.dact.lower(),
                        "bytes_per_step": algo_bytes,
                        "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
                               f"bf16 input; time = sum of the per-step event intervals" if flush else

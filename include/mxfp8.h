@@ -265,6 +265,26 @@ typedef struct mxfp8_quantize_config {
 mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream);
 
 /*
+ * Backward fusion (the `with_dact` field of the PR #3137 config key): the
+ * cast of y = dY * act'(X), with dbias (optional) = column sums of y.
+ *   grad        device bf16 [M, N]: dY, 16-byte aligned.
+ *   act_input   device bf16 [M, N]: X, the activation's input, 16-byte aligned.
+ *   activation  MXFP8_ACT_RELU .. MXFP8_ACT_QGELU: act' is the derivative of
+ *               that activation (as defined for mxfp8_activation_t),
+ *               evaluated in fp32; y is the fp32 product.  dReLU and dSReLU
+ *               are exact; the others are within a few fp32 ulps.
+ *   outputs, dbias, workspace, noop, stream: as for mxfp8_quantize
+ *               (workspace: mxfp8_quantize_workspace_bytes(M, N, 1) bytes).
+ * Shapes as for mxfp8_quantize (M >= 0, N a multiple of 16).
+ */
+mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int64_t M, int64_t N,
+                                   int fp8_fmt, int activation,
+                                   void *out_row, void *scale_row,
+                                   void *out_col, void *scale_col,
+                                   float *dbias, void *workspace, const float *noop,
+                                   void *stream);
+
+/*
  * Workspace bytes for mxfp8_quantize_grouped_dbias: one fp32 partial row per
  * 128-row tile, tiles never spanning two groups, so at most
  * (ceil(total_rows/128) + num_groups) * N * 4 bytes.  0 for invalid sizes.

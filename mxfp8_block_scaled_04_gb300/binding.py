@@ -77,6 +77,8 @@ def lib():
             L.mxfp8_quantize_grouped_dbias_workspace_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_grouped_dbias.restype = i32
             L.mxfp8_quantize_grouped_dbias.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_dact.restype = i32
+            L.mxfp8_quantize_dact.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
@@ -146,6 +148,15 @@ def mxfp8_quantize_grouped_dbias(x, total_rows, N, num_groups, offsets, fp8_fmt,
                                                   _addr(out_row), _addr(scale_row), _addr(out_col),
                                                   _addr(scale_col), _addr(dbias), _addr(workspace), _addr(noop),
                                                   _addr(err_flag), _stream(stream)))
+
+
+def mxfp8_quantize_dact(grad, act_input, M, N, fp8_fmt, activation, out_row, scale_row, out_col, scale_col,
+                        dbias=None, workspace=None, noop=None, stream=None) -> int:
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_dact(_addr(grad), _addr(act_input), M, N, fp8_fmt, int(activation),
+                                         _addr(out_row), _addr(scale_row), _addr(out_col), _addr(scale_col),
+                                         _addr(dbias), _addr(workspace), _addr(noop), _stream(stream)))
 
 
 def mxfp8_quantize_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
@@ -286,6 +297,27 @@ def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool
                              staging, staging.numel(), stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_host")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+
+
+def quantize_dact(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activation="gelu",
+                  rowwise: bool = True, colwise: bool = True, with_dbias: bool = False,
+                  noop: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """The cast of grad * act'(act_input) (both contiguous CUDA bf16 [M, N]), dbias optional."""
+    for t in (grad, act_input):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("grad and act_input must be contiguous 2-D torch.bfloat16 tensors")
+    if grad.shape != act_input.shape:
+        raise ValueError("grad and act_input must have the same shape")
+    M, N = grad.shape
+    out_row, scale_row, out_col, scale_col = _alloc(grad, rowwise, colwise)
+    dbias = torch.empty((N,), dtype=torch.float32, device=grad.device) if with_dbias else None
+    ws = (torch.empty((max(mxfp8_quantize_workspace_bytes(M, N, True), 16),), dtype=torch.uint8,
+                      device=grad.device) if with_dbias else None)
+    st = mxfp8_quantize_dact(grad, act_input, M, N, _fmt(fmt), activation, out_row, scale_row, out_col,
+                             scale_col, dbias, ws, noop, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_dact")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
 
 

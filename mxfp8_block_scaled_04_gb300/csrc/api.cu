@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/mxfp8.h"
+#include "dact.cuh"
 #include "dbias_reduce.cuh"
 #include "quantize.cuh"
 
@@ -27,6 +28,7 @@ struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int ctas_per_sm[192] = {};  // indexed by kernel variant
+    int dact_ctas_per_sm[24] = {};  // dact kernels: FMT + 2 * DBIAS + 4 * ACT
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -185,6 +187,51 @@ __global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const 
 // Enqueue the flat quantize kernel (no validation: the caller has checked every
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
+// The backward-fusion kernel (dY * act'(X)): one-time set-up per (device, variant), then launch.
+template <int FMT, bool DBIAS, int ACT>
+mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUtensorMap &map_x, const QuantParams &p,
+                               int64_t tiles, cudaStream_t stream)
+{
+    int cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (device < 0 || device >= kMaxDevices)
+            return MXFP8_ERR_DEVICE;
+        DeviceInfo &d = g_dev[device];
+        if (!d.ready) {
+            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+                return MXFP8_ERR_DEVICE;
+            d.ready = true;
+        }
+        const int v = FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT;
+        if (d.dact_ctas_per_sm[v] == 0) {
+            auto kern = quantize_dact_kernel<FMT, DBIAS, ACT>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDact) != cudaSuccess)
+                return MXFP8_ERR_LAUNCH;
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDact) != cudaSuccess || n < 1)
+                return MXFP8_ERR_LAUNCH;
+            d.dact_ctas_per_sm[v] = n;
+        }
+        cap = d.dact_ctas_per_sm[v] * d.sm_count;
+    }
+    const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+    quantize_dact_kernel<FMT, DBIAS, ACT><<<grid, kThreads, kSmemDact, stream>>>(map_g, map_x, p);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+template <int ACT>
+mxfp8_status_t launch_dact(int fmt, bool dbias, int device, const CUtensorMap &map_g, const CUtensorMap &map_x,
+                           const QuantParams &p, int64_t tiles, cudaStream_t stream)
+{
+    if (fmt == MXFP8_E4M3)
+        return dbias ? launch_dact_fmt<0, true, ACT>(device, map_g, map_x, p, tiles, stream)
+                     : launch_dact_fmt<0, false, ACT>(device, map_g, map_x, p, tiles, stream);
+    return dbias ? launch_dact_fmt<1, true, ACT>(device, map_g, map_x, p, tiles, stream)
+                 : launch_dact_fmt<1, false, ACT>(device, map_g, map_x, p, tiles, stream);
+}
+
 // Activated (ACT != 0) variants: flat, no dbias; swizzle and amax as template switches.
 template <int ACT>
 mxfp8_status_t launch_activated(int opts, int fmt, int device, const CUtensorMap &map, const QuantParams &p,
@@ -490,6 +537,72 @@ mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t
     (void)workspace;
     return grouped_impl(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col, scale_col,
                         nullptr, nullptr, noop, err_flag, static_cast<cudaStream_t>(stream_));
+}
+
+mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int64_t M, int64_t N, int fp8_fmt,
+                                   int activation, void *out_row, void *scale_row, void *out_col, void *scale_col,
+                                   float *dbias, void *workspace, const float *noop, void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    const bool empty = M == 0 || N == 0;
+    mxfp8_status_t st;
+    if (!empty) {
+        if (grad == nullptr || act_input == nullptr)
+            return MXFP8_ERR_NULL;
+        if ((st = check_outputs(out_row, scale_row, out_col, scale_col)) != MXFP8_OK)
+            return st;
+    }
+    if (!aligned(grad, 16) || !aligned(act_input, 16) || !aligned(dbias, 4) || !aligned(workspace, 16))
+        return MXFP8_ERR_ALIGN;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kDBN - 1) / kDBN;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (dbias != nullptr && workspace == nullptr && M > 0)
+        return MXFP8_ERR_WORKSPACE;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(grad, device) || !on_device(act_input, device) || !on_device(out_row, device) ||
+        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
+        !on_device(dbias, device) || !on_device(workspace, device) || !on_device(noop, device))
+        return MXFP8_ERR_DEVICE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!empty) {
+        CUtensorMap map_g, map_x;
+        if ((st = make_tensor_map(&map_g, grad, M, N)) != MXFP8_OK ||
+            (st = make_tensor_map(&map_x, act_input, M, N)) != MXFP8_OK)
+            return st;
+        QuantParams p{};
+        p.out_row = static_cast<uint8_t *>(out_row);
+        p.scale_row = static_cast<uint8_t *>(scale_row);
+        p.out_col = static_cast<uint8_t *>(out_col);
+        p.scale_col = static_cast<uint8_t *>(scale_col);
+        p.ws = dbias != nullptr ? static_cast<float *>(workspace) : nullptr;
+        p.noop = noop;
+        p.M = M;
+        p.N = N;
+        p.row_tiles = static_cast<int>(row_tiles);
+        p.col_tiles = static_cast<int>(col_tiles);
+        const bool db = dbias != nullptr;
+        const int64_t tiles = row_tiles * col_tiles;
+        switch (activation) {
+        case MXFP8_ACT_RELU: st = launch_dact<1>(fp8_fmt, db, device, map_g, map_x, p, tiles, stream); break;
+        case MXFP8_ACT_SRELU: st = launch_dact<2>(fp8_fmt, db, device, map_g, map_x, p, tiles, stream); break;
+        case MXFP8_ACT_GELU: st = launch_dact<3>(fp8_fmt, db, device, map_g, map_x, p, tiles, stream); break;
+        case MXFP8_ACT_SILU: st = launch_dact<4>(fp8_fmt, db, device, map_g, map_x, p, tiles, stream); break;
+        default: st = launch_dact<5>(fp8_fmt, db, device, map_g, map_x, p, tiles, stream); break;
+        }
+        if (st != MXFP8_OK)
+            return st;
+    }
+    if (dbias != nullptr && N > 0)
+        return enqueue_reduce(static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop, stream);
+    return MXFP8_OK;
 }
 
 size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups)

@@ -1,0 +1,259 @@
+// Backward fusion: the MXFP8 cast of dY * act'(X) (the `with_dact` field of
+// the quantization config key on "[Common] Experimental CuTeDSL MXFP8
+// backends in C++ via TVM-FFI", TransformerEngine PR #3137), with an optional
+// fused dbias of the product.
+//
+// Two BF16 inputs per element, so a tile is 128 rows x 64 columns: each stage
+// holds one 64-column TMA box of dY and one of X (16 KiB each, 128B swizzle),
+// which keeps the 32 KiB stages and 2 CTAs per SM of the main kernel.
+//   - phase 1: warp w takes rows 32*(w>>1) + 16*(w&1) .. +15 of the tile; a
+//     lane takes 4 columns x 8 rows; the two 16-row halves of a 32-row block
+//     meet in shared memory, where one thread per (row block, column) forms
+//     the column's scale, multiplier and dbias partial;
+//   - phase 2: warp w takes the 8-row groups w and w + 8; a lane takes 16
+//     columns of one row, as in the main kernel.
+// The derivative is evaluated in fp32 with the same ex2 / rcp approximations
+// as the forward activations; dReLU and dSReLU are exact.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+#include "quantize.cuh"
+
+namespace mxfp8 {
+
+constexpr int kDBN = 64;  // tile columns (one box per input)
+constexpr int kDOffColMul = kStages * kStageBytes;         // float [4][64]
+constexpr int kDOffDSum = kDOffColMul + 4 * kDBN * 4;      // float [4][64]
+constexpr int kDOffPartF = kDOffDSum + 4 * kDBN * 4;       // float [2][4][64]
+constexpr int kDOffPartD = kDOffPartF + 2 * 4 * kDBN * 4;  // float [2][4][64]
+constexpr int kDOffBars = kDOffPartD + 2 * 4 * kDBN * 4;   // uint64 [kStages]
+constexpr int kDOffCoord = kDOffBars + 8 * kStages;        // TileCoord [kStages]
+constexpr int kSmemDact = kDOffCoord + 32 * kStages + 1024;
+
+// act'(x) in fp32: 1 dReLU, 2 dSReLU, 3 dGeLU (tanh form), 4 dSiLU, 5 dQGeLU.
+// sigmoid(t) and 1 - sigmoid(t) both come from e = 2^(-|t| log2 e).
+template <int ACT>
+__device__ __forceinline__ float dactivation(float x)
+{
+    if constexpr (ACT == 1) {
+        return x > 0.f ? 1.f : 0.f;
+    } else if constexpr (ACT == 2) {
+        return x > 0.f ? 2.f * x : 0.f;
+    } else {
+        float t;
+        if constexpr (ACT == 3)
+            t = 1.5957691216057308f * (x + 0.044715f * x * x * x);
+        else if constexpr (ACT == 4)
+            t = x;
+        else
+            t = 1.702f * x;
+        const float e = ex2_approx(-1.4426950408889634f * fabsf(t));
+        const float inv = rcp_approx(1.f + e);
+        const float s = t >= 0.f ? inv : e * inv;
+        const float oms = t >= 0.f ? e * inv : inv;
+        if constexpr (ACT == 3)
+            return s + x * s * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x));
+        else if constexpr (ACT == 4)
+            return s * (1.f + x * oms);
+        else
+            return s * (1.f + 1.702f * x * oms);
+    }
+}
+
+template <int FMT, bool DBIAS, int ACT>
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_dact_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_x,
+                         const QuantParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *colmul = reinterpret_cast<float *>(smem + kDOffColMul);
+    float *dsum = reinterpret_cast<float *>(smem + kDOffDSum);
+    float *part_f = reinterpret_cast<float *>(smem + kDOffPartF);
+    float *part_d = reinterpret_cast<float *>(smem + kDOffPartD);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDOffBars);
+    TileCoord *coords = reinterpret_cast<TileCoord *>(smem + kDOffCoord);
+
+    if (p.noop != nullptr && *p.noop == 1.0f)
+        return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t N = p.N;
+    const int num_tiles = p.row_tiles * p.col_tiles;
+    const int first = blockIdx.x, stride = gridDim.x;
+    const int my_count = first < num_tiles ? (num_tiles - 1 - first) / stride + 1 : 0;
+    if (my_count == 0)
+        return;
+    const bool do_row = p.out_row != nullptr, do_col = p.out_col != nullptr;
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmap_g);
+        prefetch_tensormap(&tmap_x);
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(smem_u32(&bars[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int slot, int t) {
+        const int rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
+        TileCoord c;
+        c.row0 = static_cast<int64_t>(rt) * kBM;
+        c.row_end = min(c.row0 + kBM, p.M);
+        c.col0 = ct * kDBN;
+        c.rt = rt;
+        coords[slot] = c;  // published to the consumers by the arrive below
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t dst = smem_u32(smem + slot * kStageBytes);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_2d(dst, &tmap_g, bar, c.col0, static_cast<int32_t>(c.row0));
+        tma_load_2d(dst + kBoxBytes, &tmap_x, bar, c.col0, static_cast<int32_t>(c.row0));
+    };
+    if (tid == 0)
+        for (int s = 0; s < kStages && s < my_count; ++s)
+            issue(s, first + s * stride);
+
+    for (int it = 0; it < my_count; ++it) {
+        const int slot = it % kStages;
+        const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
+        const unsigned char *gbox = smem + slot * kStageBytes;
+        const unsigned char *xbox = gbox + kBoxBytes;
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
+        const TileCoord tc = coords[slot];
+
+        // ---- phase 1: column amax / sums over 16-row halves ----
+        if (ok) {
+            const int rb = warp >> 1, hh = warp & 1;
+            const int cq = lane & 15, q = lane >> 4;
+            const int r0 = rb * 32 + hh * 16 + q * 8;  // r0 & 7 == 0
+            float f[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int off = (r0 + i) * 128 + (((cq >> 1) ^ i) << 4) + (cq & 1) * 8;
+                const uint2 g = lds64(gbox + off), xv = lds64(xbox + off);
+                const float y0 = bf16_lo(g.x) * dactivation<ACT>(bf16_lo(xv.x));
+                const float y1 = bf16_hi(g.x) * dactivation<ACT>(bf16_hi(xv.x));
+                const float y2 = bf16_lo(g.y) * dactivation<ACT>(bf16_lo(xv.y));
+                const float y3 = bf16_hi(g.y) * dactivation<ACT>(bf16_hi(xv.y));
+                f[0] = fmaxf(f[0], fabsf(y0));
+                f[1] = fmaxf(f[1], fabsf(y1));
+                f[2] = fmaxf(f[2], fabsf(y2));
+                f[3] = fmaxf(f[3], fabsf(y3));
+                if constexpr (DBIAS) {
+                    d[0] += y0;
+                    d[1] += y1;
+                    d[2] += y2;
+                    d[3] += y3;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                f[k] = fmaxf(f[k], __shfl_xor_sync(0xffffffffu, f[k], 16));
+                if constexpr (DBIAS)
+                    d[k] += __shfl_xor_sync(0xffffffffu, d[k], 16);  // a + b == b + a
+            }
+            if (q == 0) {
+                const int o = (hh * 4 + rb) * kDBN + cq * 4;
+                *reinterpret_cast<float4 *>(part_f + o) = make_float4(f[0], f[1], f[2], f[3]);
+                if constexpr (DBIAS)
+                    *reinterpret_cast<float4 *>(part_d + o) = make_float4(d[0], d[1], d[2], d[3]);
+            }
+        }
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_fault_word, 1u);
+                for (int j = it; j < my_count && j < it + kStages; ++j)
+                    mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
+                                      kDrainLimitNs);
+            }
+            return;
+        }
+        // one thread per (32-row block, column): scale, multiplier, dbias partial
+        {
+            const int rb = tid >> 6, c = tid & 63;
+            const float amax = fmaxf(part_f[rb * kDBN + c], part_f[(4 + rb) * kDBN + c]);
+            const int e = block_exponent_f32<FMT>(__float_as_uint(amax));
+            const int64_t grow = tc.row0 + rb * 32, gcol = tc.col0 + c;
+            if (do_col && grow < tc.row_end && gcol < N)
+                p.scale_col[(grow >> 5) * N + gcol] = static_cast<uint8_t>(e);
+            const int sp = c >> 4, qq = (c >> 2) & 3;  // rotated layout, as in the main kernel
+            colmul[rb * kDBN + 4 * (4 * sp + ((qq + (sp >> 1)) & 3)) + (c & 3)] = scale_multiplier(e);
+            if constexpr (DBIAS)
+                dsum[rb * kDBN + c] = grow < tc.row_end ? part_d[rb * kDBN + c] + part_d[(4 + rb) * kDBN + c] : 0.f;
+        }
+        __syncthreads();
+        if constexpr (DBIAS) {
+            if (tid < kDBN) {
+                const int64_t gcol = tc.col0 + tid;
+                if (gcol < N)
+                    p.ws[static_cast<int64_t>(tc.rt) * N + gcol] =
+                        ((dsum[tid] + dsum[kDBN + tid]) + dsum[2 * kDBN + tid]) + dsum[3 * kDBN + tid];
+            }
+        }
+
+        // ---- phase 2: 16-column row segments ----
+        {
+            const int rr = lane >> 2, sp = lane & 3;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int rg = warp + 8 * k;
+                if (tc.row0 + rg * 8 >= tc.row_end)
+                    continue;
+                const int r = rg * 8 + rr;
+                const int p0 = (2 * sp) ^ rr;
+                const uint4 GA = lds128(gbox + r * 128 + p0 * 16), GB = lds128(gbox + r * 128 + (p0 ^ 1) * 16);
+                const uint4 XA = lds128(xbox + r * 128 + p0 * 16), XB = lds128(xbox + r * 128 + (p0 ^ 1) * 16);
+                const uint32_t gw[8] = {GA.x, GA.y, GA.z, GA.w, GB.x, GB.y, GB.z, GB.w};
+                const uint32_t xw[8] = {XA.x, XA.y, XA.z, XA.w, XB.x, XB.y, XB.z, XB.w};
+                float y[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    y[2 * j] = bf16_lo(gw[j]) * dactivation<ACT>(bf16_lo(xw[j]));
+                    y[2 * j + 1] = bf16_hi(gw[j]) * dactivation<ACT>(bf16_hi(xw[j]));
+                }
+                const int64_t grow = tc.row0 + r, gcol = tc.col0 + sp * 16;
+                const bool in = grow < tc.row_end && gcol < N;
+                if (do_row) {
+                    float fm = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        fm = fmaxf(fm, fabsf(y[i]));
+                    fm = fmaxf(fm, __shfl_xor_sync(0xffffffffu, fm, 1));
+                    const int er = block_exponent_f32<FMT>(__float_as_uint(fm));
+                    const float rm = scale_multiplier(er);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        o[j] = cvt_fp8x2<FMT>(y[4 * j] * rm, y[4 * j + 1] * rm) |
+                               (cvt_fp8x2<FMT>(y[4 * j + 2] * rm, y[4 * j + 3] * rm) << 16);
+                    if (in) {
+                        stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        if ((sp & 1) == 0)
+                            p.scale_row[grow * ((N + 31) >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                    }
+                }
+                if (do_col) {
+                    const float *cm = colmul + (r >> 5) * kDBN + sp * 16;
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
+                        o[j] = cvt_fp8x2<FMT>(y[4 * j] * c.x, y[4 * j + 1] * c.y) |
+                               (cvt_fp8x2<FMT>(y[4 * j + 2] * c.z, y[4 * j + 3] * c.w) << 16);
+                    }
+                    if (in)
+                        stg128(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                }
+            }
+        }
+        __syncthreads();  // stage, colmul and dsum are free again
+        if (tid == 0 && it + kStages < my_count)
+            issue(slot, first + (it + kStages) * stride);
+    }
+}
+
+}  // namespace mxfp8

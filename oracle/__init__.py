@@ -210,15 +210,15 @@ def quantize_f32(y: np.ndarray, fmt: int, rowwise: bool = True, colwise: bool = 
     y = np.ascontiguousarray(y, dtype=np.float32)
     M, N = y.shape
     out_row = np.empty((M, N), np.uint8) if rowwise else None
-    scale_row = np.empty((M, N // BLOCK), np.uint8) if rowwise else None
+    scale_row = np.empty((M, -(-N // BLOCK)), np.uint8) if rowwise else None
     out_col = np.empty((M, N), np.uint8) if colwise else None
-    scale_col = np.empty((M // BLOCK, N), np.uint8) if colwise else None
+    scale_col = np.empty((-(-M // BLOCK), N), np.uint8) if colwise else None
     dbias = np.empty((N,), np.float32) if with_dbias else None
     rc = _load().mxo_quantize_f32(_ptr(y, ctypes.c_float), M, N, fmt, _ptr(out_row, ctypes.c_uint8),
                                   _ptr(scale_row, ctypes.c_uint8), _ptr(out_col, ctypes.c_uint8),
                                   _ptr(scale_col, ctypes.c_uint8), _ptr(dbias, ctypes.c_float))
     if rc != 0:
-        raise ValueError("oracle: M, N must be non-negative multiples of 32")
+        raise ValueError("oracle: M, N must be non-negative")
     return out_row, scale_row, out_col, scale_col, dbias
 
 

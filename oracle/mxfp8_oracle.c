@@ -359,47 +359,50 @@ float mxo_activation(double x, int act)
 }
 
 /*
- * Quantize fp32 values y[M,N] (already activated): same blocks, scale rule
- * and rounding as mxo_quantize, evaluated exactly on the fp32 values; dbias
- * (if requested) is the column sum of y.
+ * Quantize fp32 values y[M,N] (already activated): same blocks (partial last
+ * blocks included), scale rule and rounding as mxo_quantize, evaluated
+ * exactly on the fp32 values; dbias (if requested) is the column sum of y.
  */
 int mxo_quantize_f32(const float *y, int64_t M, int64_t N, int fmt,
                      uint8_t *out_row, uint8_t *scale_row,
                      uint8_t *out_col, uint8_t *scale_col, float *dbias)
 {
     int64_t i, j, c, r, k;
-    if (M < 0 || N < 0 || M % MXO_BLOCK || N % MXO_BLOCK)
+    if (M < 0 || N < 0)
         return -1;
+    const int64_t Cr = (N + MXO_BLOCK - 1) / MXO_BLOCK, Rc = (M + MXO_BLOCK - 1) / MXO_BLOCK;
     if (out_row && scale_row) {
         for (i = 0; i < M; i++) {
-            for (c = 0; c < N / MXO_BLOCK; c++) {
-                const float *blk = y + i * N + c * MXO_BLOCK;
+            for (c = 0; c < Cr; c++) {
+                const int64_t j0 = c * MXO_BLOCK, len = N - j0 < MXO_BLOCK ? N - j0 : MXO_BLOCK;
+                const float *blk = y + i * N + j0;
                 double amax = 0.0;
-                for (k = 0; k < MXO_BLOCK; k++)
+                for (k = 0; k < len; k++)
                     if (fabs((double)blk[k]) > amax)
                         amax = fabs((double)blk[k]);
                 const int e = mxo_block_exponent(amax, fmt);
                 const double s = ldexp(1.0, 127 - e);
-                scale_row[i * (N / MXO_BLOCK) + c] = (uint8_t)e;
-                for (k = 0; k < MXO_BLOCK; k++)
-                    out_row[i * N + c * MXO_BLOCK + k] = mxo_fp8_encode((double)blk[k] * s, fmt);
+                scale_row[i * Cr + c] = (uint8_t)e;
+                for (k = 0; k < len; k++)
+                    out_row[i * N + j0 + k] = mxo_fp8_encode((double)blk[k] * s, fmt);
             }
         }
     }
     if (out_col && scale_col) {
-        for (r = 0; r < M / MXO_BLOCK; r++) {
+        for (r = 0; r < Rc; r++) {
+            const int64_t i0 = r * MXO_BLOCK, len = M - i0 < MXO_BLOCK ? M - i0 : MXO_BLOCK;
             for (j = 0; j < N; j++) {
                 double amax = 0.0;
-                for (k = 0; k < MXO_BLOCK; k++) {
-                    const double a = fabs((double)y[(r * MXO_BLOCK + k) * N + j]);
+                for (k = 0; k < len; k++) {
+                    const double a = fabs((double)y[(i0 + k) * N + j]);
                     if (a > amax)
                         amax = a;
                 }
                 const int e = mxo_block_exponent(amax, fmt);
                 const double s = ldexp(1.0, 127 - e);
                 scale_col[r * N + j] = (uint8_t)e;
-                for (k = 0; k < MXO_BLOCK; k++) {
-                    const int64_t idx = (r * MXO_BLOCK + k) * N + j;
+                for (k = 0; k < len; k++) {
+                    const int64_t idx = (i0 + k) * N + j;
                     out_col[idx] = mxo_fp8_encode((double)y[idx] * s, fmt);
                 }
             }

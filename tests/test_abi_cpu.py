@@ -184,3 +184,17 @@ def test_grouped_dbias_host_checks(cuda_lib):
     assert gd() == DEVICE
     assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 64) == (512 + 64) * 7168 * 4
     assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 0) == 0
+
+
+def test_dact_host_checks(cuda_lib):
+    def d(**kw):
+        a = dict(g=A, x=A, M=64, N=64, fmt=0, act=3, dbias=None, ws=None)
+        a.update(kw)
+        return mx.mxfp8_quantize_dact(a["g"], a["x"], a["M"], a["N"], a["fmt"], a["act"], A, A, A, A,
+                                      a["dbias"], a["ws"], None, 0)
+    assert d(act=0) == FORMAT and d(act=6) == FORMAT and d(fmt=2) == FORMAT
+    assert d(N=40) == SHAPE
+    assert d(x=None) == NULL and d(g=None) == NULL
+    assert d(x=A + 8) == ALIGN
+    assert d(dbias=A) == WORKSPACE
+    assert d() == DEVICE

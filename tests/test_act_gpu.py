@@ -45,12 +45,12 @@ def x_values(x_bits):
     return torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
 
 
-def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, x_bits, act, fmt, colwise):
-    """Compare one direction; returns how many codes needed the boundary rule."""
-    M, N = x_bits.shape
-    xv = x_values(x_bits)
-    y32 = oracle_mod.activate(x_bits, act)
-    exact = act in (1, 2)
+def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, y32, value64, exact, fmt, colwise):
+    """Compare one direction; returns how many codes needed the boundary rule.
+
+    y32: the oracle's fp32 values; value64(i, j): the exact (double) value of element (i, j).
+    """
+    M, N = y32.shape
     if exact:
         assert np.array_equal(gpu_scales, ref_scales)
         assert np.array_equal(gpu_codes, ref_codes)
@@ -59,9 +59,9 @@ def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, x_bits
     def block_of(i, j):   # element indices of the block holding (i, j)
         if colwise:
             r0 = (i // 32) * 32
-            return [(r, j) for r in range(r0, r0 + 32)]
+            return [(r, j) for r in range(r0, min(r0 + 32, M))]
         c0 = (j // 32) * 32
-        return [(i, c) for c in range(c0, c0 + 32)]
+        return [(i, c) for c in range(c0, min(c0 + 32, N))]
 
     used = 0
     expected = ref_codes.copy()
@@ -72,17 +72,17 @@ def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, x_bits
         assert abs(eg - eo) == 1, (s_idx, eg, eo)
         i, j = (s_idx[0] * 32, s_idx[1]) if colwise else (s_idx[0], s_idx[1] * 32)
         elems = block_of(i, j)
-        amax64 = max(abs(oracle_mod.activation_f64(xv[e], act)) for e in elems)
+        amax64 = max(abs(value64(*e)) for e in elems)
         boundary = FMAX[fmt] * 2.0 ** (min(eg, eo) - 127)
         assert abs(amax64 - boundary) <= TOL * boundary, (s_idx, amax64, boundary)
         for e in elems:   # this block's codes at the GPU's exponent
             expected[e] = oracle_mod.fp8_encode(float(y32[e]) * 2.0 ** (127 - eg), fmt)
-        used += 32
+        used += len(elems)
     for e in np.argwhere(gpu_codes != expected):
         e = tuple(e)
         i, j = e
         sc = int(gpu_scales[i // 32, j] if colwise else gpu_scales[i, j // 32])
-        v64 = oracle_mod.activation_f64(xv[e], act) * 2.0 ** (127 - sc)
+        v64 = value64(i, j) * 2.0 ** (127 - sc)
         dg = oracle_mod.fp8_decode(int(gpu_codes[e]), fmt)
         do = oracle_mod.fp8_decode(int(expected[e]), fmt)
         mid = (dg + do) / 2
@@ -91,6 +91,11 @@ def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, x_bits
         used += 1
     assert used <= max(1e-4 * M * N, 64), used
     return used
+
+
+def act_checker(oracle_mod, x_bits, a):
+    xv = x_values(x_bits)
+    return oracle_mod.activate(x_bits, a), (lambda i, j: oracle_mod.activation_f64(xv[i, j], a))
 
 
 @pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
@@ -102,8 +107,10 @@ def test_activation_parity(oracle_mod, act, fmt):
     r = mx.quantize(dev(x_bits), fmt, activation=act, with_amax=True)
     torch.cuda.synchronize()
     o = oracle_mod.quantize_act(x_bits, fmt, a)
-    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], x_bits, a, fmt, False)
-    check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], x_bits, a, fmt, True)
+    y32, v64 = act_checker(oracle_mod, x_bits, a)
+    exact = a in (1, 2)
+    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, v64, exact, fmt, False)
+    check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], y32, v64, exact, fmt, True)
     amax_ref = float(np.abs(oracle_mod.activate(x_bits, a)).max())
     if a in (1, 2):
         assert float(r.amax.item()) == amax_ref
@@ -133,3 +140,26 @@ def test_activation_with_dbias_is_rejected():
     x = dev(act_input(64, 64, seed=1))
     with pytest.raises(mx.MXFP8Error):
         mx.quantize(x, 0, with_dbias=True, activation="relu")
+
+
+
+# ---- backward fusion: dY * act'(X) ------------------------------------------------
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("fmt,shape", [(1, (544, 1056)), (0, (45, 80)), (1, (257, 4112))])
+def test_dact_parity_with_dbias(oracle_mod, act, fmt, shape):
+    M, N = shape
+    a = mx.binding.ACTIVATIONS[act]
+    dy_bits = wl.grad_bf16(M, N, seed=M + a)
+    x_bits = act_input(M, N, seed=N + a) if M >= 8 else wl.normal_bf16(M, N, seed=a)
+    r = mx.quantize_dact(dev(dy_bits), dev(x_bits), fmt, act, with_dbias=True)
+    torch.cuda.synchronize()
+    y32 = oracle_mod.dactivate(dy_bits, x_bits, a)
+    o = oracle_mod.quantize_f32(y32, fmt, with_dbias=True)
+    dyv, xv = x_values(dy_bits), x_values(x_bits)
+    v64 = lambda i, j: dyv[i, j] * oracle_mod.dactivation_f64(xv[i, j], a)
+    exact = a in (1, 2)
+    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, v64, exact, fmt, False)
+    check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], y32, v64, exact, fmt, True)
+    tol = 1e-5 * np.abs(y32.astype(np.float64)).sum(0) + 1e-30
+    assert np.all(np.abs(r.dbias.cpu().numpy().astype(np.float64) - o[4]) <= tol)

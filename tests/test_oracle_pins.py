@@ -391,8 +391,9 @@ def test_activation_matches_torch_float64(oracle_mod, act):
     assert np.all(got[xv < 0] >= (-0.3 if act > 2 else 0.0))
 
 
-def test_act_none_quantize_f32_equals_bf16_path(oracle_mod):
-    x = structured_input(96, 64, seed=11)
+@pytest.mark.parametrize("shape", [(96, 64), (45, 80)])
+def test_act_none_quantize_f32_equals_bf16_path(oracle_mod, shape):
+    x = structured_input(*shape, seed=11)
     y = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float().numpy()
     a = oracle_mod.quantize(x, 0, with_dbias=True)
     b = oracle_mod.quantize_f32(y, 0, with_dbias=True)
