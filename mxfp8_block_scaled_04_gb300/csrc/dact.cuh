@@ -54,8 +54,10 @@ __device__ __forceinline__ float dactivation(float x)
         const float inv = rcp_approx(1.f + e);
         const float s = t >= 0.f ? inv : e * inv;
         const float oms = t >= 0.f ? e * inv : inv;
+        // s (1 + x (1 - s) t') rather than s + x s (1 - s) t': when s underflows to 0
+        // for very negative x this keeps the sign of the (tiny, negative) derivative
         if constexpr (ACT == 3)
-            return s + x * s * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x));
+            return s * (1.f + x * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x)));
         else if constexpr (ACT == 4)
             return s * (1.f + x * oms);
         else

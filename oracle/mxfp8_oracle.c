@@ -461,7 +461,7 @@ int mxo_grouped_dbias(const uint16_t *x, int64_t total_rows, int64_t N, int num_
  * fp32 and multiplied by dY in fp32:
  *   1 dReLU    X > 0 ? 1 : 0
  *   2 dSReLU   X > 0 ? 2X : 0
- *   3 dGeLU    s + X s (1-s) t',  s = sigmoid(t), t = 2 sqrt(2/pi) (X + 0.044715 X^3),
+ *   3 dGeLU    s (1 + X (1-s) t'), s = sigmoid(t), t = 2 sqrt(2/pi) (X + 0.044715 X^3),
  *                                 t' = 2 sqrt(2/pi) (1 + 3 * 0.044715 X^2)
  *   4 dSiLU    s (1 + X (1-s)),   s = sigmoid(X)
  *   5 dQGeLU   s (1 + 1.702 X (1-s)), s = sigmoid(1.702 X)
@@ -488,7 +488,7 @@ double mxo_dactivation_f64(double x, int act)
         const double c = 2.0 * 0.7978845608028654;
         const double t = c * (x + 0.044715 * x * x * x), dt = c * (1.0 + 3.0 * 0.044715 * x * x);
         mxo_sigmoid_pair(t, &s, &oms);
-        return s + x * s * oms * dt;
+        return s * (1.0 + x * oms * dt);   /* factored: keeps the sign when s underflows */
     }
     case 4:
         mxo_sigmoid_pair(x, &s, &oms);

@@ -464,3 +464,14 @@ def test_dactivate_products_are_rounded_once(oracle_mod):
     assert np.array_equal(got.astype(np.float64), np.where(xv > 0, dyv * 2 * xv, 0.0))
     got = oracle_mod.dactivate(dy, x, 1)
     assert np.array_equal(got.astype(np.float64), np.where(xv > 0, dyv, 0.0))
+
+
+
+@pytest.mark.parametrize("act", [3, 4, 5])
+def test_dactivation_sign_for_very_negative_inputs(oracle_mod, act):
+    # for x below the activation's minimum the derivative is negative, however small:
+    # its sign must survive underflow (a negative value that rounds to zero stays -0)
+    for x in (-5.0, -12.0, -25.0, -100.0, -1e4):
+        d = oracle_mod.dactivation_f64(x, act)
+        assert d <= 0.0 and math.copysign(1.0, d) == -1.0, (act, x, d)
+    assert oracle_mod.dactivation_f64(-0.5, 4) > 0.0 and oracle_mod.dactivation_f64(1.0, 3) > 1.0
