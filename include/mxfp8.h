@@ -285,9 +285,11 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
                                    void *stream);
 
 /*
- * Workspace bytes for mxfp8_quantize_grouped_dbias: one fp32 partial row per
- * 128-row tile, tiles never spanning two groups, so at most
- * (ceil(total_rows/128) + num_groups) * N * 4 bytes.  0 for invalid sizes.
+ * Workspace bytes for mxfp8_quantize_grouped_dbias: a header of
+ * (num_groups + 1) int64 (each group's first row tile) padded to 256 bytes,
+ * then one fp32 partial row per 128-row tile, tiles never spanning two
+ * groups: at most (ceil(total_rows/128) + num_groups) * N * 4 bytes.  0 for
+ * invalid sizes.
  */
 size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups);
 

@@ -307,6 +307,13 @@ mxfp8_status_t enqueue_reduce(const float *ws, int64_t row_tiles, int64_t N, flo
     return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
 }
 
+// The grouped dbias workspace starts with an int64 header [num_groups + 1] (each
+// group's first row tile), padded to 256 bytes; the fp32 partials follow.
+int64_t grouped_header_floats(int num_groups)
+{
+    return ((static_cast<int64_t>(num_groups) + 1) * 8 + 255) / 256 * 256 / 4;
+}
+
 // The grouped call, with or without per-group dbias (ws and dbias both set).
 mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int num_groups, const int64_t *offsets,
                             int fp8_fmt, void *out_row, void *scale_row, void *out_col, void *scale_col,
@@ -349,7 +356,8 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
         p.scale_row = static_cast<uint8_t *>(scale_row);
         p.out_col = static_cast<uint8_t *>(out_col);
         p.scale_col = static_cast<uint8_t *>(scale_col);
-        p.ws = ws;
+        p.ws = ws != nullptr ? ws + grouped_header_floats(num_groups) : nullptr;
+        p.ws_hdr = reinterpret_cast<int64_t *>(ws);
         p.noop = noop;
         p.offsets = offsets;
         p.err_flag = err_flag;
@@ -364,8 +372,8 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
     }
     if (dbias != nullptr && N > 0) {
         const dim3 grid(static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols), static_cast<unsigned>(num_groups));
-        dbias_reduce_grouped_kernel<<<grid, kReduceCols * kReduceWarps, 0, stream>>>(ws, offsets, num_groups,
-                                                                                      total_rows, N, dbias, noop);
+        dbias_reduce_grouped_kernel<<<grid, kReduceCols * kReduceWarps, 0, stream>>>(
+            ws + grouped_header_floats(num_groups), reinterpret_cast<const int64_t *>(ws), N, dbias, noop);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (cudaGetLastError() != cudaSuccess)
             return MXFP8_ERR_LAUNCH;
@@ -609,7 +617,8 @@ size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t 
 {
     if (total_rows < 0 || N < 0 || num_groups < 1 || total_rows % 32 || N % 16)
         return 0;
-    return static_cast<size_t>((total_rows + kBM - 1) / kBM + num_groups) * static_cast<size_t>(N) * sizeof(float);
+    return static_cast<size_t>(grouped_header_floats(num_groups)) * sizeof(float) +
+           static_cast<size_t>((total_rows + kBM - 1) / kBM + num_groups) * static_cast<size_t>(N) * sizeof(float);
 }
 
 mxfp8_status_t mxfp8_quantize_grouped_dbias(const void *x, int64_t total_rows, int64_t N, int num_groups,

@@ -46,53 +46,23 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
 }
 
 // Per-group dbias of the grouped call: dbias[g][j] = sum over the row tiles of
-// group g of ws[t][j].  The grouped quantize kernel numbers row tiles group by
-// group (group g's tiles follow those of groups 0..g-1, ceil(rows/128) each),
-// so CTA (column block, g) first finds its group's first row tile with a block
-// sum over the offsets, re-checking them on the way (invalid offsets: write
-// nothing, as the quantize kernel does), then sums like the flat reduce.
+// group g of ws[t][j].  The grouped quantize kernel writes each group's first
+// row tile into hdr[0..G] (hdr[G] = total), or hdr[0] = -1 when the offsets are
+// invalid (then nothing is written here either).  CTA (column block, g) sums
+// its group's tiles like the flat reduce: warp w takes tiles w, w+16, ... and
+// the 16 warp sums are added in warp order.
 __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
-    dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ offsets, int G,
-                                int64_t total_rows, int64_t N, float *__restrict__ dbias, const float *noop)
+    dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ hdr, int64_t N,
+                                float *__restrict__ dbias, const float *noop)
 {
     if (noop != nullptr && *noop == 1.0f)
         return;
-    __shared__ long long s_start[kReduceWarps];
-    __shared__ int s_bad[kReduceWarps];
+    if (hdr[0] < 0)
+        return;
     __shared__ float part[kReduceWarps][kReduceCols];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = blockIdx.y;
-    long long start = 0;
-    int bad = 0;
-    for (int h = threadIdx.x; h < G; h += blockDim.x) {
-        const int64_t a = offsets[h], b = offsets[h + 1];
-        if (b < a || (b & 31))
-            bad = 1;
-        if (h < g)
-            start += (b - a + 127) / 128;
-    }
-    if (threadIdx.x == 0 && (offsets[0] != 0 || offsets[G] != total_rows))
-        bad = 1;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-        start += __shfl_xor_sync(0xffffffffu, start, d);
-        bad |= __shfl_xor_sync(0xffffffffu, bad, d);
-    }
-    if (lane == 0) {
-        s_start[warp] = start;
-        s_bad[warp] = bad;
-    }
-    __syncthreads();
-    start = 0;
-    bad = 0;
-#pragma unroll
-    for (int w = 0; w < kReduceWarps; ++w) {
-        start += s_start[w];
-        bad |= s_bad[w];
-    }
-    if (bad)
-        return;
-    const int64_t nrt = (offsets[g + 1] - offsets[g] + 127) / 128;
+    const int64_t start = hdr[g], nrt = hdr[g + 1] - hdr[g];
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kReduceCols + lane;
     float acc = 0.f;
     if (j < N) {

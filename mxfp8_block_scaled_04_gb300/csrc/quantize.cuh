@@ -77,6 +77,7 @@ struct QuantParams {
     int col_tiles;
     int row_tiles;           // flat only
     float *amax;             // per-tensor max |x| (device fp32, zeroed before the launch), AMAX variant
+    int64_t *ws_hdr;         // grouped dbias: [num_groups + 1] first row tile of each group (-1: bad offsets)
 };
 
 // Byte offset of scale (r, c) of an R x C scale matrix (C scale columns) in the
@@ -296,9 +297,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     if constexpr (GROUPED) {
         num_tiles = grouped_setup(p, goff, gpre, scan);
         if (num_tiles < 0) {
-            if (blockIdx.x == 0 && tid == 0 && p.err_flag != nullptr)
-                atomicOr(p.err_flag, 1);
+            if (blockIdx.x == 0 && tid == 0) {
+                if (p.err_flag != nullptr)
+                    atomicOr(p.err_flag, 1);
+                if (DBIAS)
+                    p.ws_hdr[0] = -1;  // tells the dbias reduce to write nothing
+            }
             return;
+        }
+        if (DBIAS && blockIdx.x == 0) {
+            // each group's first row tile in the partials (and the total), for the dbias reduce
+            for (int g = tid; g <= p.num_groups; g += kThreads)
+                p.ws_hdr[g] = gpre[g] / p.col_tiles;
         }
     } else {
         num_tiles = p.row_tiles * p.col_tiles;

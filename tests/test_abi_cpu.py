@@ -182,7 +182,7 @@ def test_grouped_dbias_host_checks(cuda_lib):
     assert gd(G=0) == GROUPS
     assert gd(dbias=A + 2) == ALIGN
     assert gd() == DEVICE
-    assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 64) == (512 + 64) * 7168 * 4
+    assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 64) == 768 + (512 + 64) * 7168 * 4
     assert mx.mxfp8_quantize_grouped_dbias_workspace_bytes(65536, 7168, 0) == 0
 
 
