@@ -9,9 +9,14 @@
 //   - phase 1: warp w takes rows 32*(w>>1) + 16*(w&1) .. +15 of the tile; a
 //     lane takes 4 columns x 8 rows; the two 16-row halves of a 32-row block
 //     meet in shared memory, where one thread per (row block, column) forms
-//     the column's scale, multiplier and dbias partial;
+//     the column's scale, multiplier and dbias partial.  For dGeLU, dSiLU and
+//     dQGeLU each fp32 product is written back over its own two inputs (low
+//     half in the dY slot, high half in the X slot: the same 4 bytes per
+//     element);
 //   - phase 2: warp w takes the 8-row groups w and w + 8; a lane takes 16
-//     columns of one row, as in the main kernel.
+//     columns of one row, as in the main kernel, reading those products back
+//     (one byte permute per element instead of a second evaluation; dReLU
+//     and dSReLU are cheaper to evaluate again).
 // The derivative is evaluated in fp32 with the same ex2 / rcp approximations
 // as the forward activations; dReLU and dSReLU are exact.
 #pragma once
@@ -43,15 +48,9 @@ __device__ __forceinline__ float dactivation(float x)
     } else if constexpr (ACT == 2) {
         return x > 0.f ? 2.f * x : 0.f;
     } else {
-        float t;
-        if constexpr (ACT == 3)
-            t = 1.5957691216057308f * (x + 0.044715f * x * x * x);
-        else if constexpr (ACT == 4)
-            t = x;
-        else
-            t = 1.702f * x;
-        const float e = ex2_approx(-1.4426950408889634f * fabsf(t));
-        const float inv = rcp_approx(1.f + e);
+        const float t = sigmoid_arg<ACT>(x);
+        const float e = exp2_nonpos(-1.4426950408889634f * fabsf(t));
+        const float inv = rcp_1to2(1.f + e);
         const float s = t >= 0.f ? inv : e * inv;
         const float oms = t >= 0.f ? e * inv : inv;
         // s (1 + x (1 - s) t') rather than s + x s (1 - s) t': when s underflows to 0
@@ -80,6 +79,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDOffBars);
     TileCoord *coords = reinterpret_cast<TileCoord *>(smem + kDOffCoord);
 
+    // the transcendental derivatives keep each product for phase 2 (see the top)
+    constexpr bool kKeep = ACT > 2;
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int it = 0; it < my_count; ++it) {
         const int slot = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
-        const unsigned char *gbox = smem + slot * kStageBytes;
-        const unsigned char *xbox = gbox + kBoxBytes;
+        unsigned char *gbox = smem + slot * kStageBytes;
+        unsigned char *xbox = gbox + kBoxBytes;
         const bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
         const TileCoord tc = coords[slot];
 
@@ -151,7 +152,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     d[2] += y2;
                     d[3] += y3;
                 }
+                if constexpr (kKeep) {
+                    const uint32_t b0 = __float_as_uint(y0), b1 = __float_as_uint(y1);
+                    const uint32_t b2 = __float_as_uint(y2), b3 = __float_as_uint(y3);
+                    sts64(gbox + off, __byte_perm(b0, b1, 0x5410), __byte_perm(b2, b3, 0x5410));
+                    sts64(xbox + off, __byte_perm(b0, b1, 0x7632), __byte_perm(b2, b3, 0x7632));
+                }
             }
+            if constexpr (kKeep)
+                fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 f[k] = fmaxf(f[k], __shfl_xor_sync(0xffffffffu, f[k], 16));
@@ -214,8 +223,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float y[16];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    y[2 * j] = bf16_lo(gw[j]) * dactivation<ACT>(bf16_lo(xw[j]));
-                    y[2 * j + 1] = bf16_hi(gw[j]) * dactivation<ACT>(bf16_hi(xw[j]));
+                    if constexpr (kKeep) {  // the products phase 1 left in the two slots
+                        y[2 * j] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x5410));
+                        y[2 * j + 1] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x7632));
+                    } else {                // dReLU, dSReLU: cheaper to evaluate again
+                        y[2 * j] = bf16_lo(gw[j]) * dactivation<ACT>(bf16_lo(xw[j]));
+                        y[2 * j + 1] = bf16_hi(gw[j]) * dactivation<ACT>(bf16_hi(xw[j]));
+                    }
                 }
                 const int64_t grow = tc.row0 + r, gcol = tc.col0 + sp * 16;
                 const bool in = grow < tc.row_end && gcol < N;

@@ -116,6 +116,7 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi)
 __device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 __device__ __forceinline__ uint2 lds64(const void *p) { return *reinterpret_cast<const uint2 *>(p); }
 __device__ __forceinline__ float4 lds128f(const void *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void sts64(void *p, uint32_t a, uint32_t b) { *reinterpret_cast<uint2 *>(p) = make_uint2(a, b); }
 
 // 16-byte global store that does not allocate in L1.
 __device__ __forceinline__ void stg128(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)

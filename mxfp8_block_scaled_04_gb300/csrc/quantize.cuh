@@ -116,20 +116,43 @@ __device__ __forceinline__ int block_exponent_f32(uint32_t amax_bits)
 // ReLU, 3 GeLU (tanh form, as x * sigmoid(2 sqrt(2/pi) (x + 0.044715 x^3))),
 // 4 SiLU, 5 QGeLU (x * sigmoid(1.702 x)).  The sigmoid is 1 / (1 + e) or
 // e / (1 + e) with e = 2^(-|t| log2 e): no overflow and no cancellation for
-// large |t|.  It uses the hardware ex2 / rcp approximations (a few ulps; no
-// flush to zero), which the parity tests allow for at decision boundaries.
-__device__ __forceinline__ float ex2_approx(float x)
+// large |t|.  It uses the hardware ex2 / rcp approximations in their
+// flush-to-zero forms (a few ulps), which the parity tests allow for at decision
+// boundaries.  Subnormal results are kept all the same: the reciprocal only ever
+// sees 1 + e in [1, 2], and 2^x for x < -64 is formed as 2^(x + 64) * 2^-64,
+// where x + 64 is exact and the fp32 product rounds into the subnormal range
+// as any product does.  (The non-flushing rcp cost 15% more time for GeLU.
+// Evaluating with the bare ex2, and redoing a row segment or a tile in this
+// form only where some exponent is out of range, was slower: the second copy
+// of the loop costs more than the few instructions it saves.)
+
+// 2^x for x <= 0 (0 below 2^-149, as in fp32 arithmetic).
+__device__ __forceinline__ float exp2_nonpos(float x)
+{
+    const bool low = x < -64.f;
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(low ? x + 64.f : x));
+    return low ? y * 5.42101086242752217e-20f : y;  // 2^-64
+}
+
+// 1 / x for x in [1, 2].
+__device__ __forceinline__ float rcp_1to2(float x)
 {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-__device__ __forceinline__ float rcp_approx(float x)
+// The argument t of the sigmoid for GeLU, SiLU and QGeLU.
+template <int ACT>
+__device__ __forceinline__ float sigmoid_arg(float x)
 {
-    float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
+    if constexpr (ACT == 3)
+        return 1.5957691216057308f * (x + 0.044715f * x * x * x);
+    else if constexpr (ACT == 4)
+        return x;
+    else
+        return 1.702f * x;
 }
 
 template <int ACT>
@@ -140,15 +163,9 @@ __device__ __forceinline__ float activation(float x)
     } else if constexpr (ACT == 2) {
         return x > 0.f ? x * x : 0.f;
     } else {
-        float t;
-        if constexpr (ACT == 3)
-            t = 1.5957691216057308f * (x + 0.044715f * x * x * x);
-        else if constexpr (ACT == 4)
-            t = x;
-        else
-            t = 1.702f * x;
-        const float e = ex2_approx(-1.4426950408889634f * fabsf(t));
-        const float r = rcp_approx(1.f + e);
+        const float t = sigmoid_arg<ACT>(x);
+        const float e = exp2_nonpos(-1.4426950408889634f * fabsf(t));
+        const float r = rcp_1to2(1.f + e);
         return x * (t >= 0.f ? r : e * r);
     }
 }
