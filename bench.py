@@ -36,9 +36,10 @@ METRIC = "MXFP8 quantize effective GB/s and % of GB300 HBM peak (rowwise+colwise
 BYTES_PER_ELEM = 2 + 1 + 1 + 1 / 16
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
-# Sources that define the dominant (quantize) kernel: a committed ncu traffic figure is only
-# reported while these are unchanged since it was taken.
-KERNEL_SOURCES = ["mxfp8_block_scaled_04_gb300/csrc/quantize.cuh", "mxfp8_block_scaled_04_gb300/csrc/ptx.cuh"]
+# Every source the kernels are built from: a committed ncu traffic figure is only reported
+# while these are unchanged since it was taken.
+KERNEL_SOURCES = [f"mxfp8_block_scaled_04_gb300/csrc/{f}"
+                  for f in ("api.cu", "dact.cuh", "dbias_reduce.cuh", "ptx.cuh", "quantize.cuh")]
 
 
 def parse_args():
@@ -110,15 +111,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"quantize_{workload}.md")
+def profile_name(args, M, N, workload_dbias):
+    """Name of the committed ncu summary (profiles/<name>.md) for this run's kernel, workload and options."""
+    name = args.workload if not args.shape else f"{args.workload.split('_')[0]}_{M}x{N}"
+    family = "quantize_dact" if args.dact.lower() != "none" else "quantize"
+    opts = [o for o, on in (("swizzled", args.swizzled), ("amax", args.amax),
+                            ("dbias", args.dbias and not workload_dbias)) if on]
+    opts += [a.lower() for a in (args.act, args.dact) if a.lower() != "none"]
+    return "_".join([family, name] + opts)
+
+
+def profiled_traffic(name):
+    """DRAM bytes per step from the committed ncu summary, if it matches the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    m_b = re.search(r"dram_bytes_per_step:\s*([0-9]+)", text)
     if not (m_sha and m_b) or m_sha.group(1) != kernel_source_sha():
         return None
     return int(m_b.group(1))
@@ -315,6 +326,10 @@ def run_ours(args):
             raise mx.MXFP8Error(st, "bench step")
 
     algo_bytes = (BYTES_PER_ELEM + (2 if dact else 0)) * M * N + (4 * N * max(G, 1) if with_dbias else 0)
+    prof = profile_name(args, M, N, w["with_dbias"])
+    kernels = (["amax_init_kernel"] if args.amax else []) + ["quantize_dact_kernel" if dact else "quantize_kernel"]
+    if with_dbias:
+        kernels.append("dbias_reduce_grouped_kernel" if grouped else "dbias_reduce_kernel")
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(local).uuid)
@@ -460,8 +475,9 @@ def run_ours(args):
             "pct_of_8tbs": 100 * value / world / 8000.0,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
-                         "traffic": profiled_traffic(args.workload),
-                         "kernel": "quantize_kernel" + (" + dbias_reduce_kernel" if with_dbias else ""),
+                         "traffic": profiled_traffic(prof),
+                         "traffic_source": f"profiles/{prof}.md",
+                         "kernel": " + ".join(kernels),
                          "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": algo_bytes},
             "clocks": clocks,
             "gpu_launches": launches,
