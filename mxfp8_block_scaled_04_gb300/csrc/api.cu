@@ -371,9 +371,10 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
             return st;
     }
     if (dbias != nullptr && N > 0) {
-        const dim3 grid(static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols), static_cast<unsigned>(num_groups));
-        dbias_reduce_grouped_kernel<<<grid, kReduceCols * kReduceWarps, 0, stream>>>(
-            ws + grouped_header_floats(num_groups), reinterpret_cast<const int64_t *>(ws), N, dbias, noop);
+        const unsigned blocks = static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols);
+        dbias_reduce_grouped_kernel<<<blocks, kReduceCols * kReduceWarps, 0, stream>>>(
+            ws + grouped_header_floats(num_groups), reinterpret_cast<const int64_t *>(ws), num_groups, N, dbias,
+            noop);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (cudaGetLastError() != cudaSuccess)
             return MXFP8_ERR_LAUNCH;

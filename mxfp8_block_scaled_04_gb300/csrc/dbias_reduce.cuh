@@ -14,6 +14,8 @@
 
 #include <cstdint>
 
+#include "quantize.cuh"  // kMaxGroups
+
 namespace mxfp8 {
 
 constexpr int kReduceCols = 32;
@@ -47,37 +49,101 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
 
 // Per-group dbias of the grouped call: dbias[g][j] = sum over the row tiles of
 // group g of ws[t][j].  The grouped quantize kernel writes each group's first
-// row tile into hdr[0..G] (hdr[G] = total), or hdr[0] = -1 when the offsets are
-// invalid (then nothing is written here either).  CTA (column block, g) sums
-// its group's tiles like the flat reduce: warp w takes tiles w, w+16, ... and
-// the 16 warp sums are added in warp order.
+// row tile into hdr[0..G] (hdr[G] = T, the total), or hdr[0] = -1 when the
+// offsets are invalid (then nothing is written here either).
+//
+// One CTA owns 32 columns of every group.  Its 16 warps split the T row tiles
+// into contiguous ranges [T w / 16, T (w + 1) / 16); a warp sums the tiles of
+// each group inside its range in tile order.  A group that lies wholly inside
+// one range is written by that warp; the partial sums of a group that crosses
+// ranges are left in shared memory, and the warp holding the group's last
+// tile adds them in warp order.  The order of every sum depends only on T and
+// hdr, so the result does not depend on scheduling.  Empty groups get zeros.
 __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
-    dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ hdr, int64_t N,
-                                float *__restrict__ dbias, const float *noop)
+    dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ hdr, int num_groups,
+                                int64_t N, float *__restrict__ dbias, const float *noop)
 {
     if (noop != nullptr && *noop == 1.0f)
         return;
     if (hdr[0] < 0)
         return;
-    __shared__ float part[kReduceWarps][kReduceCols];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = blockIdx.y;
-    const int64_t start = hdr[g], nrt = hdr[g + 1] - hdr[g];
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * kReduceCols + lane;
-    float acc = 0.f;
-    if (j < N) {
-#pragma unroll 8
-        for (int64_t t = warp; t < nrt; t += kReduceWarps)
-            acc += ws[(start + t) * N + j];
-    }
-    part[warp][lane] = acc;
+    __shared__ int64_t first[kMaxGroups + 1];
+    __shared__ float head[kReduceWarps][kReduceCols];  // partial of a group that began in an earlier range
+    __shared__ float tail[kReduceWarps][kReduceCols];  // partial of a group that goes on into a later range
+    const int G = num_groups;
+    for (int i = threadIdx.x; i <= G; i += blockDim.x)
+        first[i] = hdr[i];
     __syncthreads();
-    if (warp == 0 && j < N) {
-        float s = part[0][lane];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kReduceCols + lane;
+    const int64_t T = first[G];
+    const int64_t a = T * warp / kReduceWarps, b = T * (warp + 1) / kReduceWarps;
+
+    for (int g = warp; g < G; g += kReduceWarps)
+        if (first[g] == first[g + 1] && j < N)
+            dbias[static_cast<int64_t>(g) * N + j] = 0.f;
+
+    int g0 = 0;  // the group of tile a: first[g0] <= a < first[g0 + 1]
+    if (a < b) {
+        int lo = 0, hi = G;  // first[lo] <= a < first[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (first[mid] <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        g0 = lo;
+        // a finished group's sum: written here, or left for the warp that completes it
+        auto flush = [&](int g, float acc) {
+            const bool before = first[g] < a, after = first[g + 1] > b;
+            if (before)
+                head[warp][lane] = acc;
+            else if (after)
+                tail[warp][lane] = acc;
+            else if (j < N)
+                dbias[static_cast<int64_t>(g) * N + j] = acc;
+        };
+        int g = g0;
+        int64_t gend = first[g + 1];
+        float acc = 0.f;
+        // 8 tiles' loads in flight at a time, whatever the group boundaries
+        for (int64_t t0 = a; t0 < b; t0 += 8) {
+            float v[8];
 #pragma unroll
-        for (int w = 1; w < kReduceWarps; ++w)
-            s += part[w][lane];
-        dbias[static_cast<int64_t>(g) * N + j] = s;
+            for (int k = 0; k < 8; ++k)
+                v[k] = (t0 + k < b && j < N) ? ws[(t0 + k) * N + j] : 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int64_t t = t0 + k;
+                if (t < b) {
+                    if (t == gend) {  // warp-uniform: tile t starts the next non-empty group
+                        flush(g, acc);
+                        acc = 0.f;
+                        do
+                            ++g;
+                        while (first[g + 1] <= t);
+                        gend = first[g + 1];
+                    }
+                    acc += v[k];
+                }
+            }
+        }
+        flush(g, acc);
+    }
+    __syncthreads();
+    // a group that began before this range and ends inside it: add the partials in warp order
+    if (a < b && first[g0] < a && first[g0 + 1] <= b) {
+        int w1 = warp - 1;  // the range holding the group's first tile
+        while (w1 > 0 && T * w1 / kReduceWarps > first[g0])
+            --w1;
+        float s = tail[w1][lane];
+        for (int w = w1 + 1; w < warp; ++w)
+            if (T * w / kReduceWarps < T * (w + 1) / kReduceWarps)
+                s += head[w][lane];
+        s += head[warp][lane];
+        if (j < N)
+            dbias[static_cast<int64_t>(g0) * N + j] = s;
     }
 }
 

@@ -384,6 +384,34 @@ def test_grouped_dbias(oracle_mod, N):
     assert np.all(got[1] == 0.0) and np.all(got[4] == 0.0)
 
 
+@pytest.mark.parametrize("case", ["512_groups", "one_group", "long_and_empty"])
+def test_grouped_dbias_group_layouts(oracle_mod, case):
+    """Per-group sums across the reduce's 16 contiguous tile ranges: many small groups, one group
+    spanning every range, and long groups between empty ones, with N not a multiple of 32."""
+    rng = np.random.Generator(np.random.PCG64(len(case)))
+    if case == "512_groups":
+        sizes, N = 32 * rng.choice([0, 1, 3, 4, 5, 17], size=512), 48
+    elif case == "one_group":
+        sizes, N = np.array([8192], np.int64), 80
+    else:
+        sizes, N = np.array([0, 2080, 0, 0, 32, 4096, 0, 1024, 0], np.int64), 112
+    sizes = sizes.astype(np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = wl.moe_bf16(sizes, N, seed=7)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mx.quantize_grouped(dev_bf16(x_bits), torch.from_numpy(off).cuda(), E4M3, err_flag=err, with_dbias=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle_mod.grouped_dbias(x_bits, off)
+    xv = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().abs().numpy()
+    got = r.dbias.cpu().numpy().astype(np.float64)
+    for g in range(len(sizes)):
+        tol = 1e-5 * xv[off[g]:off[g + 1]].sum(0)
+        assert np.all(np.abs(got[g] - want[g]) <= tol), g
+        if sizes[g] == 0:
+            assert np.all(got[g] == 0.0), g
+
+
 def test_grouped_dbias_bad_offsets_write_nothing():
     x = dev_bf16(wl.normal_bf16(928, 96, seed=1))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
