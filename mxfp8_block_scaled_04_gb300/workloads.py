@@ -50,6 +50,25 @@ def normal_bf16(M: int, N: int, seed: int, std: float = 1.0) -> np.ndarray:
     return to_bf16_bits(a)
 
 
+def banded_bf16(M: int, N: int, seed: int, band: int = 256) -> np.ndarray:
+    """A large BF16 matrix [M,N] made cheaply: one N(0,1) block of `band` rows, repeated down the
+    matrix with each band scaled by its own power of two 2^k, k in [-8, 8] (seeded), applied to the
+    exponent field (exact: the block's zeros and values below 2^-118 are replaced by +-1 first, so
+    every shifted value stays in the normal range)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    block = normal_bf16(band, N, seed)
+    tiny = (block & 0x7F80) <= (8 << 7)
+    block[tiny] = (block[tiny] & 0x8000) | 0x3F80
+    assert np.all((block & 0x7F80) > 8 << 7) and np.all((block & 0x7F80) < 0x7F80 - (8 << 7))
+    k = rng.integers(-8, 9, size=(M + band - 1) // band)
+    out = np.empty((M, N), np.uint16)
+    for b in range(k.size):
+        r0 = b * band
+        rows = min(band, M - r0)
+        out[r0:r0 + rows] = (block[:rows].astype(np.int32) + (int(k[b]) << 7)).astype(np.uint16)
+    return out
+
+
 def _scatter(rng, a_flat, frac, values_fn):
     count = int(round(frac * a_flat.size))
     if count:

@@ -317,6 +317,28 @@ def test_parity_grad_16384x8192_sampled_with_dbias(oracle_mod):
     torch.cuda.empty_cache()
 
 
+def test_parity_beyond_2_32_elements_with_dbias(oracle_mod):
+    """69632 x 65536 (4.56e9 elements, ~19 GB on the device): byte offsets into both FP8 planes pass
+    2^31 and 2^32, the columnwise scale plane holds 1.4e8 bytes, and the dbias workspace 544 tiles."""
+    M, N, fmt = 69632, 65536, E5M2
+    x_bits = wl.banded_bf16(M, N, seed=32)
+    x, r = quantize_device(x_bits, fmt, with_dbias=True)
+    torch.cuda.synchronize()
+    rng = np.random.Generator(np.random.PCG64(32))
+    # stripes holding byte offsets 2^31 and 2^32 of the FP8 planes, and the last one
+    must = (0, (1 << 31) // N // 32, (1 << 32) // N // 32, M // 32 - 1)
+    check_stripes(oracle_mod, x_bits, fmt, r._asdict(), stripes_to_check(M, rng, must=must))
+    dbias = r.dbias.cpu().numpy()
+    for j0 in sorted({0, N - 32, *(32 * rng.integers(0, N // 32, 2)).tolist()}):
+        xs = np.ascontiguousarray(x_bits[:, j0:j0 + 32])
+        _, _, o_col, s_col, db = oracle_mod.quantize(xs, fmt, rowwise=False, colwise=True, with_dbias=True)
+        assert_bytes_equal(r.out_col[:, j0:j0 + 32].cpu().numpy(), o_col, f"out_col cols {j0}")
+        assert_bytes_equal(r.scale_col[:, j0:j0 + 32].cpu().numpy(), s_col, f"scale_col cols {j0}")
+        assert np.all(np.abs(dbias[j0:j0 + 32].astype(np.float64) - db) <= dbias_tolerance(xs)), j0
+    del x, r, x_bits
+    torch.cuda.empty_cache()
+
+
 def test_parity_moe_64x65536x7168_sampled(oracle_mod):
     w = wl.make("moe_64x65536x7168")
     x_bits, off = w["x"], w["offsets"]
