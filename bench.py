@@ -14,7 +14,9 @@ Under torchrun (N > 1) every rank quantizes its own copy of the workload
 bracketed by barriers and the max over ranks is reported.
 
 --impl reference times the CPU oracle (the only other implementation there
-is) on a bounded 32-row sample of the same workload per step, on rank 0.
+is) on a bounded sample of the same workload per step (32 rows per host core,
+one thread per 32-row slice), on rank 0.  `cpu_baseline` times it the same way
+on every host core, and single-threaded.
 """
 from __future__ import annotations
 
@@ -192,24 +194,55 @@ class ClockSampler:
 BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
 
 
+def host_cores():
+    """Cores this process may run on (the container's share, not the machine's count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_on_cores(oracle, x, fmt, threads):
+    """Run the oracle over x split into `threads` contiguous 32-row slices, one per thread (the C
+    oracle runs outside the GIL); returns the wall time."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    stripes = x.shape[0] // 32
+    bounds = [32 * (stripes * k // threads) for k in range(threads + 1)]
+    parts = [x[bounds[k]:bounds[k + 1]] for k in range(threads) if bounds[k + 1] > bounds[k]]
+    with ThreadPoolExecutor(max_workers=len(parts)) as pool:
+        t = time.perf_counter()
+        list(pool.map(lambda part: oracle.quantize(part, fmt), parts))
+        return time.perf_counter() - t
+
+
 def cpu_baseline(wl_x, N, fmt, target_s):
-    """Time the oracle on the first R rows of the workload (R adaptive for ~target_s of CPU work)."""
+    """Time the oracle on the first rows of the workload: single-threaded, then on every host core
+    (row slices per thread); each leg sized for about target_s / 2 of wall time."""
     import numpy as np
     import oracle
 
     oracle.build()
+    cores = host_cores()
     stripe = np.ascontiguousarray(wl_x[:32])
     t = time.perf_counter()
     oracle.quantize(stripe, fmt)
     per_stripe = max(time.perf_counter() - t, 1e-6)
-    stripes = int(max(1, min(wl_x.shape[0] // 32, target_s / per_stripe)))
-    sample = np.ascontiguousarray(wl_x[: 32 * stripes])
+    max_stripes = wl_x.shape[0] // 32
+    s1 = int(max(1, min(max_stripes, 0.5 * target_s / per_stripe)))
+    sample1 = np.ascontiguousarray(wl_x[: 32 * s1])
     t = time.perf_counter()
-    oracle.quantize(sample, fmt)
-    dt = time.perf_counter() - t
-    return {"value": BYTES_PER_ELEM * sample.size / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {32 * stripes} rows x {N} columns ({sample.size} elements) of the workload, "
-                      f"single-threaded scalar C oracle, {dt:.2f} s"}
+    oracle.quantize(sample1, fmt)
+    dt1 = time.perf_counter() - t
+    single = BYTES_PER_ELEM * sample1.size / dt1 / 1e9
+    sp = int(max(cores, min(max_stripes, 0.5 * target_s / per_stripe * cores)))
+    sample_p = np.ascontiguousarray(wl_x[: 32 * sp])
+    dtp = oracle_on_cores(oracle, sample_p, fmt, cores)
+    return {"value": BYTES_PER_ELEM * sample_p.size / dtp / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {32 * sp} rows x {N} columns ({sample_p.size} elements) of the workload, scalar C "
+                      f"oracle on {cores} threads (contiguous 32-row slices), {dtp:.2f} s",
+            "single_thread": {"value": single, "unit": "GB/s", "cores": 1,
+                              "sample": f"first {32 * s1} rows ({sample1.size} elements), {dt1:.2f} s"}}
 
 
 def run_reference(args):
@@ -229,28 +262,32 @@ def run_reference(args):
     if full is None:
         raise SystemExit("workload too large for the reference arm")
     x = full["x"]
+    cores = host_cores()
     probe = np.ascontiguousarray(x[:32, : min(N, 1024)])
     t = time.perf_counter()
     oracle.quantize(probe, fmt)
     per_elem = (time.perf_counter() - t) / probe.size
+    # each step: 32 rows per core x C columns, one 32-row slice per thread
     budget = 120.0 / max(1, args.steps + args.warmup)
     C = int(max(32, min(N, (budget / per_elem / 32) // 32 * 32)))
-    sample = np.ascontiguousarray(x[:32, :C])
+    rows = min(32 * cores, M // 32 * 32)
+    sample = np.ascontiguousarray(x[:rows, :C])
+    threads = rows // 32
     for _ in range(args.warmup):
-        oracle.quantize(sample, fmt)
-    t = time.perf_counter()
+        oracle_on_cores(oracle, sample, fmt, threads)
+    dt = 0.0
     for _ in range(args.steps):
-        oracle.quantize(sample, fmt)
-    dt = time.perf_counter() - t
+        dt += oracle_on_cores(oracle, sample, fmt, threads)
     value = BYTES_PER_ELEM * sample.size * args.steps / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
-                   "sample_per_step": f"rows 0..31 x columns 0..{C - 1}"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"32 x {C} elements of the workload per step, single-threaded scalar C oracle"},
+                   "sample_per_step": f"rows 0..{rows - 1} x columns 0..{C - 1}"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} x {C} elements of the workload per step, scalar C oracle on "
+                                   f"{threads} threads (one 32-row slice each)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
