@@ -33,7 +33,12 @@
  *     is a status code, nothing throws or aborts across this boundary.
  *   - Work is stream-ordered on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No call synchronizes the host or reads device memory
- *     from the host, except mxfp8_device_fault_word().
+ *     from the host, except mxfp8_device_fault_word().  The quantize kernels
+ *     and the dbias reduces are launched with programmatic stream
+ *     serialization: each may start while the kernel before it drains, but
+ *     waits on the device for that kernel to finish before it touches global
+ *     memory, so results are as for plain stream order.  (Captured in a CUDA
+ *     graph, consecutive calls are joined by programmatic edges.)
  *   - The device is the calling thread's current device; x must live on it.
  *   - noop: optional device fp32 scalar.  When *noop == 1.0f every kernel of
  *     the call returns without writing anything (the "Perform noop tensor

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include <cuda.h>
@@ -23,6 +24,30 @@ using namespace mxfp8;
 constexpr int kMaxDevices = 64;
 
 std::atomic<uint64_t> g_launches{0};
+
+// Launch with programmatic stream serialisation: the kernel may begin while the
+// previous kernel on the stream drains, and waits (griddepcontrol.wait) before
+// its first global memory access, so stream order holds for every buffer.
+// Only kernels that make that wait are launched this way.
+template <typename... Params, typename... Args>
+mxfp8_status_t launch_pdl(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                          Args &&...args)
+{
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    const cudaError_t last = cudaGetLastError();
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess && last == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
 
 struct DeviceInfo {
     bool ready = false;
@@ -149,11 +174,8 @@ mxfp8_status_t launch_quantize(int fmt, int device, const CUtensorMap &map, cons
     const int grid = static_cast<int>(tile_bound < cap ? tile_bound : cap);
     const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
     if (fmt == MXFP8_E4M3)
-        quantize_kernel<0, DBIAS, GROUPED, SWZ, AMAX, ACT><<<grid, kThreads, smem, stream>>>(map, p);
-    else
-        quantize_kernel<1, DBIAS, GROUPED, SWZ, AMAX, ACT><<<grid, kThreads, smem, stream>>>(map, p);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+        return launch_pdl(quantize_kernel<0, DBIAS, GROUPED, SWZ, AMAX, ACT>, grid, kThreads, smem, stream, map, p);
+    return launch_pdl(quantize_kernel<1, DBIAS, GROUPED, SWZ, AMAX, ACT>, grid, kThreads, smem, stream, map, p);
 }
 
 // Per-tensor amax output: zero it before the quantize kernel (unless noop).
@@ -216,9 +238,7 @@ mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUten
         cap = d.dact_ctas_per_sm[v] * d.sm_count;
     }
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    quantize_dact_kernel<FMT, DBIAS, ACT><<<grid, kThreads, kSmemDact, stream>>>(map_g, map_x, p);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+    return launch_pdl(quantize_dact_kernel<FMT, DBIAS, ACT>, grid, kThreads, kSmemDact, stream, map_g, map_x, p);
 }
 
 template <int ACT>
@@ -301,10 +321,8 @@ mxfp8_status_t enqueue_reduce(const float *ws, int64_t row_tiles, int64_t N, flo
                               cudaStream_t stream)
 {
     const int64_t blocks = (N + kReduceCols - 1) / kReduceCols;
-    dbias_reduce_kernel<<<static_cast<unsigned>(blocks), kReduceCols * kReduceWarps, 0, stream>>>(ws, row_tiles, N,
-                                                                                                   dbias, noop);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+    return launch_pdl(dbias_reduce_kernel, static_cast<unsigned>(blocks), kReduceCols * kReduceWarps, 0, stream, ws,
+                      row_tiles, N, dbias, noop);
 }
 
 // The grouped dbias workspace starts with an int64 header [num_groups + 1] (each
@@ -372,12 +390,12 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
     }
     if (dbias != nullptr && N > 0) {
         const unsigned blocks = static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols);
-        dbias_reduce_grouped_kernel<<<blocks, kReduceCols * kReduceWarps, 0, stream>>>(
-            ws + grouped_header_floats(num_groups), reinterpret_cast<const int64_t *>(ws), num_groups, N, dbias,
-            noop);
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (cudaGetLastError() != cudaSuccess)
-            return MXFP8_ERR_LAUNCH;
+        const float *partials = ws + grouped_header_floats(num_groups);
+        const int64_t *hdr = reinterpret_cast<const int64_t *>(ws);
+        st = launch_pdl(dbias_reduce_grouped_kernel, blocks, kReduceCols * kReduceWarps, 0, stream, partials, hdr,
+                        num_groups, N, dbias, noop);
+        if (st != MXFP8_OK)
+            return st;
     }
     return MXFP8_OK;
 }

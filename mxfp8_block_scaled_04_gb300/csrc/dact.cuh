@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // the transcendental derivatives keep each product for phase 2 (see the top)
     constexpr bool kKeep = ACT > 2;
+    pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -14,6 +14,7 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "quantize.cuh"  // kMaxGroups
 
 namespace mxfp8 {
@@ -25,6 +26,7 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     dbias_reduce_kernel(const float *__restrict__ ws, int64_t row_tiles, int64_t N, float *__restrict__ dbias,
                         const float *noop)
 {
+    pdl_wait_and_release();
     if (noop != nullptr && *noop == 1.0f)
         return;
     __shared__ float part[kReduceWarps][kReduceCols];
@@ -63,6 +65,7 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ hdr, int num_groups,
                                 int64_t N, float *__restrict__ dbias, const float *noop)
 {
+    pdl_wait_and_release();
     if (noop != nullptr && *noop == 1.0f)
         return;
     if (hdr[0] < 0)

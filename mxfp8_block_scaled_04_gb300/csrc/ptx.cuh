@@ -74,6 +74,17 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch.  The library's kernels are launched so that the
+// next kernel on the stream may start while this one drains: each lets its
+// successor launch at once, and waits, before its first global memory access,
+// until the kernel before it has finished and its writes are visible.  Without
+// the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait_and_release()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D tiled TMA load of one box into shared memory; completion is signalled
 // as transaction bytes on `bar`.  x is the innermost (column) coordinate.  The
 // input is read exactly once, so its lines are marked evict-first in L2, which

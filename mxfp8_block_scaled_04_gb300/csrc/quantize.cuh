@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
 
+    pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
 
