@@ -138,6 +138,48 @@ __device__ __forceinline__ void stg128(void *p, uint32_t a, uint32_t b, uint32_t
 }
 
 // BF16 halves of a packed word, widened exactly to fp32.
+// Two fp32 values in one 64-bit register pair, for Blackwell's packed
+// add / mul / fma.rn.f32x2 (each lane rounds exactly as the scalar operation).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_splat(float a) { return f2_pack(a, a); }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_abs(uint64_t v) { return v & 0x7FFFFFFF7FFFFFFFull; }
+
+// cvt_fp8x2 of (v0 * m.lo, v1 * m.hi), the two products as one f32x2 multiply.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2_scaled(float v0, float v1, uint64_t m)
+{
+    float a, b;
+    f2_unpack(f2_mul(f2_pack(v0, v1), m), a, b);
+    return cvt_fp8x2<FMT>(a, b);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -170,6 +170,41 @@ __device__ __forceinline__ float activation(float x)
     }
 }
 
+// The same activations on two values at once (lanes lo and hi of a packed
+// pair): the multiplies and adds run as f32x2 operations, ex2 and rcp per lane.
+// Each lane's result is the one activation<ACT> gives.
+template <int ACT>
+__device__ __forceinline__ uint64_t activation2(uint64_t x)
+{
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    if constexpr (ACT <= 2) {
+        return f2_pack(activation<ACT>(x0), activation<ACT>(x1));
+    } else {
+        uint64_t t;
+        if constexpr (ACT == 3) {  // 1.5957691216057308 * fma((0.044715 x) x, x, x)
+            uint64_t q = f2_mul(f2_splat(0.044715f), x);
+            q = f2_mul(q, x);
+            t = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, x));
+        } else if constexpr (ACT == 4) {
+            t = x;
+        } else {
+            t = f2_mul(f2_splat(1.702f), x);
+        }
+        const uint64_t z = f2_mul(f2_splat(-1.4426950408889634f), f2_abs(t));
+        float z0, z1, t0, t1;
+        f2_unpack(z, z0, z1);
+        f2_unpack(t, t0, t1);
+        const uint64_t e = f2_pack(exp2_nonpos(z0), exp2_nonpos(z1));
+        float o0, o1;
+        f2_unpack(f2_add(e, f2_splat(1.f)), o0, o1);
+        const float r0 = rcp_1to2(o0), r1 = rcp_1to2(o1);
+        float er0, er1;
+        f2_unpack(f2_mul(e, f2_pack(r0, r1)), er0, er1);
+        return f2_mul(x, f2_pack(t0 >= 0.f ? r0 : er0, t1 >= 0.f ? r1 : er1));
+    }
+}
+
 // Largest |act(x)| over x <= 0 (the activations above are monotone increasing for
 // x > 0, and bounded in magnitude by this for x <= 0): SiLU's minimum is
 // -0.2785 at x = -1.278; GeLU's and QGeLU's are smaller; ReLU's is 0.
@@ -537,11 +572,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float y[16];
                 if constexpr (ACT != 0) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        y[2 * j] = activation<ACT>(bf16_lo(w[j]));
-                        y[2 * j + 1] = activation<ACT>(bf16_hi(w[j]));
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        f2_unpack(activation2<ACT>(f2_pack(bf16_lo(w[j]), bf16_hi(w[j]))), y[2 * j], y[2 * j + 1]);
                 }
+                // two codes from two values and their multipliers (f32x2 multiplies pay
+                // on the activation paths only: measured)
+                auto cvt_pair = [](float a, float b, float ma, float mb) -> uint32_t {
+                    if constexpr (ACT != 0)
+                        return cvt_fp8x2_scaled<FMT>(a, b, f2_pack(ma, mb));
+                    else
+                        return cvt_fp8x2<FMT>(a * ma, b * mb);
+                };
                 auto val = [&](int i) -> float {
                     if constexpr (ACT == 0)
                         return (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
@@ -573,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t o[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t lo = cvt_fp8x2<FMT>(val(4 * j) * rm, val(4 * j + 1) * rm);
-                        const uint32_t hi = cvt_fp8x2<FMT>(val(4 * j + 2) * rm, val(4 * j + 3) * rm);
+                        const uint32_t lo = cvt_pair(val(4 * j), val(4 * j + 1), rm, rm);
+                        const uint32_t hi = cvt_pair(val(4 * j + 2), val(4 * j + 3), rm, rm);
                         o[j] = lo | (hi << 16);
                     }
                     if (in) {
@@ -592,8 +633,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
-                        const uint32_t lo = cvt_fp8x2<FMT>(val(4 * j) * c.x, val(4 * j + 1) * c.y);
-                        const uint32_t hi = cvt_fp8x2<FMT>(val(4 * j + 2) * c.z, val(4 * j + 3) * c.w);
+                        const uint32_t lo = cvt_pair(val(4 * j), val(4 * j + 1), c.x, c.y);
+                        const uint32_t hi = cvt_pair(val(4 * j + 2), val(4 * j + 3), c.z, c.w);
                         o[j] = lo | (hi << 16);
                     }
                     if (in)
