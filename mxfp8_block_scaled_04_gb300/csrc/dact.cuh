@@ -64,6 +64,53 @@ __device__ __forceinline__ float dactivation(float x)
     }
 }
 
+// act'(x) for two values at once (lanes of a packed pair), each lane as
+// dactivation<ACT>.  For dGeLU the multiplies and adds run as f32x2 operations
+// (ex2 and rcp per lane); the others are cheaper per lane (measured).
+template <int ACT>
+__device__ __forceinline__ uint64_t dactivation2(uint64_t x)
+{
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    if constexpr (ACT != 3) {
+        return f2_pack(dactivation<ACT>(x0), dactivation<ACT>(x1));
+    } else {
+        const uint64_t one = f2_splat(1.f);
+        uint64_t t;
+        if constexpr (ACT == 3) {
+            uint64_t q = f2_mul(f2_splat(0.044715f), x);
+            q = f2_mul(q, x);
+            t = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, x));
+        } else if constexpr (ACT == 4) {
+            t = x;
+        } else {
+            t = f2_mul(f2_splat(1.702f), x);
+        }
+        float z0, z1, t0, t1;
+        f2_unpack(f2_mul(f2_splat(-1.4426950408889634f), f2_abs(t)), z0, z1);
+        f2_unpack(t, t0, t1);
+        const uint64_t e = f2_pack(exp2_nonpos(z0), exp2_nonpos(z1));
+        float o0, o1;
+        f2_unpack(f2_add(e, one), o0, o1);
+        const float i0 = rcp_1to2(o0), i1 = rcp_1to2(o1);
+        float ei0, ei1;
+        f2_unpack(f2_mul(e, f2_pack(i0, i1)), ei0, ei1);
+        const uint64_t sg = f2_pack(t0 >= 0.f ? i0 : ei0, t1 >= 0.f ? i1 : ei1);
+        const uint64_t oms = f2_pack(t0 >= 0.f ? ei0 : i0, t1 >= 0.f ? ei1 : i1);
+        uint64_t inner;
+        if constexpr (ACT == 3) {
+            const uint64_t q = f2_mul(f2_splat(0.134145f), x);
+            const uint64_t tp = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, one));
+            inner = f2_fma(f2_mul(x, oms), tp, one);
+        } else if constexpr (ACT == 4) {
+            inner = f2_fma(x, oms, one);
+        } else {
+            inner = f2_fma(f2_mul(f2_splat(1.702f), x), oms, one);
+        }
+        return f2_mul(sg, inner);
+    }
+}
+
 template <int FMT, bool DBIAS, int ACT>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_dact_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_x,
@@ -135,23 +182,25 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int cq = lane & 15, q = lane >> 4;
             const int r0 = rb * 32 + hh * 16 + q * 8;  // r0 & 7 == 0
             float f[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
+            uint64_t d01 = 0, d23 = 0;  // packed column sums (+0.0 in both lanes)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int off = (r0 + i) * 128 + (((cq >> 1) ^ i) << 4) + (cq & 1) * 8;
                 const uint2 g = lds64(gbox + off), xv = lds64(xbox + off);
-                const float y0 = bf16_lo(g.x) * dactivation<ACT>(bf16_lo(xv.x));
-                const float y1 = bf16_hi(g.x) * dactivation<ACT>(bf16_hi(xv.x));
-                const float y2 = bf16_lo(g.y) * dactivation<ACT>(bf16_lo(xv.y));
-                const float y3 = bf16_hi(g.y) * dactivation<ACT>(bf16_hi(xv.y));
+                const uint64_t y01 = f2_mul(f2_pack(bf16_lo(g.x), bf16_hi(g.x)),
+                                            dactivation2<ACT>(f2_pack(bf16_lo(xv.x), bf16_hi(xv.x))));
+                const uint64_t y23 = f2_mul(f2_pack(bf16_lo(g.y), bf16_hi(g.y)),
+                                            dactivation2<ACT>(f2_pack(bf16_lo(xv.y), bf16_hi(xv.y))));
+                float y0, y1, y2, y3;
+                f2_unpack(y01, y0, y1);
+                f2_unpack(y23, y2, y3);
                 f[0] = fmaxf(f[0], fabsf(y0));
                 f[1] = fmaxf(f[1], fabsf(y1));
                 f[2] = fmaxf(f[2], fabsf(y2));
                 f[3] = fmaxf(f[3], fabsf(y3));
                 if constexpr (DBIAS) {
-                    d[0] += y0;
-                    d[1] += y1;
-                    d[2] += y2;
-                    d[3] += y3;
+                    d01 = f2_add(d01, y01);
+                    d23 = f2_add(d23, y23);
                 }
                 if constexpr (kKeep) {
                     const uint32_t b0 = __float_as_uint(y0), b1 = __float_as_uint(y1);
@@ -162,6 +211,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             if constexpr (kKeep)
                 fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
+            if constexpr (DBIAS) {
+                f2_unpack(d01, d[0], d[1]);
+                f2_unpack(d23, d[2], d[3]);
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 f[k] = fmaxf(f[k], __shfl_xor_sync(0xffffffffu, f[k], 16));
@@ -234,6 +287,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 const int64_t grow = tc.row0 + r, gcol = tc.col0 + sp * 16;
                 const bool in = grow < tc.row_end && gcol < N;
+                // two codes from two values and their multipliers (f32x2 for the transcendental ones)
+                auto cvt_pair = [](float a, float b, float ma, float mb) -> uint32_t {
+                    if constexpr (kKeep)
+                        return cvt_fp8x2_scaled<FMT>(a, b, f2_pack(ma, mb));
+                    else
+                        return cvt_fp8x2<FMT>(a * ma, b * mb);
+                };
                 if (do_row) {
                     float fm = 0.f;
 #pragma unroll
@@ -245,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t o[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        o[j] = cvt_fp8x2<FMT>(y[4 * j] * rm, y[4 * j + 1] * rm) |
-                               (cvt_fp8x2<FMT>(y[4 * j + 2] * rm, y[4 * j + 3] * rm) << 16);
+                        o[j] = cvt_pair(y[4 * j], y[4 * j + 1], rm, rm) |
+                               (cvt_pair(y[4 * j + 2], y[4 * j + 3], rm, rm) << 16);
                     if (in) {
                         stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
                         if ((sp & 1) == 0)
@@ -259,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
-                        o[j] = cvt_fp8x2<FMT>(y[4 * j] * c.x, y[4 * j + 1] * c.y) |
-                               (cvt_fp8x2<FMT>(y[4 * j + 2] * c.z, y[4 * j + 3] * c.w) << 16);
+                        o[j] = cvt_pair(y[4 * j], y[4 * j + 1], c.x, c.y) |
+                               (cvt_pair(y[4 * j + 2], y[4 * j + 3], c.z, c.w) << 16);
                     }
                     if (in)
                         stg128(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3]);
