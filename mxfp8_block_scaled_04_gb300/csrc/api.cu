@@ -1,6 +1,7 @@
 // C ABI of the MXFP8 quantize library (declarations and contract in
-// include/mxfp8.h).  Host-side validation, TMA descriptor encoding and
-// kernel launches; the device code is in quantize.cuh.
+// include/mxfp8.h).  Host-side validation, TMA descriptor encoding, kernel
+// launches and the host-buffer pipeline; the device code is in quantize.cuh
+// (the cast), dact.cuh (the backward fusion) and dbias_reduce.cuh.
 #include <atomic>
 #include <cstdint>
 #include <cstring>

@@ -1,5 +1,6 @@
 // Inline-PTX building blocks for sm_103a: mbarriers, 2-D TMA tile loads,
-// packed 16-bit max, FP8x2 conversion.  Every wait here is bounded.
+// programmatic dependent launch, packed 16-bit max, packed f32x2 arithmetic,
+// FP8x2 conversion.  Every wait here is bounded.
 #pragma once
 
 #include <cstdint>

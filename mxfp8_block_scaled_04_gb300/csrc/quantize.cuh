@@ -30,7 +30,10 @@
 //     converts the 16 values twice (row multiplier, 16 column multipliers)
 //     and writes two 16-byte global stores.
 // Every wait on an mbarrier is bounded; on expiry the CTA records a fault,
-// drains its own copies (again bounded) and returns.
+// drains its own copies (again bounded) and returns.  The kernel is launched
+// for programmatic dependent launch: it waits for the previous kernel on the
+// stream to finish before its first global access and lets the next one start
+// launching at once (pdl_wait_and_release).
 #pragma once
 
 #include <cstdint>
