@@ -1,0 +1,69 @@
+"""Back-to-back calls on one stream into the same buffers.
+
+The kernels are launched for programmatic dependent launch: each may start while the previous one
+drains and must wait on the device before touching global memory.  Alternating two inputs into the
+same outputs and workspace, with no synchronisation between calls, checks that no write of an
+earlier call lands after a later call's (outputs), and that no quantize kernel overwrites the dbias
+workspace while the previous call's reduce still reads it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_block_scaled_04_gb300 as mx
+from mxfp8_block_scaled_04_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def test_alternating_inputs_same_buffers_with_dbias(oracle_mod):
+    M, N, fmt = 4096, 2048, 1
+    a_bits, b_bits = wl.grad_bf16(M, N, seed=11), wl.normal_bf16(M, N, seed=12)
+    xa, xb = dev(a_bits), dev(b_bits)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    o = [torch.empty((M, N), **u8), torch.empty((M, N // 32), **u8), torch.empty((M, N), **u8),
+         torch.empty((M // 32, N), **u8)]
+    dbias = torch.empty((N,), dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), **u8)
+    for i in range(41):  # ends on xa
+        x = xa if i % 2 == 0 else xb
+        assert mx.mxfp8_quantize(x, M, N, fmt, *o, dbias, ws, None, None) == 0
+    torch.cuda.synchronize()
+    want = oracle_mod.quantize(a_bits, fmt, with_dbias=True)
+    for g, w in zip(o, want[:4]):
+        assert np.array_equal(g.cpu().numpy(), w)
+    xv = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16).double().abs().sum(0).numpy()
+    assert np.all(np.abs(dbias.cpu().numpy().astype(np.float64) - want[4]) <= 1e-5 * xv)
+
+
+def test_alternating_grouped_dbias_same_workspace(oracle_mod):
+    sizes_a = np.array([256, 0, 992, 32, 768], np.int64)
+    sizes_b = np.array([32, 1024, 0, 992, 0], np.int64)
+    N, fmt = 512, 0
+    off_a, off_b = wl.offsets_from_sizes(sizes_a), wl.offsets_from_sizes(sizes_b)
+    a_bits, b_bits = wl.moe_bf16(sizes_a, N, seed=3), wl.moe_bf16(sizes_b, N, seed=4)
+    total = int(sizes_a.sum())
+    assert total == int(sizes_b.sum())
+    xa, xb = dev(a_bits), dev(b_bits)
+    oa, ob = torch.from_numpy(off_a).cuda(), torch.from_numpy(off_b).cuda()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    o = [torch.empty((total, N), **u8), torch.empty((total, N // 32), **u8), torch.empty((total, N), **u8),
+         torch.empty((total // 32, N), **u8)]
+    G = len(sizes_a)
+    dbias = torch.empty((G, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.mxfp8_quantize_grouped_dbias_workspace_bytes(total, N, G), **u8)
+    for i in range(41):  # ends on a
+        x, off = (xa, oa) if i % 2 == 0 else (xb, ob)
+        assert mx.mxfp8_quantize_grouped_dbias(x, total, N, G, off, fmt, *o, dbias, ws, None, None, None) == 0
+    torch.cuda.synchronize()
+    for g, w in zip(o, oracle_mod.quantize_grouped(a_bits, off_a, fmt)):
+        assert np.array_equal(g.cpu().numpy(), w)
+    want = oracle_mod.grouped_dbias(a_bits, off_a)
+    xv = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16).double().abs().numpy()
+    got = dbias.cpu().numpy().astype(np.float64)
+    for g in range(G):
+        assert np.all(np.abs(got[g] - want[g]) <= 1e-5 * xv[off_a[g]:off_a[g + 1]].sum(0)), g
