@@ -181,6 +181,23 @@ __device__ __forceinline__ uint32_t cvt_fp8x2_scaled(float v0, float v1, uint64_
     return cvt_fp8x2<FMT>(a, b);
 }
 
+// acc + (the low / high BF16 of w), one mixed-precision add (the BF16 operand
+// widens exactly, the sum rounds to nearest as an fp32 add).
+__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %1;\n\t}"
+        : "=f"(r) : "f"(acc), "r"(w));
+    return r;
+}
+__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, hi, %1;\n\t}"
+        : "=f"(r) : "f"(acc), "r"(w));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -430,7 +430,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t amax_bits;  // fp32 bits of the largest of the four column amaxes
             if constexpr (ACT == 0) {
                 uint32_t mx0 = 0, mx1 = 0;
-                uint64_t d01 = 0, d23 = 0;  // packed column sums (+0.0 in both lanes)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     // row r = rb*32 + half*16 + i has (r & 7) == (i & 7): 128B swizzle
@@ -438,13 +437,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mx0 = max_u16x2(mx0, v.x & 0x7FFF7FFFu);
                     mx1 = max_u16x2(mx1, v.y & 0x7FFF7FFFu);
                     if constexpr (DBIAS) {
-                        d01 = f2_add(d01, f2_pack(bf16_lo(v.x), bf16_hi(v.x)));
-                        d23 = f2_add(d23, f2_pack(bf16_lo(v.y), bf16_hi(v.y)));
+                        d0 = add_bf16_lo(d0, v.x);
+                        d1 = add_bf16_hi(d1, v.x);
+                        d2 = add_bf16_lo(d2, v.y);
+                        d3 = add_bf16_hi(d3, v.y);
                     }
-                }
-                if constexpr (DBIAS) {
-                    f2_unpack(d01, d0, d1);
-                    f2_unpack(d23, d2, d3);
                 }
                 mx0 = max_u16x2(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
                 mx1 = max_u16x2(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
