@@ -181,6 +181,14 @@ __device__ __forceinline__ uint32_t cvt_fp8x2_scaled(float v0, float v1, uint64_
     return cvt_fp8x2<FMT>(a, b);
 }
 
+// Lane-wise signed maximum of two BF16 pairs (the larger BF16 value, exactly).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // acc + (the low / high BF16 of w), one mixed-precision add (the BF16 operand
 // widens exactly, the sum rounds to nearest as an fp32 add).
 __device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w)

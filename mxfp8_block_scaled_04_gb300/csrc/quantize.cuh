@@ -454,15 +454,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // On x > 0 every activation here is increasing, so a column's amax is
                 // act(max x) whenever that exceeds anything x <= 0 can give; ReLU and
                 // squared ReLU give 0 for x <= 0, so for them this is always exact.
-                float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                uint32_t m01 = 0xFF80FF80u, m23 = 0xFF80FF80u;  // BF16 pairs (-inf, -inf)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
-                    xm[0] = fmaxf(xm[0], bf16_lo(v.x));
-                    xm[1] = fmaxf(xm[1], bf16_hi(v.x));
-                    xm[2] = fmaxf(xm[2], bf16_lo(v.y));
-                    xm[3] = fmaxf(xm[3], bf16_hi(v.y));
+                    m01 = max_bf16x2(m01, v.x);
+                    m23 = max_bf16x2(m23, v.y);
                 }
+                float xm[4] = {bf16_lo(m01), bf16_hi(m01), bf16_lo(m23), bf16_hi(m23)};
                 float f[4];
                 bool slow = false;
 #pragma unroll
