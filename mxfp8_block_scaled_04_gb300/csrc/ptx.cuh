@@ -189,6 +189,15 @@ __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b)
     return r;
 }
 
+// Lane-wise BF16 pair whose magnitude is max(|a|, |b|) (its sign is the xor of
+// the two signs: callers keep only the magnitude bits, & 0x7FFF per lane).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // acc + (the low / high BF16 of w), one mixed-precision add (the BF16 operand
 // widens exactly, the sum rounds to nearest as an fp32 add).
 __device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w)

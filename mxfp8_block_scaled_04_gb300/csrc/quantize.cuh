@@ -217,6 +217,24 @@ __device__ __forceinline__ float negative_side_bound()
     return ACT <= 2 ? 0.f : 0.2785f * 1.01f;
 }
 
+// One step of a per-lane |x| maximum over BF16 bit pairs, and its final
+// magnitudes.  XS: max.xorsign.abs.bf16x2, one instruction (measured faster in
+// the grouped and dbias variants); else the integer form on bits & 0x7FFF
+// (measured faster in the plain cast, notably on L2-resident inputs).
+template <bool XS>
+__device__ __forceinline__ uint32_t absmax_step(uint32_t m, uint32_t v)
+{
+    if constexpr (XS)
+        return absmax_bf16x2(m, v);
+    else
+        return max_u16x2(m, v & 0x7FFF7FFFu);
+}
+template <bool XS>
+__device__ __forceinline__ uint32_t absmax_done(uint32_t m)
+{
+    return XS ? m & 0x7FFF7FFFu : m;
+}
+
 // 2^(127 - e) as fp32, for 0 <= e <= 253.
 __device__ __forceinline__ float scale_multiplier(int e)
 {
@@ -341,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
 
+    constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
     pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
@@ -434,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int i = 0; i < 16; ++i) {
                     // row r = rb*32 + half*16 + i has (r & 7) == (i & 7): 128B swizzle
                     const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
-                    mx0 = max_u16x2(mx0, v.x & 0x7FFF7FFFu);
-                    mx1 = max_u16x2(mx1, v.y & 0x7FFF7FFFu);
+                    mx0 = absmax_step<kXS>(mx0, v.x);
+                    mx1 = absmax_step<kXS>(mx1, v.y);
                     if constexpr (DBIAS) {
                         d0 = add_bf16_lo(d0, v.x);
                         d1 = add_bf16_hi(d1, v.x);
@@ -443,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         d3 = add_bf16_hi(d3, v.y);
                     }
                 }
+                mx0 = absmax_done<kXS>(mx0);
+                mx1 = absmax_done<kXS>(mx1);
                 mx0 = max_u16x2(mx0, __shfl_xor_sync(0xffffffffu, mx0, 16));
                 mx1 = max_u16x2(mx1, __shfl_xor_sync(0xffffffffu, mx1, 16));
                 e0 = block_exponent<FMT>(mx0 & 0xFFFFu);
@@ -598,7 +619,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         uint32_t m = 0;
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
+                            m = absmax_step<kXS>(m, w[j]);
+                        m = absmax_done<kXS>(m);
                         uint32_t a = max(m & 0xFFFFu, m >> 16);
                         a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
                         er = block_exponent<FMT>(a);
