@@ -49,7 +49,7 @@ __device__ __forceinline__ float dactivation(float x)
         return x > 0.f ? 2.f * x : 0.f;
     } else {
         const float t = sigmoid_arg<ACT>(x);
-        const float e = exp2_nonpos(-1.4426950408889634f * fabsf(t));
+        const float e = exp2_twice(-kHalfLog2e * fabsf(t));
         const float inv = rcp_1to2(1.f + e);
         const float s = t >= 0.f ? inv : e * inv;
         const float oms = t >= 0.f ? e * inv : inv;
@@ -87,9 +87,13 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
             t = f2_mul(f2_splat(1.702f), x);
         }
         float z0, z1, t0, t1;
-        f2_unpack(f2_mul(f2_splat(-1.4426950408889634f), f2_abs(t)), z0, z1);
+        f2_unpack(f2_mul(f2_splat(-kHalfLog2e), f2_abs(t)), z0, z1);
         f2_unpack(t, t0, t1);
-        const uint64_t e = f2_pack(exp2_nonpos(z0), exp2_nonpos(z1));
+        float h0, h1;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(z0));
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(z1));
+        const uint64_t h = f2_pack(h0, h1);
+        const uint64_t e = f2_mul(h, h);  // as exp2_twice, both lanes
         float o0, o1;
         f2_unpack(f2_add(e, one), o0, o1);
         const float i0 = rcp_1to2(o0), i1 = rcp_1to2(o1);
