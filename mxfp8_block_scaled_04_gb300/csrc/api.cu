@@ -3,6 +3,7 @@
 // launches and the host-buffer pipeline; the device code is in quantize.cuh
 // (the cast), dact.cuh (the backward fusion) and dbias_reduce.cuh.
 #include <atomic>
+#include <initializer_list>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -108,19 +109,22 @@ mxfp8_status_t prepare(int device, int *grid_cap)
         return MXFP8_ERR_DEVICE;
     DeviceInfo &d = g_dev[device];
     if (!d.ready) {
-        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+            cudaGetLastError();  // leave no error behind for the caller
             return MXFP8_ERR_DEVICE;
+        }
         d.ready = true;
     }
     const int v = variant_index<FMT, DBIAS, GROUPED, SWZ, AMAX, ACT>();
     if (d.ctas_per_sm[v] == 0) {
         const int smem = GROUPED ? kSmemGrouped : kSmemFlat;
         auto kern = quantize_kernel<FMT, DBIAS, GROUPED, SWZ, AMAX, ACT>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return MXFP8_ERR_LAUNCH;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1) {
+            cudaGetLastError();
             return MXFP8_ERR_LAUNCH;
+        }
         d.ctas_per_sm[v] = n;
     }
     *grid_cap = d.ctas_per_sm[v] * d.sm_count;
@@ -222,18 +226,21 @@ mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUten
             return MXFP8_ERR_DEVICE;
         DeviceInfo &d = g_dev[device];
         if (!d.ready) {
-            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+                cudaGetLastError();
                 return MXFP8_ERR_DEVICE;
+            }
             d.ready = true;
         }
         const int v = FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT;
         if (d.dact_ctas_per_sm[v] == 0) {
             auto kern = quantize_dact_kernel<FMT, DBIAS, ACT>;
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDact) != cudaSuccess)
-                return MXFP8_ERR_LAUNCH;
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDact) != cudaSuccess || n < 1)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDact) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDact) != cudaSuccess || n < 1) {
+                cudaGetLastError();
                 return MXFP8_ERR_LAUNCH;
+            }
             d.dact_ctas_per_sm[v] = n;
         }
         cap = d.dact_ctas_per_sm[v] * d.sm_count;
@@ -858,7 +865,24 @@ mxfp8_status_t host_pipe(int device, HostPipe **out)
             ok = cudaEventCreateWithFlags(&h.h2d_done[k], ef) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.comp_done[k], ef) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.d2h_done[k], ef) == cudaSuccess;
-        if (!ok) {
+        if (!ok) {  // release whatever was created, so that a later call starts clean
+            cudaGetLastError();
+            for (cudaStream_t *s : {&h.h2d, &h.d2h})
+                if (*s != nullptr) {
+                    cudaStreamDestroy(*s);
+                    *s = nullptr;
+                }
+            for (cudaEvent_t *e : {&h.start, &h.end, &h.reduced})
+                if (*e != nullptr) {
+                    cudaEventDestroy(*e);
+                    *e = nullptr;
+                }
+            for (int k = 0; k < kHostSlots; ++k)
+                for (cudaEvent_t *e : {&h.h2d_done[k], &h.comp_done[k], &h.d2h_done[k]})
+                    if (*e != nullptr) {
+                        cudaEventDestroy(*e);
+                        *e = nullptr;
+                    }
             cudaGetLastError();
             return MXFP8_ERR_LAUNCH;
         }
