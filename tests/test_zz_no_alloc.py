@@ -52,3 +52,19 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, mx.E4M3, A, A, A, A, A, None, None)
     assert st == 2      # MXFP8_ERR_SHAPE
     assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, mx.E4M3, A, A, A, A, None, None, None) == 1
+
+
+def test_noalloc_noop_writes_nothing():
+    """*noop == 1.0f: neither kernel of the call writes (outputs and dbias keep their prefill)."""
+    M, N = 128, 256
+    x_bits = wl.grad_bf16(M, N, seed=5)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    o = outputs(M, N)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    zero = torch.zeros(1, dtype=torch.float32, device="cuda")
+    assert mx.mxfp8_quantize_dbias_noalloc(x, M, N, mx.E5M2, *o[:4], o[4], one, None) == 0
+    torch.cuda.synchronize()
+    assert all(bool((t == 0x11).all()) for t in o[:4]) and bool((o[4] == 7.0).all())
+    assert mx.mxfp8_quantize_dbias_noalloc(x, M, N, mx.E5M2, *o[:4], o[4], zero, None) == 0
+    torch.cuda.synchronize()
+    assert not all(bool((t == 0x11).all()) for t in o[:4]) and not bool((o[4] == 7.0).all())
