@@ -330,6 +330,19 @@ uint64_t mxfp8_kernel_launch_count(void);
  */
 mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear);
 
+/*
+ * Diagnostic (no counterpart on the pages): exercises, without any fault, the
+ * bounded wait every pipeline kernel uses.  One thread waits limit_ns
+ * nanoseconds of wall time on an mbarrier phase that nothing completes; when
+ * the wait expires it sets bit 0 of the fault word, as a pipeline CTA does,
+ * writes 1 to *timed_out (device int; 0 if the phase had completed), and the
+ * kernel returns, leaving the context usable.  0 < limit_ns <= 10 s.
+ * Stream-ordered on `stream`.  Returns MXFP8_OK, MXFP8_ERR_NULL (timed_out
+ * NULL), MXFP8_ERR_SHAPE (limit out of range), MXFP8_ERR_DEVICE or
+ * MXFP8_ERR_LAUNCH.
+ */
+mxfp8_status_t mxfp8_selftest_bounded_wait(int64_t limit_ns, int *timed_out, void *stream);
+
 /* Size of the static scratch array used by mxfp8_quantize_dbias_noalloc. */
 #define MXFP8_NOALLOC_SCRATCH_BYTES (8u << 20)
 

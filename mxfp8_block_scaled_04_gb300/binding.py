@@ -93,6 +93,8 @@ def lib():
             L.mxfp8_kernel_launch_count.argtypes = []
             L.mxfp8_device_fault_word.restype = i32
             L.mxfp8_device_fault_word.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+            L.mxfp8_selftest_bounded_wait.restype = i32
+            L.mxfp8_selftest_bounded_wait.argtypes = [i64, vp, vp]
             _lib = L
     return _lib
 
@@ -205,6 +207,11 @@ def mxfp8_device_fault_word(clear: bool = False) -> int:
 
 
 # ---- torch conveniences ----------------------------------------------------------
+
+def mxfp8_selftest_bounded_wait(limit_ns: int, timed_out, stream=None) -> int:
+    """Diagnostic: a bounded wait on a phase nothing completes (device int32 ``timed_out`` gets 1)."""
+    return int(lib().mxfp8_selftest_bounded_wait(int(limit_ns), _addr(timed_out), _stream(stream)))
+
 
 class MXFP8Tensor(NamedTuple):
     """Quantized outputs; a direction that was not requested is None."""

@@ -679,6 +679,47 @@ const char *mxfp8_status_string(int status)
 
 uint64_t mxfp8_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+}  // extern "C"
+
+namespace {
+
+// Self-test of mbar_wait_bounded: the phase it waits for is never completed, so
+// the wait expires and the expiry is recorded as a pipeline CTA records it.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int *timed_out)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, limit_ns);
+        if (!ok)
+            atomicOr(&g_fault_word, 1u);
+        *timed_out = ok ? 0 : 1;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp8_status_t mxfp8_selftest_bounded_wait(int64_t limit_ns, int *timed_out, void *stream)
+{
+    if (timed_out == nullptr)
+        return MXFP8_ERR_NULL;
+    if (limit_ns <= 0 || limit_ns > int64_t{10000000000})
+        return MXFP8_ERR_SHAPE;
+    int device = 0;
+    mxfp8_status_t st = current_device(&device);
+    if (st != MXFP8_OK)
+        return st;
+    if (!on_device(timed_out, device))
+        return MXFP8_ERR_DEVICE;
+    bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_ns),
+                                                                                  timed_out);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
 mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear)
 {
     if (out == nullptr)

@@ -198,3 +198,10 @@ def test_dact_host_checks(cuda_lib):
     assert d(x=A + 8) == ALIGN
     assert d(dbias=A) == WORKSPACE
     assert d() == DEVICE
+
+
+def test_selftest_bounded_wait_rejections(cuda_lib):
+    assert mx.mxfp8_selftest_bounded_wait(1_000_000, None) == NULL
+    assert mx.mxfp8_selftest_bounded_wait(0, A) == SHAPE
+    assert mx.mxfp8_selftest_bounded_wait(-5, A) == SHAPE
+    assert mx.mxfp8_selftest_bounded_wait(10_000_000_001, A) == SHAPE
