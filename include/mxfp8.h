@@ -343,6 +343,23 @@ mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear);
  */
 mxfp8_status_t mxfp8_selftest_bounded_wait(int64_t limit_ns, int *timed_out, void *stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): the fp32 values the kernels form
+ * from BF16 inputs, so that their accuracy can be checked on every input.
+ *   x           device bf16 [n] (2-byte aligned), any bit patterns.
+ *   activation  MXFP8_ACT_RELU .. MXFP8_ACT_QGELU.
+ *   derivative  0: act(x) as the forward cast (mxfp8_quantize_ex with
+ *               `activation`) evaluates it, for its scales and codes alike;
+ *               1: act'(x) as mxfp8_quantize_dact evaluates it (the product
+ *               with dY is one further fp32 multiply).
+ *   out         device fp32 [n], 4-byte aligned.
+ * Stream-ordered on `stream`.  Returns MXFP8_OK, MXFP8_ERR_FORMAT (activation
+ * or derivative out of range), MXFP8_ERR_SHAPE (n < 0 or n >= 2^40),
+ * MXFP8_ERR_NULL, MXFP8_ERR_ALIGN, MXFP8_ERR_DEVICE or MXFP8_ERR_LAUNCH.
+ */
+mxfp8_status_t mxfp8_activation_values(const void *x, int64_t n, int activation, int derivative, float *out,
+                                       void *stream);
+
 /* Size of the static scratch array used by mxfp8_quantize_dbias_noalloc. */
 #define MXFP8_NOALLOC_SCRATCH_BYTES (8u << 20)
 

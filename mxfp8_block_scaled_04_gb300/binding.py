@@ -95,6 +95,8 @@ def lib():
             L.mxfp8_device_fault_word.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
             L.mxfp8_selftest_bounded_wait.restype = i32
             L.mxfp8_selftest_bounded_wait.argtypes = [i64, vp, vp]
+            L.mxfp8_activation_values.restype = i32
+            L.mxfp8_activation_values.argtypes = [vp, i64, i32, i32, vp, vp]
             _lib = L
     return _lib
 
@@ -211,6 +213,14 @@ def mxfp8_device_fault_word(clear: bool = False) -> int:
 def mxfp8_selftest_bounded_wait(limit_ns: int, timed_out, stream=None) -> int:
     """Diagnostic: a bounded wait on a phase nothing completes (device int32 ``timed_out`` gets 1)."""
     return int(lib().mxfp8_selftest_bounded_wait(int(limit_ns), _addr(timed_out), _stream(stream)))
+
+
+def mxfp8_activation_values(x, n, activation, derivative, out, stream=None) -> int:
+    """Diagnostic: the kernels' fp32 act(x) (derivative 0) or act'(x) (1) for device bf16 ``x`` [n]."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_activation_values(_addr(x), int(n), int(activation), int(derivative), _addr(out),
+                                             _stream(stream)))
 
 
 class MXFP8Tensor(NamedTuple):

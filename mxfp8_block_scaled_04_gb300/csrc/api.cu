@@ -698,9 +698,78 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int *timed_out)
     }
 }
 
+// The fp32 value the cast kernels form from each BF16 input: act(x) through
+// activation2 (the forward cast's only evaluation) or act'(x) through dactivation2
+// (the backward fusion's), two inputs per thread as the kernels pair them.
+template <int ACT, bool DERIV>
+__global__ void activation_values_kernel(const uint16_t *__restrict__ x, int64_t n, float *__restrict__ out)
+{
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < pairs;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = 2 * p;
+        const bool two = i + 1 < n;
+        const float a = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+        const float b = two ? __uint_as_float(static_cast<uint32_t>(x[i + 1]) << 16) : a;
+        float ya, yb;
+        if constexpr (DERIV)
+            f2_unpack(dactivation2<ACT>(f2_pack(a, b)), ya, yb);
+        else
+            f2_unpack(activation2<ACT>(f2_pack(a, b)), ya, yb);
+        out[i] = ya;
+        if (two)
+            out[i + 1] = yb;
+    }
+}
+
+template <int ACT>
+mxfp8_status_t launch_activation_values(const uint16_t *x, int64_t n, bool deriv, float *out, cudaStream_t stream)
+{
+    const int64_t pairs = (n + 1) / 2;
+    const int64_t blocks64 = (pairs + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(blocks64 < 4096 ? blocks64 : 4096);
+    if (deriv)
+        activation_values_kernel<ACT, true><<<blocks, 256, 0, stream>>>(x, n, out);
+    else
+        activation_values_kernel<ACT, false><<<blocks, 256, 0, stream>>>(x, n, out);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cudaGetLastError() == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
+
+mxfp8_status_t mxfp8_activation_values(const void *x, int64_t n, int activation, int derivative, float *out,
+                                       void *stream)
+{
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU || (derivative != 0 && derivative != 1))
+        return MXFP8_ERR_FORMAT;
+    if (n < 0 || n >= (int64_t{1} << 40))
+        return MXFP8_ERR_SHAPE;
+    if (n == 0)
+        return MXFP8_OK;
+    if (x == nullptr || out == nullptr)
+        return MXFP8_ERR_NULL;
+    if (!aligned(x, 2) || !aligned(out, 4))
+        return MXFP8_ERR_ALIGN;
+    int device = 0;
+    mxfp8_status_t st = current_device(&device);
+    if (st != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(out, device))
+        return MXFP8_ERR_DEVICE;
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool d = derivative != 0;
+    switch (activation) {
+    case MXFP8_ACT_RELU: return launch_activation_values<1>(xb, n, d, out, s);
+    case MXFP8_ACT_SRELU: return launch_activation_values<2>(xb, n, d, out, s);
+    case MXFP8_ACT_GELU: return launch_activation_values<3>(xb, n, d, out, s);
+    case MXFP8_ACT_SILU: return launch_activation_values<4>(xb, n, d, out, s);
+    default: return launch_activation_values<5>(xb, n, d, out, s);
+    }
+}
 
 mxfp8_status_t mxfp8_selftest_bounded_wait(int64_t limit_ns, int *timed_out, void *stream)
 {

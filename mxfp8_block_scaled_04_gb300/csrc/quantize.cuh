@@ -161,31 +161,28 @@ __device__ __forceinline__ float sigmoid_arg(float x)
         return 1.702f * x;
 }
 
+// ReLU and squared ReLU (exact in fp32).
 template <int ACT>
-__device__ __forceinline__ float activation(float x)
+__device__ __forceinline__ float relu_family(float x)
 {
-    if constexpr (ACT == 1) {
+    if constexpr (ACT == 1)
         return x > 0.f ? x : 0.f;
-    } else if constexpr (ACT == 2) {
+    else
         return x > 0.f ? x * x : 0.f;
-    } else {
-        const float t = sigmoid_arg<ACT>(x);
-        const float e = exp2_twice(-kHalfLog2e * fabsf(t));
-        const float r = rcp_1to2(1.f + e);
-        return x * (t >= 0.f ? r : e * r);
-    }
 }
 
-// The same activations on two values at once (lanes lo and hi of a packed
-// pair): the multiplies and adds run as f32x2 operations, ex2 and rcp per lane.
-// Each lane's result is the one activation<ACT> gives.
+// The activations on two values at once (lanes lo and hi of a packed pair): the
+// multiplies and adds run as f32x2 operations, ex2 and rcp per lane.  This is the
+// only evaluation of the activations in the kernels (phase 1's column maxima and
+// phase 2's elements both come from here), so every value a scale or a code is
+// formed from is the same function of the BF16 input.
 template <int ACT>
 __device__ __forceinline__ uint64_t activation2(uint64_t x)
 {
     float x0, x1;
     f2_unpack(x, x0, x1);
     if constexpr (ACT <= 2) {
-        return f2_pack(activation<ACT>(x0), activation<ACT>(x1));
+        return f2_pack(relu_family<ACT>(x0), relu_family<ACT>(x1));
     } else {
         uint64_t t;
         if constexpr (ACT == 3) {  // 1.5957691216057308 * fma((0.044715 x) x, x, x)
@@ -489,12 +486,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                     m23 = max_bf16x2(m23, v.y);
                 }
                 float xm[4] = {bf16_lo(m01), bf16_hi(m01), bf16_lo(m23), bf16_hi(m23)};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    xm[k] = fmaxf(xm[k], __shfl_xor_sync(0xffffffffu, xm[k], 16));
                 float f[4];
+                f2_unpack(activation2<ACT>(f2_pack(xm[0], xm[1])), f[0], f[1]);
+                f2_unpack(activation2<ACT>(f2_pack(xm[2], xm[3])), f[2], f[3]);
                 bool slow = false;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    xm[k] = fmaxf(xm[k], __shfl_xor_sync(0xffffffffu, xm[k], 16));
-                    f[k] = xm[k] > 0.f ? activation<ACT>(xm[k]) : 0.f;
+                    f[k] = xm[k] > 0.f ? f[k] : 0.f;
                     slow |= ACT > 2 && f[k] < negative_side_bound<ACT>();
                 }
                 if (__any_sync(0xffffffffu, slow)) {
@@ -503,10 +504,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint2 v = lds64(base + i * 128 + (((cq >> 1) ^ (i & 7)) << 4));
-                        g[0] = fmaxf(g[0], fabsf(activation<ACT>(bf16_lo(v.x))));
-                        g[1] = fmaxf(g[1], fabsf(activation<ACT>(bf16_hi(v.x))));
-                        g[2] = fmaxf(g[2], fabsf(activation<ACT>(bf16_lo(v.y))));
-                        g[3] = fmaxf(g[3], fabsf(activation<ACT>(bf16_hi(v.y))));
+                        float a0, a1, a2, a3;
+                        f2_unpack(activation2<ACT>(f2_pack(bf16_lo(v.x), bf16_hi(v.x))), a0, a1);
+                        f2_unpack(activation2<ACT>(f2_pack(bf16_lo(v.y), bf16_hi(v.y))), a2, a3);
+                        g[0] = fmaxf(g[0], fabsf(a0));
+                        g[1] = fmaxf(g[1], fabsf(a1));
+                        g[2] = fmaxf(g[2], fabsf(a2));
+                        g[3] = fmaxf(g[3], fabsf(a3));
                     }
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
