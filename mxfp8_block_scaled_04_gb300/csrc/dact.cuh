@@ -38,8 +38,17 @@ constexpr int kDOffBars = kDOffPartD + 2 * 4 * kDBN * 4;   // uint64 [kStages]
 constexpr int kDOffCoord = kDOffBars + 8 * kStages;        // TileCoord [kStages]
 constexpr int kSmemDact = kDOffCoord + 32 * kStages + 1024;
 
+// Beyond |x| = 200 every derivative here is at its fp32 limit (1 for x > 0, -0 for
+// x < 0), so x is clamped there first: without it x^2 or 1.702 x overflows for
+// huge |x| and meets a zero factor (inf * 0 = NaN).
+constexpr float kDactClamp = 200.f;
+
 // act'(x) in fp32: 1 dReLU, 2 dSReLU, 3 dGeLU (tanh form), 4 dSiLU, 5 dQGeLU.
-// sigmoid(t) and 1 - sigmoid(t) both come from e = 2^(-|t| log2 e).
+// sigmoid(t) = s and 1 - sigmoid(t) both come from h = 2^(-|t| log2(e) / 2), e = h h.
+// The derivative is s (1 + q) with q = x (1 - s) t', rather than s + x s (1 - s) t'
+// (the sign of a tiny negative derivative survives), evaluated for t < 0 as
+// (((1 + q) h) h) / (1 + e): multiplying 1 + q in before the second h keeps results
+// that are fp32-subnormal where s alone would already have underflowed.
 template <int ACT>
 __device__ __forceinline__ float dactivation(float x)
 {
@@ -48,19 +57,22 @@ __device__ __forceinline__ float dactivation(float x)
     } else if constexpr (ACT == 2) {
         return x > 0.f ? 2.f * x : 0.f;
     } else {
+        x = fminf(fmaxf(x, -kDactClamp), kDactClamp);
         const float t = sigmoid_arg<ACT>(x);
-        const float e = exp2_twice(-kHalfLog2e * fabsf(t));
+        float h;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(-kHalfLog2e * fabsf(t)));
+        const float e = h * h;
         const float inv = rcp_1to2(1.f + e);
-        const float s = t >= 0.f ? inv : e * inv;
         const float oms = t >= 0.f ? e * inv : inv;
-        // s (1 + x (1 - s) t') rather than s + x s (1 - s) t': when s underflows to 0
-        // for very negative x this keeps the sign of the (tiny, negative) derivative
+        float inner;
         if constexpr (ACT == 3)
-            return s * (1.f + x * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x)));
+            inner = 1.f + x * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x));
         else if constexpr (ACT == 4)
-            return s * (1.f + x * oms);
+            inner = 1.f + x * oms;
         else
-            return s * (1.f + 1.702f * x * oms);
+            inner = 1.f + 1.702f * x * oms;
+        const float a = t >= 0.f ? 1.f : h;
+        return ((inner * a) * a) * inv;
     }
 }
 
@@ -75,6 +87,9 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
     if constexpr (ACT != 3) {
         return f2_pack(dactivation<ACT>(x0), dactivation<ACT>(x1));
     } else {
+        x0 = fminf(fmaxf(x0, -kDactClamp), kDactClamp);
+        x1 = fminf(fmaxf(x1, -kDactClamp), kDactClamp);
+        x = f2_pack(x0, x1);
         const uint64_t one = f2_splat(1.f);
         uint64_t t;
         if constexpr (ACT == 3) {
@@ -93,13 +108,12 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
         asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(z0));
         asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(z1));
         const uint64_t h = f2_pack(h0, h1);
-        const uint64_t e = f2_mul(h, h);  // as exp2_twice, both lanes
+        const uint64_t e = f2_mul(h, h);
         float o0, o1;
         f2_unpack(f2_add(e, one), o0, o1);
         const float i0 = rcp_1to2(o0), i1 = rcp_1to2(o1);
         float ei0, ei1;
         f2_unpack(f2_mul(e, f2_pack(i0, i1)), ei0, ei1);
-        const uint64_t sg = f2_pack(t0 >= 0.f ? i0 : ei0, t1 >= 0.f ? i1 : ei1);
         const uint64_t oms = f2_pack(t0 >= 0.f ? ei0 : i0, t1 >= 0.f ? ei1 : i1);
         uint64_t inner;
         if constexpr (ACT == 3) {
@@ -111,7 +125,8 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
         } else {
             inner = f2_fma(f2_mul(f2_splat(1.702f), x), oms, one);
         }
-        return f2_mul(sg, inner);
+        const uint64_t a = f2_pack(t0 >= 0.f ? 1.f : h0, t1 >= 0.f ? 1.f : h1);
+        return f2_mul(f2_mul(f2_mul(inner, a), a), f2_pack(i0, i1));
     }
 }
 
