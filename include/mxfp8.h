@@ -372,8 +372,10 @@ mxfp8_status_t mxfp8_activation_values(const void *x, int64_t n, int activation,
  * from, or code that must not allocate once it is running.  This call takes
  * the same arguments as mxfp8_quantize minus the workspace, and keeps the
  * dbias workspace in a file-scope device array of MXFP8_NOALLOC_SCRATCH_BYTES
- * (8 MiB) inside the library, which every GPU that loads the library holds
- * until the process exits.  It calls no cudaMalloc or cudaFree.
+ * (8 MiB) inside the library.  Each GPU holds the array from the moment the
+ * library's device code is loaded on it (the first use of any of its
+ * kernels, or the first call of this function, on that device) until the
+ * process exits.  It calls no cudaMalloc or cudaFree.
  *
  *   dbias      required (device fp32 [N]); NULL is MXFP8_ERR_NULL.
  *   M, N       as for mxfp8_quantize; shapes whose workspace
@@ -381,6 +383,10 @@ mxfp8_status_t mxfp8_activation_values(const void *x, int64_t n, int activation,
  *              bytes) exceeds 8 MiB are rejected with MXFP8_ERR_SHAPE, e.g.
  *              16384 x 8192 fits (4 MiB), 32768 x 16384 does not.
  *   others     as for mxfp8_quantize.
+ * Statuses come in mxfp8_quantize's order: MXFP8_ERR_FORMAT, then the shape
+ * rules (MXFP8_ERR_SHAPE), then a NULL dbias (MXFP8_ERR_NULL), then a shape
+ * beyond the scratch array (MXFP8_ERR_SHAPE), then mxfp8_quantize's own
+ * remaining checks.
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream

@@ -29,6 +29,7 @@ STATUS_NAMES = {
 
 SCALES_PLAIN = 0
 SCALES_SWIZZLED = 1
+NOALLOC_SCRATCH_BYTES = 8 << 20   # MXFP8_NOALLOC_SCRATCH_BYTES in include/mxfp8.h
 
 
 class QuantizeConfig(ctypes.Structure):

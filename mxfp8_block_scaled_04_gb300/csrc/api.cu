@@ -815,7 +815,8 @@ mxfp8_status_t mxfp8_device_fault_word(unsigned int *out, int clear)
 // that is handed only its input and output tensors and has no allocator or
 // workspace to draw from, or code that must not allocate once it is running.
 // The dbias workspace such a caller cannot provide lives in this file-scope device
-// array instead: 8 MiB, held on every GPU that loads the library until the process
+// array instead: 8 MiB on each GPU where the library's device code is loaded (from
+// the first use of its kernels, or of this call, on that device) until the process
 // exits.
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MXFP8_NOALLOC_SCRATCH_BYTES];
@@ -833,10 +834,13 @@ mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N,
                                             void *scale_row, void *out_col, void *scale_col, float *dbias,
                                             const float *noop, void *stream)
 {
+    // the checks mxfp8_quantize makes first, in its order, then this call's own
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
     if (dbias == nullptr)
         return MXFP8_ERR_NULL;
-    if (M < 0 || N < 0 || N % 16)
-        return MXFP8_ERR_SHAPE;
     if (mxfp8_quantize_workspace_bytes(M, N, 1) > MXFP8_NOALLOC_SCRATCH_BYTES)
         return MXFP8_ERR_SHAPE;  // needs more than the static scratch array holds
     int device = 0;

@@ -205,3 +205,16 @@ def test_selftest_bounded_wait_rejections(cuda_lib):
     assert mx.mxfp8_selftest_bounded_wait(0, A) == SHAPE
     assert mx.mxfp8_selftest_bounded_wait(-5, A) == SHAPE
     assert mx.mxfp8_selftest_bounded_wait(10_000_000_001, A) == SHAPE
+
+
+def test_noalloc_status_order_matches_quantize(cuda_lib):
+    """The no-allocation call reports a bad format before a NULL dbias or an oversized shape, and
+    the generic shape rules before its own scratch limit, as mxfp8_quantize orders its checks."""
+    from mxfp8_block_scaled_04_gb300 import binding
+    A = 1 << 20
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, 7, A, A, A, A, None, None, None) == 4        # FORMAT
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, 7, A, A, A, A, A, None, None) == 4     # FORMAT
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 24, 0, A, A, A, A, None, None, None) == 2        # SHAPE
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 1 << 31, 64, 0, A, A, A, A, A, None, None) == 2      # SHAPE
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, 0, A, A, A, A, None, None, None) == 1        # NULL dbias
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, 0, A, A, A, A, A, None, None) == 2     # beyond 8 MiB

@@ -27,6 +27,38 @@ def outputs(M, N):
             torch.full((N,), 7.0, dtype=torch.float32, device="cuda")]
 
 
+def _compare_one_call(fmt, M, N, seed, call):
+    x_bits = wl.grad_bf16(M, N, seed=seed)
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    ref = outputs(M, N)
+    ws = torch.empty(mx.mxfp8_quantize_workspace_bytes(M, N, True), dtype=torch.uint8, device="cuda")
+    assert mx.mxfp8_quantize(x, M, N, fmt, *ref[:4], ref[4], ws, None, None) == 0
+    got = outputs(M, N)
+    assert binding.mxfp8_quantize_dbias_noalloc(x, M, N, fmt, *got[:4], got[4], None, None) == 0
+    torch.cuda.synchronize()
+    for name, a, b in zip(("out_row", "scale_row", "out_col", "scale_col"), ref[:4], got[:4]):
+        assert torch.equal(a, b), f"call {call}: {name} differs"
+    tol = 1e-5 * torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().abs().sum(0)
+    diff = (ref[4].double().cpu() - got[4].double().cpu()).abs()
+    assert bool((diff <= tol).all()), f"call {call}: dbias differs"
+
+
+@pytest.mark.parametrize("fmt", [mx.E5M2, mx.E4M3])
+def test_noalloc_larger_then_smaller_call_same_columns(fmt):
+    """A smaller call after a larger one with the same N: the array still holds the larger call's
+    partial sums past the smaller call's row tiles, which the smaller call must neither need nor read."""
+    for call, M in enumerate([4096, 1056]):
+        _compare_one_call(fmt, M, 1024, seed=200 + call, call=call)
+
+
+def test_noalloc_at_the_scratch_limit():
+    """16384 x 16384 needs exactly 128 * 16384 * 4 bytes = 8 MiB of workspace: the largest accepted size."""
+    M, N = 16384, 16384
+    assert mx.mxfp8_quantize_workspace_bytes(M, N, True) == mx.binding.NOALLOC_SCRATCH_BYTES
+    _compare_one_call(mx.E5M2, M, N, seed=300, call=0)
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("fmt", [mx.E5M2, mx.E4M3])
 def test_noalloc_matches_workspace_entry_point_two_calls(fmt):
     for call, (M, N) in enumerate([(1056, 288), (4096, 1024)]):
