@@ -138,7 +138,7 @@ def profiled_traffic(name):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in a background process."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms in a background process."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -147,7 +147,7 @@ class ClockSampler:
     def __init__(self, gpu_uuid=None):
         self.samples = []   # (host time, sm, max, power, reasons)
         self.proc = None
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
         if gpu_uuid:
             cmd += ["-i", gpu_uuid]
         try:
@@ -178,11 +178,15 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
-        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
-        window = "timed"
+    def summary(self, t0, t1, load_t0=None):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.05]
+        window = "timed region"
+        if len(inside) < 3 and load_t0 is not None:
+            inside = [s for s in self.samples if load_t0 <= s[0] <= t1 + 0.05]
+            window = ("continuous load: the second half of the warm-up and the timed region "
+                      "(timed region shorter than 3 sampling periods)")
         if not inside:
-            inside, window = self.samples, "whole run (timed region shorter than the 100 ms sampling period)"
+            inside, window = self.samples, "whole run"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         reasons = sorted({r for s in inside for r in s[4]})
@@ -293,6 +297,42 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def host_link_ceiling(h2d_bytes, d2h_bytes, reps=5):
+    """Pinned host <-> device copy rates in this run: H2D alone, D2H alone, and both at once on
+    two streams (bytes over the link / time), each the best of `reps` on buffers of the e2e step's
+    sizes.  This is the ceiling the host-buffer path (e2e) runs against."""
+    import torch
+
+    hs = torch.empty(h2d_bytes, dtype=torch.uint8, pin_memory=True)
+    hd = torch.empty(d2h_bytes, dtype=torch.uint8, pin_memory=True)
+    ds = torch.empty(h2d_bytes, dtype=torch.uint8, device="cuda")
+    dd = torch.empty(d2h_bytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn, nbytes):
+        out = 0.0
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            out = max(out, nbytes / (time.perf_counter() - t) / 1e9)
+        return out
+
+    def both():
+        with torch.cuda.stream(s1):
+            ds.copy_(hs, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hd.copy_(dd, non_blocking=True)
+
+    r = {"h2d_gbs": best(lambda: ds.copy_(hs, non_blocking=True), h2d_bytes),
+         "d2h_gbs": best(lambda: hd.copy_(dd, non_blocking=True), d2h_bytes),
+         "both_gbs": best(both, h2d_bytes + d2h_bytes),
+         "how": "pinned copies of the e2e step's sizes, best of %d, wall clock around synchronize" % reps}
+    del hs, hd, ds, dd
+    return r
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -374,12 +414,15 @@ def run_ours(args):
     except Exception:
         uuid = None
 
-    # Warm-up: at least W steps, continued until 100 ms have passed so that the
-    # clocks have left their idle state before the timed region (measured: the
-    # first ~50 calls after idle run a few percent slow).
+    # Clock sampling runs from the start of the warm-up.  Warm-up: at least W steps,
+    # continued until 300 ms have passed so that the clocks have left their idle
+    # state (measured: the first ~50 calls after idle run a few percent slow); the
+    # timed region follows it at once, with no idle gap.
+    sampler = ClockSampler(uuid)
     warm_t0 = time.perf_counter()
+    warm_wall0 = time.time()
     warmup_run = 0
-    while warmup_run < max(3, args.warmup) or time.perf_counter() - warm_t0 < 0.1:
+    while warmup_run < max(3, args.warmup) or time.perf_counter() - warm_t0 < 0.3:
         step()
         warmup_run += 1
         if warmup_run % 16 == 0:
@@ -424,15 +467,28 @@ def run_ours(args):
             per_launch = [total_ms / args.steps]
         return total_ms, per_launch, launches, h0, h1
 
-    sampler = ClockSampler(uuid)
-    time.sleep(0.3)
     total_ms, per_launch, launches, h0, h1 = timed()
-    clocks = sampler.summary(h0, h1)
+    # a timed region shorter than the sampling period is judged with the samples of the
+    # continuous load around it: the second half of the warm-up and the timed region
+    clocks = sampler.summary(h0, h1, warm_wall0 + 0.15)
     if BAD_REASONS & set(clocks.get("reasons", [])):
+        for _ in range(16):
+            step()
+        torch.cuda.synchronize()
         total_ms, per_launch, launches, h0, h1 = timed()     # re-measure once
-        clocks = sampler.summary(h0, h1)
+        clocks = sampler.summary(h0, h1, h0 - 0.05)
         clocks["remeasured"] = True
     sampler.stop()
+
+    # Host cost of one call: wall time of enqueueing back-to-back calls with no
+    # synchronisation in between (the GPU runs behind; 64 calls stay far below
+    # the launch queue's depth).
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(64):
+        step()
+    host_us = (time.perf_counter() - t0) / 64 * 1e6
+    torch.cuda.synchronize()
 
     total_ms = all_ranks_max(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
@@ -486,8 +542,12 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         e2e_ms = all_ranks_max(a.elapsed_time(b) / n_e2e, dist, "cuda")
+        link = host_link_ceiling(h2d, d2h)
+        link_gbs = (h2d + d2h) / (e2e_ms / 1e3) / 1e9
         e2e = {"value": aggregate_gbs(algo_bytes, 1, world, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
-               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": path}
+               "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": path,
+               "host_link_gbs": link_gbs, "host_link_ceiling": link,
+               "frac_of_link_ceiling": link_gbs / link["both_gbs"]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -517,6 +577,7 @@ def run_ours(args):
                          "kernel": " + ".join(kernels),
                          "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": algo_bytes},
             "clocks": clocks,
+            "host_us_per_call": host_us,
             "gpu_launches": launches,
             "e2e": e2e,
             "cpu_baseline": cpu,
