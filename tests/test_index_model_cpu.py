@@ -1,0 +1,299 @@
+"""A CPU model of the cast kernels' index arithmetic: bounds, alignment, coverage.
+
+compute-sanitizer is not available on the test machines, so the kernels'
+memory accesses are checked here instead: this file restates, for every thread
+of every CTA of one launch, the global addresses quantize_kernel (flat and
+grouped, with and without dbias, plain and GEMM-ready scales),
+quantize_dact_kernel, swizzle_pad_kernel and the dbias reduces compute, with
+the same expressions as csrc/quantize.cuh, csrc/dact.cuh, csrc/dbias_reduce.cuh
+and csrc/api.cu (persistent tile loop, per-group tile prefix, phase-1 and
+phase-2 lane maps, 16- and 8-byte stores, scale and partial-sum rows).  Each
+write increments a counter over the output it lands in, after a bounds and
+alignment check.  Every output byte must be written exactly once, every
+partial-sum entry a reduce reads must have been written, and every TMA box
+origin must be in the tensor with a 16-byte aligned inner coordinate.
+
+The model holds no arithmetic of the method (no values are computed); it is
+not the oracle.  It is kept in step with the kernels by hand: a change to a
+kernel's indexing must be mirrored here.
+"""
+import numpy as np
+import pytest
+
+BM, BN, BOX, THREADS = 128, 128, 64, 256
+DBN = 64                     # backward-fusion tile columns
+LANES = np.arange(32)
+
+
+class Plane:
+    """Write counters for one output buffer of `size` elements of `width` bytes."""
+
+    def __init__(self, name, size, width=1):
+        self.name, self.size, self.width = name, size, width
+        self.parts = []
+        self._count = None
+
+    def write(self, idx, nbytes=1, align=1):
+        idx = np.asarray(idx, np.int64).ravel()
+        if idx.size == 0:
+            return
+        assert idx.min() >= 0 and idx.max() + nbytes <= self.size, (self.name, int(idx.min()), int(idx.max()))
+        assert np.all((idx * self.width) % align == 0), (self.name, "misaligned")
+        self.parts.append((idx[:, None] + np.arange(nbytes)).ravel())
+        self._count = None
+
+    @property
+    def count(self):
+        if self._count is None:
+            allidx = np.concatenate(self.parts) if self.parts else np.zeros(0, np.int64)
+            self._count = np.bincount(allidx, minlength=self.size)
+        return self._count
+
+    def once(self, mask=None):
+        c = self.count if mask is None else self.count[mask]
+        assert np.all(c == 1), (self.name, int((c != 1).sum()), np.unique(c))
+
+
+def swizzled_offset(r, c, C):
+    col_tiles = (C + 3) >> 2
+    return (((r >> 7) * col_tiles + (c >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3)
+
+
+def swizzled_bytes(R, C):
+    return ((R + 127) // 128 * 128) * ((C + 3) // 4 * 4)
+
+
+def tile_list(M, N, offsets):
+    """The kernel's tiles in order: (row0, row_end, col0, rt) per tile index."""
+    col_tiles = -(-N // BN)
+    if offsets is None:
+        row_tiles = -(-M // BM)
+        return [(rt * BM, min(rt * BM + BM, M), ct * BN, rt) for rt in range(row_tiles) for ct in range(col_tiles)]
+    G = len(offsets) - 1
+    gpre = [0]
+    for g in range(G):
+        gpre.append(gpre[-1] + -(-(offsets[g + 1] - offsets[g]) // BM) * col_tiles)
+    tiles = []
+    for t in range(gpre[G]):
+        lo, hi = 0, G                       # binary search: gpre[lo] <= t < gpre[hi]
+        while hi - lo > 1:
+            mid = (lo + hi) >> 1
+            if gpre[mid] <= t:
+                lo = mid
+            else:
+                hi = mid
+        local = t - gpre[lo]
+        rtl, ct = local // col_tiles, local % col_tiles
+        row0 = offsets[lo] + rtl * BM
+        tiles.append((row0, min(row0 + BM, offsets[lo + 1]), ct * BN, gpre[lo] // col_tiles + rtl))
+    return tiles
+
+
+def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True):
+    rows16 = N % 16 == 0
+    Cr = -(-N // 32)
+    out_row = Plane("out_row", M * N)
+    out_col = Plane("out_col", M * N)
+    if swz:
+        scale_row = Plane("scale_row", swizzled_bytes(M, Cr))
+        scale_col = Plane("scale_col", swizzled_bytes(N, -(-M // 32)))
+    else:
+        scale_row = Plane("scale_row", M * Cr)
+        scale_col = Plane("scale_col", -(-M // 32) * N)
+    tiles = tile_list(M, N, offsets)
+    ws_rows = max([t[3] for t in tiles], default=-1) + 1
+    ws = Plane("ws", ws_rows * N, 4)
+    # phase-1 lane map: warp -> (32-row block, box); lane -> (4-column group, 16-row half)
+    w1, l1 = np.repeat(np.arange(8), 32), np.tile(LANES, 8)
+    rb1, box1, cq1, half1 = w1 >> 1, w1 & 1, l1 & 15, l1 >> 4
+    assert np.all(box1 * 16384 + (rb1 * 32 + half1 * 16 + 15) * 128 + 127 < 32768)      # stage bounds
+    # phase-2 lane map: warp, task k -> (8-row group, box); lane -> (row in group, 16-column segment)
+    w2 = np.repeat(np.arange(8), 4 * 32)
+    k2 = np.tile(np.repeat(np.arange(4), 32), 8)
+    l2 = np.tile(LANES, 32)
+    task = w2 + 8 * k2
+    rg2, box2, rr2, sp2 = task >> 1, task & 1, l2 >> 2, l2 & 3
+    for b in range(grid):
+        for t in range(b, len(tiles), grid):
+            row0, row_end, col0, rt = tiles[t]
+            for box in range(2):            # TMA box origins (x must be 16-byte aligned)
+                x = col0 + box * BOX
+                if x < N:
+                    assert (x * 2) % 16 == 0 and 0 <= row0 < M
+            grow, gcol = row0 + rb1 * 32, col0 + box1 * BOX + cq1 * 4
+            sel = (grow < row_end) & (half1 == 0) & (gcol < N) & do_col
+            if swz:
+                C = -(-M // 32)
+                for j in range(4):
+                    scale_col.write(swizzled_offset(gcol[sel] + j, grow[sel] >> 5, C))
+            else:
+                scale_col.write((grow[sel] >> 5) * N + gcol[sel], 4, align=4)
+            if dbias:
+                gc = col0 + np.arange(BN)
+                ws.write(rt * N + gc[gc < N], 1, align=4)
+            grow = row0 + rg2 * 8 + rr2
+            gcol = col0 + box2 * BOX + sp2 * 16
+            ok = (row0 + rg2 * 8 < row_end) & (grow < row_end) & (gcol < N)
+            half_seg = gcol + 16 > N
+            assert not (rows16 and np.any(ok & half_seg))
+            full, part = ok & ~half_seg, ok & half_seg
+            for plane, on in ((out_row, do_row), (out_col, do_col)):
+                if on:
+                    plane.write(grow[full] * N + gcol[full], 16, align=16 if rows16 else 8)
+                    plane.write(grow[part] * N + gcol[part], 8, align=8)
+            if do_row:
+                se = ok & (sp2 % 2 == 0)
+                scale_row.write(swizzled_offset(grow[se], gcol[se] >> 5, Cr) if swz else grow[se] * Cr + (gcol[se] >> 5))
+    return dict(out_row=out_row, out_col=out_col, scale_row=scale_row, scale_col=scale_col, ws=ws,
+                ws_rows=ws_rows, tiles=tiles)
+
+
+def model_swizzle_pad(R, C, plane):
+    """swizzle_pad_kernel: zero the padding entries of the last row tile and the last column tile."""
+    col_tiles, row_tiles = (C + 3) // 4, (R + 127) // 128
+    if R % 128 == 0 and C % 4 == 0:
+        return
+    for t in range(col_tiles + row_tiles - 1):
+        rt = row_tiles - 1 if t < col_tiles else t - col_tiles
+        ct = t if t < col_tiles else col_tiles - 1
+        for w in range(512):
+            r, c = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), ct * 4 + (w & 3)
+            if r >= R or c >= C:
+                plane.write(((rt * col_tiles + ct) << 9) + w)
+
+
+def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True):
+    m = model_quantize(M, N, grid, offsets, dbias, swz, do_row, do_col)
+    for name, on in (("out_row", do_row), ("out_col", do_col)):
+        if on:
+            m[name].once()
+        else:
+            assert not m[name].count.any()
+    if swz:
+        Cr = -(-N // 32)
+        if do_row:
+            model_swizzle_pad(M, Cr, m["scale_row"])
+            m["scale_row"].once()
+        if do_col:
+            model_swizzle_pad(N, -(-M // 32), m["scale_col"])
+            m["scale_col"].once()
+    else:
+        if do_row:
+            m["scale_row"].once()
+        if do_col:
+            m["scale_col"].once()
+    if dbias:
+        # the reduce reads ws[t * N + j] for every tile row t < ws_rows and column j < N
+        m["ws"].once()
+    return m
+
+
+FLAT = [(1, 8), (33, 8), (45, 80), (96, 40), (128, 256), (257, 1032), (130, 144), (1000, 2056), (31, 4096),
+        (544, 1056), (384, 224)]
+
+
+@pytest.mark.parametrize("shape", FLAT)
+@pytest.mark.parametrize("grid", [1, 7, 304])
+def test_flat_cast_writes_every_byte_once(shape, grid):
+    M, N = shape
+    check_quantize(M, N, grid, dbias=True)
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (96, 40), (257, 1032), (130, 144)])
+@pytest.mark.parametrize("dirs", [(True, False), (False, True)])
+def test_flat_cast_swizzled_single_direction(shape, dirs):
+    check_quantize(*shape, grid=5, swz=True, do_row=dirs[0], do_col=dirs[1])
+    check_quantize(*shape, grid=5, swz=True)
+
+
+@pytest.mark.parametrize("N", [24, 40, 96, 160, 1032])
+@pytest.mark.parametrize("grid", [3, 304])
+def test_grouped_cast_writes_every_byte_once(N, grid):
+    sizes = [64, 0, 32, 416, 0, 0, 128, 96, 160, 32]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    m = check_quantize(off[-1], N, grid, offsets=off, dbias=True)
+    # no tile straddles two groups; each group's tiles are contiguous in the partial-sum rows
+    for row0, row_end, col0, rt in m["tiles"]:
+        g = max(i for i in range(len(off) - 1) if off[i] <= row0)
+        assert row_end <= off[g + 1]
+
+
+def test_grouped_many_groups_and_empty_ones():
+    rng = np.random.Generator(np.random.PCG64(5))
+    sizes = (32 * rng.choice([0, 1, 3, 4, 5, 17], size=200)).tolist()
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    check_quantize(off[-1], 48, 304, offsets=off, dbias=True)
+
+
+def model_dact(M, N, grid, dbias=True):
+    rows16 = N % 16 == 0
+    out_row, out_col = Plane("out_row", M * N), Plane("out_col", M * N)
+    scale_row, scale_col = Plane("scale_row", M * -(-N // 32)), Plane("scale_col", -(-M // 32) * N)
+    row_tiles, col_tiles = -(-M // BM), -(-N // DBN)
+    ws = Plane("ws", row_tiles * N, 4)
+    tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN, rt) for rt in range(row_tiles) for ct in range(col_tiles)]
+    tid = np.arange(THREADS)
+    rb1, c1 = tid >> 6, tid & 63                       # one thread per (32-row block, column)
+    w2 = np.repeat(np.arange(8), 2 * 32)
+    k2 = np.tile(np.repeat(np.arange(2), 32), 8)
+    l2 = np.tile(LANES, 16)
+    rg2, rr2, sp2 = w2 + 8 * k2, l2 >> 2, l2 & 3
+    for b in range(grid):
+        for t in range(b, len(tiles), grid):
+            row0, row_end, col0, rt = tiles[t]
+            assert (col0 * 2) % 16 == 0 and col0 < N and row0 < M
+            grow, gcol = row0 + rb1 * 32, col0 + c1
+            sel = (grow < row_end) & (gcol < N)
+            scale_col.write((grow[sel] >> 5) * N + gcol[sel])
+            if dbias:
+                gc = col0 + np.arange(DBN)
+                ws.write(rt * N + gc[gc < N], 1, align=4)
+            grow, gcol = row0 + rg2 * 8 + rr2, col0 + sp2 * 16
+            ok = (row0 + rg2 * 8 < row_end) & (grow < row_end) & (gcol < N)
+            half_seg = gcol + 16 > N
+            full, part = ok & ~half_seg, ok & half_seg
+            for plane in (out_row, out_col):
+                plane.write(grow[full] * N + gcol[full], 16, align=16 if rows16 else 8)
+                plane.write(grow[part] * N + gcol[part], 8, align=8)
+            se = ok & (sp2 % 2 == 0)
+            scale_row.write(grow[se] * -(-N // 32) + (gcol[se] >> 5))
+    for p in (out_row, out_col, scale_row, scale_col, ws):
+        p.once()
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (70, 24), (257, 1032), (130, 144), (256, 64)])
+def test_backward_fusion_writes_every_byte_once(shape):
+    model_dact(*shape, grid=5)
+    model_dact(*shape, grid=304)
+
+
+def grouped_reduce_reads(hdr, N):
+    """dbias_reduce_grouped_kernel: the partial rows each (group, column) sums, for one CTA of 32
+    columns, following its 16 contiguous warp ranges and the head / tail hand-over."""
+    G = len(hdr) - 1
+    T = hdr[G]
+    sums = {g: [] for g in range(G)}
+    for w in range(16):
+        a, b = T * w // 16, T * (w + 1) // 16
+        for t in range(a, b):
+            g = max(i for i in range(G) if hdr[i] <= t)
+            sums[g].append(t)
+    return sums
+
+
+@pytest.mark.parametrize("sizes", [[64, 0, 32, 416, 0, 0, 128, 96, 160, 32], [8192], [0, 2080, 0, 0, 32, 4096, 0]])
+def test_grouped_reduce_reads_each_partial_row_of_its_group_once(sizes):
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    N = 96
+    m = model_quantize(off[-1], N, 304, offsets=off, dbias=True)
+    col_tiles = -(-N // BN)
+    G = len(sizes)
+    hdr, acc = [0], 0
+    for g in range(G):
+        acc += -(-sizes[g] // BM) * col_tiles
+        hdr.append(acc // col_tiles)
+    sums = grouped_reduce_reads(hdr, N)
+    written_rows = {t[3] for t in m["tiles"]}
+    for g in range(G):
+        assert sorted(sums[g]) == list(range(hdr[g], hdr[g + 1]))
+        assert set(sums[g]) <= written_rows
