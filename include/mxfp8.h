@@ -8,8 +8,9 @@
  * this ABI exposes: fp8_dtype, rowwise, colwise, with_dbias and with_noop;
  * the "non-32-divisible shapes" review fixes the 32-element block.  Shapes
  * that are not multiples of 32 are accepted here: M may be any size and N
- * any multiple of 16; a row's (column's) last block then holds the
- * remaining N % 32 (M % 32) elements and takes its amax over those only.
+ * any multiple of 8 (a 16-byte BF16 row pitch, which the TMA loads need); a
+ * row's (column's) last block then holds the remaining N % 32 (M % 32)
+ * elements and takes its amax over those only.
  *
  * Arithmetic, per 32-element block with amax = max |x| over the block:
  *     e = clamp(ceil(log2(amax / Fmax)) + 127, 0, 254)   (amax == 0 -> e = 127)
@@ -63,7 +64,7 @@ typedef enum {
 typedef enum {
     MXFP8_OK = 0,
     MXFP8_ERR_NULL = 1,      /* required pointer NULL, a data/scale pair half set, or no direction */
-    MXFP8_ERR_SHAPE = 2,     /* M or N negative, N not a multiple of 16, or too large */
+    MXFP8_ERR_SHAPE = 2,     /* M or N negative, N not a multiple of 8, or too large */
     MXFP8_ERR_ALIGN = 3,     /* x/out/workspace not 16-byte aligned, scale_col/dbias not 4-byte */
     MXFP8_ERR_FORMAT = 4,    /* fp8_fmt not MXFP8_E4M3 / MXFP8_E5M2 */
     MXFP8_ERR_WORKSPACE = 5, /* dbias requested and workspace NULL */
@@ -88,8 +89,9 @@ size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias);
  * with_dbias / with_noop config fields).
  *
  *   x           device, bf16 [M,N], 16-byte aligned.
- *   M, N        M >= 0, N >= 0 a multiple of 16 (the TMA row pitch and the
- *               16-byte stores need 16-byte rows).  M == 0 or N == 0: nothing to quantize,
+ *   M, N        M >= 0, N >= 0 a multiple of 8 (the TMA loads need a 16-byte
+ *               BF16 row pitch; FP8 rows of N % 16 == 8 bytes are written with
+ *               8-byte stores).  M == 0 or N == 0: nothing to quantize,
  *               x and the output pointers may then be NULL (dbias, if
  *               requested, is set to zeros unless noop).
  *   fp8_fmt     MXFP8_E4M3 or MXFP8_E5M2.
@@ -142,7 +144,7 @@ size_t mxfp8_quantize_grouped_workspace_bytes(int64_t total_rows, int64_t N, int
  *                kernel writes nothing and sets *err_flag = 1.  It is never
  *                cleared by the library.
  *
- * total_rows must be a multiple of 32 (as every group is) and N of 16.
+ * total_rows must be a multiple of 32 (as every group is) and N of 8.
  */
 mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t N,
                                       int num_groups, const int64_t *offsets, int fp8_fmt,
@@ -172,7 +174,7 @@ size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias);
  *               mxfp8_quantize; a direction is skipped as there.  Pinned
  *               memory (cudaHostAlloc / cudaHostRegister) lets the copies
  *               overlap; pageable memory works but serialises them.
- *   M, N        M > 0, N > 0 a multiple of 16.
+ *   M, N        M > 0, N > 0 a multiple of 8.
  *   staging     device buffer, 256-byte aligned, at least
  *               mxfp8_quantize_host_staging_bytes(M, N, dbias_host != NULL)
  *               bytes (otherwise MXFP8_ERR_WORKSPACE); owned by the caller.
@@ -241,7 +243,7 @@ typedef enum {
  */
 typedef struct mxfp8_quantize_config {
     const void *x;         /* device bf16 [M, N] */
-    int64_t M, N;          /* M >= 0, N >= 0 a multiple of 16 */
+    int64_t M, N;          /* M >= 0, N >= 0 a multiple of 8 */
     int fp8_fmt;           /* MXFP8_E4M3 / MXFP8_E5M2 */
     void *out_row;         /* uint8 [M, N] or NULL */
     void *scale_row;       /* mxfp8_scale_bytes(M, ceil(N/32), scale_layout) bytes */
@@ -280,7 +282,7 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
  *               are exact; the others are within a few fp32 ulps.
  *   outputs, dbias, workspace, noop, stream: as for mxfp8_quantize
  *               (workspace: mxfp8_quantize_workspace_bytes(M, N, 1) bytes).
- * Shapes as for mxfp8_quantize (M >= 0, N a multiple of 16).
+ * Shapes as for mxfp8_quantize (M >= 0, N a multiple of 8).
  */
 mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int64_t M, int64_t N,
                                    int fp8_fmt, int activation,

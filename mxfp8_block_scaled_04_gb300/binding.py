@@ -254,7 +254,7 @@ def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = Tr
              with_dbias: bool = False, noop: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, stream=None, swizzled: bool = False,
              with_amax: bool = False, activation="none") -> MXFP8Tensor:
-    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (any M, N a multiple of 16).
+    """MXFP8-quantize a contiguous CUDA bf16 tensor [M, N] (any M, N a multiple of 8).
 
     ``swizzled`` writes both scale planes in the GEMM-ready layout (1-D tensors of
     mxfp8_scale_bytes bytes); ``with_amax`` also returns max |x| as a float32 [1];

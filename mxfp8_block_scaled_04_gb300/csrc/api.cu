@@ -347,7 +347,7 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 16 || total_rows >= (int64_t{1} << 31) ||
+    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 8 || total_rows >= (int64_t{1} << 31) ||
         N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
@@ -414,7 +414,7 @@ extern "C" {
 
 size_t mxfp8_quantize_workspace_bytes(int64_t M, int64_t N, int with_dbias)
 {
-    if (!with_dbias || M < 0 || N < 0 || N % 16)
+    if (!with_dbias || M < 0 || N < 0 || N % 8)
         return 0;
     return static_cast<size_t>((M + kBM - 1) / kBM) * static_cast<size_t>(N) * sizeof(float);
 }
@@ -428,7 +428,7 @@ mxfp8_status_t mxfp8_quantize(const void *x, int64_t M, int64_t N, int fp8_fmt, 
     // ---- host-only checks, in a fixed order, before touching the device ----
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     const bool empty = M == 0 || N == 0;  // nothing to read or write: data pointers may be NULL
     mxfp8_status_t st;
@@ -500,7 +500,7 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
     const int64_t M = cfg->M, N = cfg->N;
     if (cfg->fp8_fmt != MXFP8_E4M3 && cfg->fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     const bool swz = cfg->scale_layout == MXFP8_SCALES_SWIZZLED;
     const bool empty = M == 0 || N == 0;
@@ -582,7 +582,7 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
         return MXFP8_ERR_FORMAT;
     if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     const bool empty = M == 0 || N == 0;
     mxfp8_status_t st;
@@ -642,7 +642,7 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
 
 size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups)
 {
-    if (total_rows < 0 || N < 0 || num_groups < 1 || total_rows % 32 || N % 16)
+    if (total_rows < 0 || N < 0 || num_groups < 1 || total_rows % 32 || N % 8)
         return 0;
     return static_cast<size_t>(grouped_header_floats(num_groups)) * sizeof(float) +
            static_cast<size_t>((total_rows + kBM - 1) / kBM + num_groups) * static_cast<size_t>(N) * sizeof(float);
@@ -666,7 +666,7 @@ const char *mxfp8_status_string(int status)
     switch (status) {
     case MXFP8_OK: return "ok";
     case MXFP8_ERR_NULL: return "required pointer is NULL, a data/scale pair is half set, or no direction requested";
-    case MXFP8_ERR_SHAPE: return "M must be >= 0, N a non-negative multiple of 16, both below 2^31 (grouped: rows in multiples of 32)";
+    case MXFP8_ERR_SHAPE: return "M must be >= 0, N a non-negative multiple of 8, both below 2^31 (grouped: rows in multiples of 32)";
     case MXFP8_ERR_ALIGN: return "x/out/workspace must be 16-byte aligned, scale_col/dbias 4-byte aligned";
     case MXFP8_ERR_FORMAT: return "fp8_fmt must be MXFP8_E4M3 (0) or MXFP8_E5M2 (1)";
     case MXFP8_ERR_WORKSPACE: return "dbias requested without a workspace";
@@ -837,7 +837,7 @@ mxfp8_status_t mxfp8_quantize_dbias_noalloc(const void *x, int64_t M, int64_t N,
     // the checks mxfp8_quantize makes first, in its order, then this call's own
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M < 0 || N < 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (dbias == nullptr)
         return MXFP8_ERR_NULL;
@@ -1020,7 +1020,7 @@ extern "C" {
 
 size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias)
 {
-    if (M <= 0 || N <= 0 || N % 16)
+    if (M <= 0 || N <= 0 || N % 8)
         return 0;
     const SlotLayout L = slot_layout(host_chunk_rows(M, N), N);
     size_t b = kHostSlots * L.bytes;
@@ -1035,7 +1035,7 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (M <= 0 || N <= 0 || N % 16 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+    if (M <= 0 || N <= 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (x_host == nullptr || staging == nullptr)
         return MXFP8_ERR_NULL;

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (my_count == 0)
         return;
     const bool do_row = p.out_row != nullptr, do_col = p.out_col != nullptr;
+    const bool rows16 = (N & 15) == 0;  // FP8 rows 16-byte aligned (else N % 16 == 8: 8-byte)
 
     if (tid == 0) {
         prefetch_tensormap(&tmap_g);
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         o[j] = cvt_pair(y[4 * j], y[4 * j + 1], rm, rm) |
                                (cvt_pair(y[4 * j + 2], y[4 * j + 3], rm, rm) << 16);
                     if (in) {
-                        stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        store_codes(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                         if ((sp & 1) == 0)
                             p.scale_row[grow * ((N + 31) >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
                     }
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                (cvt_pair(y[4 * j + 2], y[4 * j + 3], c.z, c.w) << 16);
                     }
                     if (in)
-                        stg128(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        store_codes(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                 }
             }
         }

@@ -138,6 +138,27 @@ __device__ __forceinline__ void stg128(void *p, uint32_t a, uint32_t b, uint32_t
                  : "memory");
 }
 
+// 8-byte global store that does not allocate in L1.
+__device__ __forceinline__ void stg64(void *p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// The 16 FP8 codes of one row segment, stored at p.  Rows are 16-byte aligned when
+// N % 16 == 0 (one 16-byte store); when N % 16 == 8 they are only 8-byte aligned
+// (two 8-byte stores), and the row's last segment holds 8 columns (first half only).
+__device__ __forceinline__ void store_codes(uint8_t *p, uint32_t o0, uint32_t o1, uint32_t o2, uint32_t o3,
+                                            bool rows16, bool half)
+{
+    if (rows16) {
+        stg128(p, o0, o1, o2, o3);
+    } else {
+        stg64(p, o0, o1);
+        if (!half)
+            stg64(p + 8, o2, o3);
+    }
+}
+
 // BF16 halves of a packed word, widened exactly to fp32.
 // Two fp32 values in one 64-bit register pair, for Blackwell's packed
 // add / mul / fma.rn.f32x2 (each lane rounds exactly as the scalar operation).

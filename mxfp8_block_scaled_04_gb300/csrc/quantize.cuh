@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const bool do_row = p.out_row != nullptr;
     const bool do_col = p.out_col != nullptr;
+    const bool rows16 = (N & 15) == 0;  // FP8 rows 16-byte aligned (else N % 16 == 8: 8-byte)
 
     if (tid == 0) {
         prefetch_tensormap(&tmap);
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         o[j] = lo | (hi << 16);
                     }
                     if (in) {
-                        stg128(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        store_codes(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                         if ((sp & 1) == 0)
                             p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, (N + 31) >> 5)
                                             : grow * ((N + 31) >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         o[j] = lo | (hi << 16);
                     }
                     if (in)
-                        stg128(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3]);
+                        store_codes(p.out_col + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                 }
             }
         }

@@ -162,7 +162,7 @@ def quantize_grouped(x_bits: np.ndarray, offsets: np.ndarray, fmt: int):
     off = np.ascontiguousarray(offsets, dtype=np.int64)
     G = off.shape[0] - 1
     out_row = np.zeros((total, N), np.uint8)
-    scale_row = np.zeros((total, N // BLOCK), np.uint8)
+    scale_row = np.zeros((total, -(-N // BLOCK)), np.uint8)
     out_col = np.zeros((total, N), np.uint8)
     scale_col = np.zeros((total // BLOCK, N), np.uint8)
     rc = _load().mxo_quantize_grouped(_ptr(x, ctypes.c_uint16), total, N, G, _ptr(off, ctypes.c_int64), fmt,

@@ -48,7 +48,8 @@ def test_workspace_bytes(cuda_lib):
     assert mx.mxfp8_quantize_workspace_bytes(96, 64, True) == 1 * 64 * 4
     assert mx.mxfp8_quantize_workspace_bytes(160, 64, True) == 2 * 64 * 4
     assert mx.mxfp8_quantize_workspace_bytes(100, 64, True) == 1 * 64 * 4  # any M
-    assert mx.mxfp8_quantize_workspace_bytes(100, 72, True) == 0          # N not a multiple of 16
+    assert mx.mxfp8_quantize_workspace_bytes(100, 72, True) == 1 * 72 * 4     # N a multiple of 8
+    assert mx.mxfp8_quantize_workspace_bytes(100, 68, True) == 0          # N not a multiple of 8
     assert mx.mxfp8_quantize_grouped_workspace_bytes(65536, 7168, 64) == 0
 
 
@@ -58,7 +59,7 @@ def q(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, ws=Non
 
 @pytest.mark.parametrize("kw,status", [
     (dict(fmt=2), FORMAT), (dict(fmt=-1), FORMAT),
-    (dict(N=100), SHAPE), (dict(N=40), SHAPE), (dict(M=-32), SHAPE), (dict(N=1 << 31), SHAPE),
+    (dict(N=100), SHAPE), (dict(N=36), SHAPE), (dict(N=4), SHAPE), (dict(M=-32), SHAPE), (dict(N=1 << 31), SHAPE),
     (dict(x=None), NULL), (dict(orow=None), NULL), (dict(scol=None), NULL),
     (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(x=A + 8), ALIGN), (dict(orow=A + 4), ALIGN), (dict(ocol=A + 8), ALIGN), (dict(scol=A + 2), ALIGN),
@@ -81,7 +82,7 @@ def g(x=A, total=128, N=64, G=2, off=A, fmt=0, orow=A, srow=A, ocol=A, scol=A, e
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=40), SHAPE),
+    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=36), SHAPE),
     (dict(G=0), GROUPS), (dict(G=mx.MAX_GROUPS + 1), GROUPS), (dict(off=None), GROUPS),
     (dict(x=None), NULL), (dict(orow=None), NULL), (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(x=A + 2), ALIGN), (dict(off=A + 4), ALIGN), (dict(err=A + 2), ALIGN),
@@ -103,7 +104,7 @@ def h(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, stagin
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=5), FORMAT), (dict(M=0), SHAPE), (dict(N=40), SHAPE),
+    (dict(fmt=5), FORMAT), (dict(M=0), SHAPE), (dict(N=36), SHAPE),
     (dict(x=None), NULL), (dict(staging=None), NULL), (dict(orow=None), NULL),
     (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(staging=A + 16), ALIGN), (dict(nbytes=1024), WORKSPACE),
@@ -153,7 +154,7 @@ def test_ex_rejections(cuda_lib):
     cfg = mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1)
     cfg.reserved[3] = 1
     assert mx.mxfp8_quantize_ex(cfg, 0) == FORMAT
-    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 40, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
+    assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 36, 0, A, A, A, A, scale_layout=1), 0) == SHAPE
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, None, A, A, A, scale_layout=1), 0) == NULL
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, scale_layout=1, amax=A + 2), 0) == ALIGN
     assert mx.mxfp8_quantize_ex(mx.make_config(A, 64, 64, 0, A, A, A, A, activation=6), 0) == FORMAT
@@ -164,10 +165,12 @@ def test_ex_rejections(cuda_lib):
 
 
 def test_ragged_shapes_pass_host_checks(cuda_lib):
-    # M not a multiple of 32 and N a multiple of 16 are valid shapes: with fake
+    # M not a multiple of 32 and N a multiple of 8 are valid shapes: with fake
     # pointers the call gets past every host check and stops at the device stage
     assert q(M=45, N=80) == DEVICE
     assert q(M=1, N=16) == DEVICE
+    assert q(M=33, N=8) == DEVICE
+    assert q(M=7, N=40) == DEVICE
 
 
 def test_grouped_dbias_host_checks(cuda_lib):
@@ -193,7 +196,7 @@ def test_dact_host_checks(cuda_lib):
         return mx.mxfp8_quantize_dact(a["g"], a["x"], a["M"], a["N"], a["fmt"], a["act"], A, A, A, A,
                                       a["dbias"], a["ws"], None, 0)
     assert d(act=0) == FORMAT and d(act=6) == FORMAT and d(fmt=2) == FORMAT
-    assert d(N=40) == SHAPE
+    assert d(N=36) == SHAPE
     assert d(x=None) == NULL and d(g=None) == NULL
     assert d(x=A + 8) == ALIGN
     assert d(dbias=A) == WORKSPACE
@@ -214,7 +217,7 @@ def test_noalloc_status_order_matches_quantize(cuda_lib):
     A = 1 << 20
     assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, 7, A, A, A, A, None, None, None) == 4        # FORMAT
     assert binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, 7, A, A, A, A, A, None, None) == 4     # FORMAT
-    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 24, 0, A, A, A, A, None, None, None) == 2        # SHAPE
+    assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 20, 0, A, A, A, A, None, None, None) == 2        # SHAPE
     assert binding.mxfp8_quantize_dbias_noalloc(A, 1 << 31, 64, 0, A, A, A, A, A, None, None) == 2      # SHAPE
     assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, 0, A, A, A, A, None, None, None) == 1        # NULL dbias
     assert binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, 0, A, A, A, A, A, None, None) == 2     # beyond 8 MiB

@@ -1,6 +1,6 @@
 """Seeded random sweep against the oracle.
 
-Each case draws a shape (M any in 1..699, N a multiple of 16 up to 1200), a format, the directions,
+Each case draws a shape (M any in 1..699, N a multiple of 8 up to 1200), a format, the directions,
 and the options (dbias, GEMM-ready scales, amax), plus one of the value recipes, and compares every
 FP8 byte and scale byte with the oracle (dbias within 1e-5 * sum |x| per column, amax exactly).
 """
@@ -17,7 +17,7 @@ CASES = 48
 def draw(i):
     rng = np.random.Generator(np.random.PCG64(7000 + i))
     M = int(rng.integers(1, 700))
-    N = 16 * int(rng.integers(1, 76))
+    N = 8 * int(rng.integers(1, 151))
     fmt = int(rng.integers(0, 2))
     dirs = int(rng.integers(1, 4))  # 1 rowwise, 2 columnwise, 3 both
     opts = dict(with_dbias=bool(rng.integers(0, 2)), swizzled=bool(rng.integers(0, 2)),
@@ -56,8 +56,10 @@ def test_draws_cover_the_options():
     seen = set()
     for i in range(CASES):
         M, N, fmt, dirs, opts, _ = draw(i)
-        seen |= {("fmt", fmt), ("dirs", dirs), ("ragged_M", M % 32 != 0), ("ragged_N", N % 32 != 0)}
+        seen |= {("fmt", fmt), ("dirs", dirs), ("ragged_M", M % 32 != 0), ("ragged_N", N % 32 != 0),
+                 ("N_8_mod_16", N % 16 == 8)}
         seen |= {(k, v) for k, v in opts.items()}
     for need in [("fmt", 0), ("fmt", 1), ("dirs", 1), ("dirs", 2), ("dirs", 3), ("ragged_M", True),
-                 ("ragged_N", True), ("with_dbias", True), ("swizzled", True), ("with_amax", True)]:
+                 ("ragged_N", True), ("N_8_mod_16", True), ("with_dbias", True), ("swizzled", True),
+                 ("with_amax", True)]:
         assert need in seen, need

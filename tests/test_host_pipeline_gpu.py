@@ -29,6 +29,7 @@ def device_reference(x_bits, fmt, with_dbias, rowwise=True, colwise=True):
     ((96, 160), mx.E4M3, True, True),         # a single chunk smaller than a tile
     ((4195, 4096), mx.E5M2, True, True),      # M not a multiple of 32: last chunk 99 rows
     ((1000, 1040), mx.E4M3, False, True),     # N = 16 mod 32
+    ((1033, 1032), mx.E5M2, True, True),      # N = 8 mod 16: FP8 rows 8-byte aligned
 ])
 def test_host_pipeline_matches_device_path(shape, fmt, with_dbias, pinned):
     M, N = shape

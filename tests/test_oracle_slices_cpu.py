@@ -23,12 +23,16 @@ def test_slices_equal_whole_matrix(oracle_mod, shape, threads, fmt):
         assert np.array_equal(g, w)
 
 
-def test_slices_grouped_equal_whole_matrix(oracle_mod):
+@pytest.mark.parametrize("N", [224, 200, 40])
+def test_slices_grouped_equal_whole_matrix(oracle_mod, N):
     sizes = np.array([64, 0, 32, 416, 0, 128, 96], np.int64)
     off = wl.offsets_from_sizes(sizes)
-    x = wl.moe_bf16(sizes, 224, seed=4)
+    x = wl.moe_bf16(sizes, N, seed=4)
     for g, w in zip(oracle_slices.quantize_grouped(oracle_mod, x, off, 0, threads=3),
                     oracle_mod.quantize_grouped(x, off, 0)):
+        assert np.array_equal(g, w)
+    # the grouped oracle is the flat oracle on the concatenated rows, partial last blocks included
+    for g, w in zip(oracle_mod.quantize_grouped(x, off, 0), oracle_mod.quantize(x, 0)[:4]):
         assert np.array_equal(g, w)
     assert np.array_equal(oracle_slices.grouped_dbias(oracle_mod, x, off, threads=3),
                           oracle_mod.grouped_dbias(x, off))

@@ -186,7 +186,7 @@ def run_grouped(x_bits, offsets, fmt, noop=None, prefill=CANARY):
     total, N = x_bits.shape
     x = dev_bf16(x_bits)
     off = torch.from_numpy(np.asarray(offsets, np.int64)).cuda()
-    bufs = dict(out_row=Guarded((total, N), fill=prefill), scale_row=Guarded((total, N // 32), fill=prefill),
+    bufs = dict(out_row=Guarded((total, N), fill=prefill), scale_row=Guarded((total, -(-N // 32)), fill=prefill),
                 out_col=Guarded((total, N), fill=prefill), scale_col=Guarded((total // 32, N), fill=prefill))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     st = mx.mxfp8_quantize_grouped(x, total, N, off.numel() - 1, off, fmt, bufs["out_row"].t,
@@ -364,6 +364,40 @@ def test_parity_ragged_shapes(oracle_mod, shape, fmt):
     x = mixed_input(M, N, seed=M * 13 + N + fmt)
     host = run_quantize(x, fmt)
     check_against_oracle(oracle_mod, x, fmt, host)
+
+
+# N a multiple of 8 but not of 16: FP8 rows only 8-byte aligned, each row's last segment 8 columns
+NARROW = [(64, 8), (45, 24), (96, 40), (33, 8), (257, 1032), (130, 136), (1000, 2056)]
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+@pytest.mark.parametrize("shape", NARROW)
+def test_parity_n_multiple_of_8(oracle_mod, shape, fmt):
+    M, N = shape
+    x = mixed_input(M, N, seed=M * 17 + N + fmt)
+    host = run_quantize(x, fmt, with_dbias=True)
+    check_against_oracle(oracle_mod, x, fmt, host)
+    want = oracle_mod.quantize(x, fmt, False, False, with_dbias=True)[4]
+    assert np.all(np.abs(host["dbias"].astype(np.float64) - want) <= dbias_tolerance(x))
+
+
+@pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
+def test_parity_n_multiple_of_8_single_direction(oracle_mod, rowwise, colwise):
+    x = mixed_input(160, 40, seed=41)
+    host = run_quantize(x, E4M3, rowwise=rowwise, colwise=colwise)
+    check_against_oracle(oracle_mod, x, E4M3, host, rowwise, colwise)
+
+
+@pytest.mark.parametrize("N", [24, 40, 1032])
+def test_parity_grouped_n_multiple_of_8(oracle_mod, N):
+    sizes = np.array([64, 0, 32, 224, 96], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    x = wl.moe_bf16(sizes, N, seed=N + 5)
+    host, err = run_grouped(x, off, E5M2)
+    assert err == 0
+    o = oracle_mod.quantize_grouped(x, off, E5M2)
+    for name, w in zip(("out_row", "scale_row", "out_col", "scale_col"), o):
+        assert_bytes_equal(host[name], w, name)
 
 
 @pytest.mark.parametrize("shape", [(45, 80), (1000, 1040)])
