@@ -39,74 +39,44 @@ constexpr int kDOffCoord = kDOffBars + 8 * kStages;        // TileCoord [kStages
 constexpr int kSmemDact = kDOffCoord + 32 * kStages + 1024;
 
 // Beyond |x| = 200 every derivative here is at its fp32 limit (1 for x > 0, -0 for
-// x < 0), so x is clamped there first: without it x^2 or 1.702 x overflows for
-// huge |x| and meets a zero factor (inf * 0 = NaN).
+// x < 0).  The factors that overflow for huge |x| (x^2 in dGeLU's t', 1.702 x in
+// dQGeLU) take x clamped there, or they would meet a zero factor (inf * 0 = NaN);
+// dSiLU's x (1 - s) cannot overflow.
 constexpr float kDactClamp = 200.f;
 
-// act'(x) in fp32: 1 dReLU, 2 dSReLU, 3 dGeLU (tanh form), 4 dSiLU, 5 dQGeLU.
-// sigmoid(t) = s and 1 - sigmoid(t) both come from h = 2^(-|t| log2(e) / 2), e = h h.
-// The derivative is s (1 + q) with q = x (1 - s) t', rather than s + x s (1 - s) t'
-// (the sign of a tiny negative derivative survives), evaluated for t < 0 as
-// (((1 + q) h) h) / (1 + e): multiplying 1 + q in before the second h keeps results
-// that are fp32-subnormal where s alone would already have underflowed.
+// dReLU and dSReLU in fp32 (exact).
 template <int ACT>
 __device__ __forceinline__ float dactivation(float x)
 {
-    if constexpr (ACT == 1) {
+    static_assert(ACT == 1 || ACT == 2, "the transcendental derivatives are in dactivation2");
+    if constexpr (ACT == 1)
         return x > 0.f ? 1.f : 0.f;
-    } else if constexpr (ACT == 2) {
+    else
         return x > 0.f ? 2.f * x : 0.f;
-    } else {
-        x = fminf(fmaxf(x, -kDactClamp), kDactClamp);
-        const float t = sigmoid_arg<ACT>(x);
-        float h;
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(-kHalfLog2e * fabsf(t)));
-        const float e = h * h;
-        const float inv = rcp_1to2(1.f + e);
-        const float oms = t >= 0.f ? e * inv : inv;
-        float inner;
-        if constexpr (ACT == 3)
-            inner = 1.f + x * oms * (1.5957691216057308f * (1.f + 0.134145f * x * x));
-        else if constexpr (ACT == 4)
-            inner = 1.f + x * oms;
-        else
-            inner = 1.f + 1.702f * x * oms;
-        const float a = t >= 0.f ? 1.f : h;
-        return ((inner * a) * a) * inv;
-    }
 }
 
-// act'(x) for two values at once (lanes of a packed pair), each lane as
-// dactivation<ACT>.  For dGeLU the multiplies and adds run as f32x2 operations
-// (ex2 and rcp per lane); the others are cheaper per lane (measured).
+// act'(x) in fp32 for two values at once (lanes of a packed pair): 1 dReLU, 2 dSReLU
+// (per lane, exact), 3 dGeLU (tanh form), 4 dSiLU, 5 dQGeLU (multiplies and adds as
+// f32x2 operations, ex2 and rcp per lane).  sigmoid(t) = s and 1 - sigmoid(t) both come
+// from h = 2^(-|t| log2(e) / 2), e = h h.  The derivative is s (1 + q) with
+// q = x (1 - s) t', rather than s + x s (1 - s) t' (the sign of a tiny negative
+// derivative survives), evaluated for t < 0 as (((1 + q) h) h) / (1 + e): multiplying
+// 1 + q in before the second h keeps results that are fp32-subnormal where s alone would
+// already have underflowed.
 template <int ACT>
 __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
 {
     float x0, x1;
     f2_unpack(x, x0, x1);
-    if constexpr (ACT != 3) {
+    if constexpr (ACT < 3) {
         return f2_pack(dactivation<ACT>(x0), dactivation<ACT>(x1));
     } else {
-        x0 = fminf(fmaxf(x0, -kDactClamp), kDactClamp);
-        x1 = fminf(fmaxf(x1, -kDactClamp), kDactClamp);
-        x = f2_pack(x0, x1);
         const uint64_t one = f2_splat(1.f);
-        uint64_t t;
-        if constexpr (ACT == 3) {
-            uint64_t q = f2_mul(f2_splat(0.044715f), x);
-            q = f2_mul(q, x);
-            t = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, x));
-        } else if constexpr (ACT == 4) {
-            t = x;
-        } else {
-            t = f2_mul(f2_splat(1.702f), x);
-        }
-        float z0, z1, t0, t1;
-        f2_unpack(f2_mul(f2_splat(-kHalfLog2e), f2_abs(t)), z0, z1);
-        f2_unpack(t, t0, t1);
-        float h0, h1;
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(z0));
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(z1));
+        float u0, u1, h0, h1;
+        f2_unpack(half_log2e_arg2<ACT>(x), u0, u1);
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(-fabsf(u0)));
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(-fabsf(u1)));
+        const float t0 = x0, t1 = x1;  // the sign tests only need sign(t) = sign(x)
         const uint64_t h = f2_pack(h0, h1);
         const uint64_t e = f2_mul(h, h);
         float o0, o1;
@@ -117,13 +87,17 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
         const uint64_t oms = f2_pack(t0 >= 0.f ? ei0 : i0, t1 >= 0.f ? ei1 : i1);
         uint64_t inner;
         if constexpr (ACT == 3) {
-            const uint64_t q = f2_mul(f2_splat(0.134145f), x);
-            const uint64_t tp = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, one));
-            inner = f2_fma(f2_mul(x, oms), tp, one);
+            const uint64_t xc = f2_pack(fminf(fmaxf(x0, -kDactClamp), kDactClamp),
+                                        fminf(fmaxf(x1, -kDactClamp), kDactClamp));
+            const uint64_t q = f2_mul(f2_splat(0.134145f), xc);
+            const uint64_t tp = f2_mul(f2_splat(kGeluC0), f2_fma(q, xc, one));
+            inner = f2_fma(f2_mul(xc, oms), tp, one);
         } else if constexpr (ACT == 4) {
             inner = f2_fma(x, oms, one);
         } else {
-            inner = f2_fma(f2_mul(f2_splat(1.702f), x), oms, one);
+            const uint64_t xc = f2_pack(fminf(fmaxf(x0, -kDactClamp), kDactClamp),
+                                        fminf(fmaxf(x1, -kDactClamp), kDactClamp));
+            inner = f2_fma(f2_mul(f2_splat(1.702f), xc), oms, one);
         }
         const uint64_t a = f2_pack(t0 >= 0.f ? 1.f : h0, t1 >= 0.f ? 1.f : h1);
         return f2_mul(f2_mul(f2_mul(inner, a), a), f2_pack(i0, i1));

@@ -191,7 +191,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
-__device__ __forceinline__ uint64_t f2_abs(uint64_t v) { return v & 0x7FFFFFFF7FFFFFFFull; }
 
 // cvt_fp8x2 of (v0 * m.lo, v1 * m.hi), the two products as one f32x2 multiply.
 template <int FMT>

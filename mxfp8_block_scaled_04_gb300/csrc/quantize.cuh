@@ -140,16 +140,20 @@ __device__ __forceinline__ float rcp_1to2(float x)
     return y;
 }
 
-// The argument t of the sigmoid for GeLU, SiLU and QGeLU.
+// The sigmoid's argument t for GeLU (2 sqrt(2/pi) (x + 0.044715 x^3)), SiLU (x) and
+// QGeLU (1.702 x), formed directly as u = t log2(e) / 2 with the constants folded in
+// (GeLU: x (k c0 + k c1 x^2)).  t, and so u, has the sign of x for all three.
+constexpr float kGeluC0 = 1.5957691216057308f;           // 2 sqrt(2/pi)
+constexpr float kGeluC1 = 1.5957691216057308f * 0.044715f;
 template <int ACT>
-__device__ __forceinline__ float sigmoid_arg(float x)
+__device__ __forceinline__ uint64_t half_log2e_arg2(uint64_t x)
 {
     if constexpr (ACT == 3)
-        return 1.5957691216057308f * (x + 0.044715f * x * x * x);
+        return f2_mul(x, f2_fma(f2_mul(x, x), f2_splat(kHalfLog2e * kGeluC1), f2_splat(kHalfLog2e * kGeluC0)));
     else if constexpr (ACT == 4)
-        return x;
+        return f2_mul(f2_splat(kHalfLog2e), x);
     else
-        return 1.702f * x;
+        return f2_mul(f2_splat(kHalfLog2e * 1.702f), x);
 }
 
 // ReLU and squared ReLU (exact in fp32).
@@ -175,22 +179,10 @@ __device__ __forceinline__ uint64_t activation2(uint64_t x)
     if constexpr (ACT <= 2) {
         return f2_pack(relu_family<ACT>(x0), relu_family<ACT>(x1));
     } else {
-        uint64_t t;
-        if constexpr (ACT == 3) {  // 1.5957691216057308 * fma((0.044715 x) x, x, x)
-            uint64_t q = f2_mul(f2_splat(0.044715f), x);
-            q = f2_mul(q, x);
-            t = f2_mul(f2_splat(1.5957691216057308f), f2_fma(q, x, x));
-        } else if constexpr (ACT == 4) {
-            t = x;
-        } else {
-            t = f2_mul(f2_splat(1.702f), x);
-        }
-        const uint64_t zh = f2_mul(f2_splat(-kHalfLog2e), f2_abs(t));
-        float z0, z1, t0, t1, h0, h1;
-        f2_unpack(zh, z0, z1);
-        f2_unpack(t, t0, t1);
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(z0));
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(z1));
+        float u0, u1, h0, h1;
+        f2_unpack(half_log2e_arg2<ACT>(x), u0, u1);
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h0) : "f"(-fabsf(u0)));  // h = 2^(-|t| log2(e) / 2)
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h1) : "f"(-fabsf(u1)));
         const uint64_t h = f2_pack(h0, h1);
         const uint64_t e = f2_mul(h, h);
         float o0, o1;
@@ -199,7 +191,7 @@ __device__ __forceinline__ uint64_t activation2(uint64_t x)
         // x sigmoid(t) = x r for t >= 0 and ((x h) h) r for t < 0: multiplying x in
         // before the second h keeps results that are fp32-subnormal where e = h h
         // alone would already have underflowed (SiLU(-104) = -7e-44, for one)
-        const uint64_t a = f2_pack(t0 >= 0.f ? 1.f : h0, t1 >= 0.f ? 1.f : h1);
+        const uint64_t a = f2_pack(x0 >= 0.f ? 1.f : h0, x1 >= 0.f ? 1.f : h1);  // t >= 0 iff x >= 0
         return f2_mul(f2_mul(f2_mul(x, a), a), f2_pack(r0, r1));
     }
 }
