@@ -348,6 +348,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
 
     constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
+    // With a transcendental activation (bound on the SM side) a warp's phase-2 tasks are the
+    // 8-row groups of the (32-row block, box) it handles in phase 1, so phase 2 reads only
+    // shared data its own warp wrote: a warp barrier replaces the CTA barrier between the
+    // phases, and the lane's 16 column multipliers are loaded once per tile (both measured
+    // faster there).  Without one (bound by memory) the tasks step through the row blocks:
+    // the order of the stores that measured fastest.
+    constexpr bool kWarpLocal = ACT > 2;
     pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
@@ -416,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
         const unsigned char *stage = smem + slot * kStageBytes;
 
-        const bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
+        bool ok = mbar_wait_bounded(smem_u32(&bars[slot]), parity, kWaitLimitNs);
+        if constexpr (kWarpLocal)
+            ok = __all_sync(0xffffffffu, ok);  // warp-uniform: phase 2 may skip on it, with shuffles inside
         const TileCoord tc = coords[slot];
 
         // ---- phase 1: column blocks (rb = 32-row block, box = 64-column half) ----
@@ -547,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 scale_multiplier(e3));
             }
         }
-        if (__syncthreads_or(!ok)) {
+        // a bounded wait that expired: record it, drain this CTA's own copies, return
+        auto give_up = [&]() {
             if (tid == 0) {
                 atomicOr(&g_fault_word, 1u);
                 if (GROUPED && p.err_flag != nullptr)
@@ -556,6 +566,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
                                       kDrainLimitNs);
             }
+        };
+        if constexpr (kWarpLocal) {
+            __syncwarp();  // phase 2 reads what this warp wrote in phase 1; the fault test is at the tile's end
+        } else if (__syncthreads_or(!ok)) {
+            give_up();
             return;
         }
 
@@ -572,11 +587,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- phase 2: row segments of 16 columns ----
         {
             const int rr = lane >> 2, sp = lane & 3;
+            constexpr bool kReuse = kWarpLocal;
+            float4 cmv[4];
+            if (kReuse && do_col) {
+                const float *cm0 = colmul + (warp >> 1) * kBN + (warp & 1) * kBoxCols + sp * 16;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    cmv[j] = lds128f(cm0 + 4 * ((j + (sp >> 1)) & 3));
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int task = warp + 8 * k;
-                const int box = task & 1, rg = task >> 1;
-                if (tc.row0 + rg * 8 >= tc.row_end)
+                const int box = kReuse ? (warp & 1) : (task & 1);
+                const int rg = kReuse ? (warp >> 1) * 4 + k : (task >> 1);
+                if (tc.row0 + rg * 8 >= tc.row_end || (kWarpLocal && !ok))
                     continue;               // warp-uniform: the whole 8-row group is past the tile end
                 const int r = rg * 8 + rr;  // (r & 7) == rr
                 const unsigned char *rowp = stage + box * kBoxBytes + r * 128;
@@ -652,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t o[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
+                        const float4 c = kReuse ? cmv[j] : lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
                         const uint32_t lo = cvt_pair(val(4 * j), val(4 * j + 1), c.x, c.y);
                         const uint32_t hi = cvt_pair(val(4 * j + 2), val(4 * j + 3), c.z, c.w);
                         o[j] = lo | (hi << 16);
@@ -662,7 +686,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-        __syncthreads();  // stage `slot` and colmul are free again
+        if constexpr (kWarpLocal) {
+            if (__syncthreads_or(!ok)) {  // stage `slot` is free again, or a wait expired
+                give_up();
+                return;
+            }
+        } else {
+            __syncthreads();  // stage `slot` and colmul are free again
+        }
 
         if (tid == 0 && it + kStages < my_count) {
             fence_proxy_async_smem();

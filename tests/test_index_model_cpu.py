@@ -89,7 +89,7 @@ def tile_list(M, N, offsets):
     return tiles
 
 
-def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True):
+def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True, reuse=False):
     rows16 = N % 16 == 0
     Cr = -(-N // 32)
     out_row = Plane("out_row", M * N)
@@ -112,7 +112,11 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
     k2 = np.tile(np.repeat(np.arange(4), 32), 8)
     l2 = np.tile(LANES, 32)
     task = w2 + 8 * k2
-    rg2, box2, rr2, sp2 = task >> 1, task & 1, l2 >> 2, l2 & 3
+    if reuse:   # transcendental activations: warp = (32-row block, box), tasks = its 8-row groups
+        rg2, box2 = (w2 >> 1) * 4 + k2, w2 & 1
+    else:
+        rg2, box2 = task >> 1, task & 1
+    rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
             row0, row_end, col0, rt = tiles[t]
@@ -162,8 +166,8 @@ def model_swizzle_pad(R, C, plane):
                 plane.write(((rt * col_tiles + ct) << 9) + w)
 
 
-def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True):
-    m = model_quantize(M, N, grid, offsets, dbias, swz, do_row, do_col)
+def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True, reuse=False):
+    m = model_quantize(M, N, grid, offsets, dbias, swz, do_row, do_col, reuse)
     for name, on in (("out_row", do_row), ("out_col", do_col)):
         if on:
             m[name].once()
@@ -197,6 +201,13 @@ FLAT = [(1, 8), (33, 8), (45, 80), (96, 40), (128, 256), (257, 1032), (130, 144)
 def test_flat_cast_writes_every_byte_once(shape, grid):
     M, N = shape
     check_quantize(M, N, grid, dbias=True)
+
+
+@pytest.mark.parametrize("shape", FLAT)
+def test_activated_cast_task_map_writes_every_byte_once(shape):
+    """The transcendental activations' phase-2 task map (a warp's tasks in one 32-row block)."""
+    check_quantize(*shape, grid=7, reuse=True)
+    check_quantize(*shape, grid=7, swz=True, reuse=True)
 
 
 @pytest.mark.parametrize("shape", [(45, 80), (96, 40), (257, 1032), (130, 144)])
