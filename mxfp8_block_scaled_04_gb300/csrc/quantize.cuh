@@ -346,15 +346,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     int *scan = reinterpret_cast<int *>(smem + kOffScan);
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
+    unsigned *stage_done = reinterpret_cast<unsigned *>(smem + kOffScan);  // warp-local: [kStages] warps done
 
     constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
     // With a transcendental activation (bound on the SM side) a warp's phase-2 tasks are the
     // 8-row groups of the (32-row block, box) it handles in phase 1, so phase 2 reads only
     // shared data its own warp wrote: a warp barrier replaces the CTA barrier between the
-    // phases, and the lane's 16 column multipliers are loaded once per tile (both measured
-    // faster there).  Without one (bound by memory) the tasks step through the row blocks:
-    // the order of the stores that measured fastest.
+    // phases, the lane's 16 column multipliers are loaded once per tile, and no CTA barrier
+    // closes the tile either (the last warp done with a stage refills it): all measured
+    // faster there.  Without one (bound by memory) the tasks step through the row blocks and
+    // CTA barriers pace the tile: the order of the stores that measured fastest.
     constexpr bool kWarpLocal = ACT > 2;
+    static_assert(!(kWarpLocal && (GROUPED || DBIAS)), "warp-local phases: flat casts without dbias");
     pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
@@ -397,6 +400,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int s = 0; s < kStages; ++s)
             mbar_init(smem_u32(&bars[s]), 1);
         fence_mbar_init();
+        if constexpr (kWarpLocal)
+            for (int s = 0; s < kStages; ++s)
+                stage_done[s] = 0;
     }
     __syncthreads();
 
@@ -687,10 +693,36 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         if constexpr (kWarpLocal) {
-            if (__syncthreads_or(!ok)) {  // stage `slot` is free again, or a wait expired
-                give_up();
+            // No CTA barrier: each warp counts itself done with the stage, and the eighth to
+            // finish refills it.  A warp whose wait expired records the fault, drains the copies
+            // that can still be in flight (tiles it .. it + kStages - 1: no later tile is issued
+            // while this one is unfinished) and leaves; the stage it abandons is never refilled,
+            // so the other warps' bounded waits expire in turn and they leave the same way.
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(&g_fault_word, 1u);
+                    for (int j = it; j < my_count && j < it + kStages; ++j)
+                        mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
+                                          kDrainLimitNs);
+                }
                 return;
             }
+            __syncwarp();
+            if (lane == 0) {
+                unsigned before;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                             : "=r"(before)
+                             : "r"(smem_u32(&stage_done[slot]))
+                             : "memory");
+                if (before == kThreads / 32 - 1) {
+                    stage_done[slot] = 0;  // no warp touches it again before the refill completes
+                    if (it + kStages < my_count) {
+                        fence_proxy_async_smem();
+                        issue(slot, first + (it + kStages) * stride);
+                    }
+                }
+            }
+            continue;
         } else {
             __syncthreads();  // stage `slot` and colmul are free again
         }
