@@ -13,10 +13,11 @@
 //     dQGeLU each fp32 product is written back over its own two inputs (low
 //     half in the dY slot, high half in the X slot: the same 4 bytes per
 //     element);
-//   - phase 2: warp w takes the 8-row groups w and w + 8; a lane takes 16
-//     columns of one row, as in the main kernel, reading those products back
-//     (one byte permute per element instead of a second evaluation; dReLU
-//     and dSReLU are cheaper to evaluate again).
+//   - phase 2: warp w takes the 8-row groups 2w and 2w + 1 (one 32-row block,
+//     whose column multipliers it loads once per tile; dReLU: w and w + 8); a
+//     lane takes 16 columns of one row, as in the main kernel, reading those
+//     products back (one byte permute per element instead of a second
+//     evaluation; dReLU and dSReLU are cheaper to evaluate again).
 // The derivative is evaluated in fp32 with the same ex2 / rcp approximations
 // as the forward activations; dReLU and dSReLU are exact.
 #pragma once
@@ -257,9 +258,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- phase 2: 16-column row segments ----
         {
             const int rr = lane >> 2, sp = lane & 3;
+            // Except for dReLU (bound by memory: measured slower so), a warp's two tasks are
+            // adjacent 8-row groups of one 32-row block, whose 16 column multipliers the lane
+            // loads once per tile; dReLU's tasks step through the row blocks.
+            constexpr bool kReuse = ACT >= 2;
+            float4 cmv[4];
+            if (kReuse && do_col) {
+                const float *cm0 = colmul + (warp >> 1) * kDBN + sp * 16;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    cmv[j] = lds128f(cm0 + 4 * ((j + (sp >> 1)) & 3));
+            }
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const int rg = warp + 8 * k;
+                const int rg = kReuse ? 2 * warp + k : warp + 8 * k;
                 if (tc.row0 + rg * 8 >= tc.row_end)
                     continue;
                 const int r = rg * 8 + rr;
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t o[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float4 c = lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
+                        const float4 c = kReuse ? cmv[j] : lds128f(cm + 4 * ((j + (sp >> 1)) & 3));
                         o[j] = cvt_pair(y[4 * j], y[4 * j + 1], c.x, c.y) |
                                (cvt_pair(y[4 * j + 2], y[4 * j + 3], c.z, c.w) << 16);
                     }

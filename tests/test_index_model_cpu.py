@@ -236,7 +236,7 @@ def test_grouped_many_groups_and_empty_ones():
     check_quantize(off[-1], 48, 304, offsets=off, dbias=True)
 
 
-def model_dact(M, N, grid, dbias=True):
+def model_dact(M, N, grid, dbias=True, reuse=False):
     rows16 = N % 16 == 0
     out_row, out_col = Plane("out_row", M * N), Plane("out_col", M * N)
     scale_row, scale_col = Plane("scale_row", M * -(-N // 32)), Plane("scale_col", -(-M // 32) * N)
@@ -248,7 +248,8 @@ def model_dact(M, N, grid, dbias=True):
     w2 = np.repeat(np.arange(8), 2 * 32)
     k2 = np.tile(np.repeat(np.arange(2), 32), 8)
     l2 = np.tile(LANES, 16)
-    rg2, rr2, sp2 = w2 + 8 * k2, l2 >> 2, l2 & 3
+    rg2 = 2 * w2 + k2 if reuse else w2 + 8 * k2   # dSReLU .. dQGeLU: one 32-row block per warp
+    rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
             row0, row_end, col0, rt = tiles[t]
@@ -274,8 +275,9 @@ def model_dact(M, N, grid, dbias=True):
 
 @pytest.mark.parametrize("shape", [(45, 80), (70, 24), (257, 1032), (130, 144), (256, 64)])
 def test_backward_fusion_writes_every_byte_once(shape):
-    model_dact(*shape, grid=5)
-    model_dact(*shape, grid=304)
+    for reuse in (False, True):
+        model_dact(*shape, grid=5, reuse=reuse)
+        model_dact(*shape, grid=304, reuse=reuse)
 
 
 def grouped_reduce_reads(hdr, N):
