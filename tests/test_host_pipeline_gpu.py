@@ -1,15 +1,18 @@
 """mxfp8_quantize_host: host buffers in and out, pipelined over row chunks.
 
 Its results must be byte-identical to mxfp8_quantize on the same data (dbias
-too: the chunks fill one workspace and the same reduce runs once).  Shapes
-are chosen so the call cuts the rows into several chunks with a ragged last
-one; pageable host memory must give the same bytes as pinned memory.
+too: the chunks fill one workspace and the same reduce runs once), and every
+FP8 and scale byte must equal the CPU oracle's, dbias within 1e-5 * sum|x| of
+the oracle's fp64 column sum.  Shapes are chosen so the call cuts the rows
+into several chunks with a ragged last one; pageable host memory must give
+the same bytes as pinned memory.
 """
 import numpy as np
 import pytest
 import torch
 
 import mxfp8_block_scaled_04_gb300 as mx
+import oracle_slices
 from mxfp8_block_scaled_04_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -46,6 +49,25 @@ def test_host_pipeline_matches_device_path(shape, fmt, with_dbias, pinned):
             assert g is None
             continue
         assert torch.equal(g, w), name
+
+
+@pytest.mark.parametrize("shape,fmt", [
+    ((4195, 4096), mx.E5M2),      # five chunks, the last one 99 rows
+    ((1033, 1032), mx.E4M3),      # N = 8 mod 16, ragged row and column blocks
+])
+def test_host_pipeline_matches_oracle(oracle_mod, shape, fmt):
+    M, N = shape
+    x_bits = wl.grad_bf16(M, N, seed=7 * M + N)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    got = mx.quantize_host(x_host, fmt, with_dbias=True)
+    torch.cuda.synchronize()
+    o_row, s_row, o_col, s_col, dbias = oracle_slices.quantize(oracle_mod, x_bits, fmt, with_dbias=True)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"),
+                          (got.out_row, got.scale_row, got.out_col, got.scale_col),
+                          (o_row, s_row, o_col, s_col)):
+        assert np.array_equal(g.numpy(), w), name
+    tol = 1e-5 * np.abs(torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().numpy()).sum(0)
+    assert bool((np.abs(got.dbias.double().numpy() - dbias) <= tol).all())
 
 
 def test_host_pipeline_single_direction_and_staging_reuse():

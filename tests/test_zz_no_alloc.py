@@ -7,13 +7,15 @@ point keeps that workspace in a static 8 MiB device array inside the library.
 The test calls it through the C ABI twice in a row, on different inputs and
 shapes, and checks that every output matches the regular entry point given an
 explicit workspace: FP8 and scale bytes identical, dbias within
-1e-5 * sum|x| per column (the same tolerance as the other dbias tests).
+1e-5 * sum|x| per column (the same tolerance as the other dbias tests).  Two
+calls in a row are also held to the CPU oracle directly.
 """
 import numpy as np
 import pytest
 import torch
 
 import mxfp8_block_scaled_04_gb300 as mx
+import oracle_slices
 from mxfp8_block_scaled_04_gb300 import binding
 from mxfp8_block_scaled_04_gb300 import workloads as wl
 
@@ -75,6 +77,23 @@ def test_noalloc_matches_workspace_entry_point_two_calls(fmt):
         tol = 1e-5 * torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().abs().sum(0)
         diff = (ref[4].double().cpu() - got[4].double().cpu()).abs()
         assert bool((diff <= tol).all()), f"call {call}: dbias differs"
+
+
+def test_noalloc_matches_oracle_two_calls(oracle_mod):
+    for call, (M, N, fmt) in enumerate([(2080, 4096, mx.E5M2), (1000, 1032, mx.E4M3)]):
+        x_bits = wl.grad_bf16(M, N, seed=400 + call)
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        u8 = dict(dtype=torch.uint8, device="cuda")
+        got = [torch.full((M, N), 0x11, **u8), torch.full((M, -(-N // 32)), 0x11, **u8),
+               torch.full((M, N), 0x11, **u8), torch.full((-(-M // 32), N), 0x11, **u8),
+               torch.full((N,), 7.0, dtype=torch.float32, device="cuda")]
+        assert binding.mxfp8_quantize_dbias_noalloc(x, M, N, fmt, *got[:4], got[4], None, None) == 0
+        torch.cuda.synchronize()
+        want = oracle_slices.quantize(oracle_mod, x_bits, fmt, with_dbias=True)
+        for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got[:4], want[:4]):
+            assert np.array_equal(g.cpu().numpy(), w), f"call {call}: {name} differs from the oracle"
+        tol = 1e-5 * np.abs(torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).double().numpy()).sum(0)
+        assert bool((np.abs(got[4].double().cpu().numpy() - want[4]) <= tol).all()), f"call {call}: dbias"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
