@@ -152,10 +152,13 @@ def quantize(x_bits: np.ndarray, fmt: int, rowwise: bool = True, colwise: bool =
 
 
 def quantize_grouped(x_bits: np.ndarray, offsets: np.ndarray, fmt: int):
-    """Grouped quantize: rows [offsets[g], offsets[g+1]) are group g.
+    """Grouped quantize: rows [offsets[g], offsets[g+1]) are group g, each its own flat problem.
 
-    Returns ``(out_row, scale_row, out_col, scale_col)`` laid out as for the flat
-    call on the concatenated rows.  Raises ValueError on invalid offsets.
+    Returns ``(out_row, scale_row, out_col, scale_col)``: the row-indexed outputs at
+    each group's rows; ``scale_col`` has ``grouped_scale_col_rows(offsets)`` rows, group
+    g's ``ceil(rows_g/32)`` after those of the groups before it (with every offset a
+    multiple of 32 this is the flat call's layout on the concatenated rows).  Raises
+    ValueError on invalid offsets.
     """
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     total, N = x.shape
@@ -164,13 +167,19 @@ def quantize_grouped(x_bits: np.ndarray, offsets: np.ndarray, fmt: int):
     out_row = np.zeros((total, N), np.uint8)
     scale_row = np.zeros((total, -(-N // BLOCK)), np.uint8)
     out_col = np.zeros((total, N), np.uint8)
-    scale_col = np.zeros((total // BLOCK, N), np.uint8)
+    scale_col = np.zeros((max(grouped_scale_col_rows(off), 0), N), np.uint8)
     rc = _load().mxo_quantize_grouped(_ptr(x, ctypes.c_uint16), total, N, G, _ptr(off, ctypes.c_int64), fmt,
                                       _ptr(out_row, ctypes.c_uint8), _ptr(scale_row, ctypes.c_uint8),
                                       _ptr(out_col, ctypes.c_uint8), _ptr(scale_col, ctypes.c_uint8))
     if rc != 0:
         raise ValueError("oracle: invalid group offsets")
     return out_row, scale_row, out_col, scale_col
+
+
+def grouped_scale_col_rows(offsets) -> int:
+    """Rows of a grouped call's columnwise scale plane: sum over groups of ceil(rows_g / 32)."""
+    off = np.asarray(offsets, dtype=np.int64)
+    return int(np.sum(-(-np.diff(off) // BLOCK))) if off.size > 1 else 0
 
 
 def swizzle_offset(r: int, c: int, C: int) -> int:

@@ -235,10 +235,15 @@ int mxo_quantize(const uint16_t *x, int64_t M, int64_t N, int fmt,
 
 /*
  * Grouped quantize: rows [offsets[g], offsets[g+1]) form group g; each
- * group is quantized as its own flat problem and written at its own row
- * offset in the same output buffers.  offsets has num_groups+1 entries.
- * Returns 0, or -1 when the offsets are not a prefix-sum vector starting at
- * 0, ending at total_rows, non-decreasing, with every entry a multiple of 32.
+ * group is quantized as its own flat problem (its columnwise blocks start at
+ * the group's first row, and its last block holds the rows the group has
+ * left).  Row-indexed outputs (out_row, scale_row, out_col) sit at the
+ * group's row offset; the group's ceil(rows_g/32) columnwise scale rows
+ * follow those of the groups before it, i.e. start at scale row
+ * sum_{h<g} ceil(rows_h/32) (= offsets[g]/32 when every offset is a
+ * multiple of 32, the flat call's layout).  offsets has num_groups+1
+ * entries.  Returns 0, or -1 when the offsets are not a prefix-sum vector
+ * starting at 0, ending at total_rows and non-decreasing.
  */
 int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int num_groups,
                          const int64_t *offsets, int fmt,
@@ -250,8 +255,9 @@ int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int n
         return -1;
     if (offsets[0] != 0 || offsets[num_groups] != total_rows)
         return -1;
+    int64_t s0 = 0; /* first columnwise scale row of group g */
     for (g = 0; g < num_groups; g++)
-        if (offsets[g + 1] < offsets[g] || offsets[g + 1] % MXO_BLOCK)
+        if (offsets[g + 1] < offsets[g])
             return -1;
     for (g = 0; g < num_groups; g++) {
         const int64_t r0 = offsets[g], rows = offsets[g + 1] - offsets[g];
@@ -260,8 +266,9 @@ int mxo_quantize_grouped(const uint16_t *x, int64_t total_rows, int64_t N, int n
         mxo_quantize(x + r0 * N, rows, N, fmt,
                      out_row ? out_row + r0 * N : 0,
                      scale_row ? scale_row + r0 * ((N + MXO_BLOCK - 1) / MXO_BLOCK) : 0,
-                     out_col ? out_col + r0 * N : 0, scale_col ? scale_col + (r0 / MXO_BLOCK) * N : 0,
+                     out_col ? out_col + r0 * N : 0, scale_col ? scale_col + s0 * N : 0,
                      0);
+        s0 += (rows + MXO_BLOCK - 1) / MXO_BLOCK;
     }
     return 0;
 }
@@ -441,7 +448,7 @@ int mxo_grouped_dbias(const uint16_t *x, int64_t total_rows, int64_t N, int num_
     if (num_groups < 0 || total_rows < 0 || N < 0 || offsets[0] != 0 || offsets[num_groups] != total_rows)
         return -1;
     for (g = 0; g < num_groups; g++)
-        if (offsets[g + 1] < offsets[g] || offsets[g + 1] % MXO_BLOCK)
+        if (offsets[g + 1] < offsets[g])
             return -1;
     for (g = 0; g < num_groups; g++)
         for (j = 0; j < N; j++) {

@@ -71,7 +71,7 @@ def quantize_grouped(oracle, x_bits, offsets, fmt, threads=None):
     out_row = np.empty((M, N), np.uint8)
     scale_row = np.empty((M, -(-N // 32)), np.uint8)
     out_col = np.empty((M, N), np.uint8)
-    scale_col = np.empty((M // 32, N), np.uint8)
+    scale_col = np.empty((oracle.grouped_scale_col_rows(offsets), N), np.uint8)
     for (j0, j1), (o_r, s_r, o_c, s_c) in zip(slices, parts):
         out_row[:, j0:j1] = o_r
         scale_row[:, j0 // 32:j0 // 32 + s_r.shape[1]] = s_r

@@ -38,6 +38,10 @@ MUTATIONS = [
     ("GeLU cubic coefficient wrong", "(x + 0.044715 * x * x * x));", "(x + 0.04715 * x * x * x));"),
     ("dGeLU derivative of the cubic wrong", "dt = c * (1.0 + 3.0 * 0.044715 * x * x)", "dt = c * (1.0 + 0.044715 * x * x)"),
     ("dSiLU factor sign", "return s * (1.0 + x * oms);", "return s * (1.0 - x * oms);"),
+    ("grouped columnwise scales at the flat call's row", "scale_col ? scale_col + s0 * N : 0",
+     "scale_col ? scale_col + (r0 / MXO_BLOCK) * N : 0"),
+    ("grouped scale rows counted with floor", "s0 += (rows + MXO_BLOCK - 1) / MXO_BLOCK;",
+     "s0 += rows / MXO_BLOCK;"),
 ]
 
 

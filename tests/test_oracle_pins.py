@@ -310,9 +310,52 @@ def test_grouped_equals_flat_and_rejects_bad_offsets(oracle_mod):
     grouped = oracle_mod.quantize_grouped(x, off, E4M3)
     for f, g in zip(flat, grouped):
         assert np.array_equal(f, g)
-    for bad in ([0, 16, 512], [0, 256, 128, 512], [0, 256, 480], [32, 512]):
+    for bad in ([0, 256, 128, 512], [0, 256, 480], [32, 512], [0, 16, 8, 512]):
         with pytest.raises(ValueError):
             oracle_mod.quantize_grouped(x, np.array(bad), E4M3)
+
+
+def test_grouped_unaligned_groups_are_separate_flat_problems(oracle_mod):
+    """Offsets that are not multiples of 32: every group is quantized on its own (its columnwise
+    blocks start at its first row and its last block is partial), and its ceil(rows/32) columnwise
+    scale rows follow those of the groups before it.  The flat oracle is pinned on its own above."""
+    sizes = np.array([45, 0, 1, 31, 33, 96, 70], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    N = 72
+    x = wl.moe_bf16(sizes, N, seed=11)
+    for fmt in (E4M3, E5M2):
+        o_row, s_row, o_col, s_col = oracle_mod.quantize_grouped(x, off, fmt)
+        assert s_col.shape == (2 + 0 + 1 + 1 + 2 + 3 + 3, N) == (oracle_mod.grouped_scale_col_rows(off), N)
+        s0 = 0
+        for g in range(len(sizes)):
+            a, b = off[g], off[g + 1]
+            if a == b:
+                continue
+            f_row, f_srow, f_col, f_scol, _ = oracle_mod.quantize(x[a:b], fmt)
+            assert np.array_equal(o_row[a:b], f_row) and np.array_equal(s_row[a:b], f_srow)
+            assert np.array_equal(o_col[a:b], f_col)
+            assert np.array_equal(s_col[s0:s0 + f_scol.shape[0]], f_scol)
+            s0 += f_scol.shape[0]
+        assert s0 == s_col.shape[0]
+
+
+def test_grouped_partial_block_takes_its_own_rows_only(oracle_mod):
+    """Hand-worked: group 0 has 45 rows, so its second columnwise block is rows 32..44 only.  Those
+    rows hold 1.0 and the next group's rows hold 1000, which must not reach that block's scale:
+    e = ceil(log2(1/448)) + 127 = 119 and 1.0 * 2^(127-119) = 256 -> E4M3 0x78; group 1's first
+    block (1000) gets ceil(log2(1000/448)) + 127 = 129 at scale row ceil(45/32) = 2, and
+    1000 * 2^-2 = 250 rounds to 256 in E4M3 (neighbours 240 and 256, tie-free) -> 0x78."""
+    N = 32
+    a = np.zeros((45 + 40, N))
+    a[:32] = 0.5
+    a[32:45] = 1.0
+    a[45:] = 1000.0
+    off = np.array([0, 45, 85], np.int64)
+    _, _, o_col, s_col = oracle_mod.quantize_grouped(wl.to_bf16_bits(a), off, E4M3)
+    assert s_col.shape == (2 + 2, N)
+    assert np.all(s_col[0] == 118) and np.all(s_col[1] == 119) and np.all(s_col[2] == 129)
+    assert np.all(o_col[32:45] == 0x78) and np.all(o_col[45:77] == 0x78)
+    assert np.all(s_col[3] == 129)                     # rows 77..84: a block of 8 rows of 1000
 
 
 def test_moe_sizes_recipe():
@@ -424,7 +467,13 @@ def test_grouped_dbias_is_per_group_fsum(oracle_mod):
     flat = oracle_mod.quantize(x, 0, False, False, with_dbias=True)[4]
     assert np.allclose(got.astype(np.float64).sum(0), flat, rtol=1e-6, atol=1e-30)
     with pytest.raises(ValueError):
-        oracle_mod.grouped_dbias(x, np.array([0, 64, 100, 192]))
+        oracle_mod.grouped_dbias(x, np.array([0, 100, 64, 192]))
+    # unaligned groups: each group's exact column sums as well
+    off2 = np.array([0, 45, 45, 46, 192], np.int64)
+    got2 = oracle_mod.grouped_dbias(x, off2)
+    for g in range(4):
+        rows = xv[off2[g]:off2[g + 1]]
+        assert np.array_equal(got2[g], np.array([math.fsum(rows[:, j]) for j in range(48)], np.float32))
 
 
 
