@@ -134,17 +134,27 @@ size_t mxfp8_quantize_grouped_workspace_bytes(int64_t total_rows, int64_t N, int
  *   x            device bf16 [total_rows, N], 16-byte aligned.
  *   num_groups   1 .. MXFP8_MAX_GROUPS.
  *   offsets      device int64 [num_groups + 1]: offsets[0] == 0,
- *                offsets[num_groups] == total_rows, non-decreasing, every
- *                entry a multiple of 32.  Read only on the device.  Empty
- *                groups produce no work.  No tile straddles two groups.
- *   outputs      as for mxfp8_quantize on the concatenated rows (so the
- *                result equals the flat call on x); no dbias.
+ *                offsets[num_groups] == total_rows, non-decreasing.  Read
+ *                only on the device.  Empty groups produce no work.  No tile
+ *                straddles two groups.
+ *   outputs      every group is quantized as its own flat problem (the
+ *                "non-32-divisible shapes" review: its columnwise blocks
+ *                start at its first row and its last block holds the rows it
+ *                has left, so no block mixes two groups).  out_row,
+ *                scale_row and out_col are indexed by row as for
+ *                mxfp8_quantize on the concatenated rows.  scale_col holds
+ *                S = sum_g ceil(rows_g / 32) rows: group g's ceil(rows_g / 32)
+ *                scale rows start at row sum_{h<g} ceil(rows_h / 32).  With
+ *                every offset a multiple of 32, S = total_rows / 32 and the
+ *                result equals the flat call on x; in general
+ *                ceil(total_rows / 32) <= S <= total_rows / 32 + num_groups,
+ *                and the caller allocates at least S rows.  No dbias.
  *   workspace    may be NULL (see mxfp8_quantize_grouped_workspace_bytes).
  *   err_flag     device int or NULL.  If the offsets break a rule above, the
  *                kernel writes nothing and sets *err_flag = 1.  It is never
  *                cleared by the library.
  *
- * total_rows must be a multiple of 32 (as every group is) and N of 8.
+ * total_rows is any size below 2^31; N a multiple of 8.
  */
 mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t N,
                                       int num_groups, const int64_t *offsets, int fp8_fmt,

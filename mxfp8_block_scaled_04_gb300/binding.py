@@ -240,14 +240,22 @@ def _fmt(fmt) -> int:
     return int(fmt)
 
 
-def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool):
+def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool, scale_col_rows: Optional[int] = None):
     M, N = x.shape
     dev = x.device
     u8 = torch.uint8
+    sc = -(-M // BLOCK) if scale_col_rows is None else scale_col_rows
     return (torch.empty((M, N), dtype=u8, device=dev) if rowwise else None,
             torch.empty((M, -(-N // BLOCK)), dtype=u8, device=dev) if rowwise else None,
             torch.empty((M, N), dtype=u8, device=dev) if colwise else None,
-            torch.empty((-(-M // BLOCK), N), dtype=u8, device=dev) if colwise else None)
+            torch.empty((sc, N), dtype=u8, device=dev) if colwise else None)
+
+
+def grouped_scale_col_rows(offsets) -> int:
+    """Rows of a grouped call's columnwise scale plane: the sum over groups of ceil(rows_g / 32)
+    (total_rows / 32 when every offset is a multiple of 32).  ``offsets`` on the host."""
+    off = torch.as_tensor(offsets, dtype=torch.int64, device="cpu")
+    return int(((off[1:] - off[:-1]).clamp(min=0) + BLOCK - 1).div(BLOCK, rounding_mode="floor").sum())
 
 
 def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
@@ -341,10 +349,15 @@ def quantize_dact(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activat
 
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,
                      colwise: bool = True, noop: Optional[torch.Tensor] = None,
-                     err_flag: Optional[torch.Tensor] = None, stream=None, with_dbias: bool = False) -> MXFP8Tensor:
+                     err_flag: Optional[torch.Tensor] = None, stream=None, with_dbias: bool = False,
+                     scale_col_rows: Optional[int] = None) -> MXFP8Tensor:
     """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device).
 
-    ``with_dbias`` also returns the per-group column sums as float32 [G, N].
+    Every group is quantized as its own flat problem; ``scale_col`` has
+    ``grouped_scale_col_rows(offsets)`` rows, group g's after those of the groups before it.
+    Pass ``scale_col_rows`` when it is known on the host; otherwise it is computed from a
+    host copy of ``offsets`` (one device-to-host read).  ``with_dbias`` also returns the
+    per-group column sums as float32 [G, N].
     """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
@@ -352,7 +365,9 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: 
         raise ValueError("offsets must be a contiguous 1-D torch.int64 tensor")
     total, N = x.shape
     G = offsets.numel() - 1
-    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise)
+    if colwise and scale_col_rows is None:
+        scale_col_rows = grouped_scale_col_rows(offsets.cpu())
+    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise, scale_col_rows)
     if with_dbias:
         dbias = torch.empty((G, N), dtype=torch.float32, device=x.device)
         ws = torch.empty((max(mxfp8_quantize_grouped_dbias_workspace_bytes(total, N, G), 16),), dtype=torch.uint8,

@@ -347,8 +347,7 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (total_rows < 0 || N < 0 || total_rows % 32 || N % 8 || total_rows >= (int64_t{1} << 31) ||
-        N >= (int64_t{1} << 31))
+    if (total_rows < 0 || N < 0 || N % 8 || total_rows >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
         return MXFP8_ERR_GROUPS;
@@ -642,7 +641,7 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
 
 size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups)
 {
-    if (total_rows < 0 || N < 0 || num_groups < 1 || total_rows % 32 || N % 8)
+    if (total_rows < 0 || N < 0 || num_groups < 1 || N % 8)
         return 0;
     return static_cast<size_t>(grouped_header_floats(num_groups)) * sizeof(float) +
            static_cast<size_t>((total_rows + kBM - 1) / kBM + num_groups) * static_cast<size_t>(N) * sizeof(float);
@@ -666,7 +665,7 @@ const char *mxfp8_status_string(int status)
     switch (status) {
     case MXFP8_OK: return "ok";
     case MXFP8_ERR_NULL: return "required pointer is NULL, a data/scale pair is half set, or no direction requested";
-    case MXFP8_ERR_SHAPE: return "M must be >= 0, N a non-negative multiple of 8, both below 2^31 (grouped: rows in multiples of 32)";
+    case MXFP8_ERR_SHAPE: return "M must be >= 0, N a non-negative multiple of 8, both below 2^31";
     case MXFP8_ERR_ALIGN: return "x/out/workspace must be 16-byte aligned, scale_col/dbias 4-byte aligned";
     case MXFP8_ERR_FORMAT: return "fp8_fmt must be MXFP8_E4M3 (0) or MXFP8_E5M2 (1)";
     case MXFP8_ERR_WORKSPACE: return "dbias requested without a workspace";

@@ -59,11 +59,12 @@ constexpr int kOffColMul = kStages * kStageBytes;      // float [4][128]
 constexpr int kOffDSum = kOffColMul + 4 * kBN * 4;     // float [4][128]
 constexpr int kOffBars = kOffDSum + 4 * kBN * 4;       // uint64 [kStages]
 constexpr int kOffCoord = kOffBars + 8 * kStages;      // TileCoord [kStages]
-constexpr int kOffScan = kOffCoord + 32 * kStages;     // int [kThreads / 32]
-constexpr int kOffGOff = kOffScan + 4 * (kThreads / 32);   // int64 [kMaxGroups + 1]
+constexpr int kOffScan = kOffCoord + 32 * kStages;     // int64 [kThreads / 32]
+constexpr int kOffGOff = kOffScan + 8 * (kThreads / 32);   // int64 [kMaxGroups + 1]
 constexpr int kOffGPre = kOffGOff + 8 * (kMaxGroups + 1);  // int [kMaxGroups + 1]
+constexpr int kOffGSB = kOffGPre + 4 * (kMaxGroups + 1);   // int [kMaxGroups + 1]
 constexpr int kSmemFlat = kOffGOff + 1024;                 // + alignment slack
-constexpr int kSmemGrouped = kOffGPre + 4 * (kMaxGroups + 1) + 1024;
+constexpr int kSmemGrouped = kOffGSB + 4 * (kMaxGroups + 1) + 1024;
 
 struct QuantParams {
     uint8_t *out_row;
@@ -234,12 +235,13 @@ struct TileCoord {
     int64_t row_end;  // one past the last row that belongs to the tile
     int col0;
     int rt;           // flat row-tile index (dbias partial row)
+    int sb;           // columnwise scale row of the tile's first 32-row block
 };
 static_assert(sizeof(TileCoord) <= 32, "coordinate slot");
 
 template <bool GROUPED>
 __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, const int64_t *goff,
-                                                const int *gpre)
+                                                const int *gpre, const int *gsb)
 {
     TileCoord c;
     if constexpr (GROUPED) {
@@ -258,6 +260,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         c.row_end = min(c.row0 + kBM, goff[lo + 1]);
         c.col0 = ct * kBN;
         c.rt = gpre[lo] / p.col_tiles + rtl;  // global row-tile index (per-group dbias partial row)
+        c.sb = gsb[lo] + rtl * (kBM / 32);     // the group's scale rows follow the groups before it
     } else {
         const int rt = t / p.col_tiles;
         const int ct = t - rt * p.col_tiles;
@@ -265,68 +268,75 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         c.row_end = min(c.row0 + kBM, p.M);
         c.col0 = ct * kBN;
         c.rt = rt;
+        c.sb = rt * (kBM / 32);
     }
     return c;
 }
 
-// Grouped set-up: load and check the offsets, build the per-group tile
-// prefix in shared memory.  Returns the tile count, or -1 for bad offsets.
-__device__ __forceinline__ int grouped_setup(const QuantParams &p, int64_t *goff, int *gpre, int *scan)
+// Grouped set-up: load and check the offsets, build the per-group prefixes of
+// row tiles (gpre, in tiles of all column tiles) and of columnwise scale rows
+// (gsb) in shared memory.  Returns the tile count, or -1 for bad offsets.
+// Both prefixes come from one exclusive scan of a packed count (tiles in the
+// high 32 bits, scale rows in the low: the low sum stays below 2^32, so it never
+// carries); thread t counts groups 2t and 2t+1 (kMaxGroups == 2 * kThreads).
+__device__ __forceinline__ int grouped_setup(const QuantParams &p, int64_t *goff, int *gpre, int *gsb,
+                                             int64_t *scan)
 {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.num_groups;
     for (int g = tid; g <= G; g += kThreads)
         goff[g] = p.offsets[g];
     __syncthreads();
     int bad = 0;
-    for (int g = tid; g < G; g += kThreads) {
-        const int64_t a = goff[g], b = goff[g + 1];
-        if (b < a || (b & 31))
+    for (int g = tid; g < G; g += kThreads)
+        if (goff[g + 1] < goff[g])
             bad = 1;
-    }
     if (tid == 0 && (goff[0] != 0 || goff[G] != p.M))
         bad = 1;
     if (__syncthreads_or(bad))
         return -1;
-
-    // tiles of group g = ceil(rows_g / 128) * col_tiles; exclusive scan over g.
-    // Thread t owns groups 2t and 2t+1 (kMaxGroups == 2 * kThreads).
-    int c[2];
+    // a group of rows_g rows: ceil(rows_g / 128) row tiles (times the column tiles) and
+    // ceil(rows_g / 32) columnwise scale rows
+    int64_t c[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int g = 2 * tid + k;
         c[k] = 0;
         if (g < G) {
             const int64_t rows = goff[g + 1] - goff[g];
-            c[k] = static_cast<int>((rows + kBM - 1) / kBM) * p.col_tiles;
+            c[k] = (((rows + kBM - 1) / kBM * p.col_tiles) << 32) + (rows + 31) / 32;
         }
     }
-    const int lane = tid & 31, warp = tid >> 5;
-    int incl = c[0] + c[1];
+    int64_t incl = c[0] + c[1];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        const int64_t v = __shfl_up_sync(0xffffffffu, incl, d);
         if (lane >= d)
             incl += v;
     }
     if (lane == 31)
         scan[warp] = incl;
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w)
-        base += scan[w];
-    const int excl = base + incl - (c[0] + c[1]);
-    if (2 * tid < G)
-        gpre[2 * tid] = excl;
-    if (2 * tid + 1 < G)
-        gpre[2 * tid + 1] = excl + c[0];
-    int total = 0;
-    for (int w = 0; w < kThreads / 32; ++w)
+    int64_t base = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+        base += w < warp ? scan[w] : 0;
         total += scan[w];
-    if (tid == 0)
-        gpre[G] = total;
+    }
+    const int64_t e0 = base + incl - (c[0] + c[1]), e1 = e0 + c[0];
+    if (2 * tid < G) {
+        gpre[2 * tid] = static_cast<int>(e0 >> 32);
+        gsb[2 * tid] = static_cast<int>(e0 & 0xFFFFFFFF);
+    }
+    if (2 * tid + 1 < G) {
+        gpre[2 * tid + 1] = static_cast<int>(e1 >> 32);
+        gsb[2 * tid + 1] = static_cast<int>(e1 & 0xFFFFFFFF);
+    }
+    if (tid == 0) {
+        gpre[G] = static_cast<int>(total >> 32);
+        gsb[G] = static_cast<int>(total & 0xFFFFFFFF);
+    }
     __syncthreads();
-    return total;
+    return static_cast<int>(total >> 32);
 }
 
 // SWZ: scale planes in the GEMM-ready layout; AMAX: also produce max |x|; ACT: an
@@ -343,9 +353,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *dsum = reinterpret_cast<float *>(smem + kOffDSum);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     TileCoord *coords = reinterpret_cast<TileCoord *>(smem + kOffCoord);
-    int *scan = reinterpret_cast<int *>(smem + kOffScan);
+    int64_t *scan = reinterpret_cast<int64_t *>(smem + kOffScan);
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
+    int *gsb = reinterpret_cast<int *>(smem + kOffGSB);
     unsigned *stage_done = reinterpret_cast<unsigned *>(smem + kOffScan);  // warp-local: [kStages] warps done
 
     constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
@@ -368,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     int num_tiles;
     if constexpr (GROUPED) {
-        num_tiles = grouped_setup(p, goff, gpre, scan);
+        num_tiles = grouped_setup(p, goff, gpre, gsb, scan);
         if (num_tiles < 0) {
             if (blockIdx.x == 0 && tid == 0) {
                 if (p.err_flag != nullptr)
@@ -407,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     auto issue = [&](int slot, int t) {
-        const TileCoord c = tile_coord<GROUPED>(t, p, goff, gpre);
+        const TileCoord c = tile_coord<GROUPED>(t, p, goff, gpre, gsb);
         coords[slot] = c;  // published to the consumers by the arrive below
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * kStageBytes);
@@ -451,6 +462,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
             int e0, e1, e2, e3;
             uint32_t amax_bits;  // fp32 bits of the largest of the four column amaxes
+            if constexpr (GROUPED) {
+                // A group's last block may end inside this 32-row block: the rows after it
+                // (the next group's, loaded with the tile) are zeroed in this warp's box, so
+                // they add nothing to the block's amax or column sums (phase 2 does not store
+                // them).  Flat tiles need this nowhere: rows past M are loaded as zeros.
+                const int64_t left = tc.row_end - (tc.row0 + rb * 32);
+                const int live = left < 32 ? static_cast<int>(left) : 32;
+                if (live < 32) {
+                    unsigned char *blk = const_cast<unsigned char *>(stage) + box * kBoxBytes + rb * 32 * 128;
+                    for (int c = live * 8 + lane; c < 32 * 8; c += 32)
+                        *reinterpret_cast<uint4 *>(blk + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();  // before the stage is refilled by TMA
+                    __syncwarp();
+                }
+            }
             if constexpr (ACT == 0) {
                 uint32_t mx0 = 0, mx1 = 0;
 #pragma unroll
@@ -537,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (half == 0) {
                 if (do_col && gcol < N && grow < tc.row_end) {
                     if constexpr (!SWZ) {
-                        *reinterpret_cast<uint32_t *>(p.scale_col + (grow >> 5) * N + gcol) =
+                        *reinterpret_cast<uint32_t *>(p.scale_col + static_cast<int64_t>(tc.sb + rb) * N + gcol) =
                             static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
                             (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
                     } else {

@@ -82,13 +82,25 @@ def g(x=A, total=128, N=64, G=2, off=A, fmt=0, orow=A, srow=A, ocol=A, scol=A, e
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(fmt=3), FORMAT), (dict(total=40), SHAPE), (dict(N=36), SHAPE),
+    (dict(fmt=3), FORMAT), (dict(total=-32), SHAPE), (dict(N=36), SHAPE), (dict(total=1 << 31), SHAPE),
     (dict(G=0), GROUPS), (dict(G=mx.MAX_GROUPS + 1), GROUPS), (dict(off=None), GROUPS),
     (dict(x=None), NULL), (dict(orow=None), NULL), (dict(orow=None, srow=None, ocol=None, scol=None), NULL),
     (dict(x=A + 2), ALIGN), (dict(off=A + 4), ALIGN), (dict(err=A + 2), ALIGN),
 ])
 def test_grouped_rejections(cuda_lib, kw, status):
     assert g(**kw) == status
+
+
+def test_grouped_any_row_count_passes_host_checks(cuda_lib):
+    # offsets are read only on the device, so total_rows that is not a multiple of 32 goes on to
+    # the device stage (which fails here without a usable GPU)
+    assert g(total=45) == DEVICE and g(total=1) == DEVICE and g(total=0) == DEVICE
+
+
+def test_grouped_scale_col_rows():
+    assert mx.grouped_scale_col_rows([0, 45, 45, 46, 192]) == 2 + 0 + 1 + 5
+    assert mx.grouped_scale_col_rows([0, 64, 96, 512]) == 512 // 32
+    assert mx.grouped_scale_col_rows([0, 0]) == 0
 
 
 def test_binding_wrappers_reject_bad_tensors(cuda_lib):
@@ -181,7 +193,8 @@ def test_grouped_dbias_host_checks(cuda_lib):
                                                args["fmt"], A, A, A, A, dbias, ws, None, None, 0)
     assert gd(dbias=None) == NULL
     assert gd(ws=None) == WORKSPACE
-    assert gd(total=40) == SHAPE
+    assert gd(total=-1) == SHAPE
+    assert gd(total=40) == DEVICE      # any row count passes the host checks (groups may be unaligned)
     assert gd(G=0) == GROUPS
     assert gd(dbias=A + 2) == ALIGN
     assert gd() == DEVICE

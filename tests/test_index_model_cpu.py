@@ -64,15 +64,18 @@ def swizzled_bytes(R, C):
 
 
 def tile_list(M, N, offsets):
-    """The kernel's tiles in order: (row0, row_end, col0, rt) per tile index."""
+    """The kernel's tiles in order: (row0, row_end, col0, rt, sb) per tile index; sb is the
+    columnwise scale row of the tile's first 32-row block."""
     col_tiles = -(-N // BN)
     if offsets is None:
         row_tiles = -(-M // BM)
-        return [(rt * BM, min(rt * BM + BM, M), ct * BN, rt) for rt in range(row_tiles) for ct in range(col_tiles)]
+        return [(rt * BM, min(rt * BM + BM, M), ct * BN, rt, rt * (BM // 32))
+                for rt in range(row_tiles) for ct in range(col_tiles)]
     G = len(offsets) - 1
-    gpre = [0]
+    gpre, gsb = [0], [0]
     for g in range(G):
         gpre.append(gpre[-1] + -(-(offsets[g + 1] - offsets[g]) // BM) * col_tiles)
+        gsb.append(gsb[-1] + -(-(offsets[g + 1] - offsets[g]) // 32))
     tiles = []
     for t in range(gpre[G]):
         lo, hi = 0, G                       # binary search: gpre[lo] <= t < gpre[hi]
@@ -85,8 +88,15 @@ def tile_list(M, N, offsets):
         local = t - gpre[lo]
         rtl, ct = local // col_tiles, local % col_tiles
         row0 = offsets[lo] + rtl * BM
-        tiles.append((row0, min(row0 + BM, offsets[lo + 1]), ct * BN, gpre[lo] // col_tiles + rtl))
+        tiles.append((row0, min(row0 + BM, offsets[lo + 1]), ct * BN, gpre[lo] // col_tiles + rtl,
+                      gsb[lo] + rtl * (BM // 32)))
     return tiles
+
+
+def scale_col_rows(M, offsets):
+    if offsets is None:
+        return -(-M // 32)
+    return sum(-(-(offsets[g + 1] - offsets[g]) // 32) for g in range(len(offsets) - 1))
 
 
 def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True, reuse=False):
@@ -99,7 +109,7 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
         scale_col = Plane("scale_col", swizzled_bytes(N, -(-M // 32)))
     else:
         scale_row = Plane("scale_row", M * Cr)
-        scale_col = Plane("scale_col", -(-M // 32) * N)
+        scale_col = Plane("scale_col", scale_col_rows(M, offsets) * N)
     tiles = tile_list(M, N, offsets)
     ws_rows = max([t[3] for t in tiles], default=-1) + 1
     ws = Plane("ws", ws_rows * N, 4)
@@ -119,11 +129,30 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
     rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
-            row0, row_end, col0, rt = tiles[t]
+            row0, row_end, col0, rt, sb = tiles[t]
             for box in range(2):            # TMA box origins (x must be 16-byte aligned)
                 x = col0 + box * BOX
                 if x < N:
                     assert (x * 2) % 16 == 0 and 0 <= row0 < M
+            # phase 1 of a grouped tile: the warp of (32-row block rb, box) zeroes the block's rows
+            # past the group's end in its own box (16-byte chunks c = live*8 + lane, step 32) before
+            # its column pass, so the next group's rows (loaded with the tile) count as zeros; the
+            # chunks stay inside the warp's own 4 KiB of the stage, and the nonzero rows left are
+            # exactly the group's rows of the block
+            if offsets is not None:
+                for rb in range(4):
+                    first = row0 + rb * 32
+                    if first >= row_end:
+                        continue
+                    live = min(32, row_end - first)
+                    for box in range(2):
+                        chunks = [live * 8 + lane + 32 * j for lane in range(32) for j in range(8)
+                                  if live * 8 + lane + 32 * j < 256]
+                        byte = box * 16384 + rb * 32 * 128 + np.array(chunks, int) * 16
+                        assert np.all((byte >= box * 16384 + rb * 4096) & (byte + 16 <= box * 16384 + rb * 4096 + 4096))
+                        zeroed_rows = sorted({first + c // 8 for c in chunks})
+                        assert zeroed_rows == list(range(first + live, first + 32))
+                        assert len(chunks) == len(set(chunks)) == (32 - live) * 8
             grow, gcol = row0 + rb1 * 32, col0 + box1 * BOX + cq1 * 4
             sel = (grow < row_end) & (half1 == 0) & (gcol < N) & do_col
             if swz:
@@ -131,7 +160,7 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                 for j in range(4):
                     scale_col.write(swizzled_offset(gcol[sel] + j, grow[sel] >> 5, C))
             else:
-                scale_col.write((grow[sel] >> 5) * N + gcol[sel], 4, align=4)
+                scale_col.write((sb + rb1[sel]) * N + gcol[sel], 4, align=4)
             if dbias:
                 gc = col0 + np.arange(BN)
                 ws.write(rt * N + gc[gc < N], 1, align=4)
@@ -224,7 +253,7 @@ def test_grouped_cast_writes_every_byte_once(N, grid):
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
     m = check_quantize(off[-1], N, grid, offsets=off, dbias=True)
     # no tile straddles two groups; each group's tiles are contiguous in the partial-sum rows
-    for row0, row_end, col0, rt in m["tiles"]:
+    for row0, row_end, col0, rt, sb in m["tiles"]:
         g = max(i for i in range(len(off) - 1) if off[i] <= row0)
         assert row_end <= off[g + 1]
 
@@ -234,6 +263,22 @@ def test_grouped_many_groups_and_empty_ones():
     sizes = (32 * rng.choice([0, 1, 3, 4, 5, 17], size=200)).tolist()
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
     check_quantize(off[-1], 48, 304, offsets=off, dbias=True)
+
+
+@pytest.mark.parametrize("sizes", [[45, 0, 1, 31, 33, 96, 70, 127, 129, 0, 13], [1] * 40 + [300], [17, 15],
+                                   [0, 200, 0]])
+@pytest.mark.parametrize("N", [40, 160])
+def test_grouped_unaligned_offsets_write_every_byte_once(sizes, N):
+    """Groups that are not multiples of 32 rows: each group's columnwise scale rows follow the
+    previous group's (sum of ceil(rows/32)), every output byte is written once, and no tile or
+    block takes rows of two groups."""
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    m = check_quantize(off[-1], N, 7, offsets=off, dbias=True)
+    assert m["scale_col"].count.size == scale_col_rows(off[-1], off) * N
+    for row0, row_end, col0, rt, sb in m["tiles"]:
+        g = max(i for i in range(len(off) - 1) if off[i] <= row0 and off[i + 1] > off[i])
+        assert off[g] <= row0 < row_end <= off[g + 1]
+        assert sb == sum(-(-(off[h + 1] - off[h]) // 32) for h in range(g)) + (row0 - off[g]) // 32
 
 
 def model_dact(M, N, grid, dbias=True, reuse=False):

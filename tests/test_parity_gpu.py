@@ -186,8 +186,9 @@ def run_grouped(x_bits, offsets, fmt, noop=None, prefill=CANARY):
     total, N = x_bits.shape
     x = dev_bf16(x_bits)
     off = torch.from_numpy(np.asarray(offsets, np.int64)).cuda()
+    srows = max(mx.grouped_scale_col_rows(np.maximum.accumulate(np.asarray(offsets, np.int64))), 1)
     bufs = dict(out_row=Guarded((total, N), fill=prefill), scale_row=Guarded((total, -(-N // 32)), fill=prefill),
-                out_col=Guarded((total, N), fill=prefill), scale_col=Guarded((total // 32, N), fill=prefill))
+                out_col=Guarded((total, N), fill=prefill), scale_col=Guarded((srows, N), fill=prefill))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     st = mx.mxfp8_quantize_grouped(x, total, N, off.numel() - 1, off, fmt, bufs["out_row"].t,
                                    bufs["scale_row"].t, bufs["out_col"].t, bufs["scale_col"].t,
@@ -212,8 +213,48 @@ def test_parity_grouped(oracle_mod, N):
         assert_bytes_equal(g, w, name)
 
 
+UNALIGNED_SIZES = [
+    np.array([45, 0, 1, 31, 33, 96, 70, 127, 129, 0, 13], np.int64),   # partial blocks everywhere
+    np.array([1] * 40 + [300], np.int64),                                 # many one-row groups
+    np.array([0, 200, 0], np.int64),                                      # one group, empties around it
+    np.array([17, 15], np.int64),                                         # both groups inside one block
+]
+
+
+@pytest.mark.parametrize("case", range(len(UNALIGNED_SIZES)))
+@pytest.mark.parametrize("fmt,N", [(E4M3, 96), (E5M2, 160), (E4M3, 40), (E5M2, 1032)])
+def test_parity_grouped_unaligned_offsets(oracle_mod, case, fmt, N):
+    """Groups that are not multiples of 32 rows: each is its own flat problem, whose last
+    columnwise block must not take in the next group's rows (which the tile loads with it)."""
+    sizes = UNALIGNED_SIZES[case]
+    off = wl.offsets_from_sizes(sizes)
+    x = wl.moe_bf16(sizes, N, seed=int(sizes.sum()) + N)
+    host, err = run_grouped(x, off, fmt)
+    assert err == 0
+    o = oracle_mod.quantize_grouped(x, off, fmt)
+    for name, w in zip(("out_row", "scale_row", "out_col", "scale_col"), o):
+        assert_bytes_equal(host[name], w, name)
+
+
+def test_parity_grouped_unaligned_next_group_dominates(oracle_mod):
+    """The rows after a group's partial last block are 1000x larger: any leak into that block's
+    amax changes its scale byte."""
+    sizes = np.array([45, 83, 1, 64], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    a = np.random.Generator(np.random.PCG64(3)).standard_normal((int(sizes.sum()), 128))
+    a[45:128] *= 1000.0
+    a[129:] *= 1000.0
+    x = wl.to_bf16_bits(a)
+    host, err = run_grouped(x, off, E4M3)
+    assert err == 0
+    o = oracle_mod.quantize_grouped(x, off, E4M3)
+    for name, w in zip(("out_row", "scale_row", "out_col", "scale_col"), o):
+        assert_bytes_equal(host[name], w, name)
+
+
 @pytest.mark.parametrize("offsets,valid", [
-    ([0, 16, 928], False),          # 16 is not a multiple of 32
+    ([0, 16, 928], True),           # valid: groups of 16 and 912 rows (each its own flat problem)
+    ([0, 16, 8, 928], False),       # decreasing
     ([0, 512, 256, 928], False),    # decreasing
     ([0, 512, 896], False),         # last entry != total rows
     ([32, 928], False),             # first entry != 0
@@ -434,13 +475,15 @@ def test_grouped_dbias(oracle_mod, N):
     assert np.all(got[1] == 0.0) and np.all(got[4] == 0.0)
 
 
-@pytest.mark.parametrize("case", ["512_groups", "one_group", "long_and_empty"])
+@pytest.mark.parametrize("case", ["512_groups", "512_unaligned_groups", "one_group", "long_and_empty"])
 def test_grouped_dbias_group_layouts(oracle_mod, case):
     """Per-group sums across the reduce's 16 contiguous tile ranges: many small groups, one group
     spanning every range, and long groups between empty ones, with N not a multiple of 32."""
     rng = np.random.Generator(np.random.PCG64(len(case)))
     if case == "512_groups":
         sizes, N = 32 * rng.choice([0, 1, 3, 4, 5, 17], size=512), 48
+    elif case == "512_unaligned_groups":
+        sizes, N = rng.choice([0, 1, 7, 31, 33, 100, 129, 600], size=512), 48
     elif case == "one_group":
         sizes, N = np.array([8192], np.int64), 80
     else:
@@ -460,12 +503,16 @@ def test_grouped_dbias_group_layouts(oracle_mod, case):
         assert np.all(np.abs(got[g] - want[g]) <= tol), g
         if sizes[g] == 0:
             assert np.all(got[g] == 0.0), g
+    if case == "512_unaligned_groups":
+        for name, gq, w in zip(("out_row", "scale_row", "out_col", "scale_col"), r[:4],
+                               oracle_mod.quantize_grouped(x_bits, off, E4M3)):
+            assert_bytes_equal(gq.cpu().numpy(), w, name)
 
 
 def test_grouped_dbias_bad_offsets_write_nothing():
     x = dev_bf16(wl.normal_bf16(928, 96, seed=1))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    off = torch.tensor([0, 16, 928], dtype=torch.int64, device="cuda")
+    off = torch.tensor([0, 929, 928], dtype=torch.int64, device="cuda")   # decreasing
     dbias = torch.full((2, 96), 3.0, dtype=torch.float32, device="cuda")
     ws = torch.empty(mx.mxfp8_quantize_grouped_dbias_workspace_bytes(928, 96, 2), dtype=torch.uint8, device="cuda")
     u8 = dict(dtype=torch.uint8, device="cuda")
@@ -476,6 +523,28 @@ def test_grouped_dbias_bad_offsets_write_nothing():
     torch.cuda.synchronize()
     assert int(err.item()) == 1
     assert bool((dbias == 3.0).all()) and all(bool((t == 0x3C).all()) for t in outs)
+
+
+def test_parity_moe_64x65536x7168_unaligned_full(oracle_mod):
+    """The MoE workload's shape with ragged token counts that are not multiples of 32 (Zipf split
+    of single rows): every byte against the oracle, per-group dbias within 1e-5 * sum|x|."""
+    sizes = wl.moe_group_sizes(64, 65536, seed=9, unit=1)
+    assert np.any(sizes % 32 != 0)
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = wl.moe_bf16(sizes, 7168, seed=9)
+    r = mx.quantize_grouped(dev_bf16(x_bits), torch.from_numpy(off).cuda(), E4M3, with_dbias=True,
+                            scale_col_rows=mx.grouped_scale_col_rows(off))
+    torch.cuda.synchronize()
+    want_q = oracle_slices.quantize_grouped(oracle_mod, x_bits, off, E4M3)
+    check_whole([t.cpu().numpy() for t in r[:4]], want_q)
+    want = oracle_slices.grouped_dbias(oracle_mod, x_bits, off)
+    got = r.dbias.cpu().numpy().astype(np.float64)
+    xv = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).float().abs()
+    for g in range(len(off) - 1):
+        tol = 1e-5 * xv[off[g]:off[g + 1]].double().sum(0).numpy()
+        assert np.all(np.abs(got[g] - want[g]) <= tol), g
+    del r
+    torch.cuda.empty_cache()
 
 
 def test_grouped_dbias_moe_64x65536x7168_full(oracle_mod):
