@@ -90,6 +90,8 @@ def _load():
             lib.mxo_quantize_f32.argtypes = [f32p, i64, i64, ctypes.c_int, u8p, u8p, u8p, u8p, f32p]
             lib.mxo_activate.restype = None
             lib.mxo_activate.argtypes = [u16p, i64, ctypes.c_int, f32p]
+            lib.mxo_gate.restype = None
+            lib.mxo_gate.argtypes = [u16p, i64, i64, ctypes.c_int, f32p]
             _lib = lib
     return _lib
 
@@ -235,6 +237,22 @@ def quantize_act(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True, c
                  with_dbias: bool = False):
     """Activation in fp32, then the MXFP8 cast of the fp32 values."""
     return quantize_f32(activate(x_bits, act), fmt, rowwise, colwise, with_dbias)
+
+
+def gate(x_bits: np.ndarray, act: int) -> np.ndarray:
+    """fp32 act(a) * b of a BF16 matrix [M, 2N] with a = its first N columns, b = its last N (mxo_gate)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N2 = x.shape
+    if N2 % 2:
+        raise ValueError("oracle: a gated input has an even number of columns")
+    y = np.empty((M, N2 // 2), np.float32)
+    _load().mxo_gate(_ptr(x, ctypes.c_uint16), M, N2 // 2, act, _ptr(y, ctypes.c_float))
+    return y
+
+
+def quantize_gated(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True, colwise: bool = True):
+    """The MXFP8 cast of act(a) * b for a gated input [M, 2N] (no dbias)."""
+    return quantize_f32(gate(x_bits, act), fmt, rowwise, colwise)[:4]
 
 
 def activation_f64(v: float, act: int) -> float:

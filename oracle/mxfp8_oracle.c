@@ -435,6 +435,27 @@ void mxo_activate(const uint16_t *x, int64_t n, int act, float *y)
 }
 
 /*
+ * Gated activation before the cast (the GLU family: ReGLU, squared-ReLU GLU,
+ * GeGLU, SwiGLU, QGeGLU for act = 1..5).  The pages name the fused activation
+ * field but give neither the gated forms nor their layout; the reading used:
+ * x is BF16 [M, 2N], its first N columns are the activation's input a and its
+ * last N the linear input b, and the value cast is
+ *     y[i][j] = act(a[i][j]) * b[i][j],   a = x[i][j], b = x[i][N + j],
+ * evaluated in double (act as in mxo_activation_f64) and rounded once to fp32.
+ * y is [M, N] fp32.
+ */
+void mxo_gate(const uint16_t *x, int64_t M, int64_t N, int act, float *y)
+{
+    int64_t i, j;
+    for (i = 0; i < M; i++)
+        for (j = 0; j < N; j++) {
+            const double a = mxo_bf16_to_double(x[i * 2 * N + j]);
+            const double b = mxo_bf16_to_double(x[i * 2 * N + N + j]);
+            y[i * N + j] = (float)(mxo_activation_f64(a, act) * b);
+        }
+}
+
+/*
  * Per-expert dbias of a grouped call (the survey's "grouped-call dbias per
  * expert"): dbias[g][j] = sum of x[i][j] over the rows i of group g, in
  * double, rounded once to fp32; an empty group gets zeros.  Returns -1 for

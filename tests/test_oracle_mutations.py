@@ -42,6 +42,8 @@ MUTATIONS = [
      "scale_col ? scale_col + (r0 / MXO_BLOCK) * N : 0"),
     ("grouped scale rows counted with floor", "s0 += (rows + MXO_BLOCK - 1) / MXO_BLOCK;",
      "s0 += rows / MXO_BLOCK;"),
+    ("gated halves swapped", "const double a = mxo_bf16_to_double(x[i * 2 * N + j]);",
+     "const double a = mxo_bf16_to_double(x[i * 2 * N + N + j]);"),
 ]
 
 

@@ -524,3 +524,65 @@ def test_dactivation_sign_for_very_negative_inputs(oracle_mod, act):
         d = oracle_mod.dactivation_f64(x, act)
         assert d <= 0.0 and math.copysign(1.0, d) == -1.0, (act, x, d)
     assert oracle_mod.dactivation_f64(-0.5, 4) > 0.0 and oracle_mod.dactivation_f64(1.0, 3) > 1.0
+
+
+# ---- gated activations: act(a) * b with x = [a | b] -----------------------------------
+
+_BF16_FINITE = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+_BF16_FINITE = _BF16_FINITE[(_BF16_FINITE & 0x7F80) != 0x7F80]
+
+
+@pytest.mark.parametrize("act", [1, 2, 3, 4, 5])
+def test_gate_with_unit_linear_half_is_the_activation(oracle_mod, act):
+    """b = 1 everywhere: act(a) * 1 rounds once to fp32 just as the activation alone, for every
+    finite BF16 a; with b = 2^-3 the result is that value scaled exactly, wherever the scaled value
+    is a normal fp32 number (an eighth of a subnormal is rounded again)."""
+    a = _BF16_FINITE[: (_BF16_FINITE.size // 64) * 64].reshape(-1, 64)
+    if act == 2:   # squared ReLU overflows fp32 for |a| >= 2^64
+        a = np.where((a & 0x7F80) >= ((127 + 64) << 7), 0, a).astype(np.uint16)
+    one = np.full_like(a, 0x3F80)
+    got = oracle_mod.gate(np.concatenate([a, one], axis=1), act)
+    assert np.array_equal(got.view(np.uint32), oracle_mod.activate(a, act).view(np.uint32))
+    eighth = np.full_like(a, 0x3E00)                          # BF16 0.125
+    got8 = oracle_mod.gate(np.concatenate([a, eighth], axis=1), act).astype(np.float64)
+    ref = oracle_mod.activate(a, act).astype(np.float64) / 8
+    normal = np.abs(ref) >= 2.0 ** -126
+    assert np.array_equal(got8[normal], ref[normal])
+
+
+def test_gate_hand_worked(oracle_mod):
+    # a = [-2, 3, 0, 20], b = [5, -4, 7, 0.5]:
+    #   ReGLU   [0, -12, 0, 10];  squared-ReLU GLU [0, -36, 0, 200];
+    #   SwiGLU of a = 0 is 0; GeGLU(20) = 20 (sigmoid(603) is 1 in double) -> 20 * 0.5 = 10
+    x = wl.to_bf16_bits(np.array([[-2.0, 3.0, 0.0, 20.0, 5.0, -4.0, 7.0, 0.5]]))
+    assert oracle_mod.gate(x, 1).tolist() == [[0.0, -12.0, 0.0, 10.0]]
+    assert oracle_mod.gate(x, 2).tolist() == [[0.0, -36.0, 0.0, 200.0]]
+    assert oracle_mod.gate(x, 4)[0, 2] == 0.0 and oracle_mod.gate(x, 3)[0, 3] == 10.0
+    # the halves are not interchangeable: with them swapped, ReGLU would give [-10, 0, 0, 10]
+    assert oracle_mod.gate(x, 1)[0, 0] == 0.0
+
+
+@pytest.mark.parametrize("act", [3, 4, 5])
+def test_gate_matches_torch_float64(oracle_mod, act):
+    import torch.nn.functional as F
+    x = structured_input(48, 2 * 40, seed=20 + act)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    a, b = xv[:, :40], xv[:, 40:]
+    if act == 3:
+        want = F.gelu(a, approximate="tanh") * b
+    elif act == 4:
+        want = F.silu(a) * b
+    else:
+        want = a * torch.sigmoid(1.702 * a) * b
+    want = want.numpy()
+    got = oracle_mod.gate(x, act).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 2 ** -22 * np.abs(want) + 1e-15 * np.abs(a.numpy() * b.numpy()) + 1e-38)
+
+
+def test_quantize_gated_is_the_cast_of_the_gate(oracle_mod):
+    x = structured_input(64, 2 * 96, seed=5)
+    for act in (1, 4):
+        q = oracle_mod.quantize_gated(x, 1, act)
+        r = oracle_mod.quantize_f32(oracle_mod.gate(x, act), 1)
+        for u, v in zip(q, r[:4]):
+            assert np.array_equal(u, v)
