@@ -58,6 +58,9 @@ def parse_args():
     ap.add_argument("--act", default="none", help="activation before the cast: relu, srelu, gelu, silu, qgelu")
     ap.add_argument("--dact", default="none",
                     help="backward fusion: quantize dY * act'(X), dY = the workload, X = N(0,1) of the same shape")
+    ap.add_argument("--glu", default="none",
+                    help="gated activation act(a) * b before the cast: x = [a | b] with a = the workload and "
+                         "b = N(0,1) of the same shape (relu, srelu, gelu, silu = SwiGLU, qgelu)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -116,10 +119,11 @@ def measured_peak():
 def profile_name(args, M, N, workload_dbias):
     """Name of the committed ncu summary (profiles/<name>.md) for this run's kernel, workload and options."""
     name = args.workload if not args.shape else f"{args.workload.split('_')[0]}_{M}x{N}"
-    family = "quantize_dact" if args.dact.lower() != "none" else "quantize"
+    family = ("quantize_dact" if args.dact.lower() != "none" else
+              "quantize_gated" if args.glu.lower() != "none" else "quantize")
     opts = [o for o, on in (("swizzled", args.swizzled), ("amax", args.amax),
                             ("dbias", args.dbias and not workload_dbias)) if on]
-    opts += [a.lower() for a in (args.act, args.dact) if a.lower() != "none"]
+    opts += [a.lower() for a in (args.act, args.dact, args.glu) if a.lower() != "none"]
     return "_".join([family, name] + opts)
 
 
@@ -370,6 +374,13 @@ def run_ours(args):
         raise SystemExit("--dact takes a flat workload without --act / --swizzled / --amax")
     x_act = (torch.from_numpy(wl.normal_bf16(M, N, seed=1234).view(np.int16)).view(torch.bfloat16).cuda()
              if dact else None)
+    glu = mx.binding.ACTIVATIONS[args.glu.lower()]
+    x_in_bits = x_bits
+    if glu:
+        if act or dact or args.swizzled or args.amax or grouped or with_dbias:
+            raise SystemExit("--glu takes a flat workload without dbias or other options")
+        x_in_bits = np.ascontiguousarray(np.concatenate([x_bits, wl.normal_bf16(M, N, seed=4321)], axis=1))
+        x = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).cuda()
     if (args.swizzled or args.amax or act) and offsets is not None:
         raise SystemExit("--swizzled / --amax / --act apply to the flat workloads")
     if act and with_dbias:
@@ -392,6 +403,8 @@ def run_ours(args):
         elif dact:
             st = mx.mxfp8_quantize_dact(xin, x_act, M, N, fmt, dact, out_row, scale_row, out_col, scale_col,
                                         dbias, ws, None, stream)
+        elif glu:
+            st = mx.mxfp8_quantize_gated(xin, M, N, fmt, glu, out_row, scale_row, out_col, scale_col, None, stream)
         elif args.swizzled or args.amax or act:
             cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
                                  layout, amax, act)
@@ -402,9 +415,9 @@ def run_ours(args):
         if st != 0:
             raise mx.MXFP8Error(st, "bench step")
 
-    algo_bytes = (BYTES_PER_ELEM + (2 if dact else 0)) * M * N + (4 * N * max(G, 1) if with_dbias else 0)
+    algo_bytes = (BYTES_PER_ELEM + (2 if dact or glu else 0)) * M * N + (4 * N * max(G, 1) if with_dbias else 0)
     prof = profile_name(args, M, N, w["with_dbias"])
-    kernels = (["amax_init_kernel"] if args.amax else []) + ["quantize_dact_kernel" if dact else "quantize_kernel"]
+    kernels = (["amax_init_kernel"] if args.amax else []) + ["quantize_dact_kernel" if dact or glu else "quantize_kernel"]
     if with_dbias:
         kernels.append("dbias_reduce_grouped_kernel" if grouped else "dbias_reduce_kernel")
     uuid = None
@@ -500,12 +513,12 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host in, pinned host out ----
     e2e = None
     if not args.no_e2e:
-        x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        x_host = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
         outs_dev = [out_row, scale_row, out_col, scale_col] + ([dbias] if with_dbias else [])
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped or args.swizzled or args.amax or act or dact:
+        if grouped or args.swizzled or args.amax or act or dact or glu:
             # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
             path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"
@@ -562,7 +575,7 @@ def run_ours(args):
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "scales": "swizzled" if args.swizzled else "plain", "amax": bool(args.amax),
-                       "activation": args.act.lower(), "dact": args.dact.lower(),
+                       "activation": args.act.lower(), "dact": args.dact.lower(), "glu": args.glu.lower(),
                        "bytes_per_step": algo_bytes,
                        "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
                               f"bf16 input; time = sum of the per-step event intervals" if flush else

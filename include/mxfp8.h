@@ -302,6 +302,30 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
                                    void *stream);
 
 /*
+ * Gated activation before the cast (the GLU family; the `activation` field of
+ * the PR #3137 config key names the fused activation, the pages give no gated
+ * form, so this library's reading is stated here): x = [a | b] is BF16
+ * [M, 2N], a its first N columns (the activation's input) and b its last N
+ * (the linear input), and the cast is of the fp32 value y = act(a) * b, an
+ * [M, N] tensor quantized as by mxfp8_quantize:
+ *   MXFP8_ACT_RELU   ReGLU            MXFP8_ACT_GELU   GeGLU (tanh form)
+ *   MXFP8_ACT_SRELU  squared-ReLU GLU MXFP8_ACT_SILU   SwiGLU
+ *   MXFP8_ACT_QGELU  QGeGLU
+ *   x           device bf16 [M, 2N], row pitch 2N elements, 16-byte aligned.
+ *   outputs     out_row / out_col uint8 [M, N], scale_row [M, ceil(N/32)],
+ *               scale_col [ceil(M/32), N]; either direction may be NULL.
+ *   noop, stream: as for mxfp8_quantize.  No dbias.
+ * act is evaluated as for mxfp8_activation_t (ReGLU and the squared-ReLU GLU
+ * are exact: y is a product of at most 24 significant bits; the others within
+ * a few fp32 ulps).  M >= 0 and N a multiple of 8 (so that b starts on a
+ * 16-byte boundary), N < 2^30.  Status codes as for mxfp8_quantize_dact.
+ */
+mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8_fmt, int activation,
+                                    void *out_row, void *scale_row,
+                                    void *out_col, void *scale_col,
+                                    const float *noop, void *stream);
+
+/*
  * Workspace bytes for mxfp8_quantize_grouped_dbias: a header of
  * (num_groups + 1) int64 (each group's first row tile) padded to 256 bytes,
  * then one fp32 partial row per 128-row tile, tiles never spanning two

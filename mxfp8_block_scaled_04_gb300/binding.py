@@ -80,6 +80,8 @@ def lib():
             L.mxfp8_quantize_grouped_dbias.argtypes = [vp, i64, i64, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_dact.restype = i32
             L.mxfp8_quantize_dact.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_gated.restype = i32
+            L.mxfp8_quantize_gated.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
@@ -162,6 +164,16 @@ def mxfp8_quantize_dact(grad, act_input, M, N, fp8_fmt, activation, out_row, sca
     return int(lib().mxfp8_quantize_dact(_addr(grad), _addr(act_input), M, N, fp8_fmt, int(activation),
                                          _addr(out_row), _addr(scale_row), _addr(out_col), _addr(scale_col),
                                          _addr(dbias), _addr(workspace), _addr(noop), _stream(stream)))
+
+
+def mxfp8_quantize_gated(x, M, N, fp8_fmt, activation, out_row, scale_row, out_col, scale_col,
+                         noop=None, stream=None) -> int:
+    """The cast of act(a) * b for x = [a | b] (bf16 [M, 2N]); see include/mxfp8.h."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_gated(_addr(x), M, N, fp8_fmt, int(activation), _addr(out_row),
+                                          _addr(scale_row), _addr(out_col), _addr(scale_col), _addr(noop),
+                                          _stream(stream)))
 
 
 def mxfp8_quantize_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
@@ -345,6 +357,25 @@ def quantize_dact(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activat
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_dact")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+
+
+def quantize_gated(x: torch.Tensor, fmt=E4M3, activation="silu", rowwise: bool = True, colwise: bool = True,
+                   noop: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """The cast of act(a) * b for a contiguous CUDA bf16 x = [a | b] of shape [M, 2N].
+
+    ``activation`` "silu" gives SwiGLU, "gelu" GeGLU, "relu" ReGLU, "srelu" the squared-ReLU
+    GLU, "qgelu" QGeGLU; the outputs are [M, N].
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
+    if x.shape[1] % 2:
+        raise ValueError("a gated input has an even number of columns")
+    M, N = x.shape[0], x.shape[1] // 2
+    out_row, scale_row, out_col, scale_col = _alloc(x[:, :N], rowwise, colwise)
+    st = mxfp8_quantize_gated(x, M, N, _fmt(fmt), activation, out_row, scale_row, out_col, scale_col, noop, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_gated")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
 
 
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,

@@ -55,7 +55,7 @@ struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int ctas_per_sm[192] = {};  // indexed by kernel variant
-    int dact_ctas_per_sm[24] = {};  // dact kernels: FMT + 2 * DBIAS + 4 * ACT
+    int dact_ctas_per_sm[48] = {};  // two-input kernels: FMT + 2 * DBIAS + 4 * ACT + 24 * GATED
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -131,19 +131,25 @@ mxfp8_status_t prepare(int device, int *grid_cap)
     return MXFP8_OK;
 }
 
-mxfp8_status_t make_tensor_map(CUtensorMap *map, const void *x, int64_t rows, int64_t N)
+// TMA map of a BF16 matrix [rows, N] whose rows are `pitch` elements apart (pitch >= N).
+mxfp8_status_t make_tensor_map_pitch(CUtensorMap *map, const void *x, int64_t rows, int64_t N, int64_t pitch)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr)
         return MXFP8_ERR_DEVICE;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
     cuuint32_t box[2] = {kBoxCols, kBM};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+}
+
+mxfp8_status_t make_tensor_map(CUtensorMap *map, const void *x, int64_t rows, int64_t N)
+{
+    return make_tensor_map_pitch(map, x, rows, N, N);
 }
 
 // Shared host-side checks of the direction pointers.
@@ -215,7 +221,7 @@ __global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const 
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
 // The backward-fusion kernel (dY * act'(X)): one-time set-up per (device, variant), then launch.
-template <int FMT, bool DBIAS, int ACT>
+template <int FMT, bool DBIAS, int ACT, bool GATED = false>
 mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUtensorMap &map_x, const QuantParams &p,
                                int64_t tiles, cudaStream_t stream)
 {
@@ -232,9 +238,9 @@ mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUten
             }
             d.ready = true;
         }
-        const int v = FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT;
+        const int v = FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT + (GATED ? 24 : 0);
         if (d.dact_ctas_per_sm[v] == 0) {
-            auto kern = quantize_dact_kernel<FMT, DBIAS, ACT>;
+            auto kern = quantize_dact_kernel<FMT, DBIAS, ACT, GATED>;
             int n = 0;
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDact) != cudaSuccess ||
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDact) != cudaSuccess || n < 1) {
@@ -246,7 +252,8 @@ mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUten
         cap = d.dact_ctas_per_sm[v] * d.sm_count;
     }
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    return launch_pdl(quantize_dact_kernel<FMT, DBIAS, ACT>, grid, kThreads, kSmemDact, stream, map_g, map_x, p);
+    return launch_pdl(quantize_dact_kernel<FMT, DBIAS, ACT, GATED>, grid, kThreads, kSmemDact, stream, map_g, map_x,
+                      p);
 }
 
 template <int ACT>
@@ -258,6 +265,14 @@ mxfp8_status_t launch_dact(int fmt, bool dbias, int device, const CUtensorMap &m
                      : launch_dact_fmt<0, false, ACT>(device, map_g, map_x, p, tiles, stream);
     return dbias ? launch_dact_fmt<1, true, ACT>(device, map_g, map_x, p, tiles, stream)
                  : launch_dact_fmt<1, false, ACT>(device, map_g, map_x, p, tiles, stream);
+}
+
+template <int ACT>
+mxfp8_status_t launch_gated(int fmt, int device, const CUtensorMap &map_b, const CUtensorMap &map_a,
+                            const QuantParams &p, int64_t tiles, cudaStream_t stream)
+{
+    return fmt == MXFP8_E4M3 ? launch_dact_fmt<0, false, ACT, true>(device, map_b, map_a, p, tiles, stream)
+                             : launch_dact_fmt<1, false, ACT, true>(device, map_b, map_a, p, tiles, stream);
 }
 
 // Activated (ACT != 0) variants: flat, no dbias; swizzle and amax as template switches.
@@ -637,6 +652,64 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
     if (dbias != nullptr && N > 0)
         return enqueue_reduce(static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop, stream);
     return MXFP8_OK;
+}
+
+mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8_fmt, int activation, void *out_row,
+                                    void *scale_row, void *out_col, void *scale_col, const float *noop,
+                                    void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 30))
+        return MXFP8_ERR_SHAPE;
+    const bool empty = M == 0 || N == 0;
+    mxfp8_status_t st;
+    if (!empty) {
+        if (x == nullptr)
+            return MXFP8_ERR_NULL;
+        if ((st = check_outputs(out_row, scale_row, out_col, scale_col)) != MXFP8_OK)
+            return st;
+    }
+    if (!aligned(x, 16))
+        return MXFP8_ERR_ALIGN;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kDBN - 1) / kDBN;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(out_row, device) || !on_device(scale_row, device) ||
+        !on_device(out_col, device) || !on_device(scale_col, device) || !on_device(noop, device))
+        return MXFP8_ERR_DEVICE;
+    if (empty)
+        return MXFP8_OK;
+    // a = columns 0 .. N-1 of x, b = columns N .. 2N-1 (16-byte aligned: N is a multiple of 8)
+    CUtensorMap map_a, map_b;
+    const void *b = static_cast<const uint16_t *>(x) + N;
+    if ((st = make_tensor_map_pitch(&map_a, x, M, N, 2 * N)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_b, b, M, N, 2 * N)) != MXFP8_OK)
+        return st;
+    QuantParams p{};
+    p.out_row = static_cast<uint8_t *>(out_row);
+    p.scale_row = static_cast<uint8_t *>(scale_row);
+    p.out_col = static_cast<uint8_t *>(out_col);
+    p.scale_col = static_cast<uint8_t *>(scale_col);
+    p.noop = noop;
+    p.M = M;
+    p.N = N;
+    p.row_tiles = static_cast<int>(row_tiles);
+    p.col_tiles = static_cast<int>(col_tiles);
+    const int64_t tiles = row_tiles * col_tiles;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    switch (activation) {
+    case MXFP8_ACT_RELU: return launch_gated<1>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    case MXFP8_ACT_SRELU: return launch_gated<2>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    case MXFP8_ACT_GELU: return launch_gated<3>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    case MXFP8_ACT_SILU: return launch_gated<4>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    default: return launch_gated<5>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    }
 }
 
 size_t mxfp8_quantize_grouped_dbias_workspace_bytes(int64_t total_rows, int64_t N, int num_groups)

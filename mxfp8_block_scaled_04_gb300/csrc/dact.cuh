@@ -20,6 +20,11 @@
 //     evaluation; dReLU and dSReLU are cheaper to evaluate again).
 // The derivative is evaluated in fp32 with the same ex2 / rcp approximations
 // as the forward activations; dReLU and dSReLU are exact.
+//
+// GATED: the same kernel casts a gated activation act(a) * b (ReGLU, squared-ReLU
+// GLU, GeGLU, SwiGLU, QGeGLU) of an input x = [a | b], BF16 [M, 2N]: the dY slot
+// holds the box of b (columns N.. of x), the X slot the box of a, and the forward
+// activation takes the derivative's place.  No dbias.
 #pragma once
 
 #include <cstdint>
@@ -105,7 +110,7 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
     }
 }
 
-template <int FMT, bool DBIAS, int ACT>
+template <int FMT, bool DBIAS, int ACT, bool GATED = false>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_dact_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_x,
                          const QuantParams p)
@@ -122,6 +127,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // the transcendental derivatives keep each product for phase 2 (see the top)
     constexpr bool kKeep = ACT > 2;
+    static_assert(!(GATED && DBIAS), "the gated cast has no dbias");
+    // act'(x) for the backward fusion, act(x) for the gated cast (two lanes)
+    auto factor2 = [](uint64_t x) -> uint64_t {
+        if constexpr (GATED)
+            return activation2<ACT>(x);
+        else
+            return dactivation2<ACT>(x);
+    };
     pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
@@ -183,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int off = (r0 + i) * 128 + (((cq >> 1) ^ i) << 4) + (cq & 1) * 8;
                 const uint2 g = lds64(gbox + off), xv = lds64(xbox + off);
                 const uint64_t y01 = f2_mul(f2_pack(bf16_lo(g.x), bf16_hi(g.x)),
-                                            dactivation2<ACT>(f2_pack(bf16_lo(xv.x), bf16_hi(xv.x))));
+                                            factor2(f2_pack(bf16_lo(xv.x), bf16_hi(xv.x))));
                 const uint64_t y23 = f2_mul(f2_pack(bf16_lo(g.y), bf16_hi(g.y)),
-                                            dactivation2<ACT>(f2_pack(bf16_lo(xv.y), bf16_hi(xv.y))));
+                                            factor2(f2_pack(bf16_lo(xv.y), bf16_hi(xv.y))));
                 float y0, y1, y2, y3;
                 f2_unpack(y01, y0, y1);
                 f2_unpack(y23, y2, y3);
@@ -286,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if constexpr (kKeep) {  // the products phase 1 left in the two slots
                         y[2 * j] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x5410));
                         y[2 * j + 1] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x7632));
+                    } else if constexpr (GATED) {  // ReGLU, squared-ReLU GLU: exact, evaluated again
+                        y[2 * j] = bf16_lo(gw[j]) * relu_family<ACT>(bf16_lo(xw[j]));
+                        y[2 * j + 1] = bf16_hi(gw[j]) * relu_family<ACT>(bf16_hi(xw[j]));
                     } else {                // dReLU, dSReLU: cheaper to evaluate again
                         y[2 * j] = bf16_lo(gw[j]) * dactivation<ACT>(bf16_lo(xw[j]));
                         y[2 * j + 1] = bf16_hi(gw[j]) * dactivation<ACT>(bf16_hi(xw[j]));

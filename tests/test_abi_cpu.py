@@ -216,6 +216,22 @@ def test_dact_host_checks(cuda_lib):
     assert d() == DEVICE
 
 
+def test_gated_host_checks(cuda_lib):
+    def gt(**kw):
+        a = dict(x=A, M=64, N=64, fmt=0, act=4, orow=A, srow=A, ocol=A, scol=A)
+        a.update(kw)
+        return mx.mxfp8_quantize_gated(a["x"], a["M"], a["N"], a["fmt"], a["act"], a["orow"], a["srow"],
+                                       a["ocol"], a["scol"], None, 0)
+    assert gt(act=0) == FORMAT and gt(act=6) == FORMAT and gt(fmt=2) == FORMAT
+    assert gt(N=36) == SHAPE and gt(M=-1) == SHAPE and gt(N=1 << 30) == SHAPE
+    assert gt(x=None) == NULL and gt(orow=None) == NULL and gt(orow=None, srow=None, ocol=None, scol=None) == NULL
+    assert gt(x=A + 8) == ALIGN and gt(ocol=A + 8) == ALIGN
+    assert gt() == DEVICE and gt(N=40) == DEVICE      # N a multiple of 8: b starts 16-byte aligned
+    import torch
+    with pytest.raises(ValueError):
+        mx.quantize_gated(torch.zeros(4, 6, dtype=torch.bfloat16)[:, :5].contiguous())
+
+
 def test_selftest_bounded_wait_rejections(cuda_lib):
     assert mx.mxfp8_selftest_bounded_wait(1_000_000, None) == NULL
     assert mx.mxfp8_selftest_bounded_wait(0, A) == SHAPE

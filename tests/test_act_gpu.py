@@ -24,8 +24,11 @@ of the exact value v, and a rounding decision between them lies within w of v
 The rule.  A code may differ from the oracle's only if the exact scaled value
 lies within w of the midpoint between the two codes.  A scale byte may differ
 by one only if the block's exact amax lies within the block's largest w of the
-power-of-two boundary between the two exponents; the block's codes are then
-checked against the oracle's rounding at the GPU's exponent.  The number of
+power-of-two boundary between the two exponents.  The exponent rule's other
+decision is amax == 0 (e = 127): a scale byte may be 127 on one side and any
+value on the other only if every exact value of the block lies within its w of
+zero, and the side with 127 then holds only zero codes.  In both cases the
+block's codes are checked against the oracle's rounding at the GPU's exponent.  The number of
 codes that used the rule may not exceed the number of elements whose exact
 scaled value lies within w of a rounding decision, counted from the oracle's
 values alone before the comparison (there is no fixed share).  Elements whose
@@ -130,13 +133,18 @@ def check_codes(oracle_mod, gpu_codes, ref_codes, gpu_scales, ref_scales, y32, y
     for s_idx in np.argwhere(gpu_scales != ref_scales):
         s_idx = tuple(s_idx)
         eg, eo = int(gpu_scales[s_idx]), int(ref_scales[s_idx])
-        assert abs(eg - eo) == 1, (s_idx, eg, eo)
         i, j = (s_idx[0] * 32, s_idx[1]) if colwise else (s_idx[0], s_idx[1] * 32)
         elems = block_of(i, j)
         amax64 = max(abs(float(y64[e])) for e in elems)
-        boundary = FMAX[fmt] * 2.0 ** (min(eg, eo) - 127)
         w = max(float(wabs[e]) for e in elems)
-        assert abs(amax64 - boundary) <= w, (s_idx, amax64, boundary, w)
+        if abs(eg - eo) == 1:
+            boundary = FMAX[fmt] * 2.0 ** (min(eg, eo) - 127)
+            assert abs(amax64 - boundary) <= w, (s_idx, amax64, boundary, w)
+        else:   # amax == 0 on one side: every exact value within its window of zero
+            assert 127 in (eg, eo), (s_idx, eg, eo)
+            assert all(abs(float(y64[e])) <= float(wabs[e]) for e in elems), (s_idx, eg, eo, amax64)
+            zero_side = gpu_codes if eg == 127 else ref_codes
+            assert all(int(zero_side[e]) & 0x7F == 0 for e in elems), (s_idx, eg, eo)
         for e in elems:   # this block's codes at the GPU's exponent
             expected[e] = oracle_mod.fp8_encode(float(y32[e]) * 2.0 ** (127 - eg), fmt)
         used += len(elems)
@@ -291,4 +299,95 @@ def test_every_bf16_value_rowwise_against_the_oracle(oracle_mod, act, fmt):
     torch.cuda.synchronize()
     o = oracle_mod.quantize_act(x, fmt, a, rowwise=True, colwise=False)
     y32, y64, w = forward_case(oracle_mod, x, a)
+    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, y64, w, fmt, False)
+
+
+# ---- gated activations: act(a) * b for x = [a | b] --------------------------------------
+
+def gated_input(M, N, seed):
+    """x = [a | b]: a as for the activations (tails, zeros, subnormals), b N(0,1) with per-row
+    exponents, a few zeros and subnormals."""
+    a = act_input(M, N, seed) if M >= 8 else wl.normal_bf16(M, N, seed=seed)
+    rng = np.random.Generator(np.random.PCG64(seed + 1))
+    bv = rng.standard_normal((M, N)) * np.exp2(rng.integers(-8, 8, (M, 1)))
+    bv.reshape(-1)[rng.integers(0, M * N, max(1, M * N // 200))] = 0.0
+    bv.reshape(-1)[rng.integers(0, M * N, max(1, M * N // 200))] *= 1e-39
+    return np.ascontiguousarray(np.concatenate([a, wl.to_bf16_bits(bv)], axis=1))
+
+
+def gated_window(oracle_mod, x_bits, a):
+    """(exact values, absolute windows w) of act(a) * b: the activation's window scaled by |b|,
+    plus the product's fp32 rounding on both sides."""
+    N = x_bits.shape[1] // 2
+    av, bv = x_values(x_bits[:, :N]), x_values(x_bits[:, N:])
+    act64 = np.vectorize(lambda v: oracle_mod.activation_f64(v, a))(av)
+    y64 = act64 * bv
+    w = np.abs(bv) * (DELTA * forward_cond(av, a) * np.abs(act64) + SUB) + ROUND * np.abs(y64) + 2.0 ** -148
+    return y64, w
+
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("fmt,shape", [(0, (544, 1056)), (1, (544, 1056)), (0, (45, 80)), (1, (257, 4112)),
+                                       (0, (70, 24))])
+def test_gated_parity(oracle_mod, act, fmt, shape):
+    M, N = shape
+    a = mx.binding.ACTIVATIONS[act]
+    x_bits = gated_input(M, N, seed=M + 3 * a + fmt)
+    r = mx.quantize_gated(dev(x_bits), fmt, act)
+    torch.cuda.synchronize()
+    y32 = oracle_mod.gate(x_bits, a)
+    o = oracle_mod.quantize_f32(y32, fmt)
+    y64, w = (None, None) if a in (1, 2) else gated_window(oracle_mod, x_bits, a)
+    check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, y64, w, fmt, False)
+    check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], y32, y64, w, fmt, True)
+
+
+@pytest.mark.parametrize("act", ["relu", "silu"])
+@pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
+def test_gated_single_direction(oracle_mod, act, rowwise, colwise):
+    a = mx.binding.ACTIVATIONS[act]
+    x_bits = gated_input(160, 72, seed=8)
+    r = mx.quantize_gated(dev(x_bits), 1, act, rowwise=rowwise, colwise=colwise)
+    torch.cuda.synchronize()
+    y32 = oracle_mod.gate(x_bits, a)
+    o = oracle_mod.quantize_f32(y32, 1, rowwise, colwise)
+    y64, w = (None, None) if a == 1 else gated_window(oracle_mod, x_bits, a)
+    if rowwise:
+        assert r.out_col is None
+        check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, y64, w, 1, False)
+    else:
+        assert r.out_row is None
+        check_codes(oracle_mod, r.out_col.cpu().numpy(), o[2], r.scale_col.cpu().numpy(), o[3], y32, y64, w, 1, True)
+
+
+def test_gated_noop_writes_nothing():
+    x = dev(gated_input(96, 64, seed=3))
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    outs = [torch.full((96, 64), 0x3C, **u8), torch.full((96, 2), 0x3C, **u8),
+            torch.full((96, 64), 0x3C, **u8), torch.full((3, 64), 0x3C, **u8)]
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert mx.mxfp8_quantize_gated(x, 96, 64, 0, "silu", *outs, one, None) == 0
+    torch.cuda.synchronize()
+    assert all(bool((t == 0x3C).all()) for t in outs)
+
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_gated_every_bf16_activation_input_rowwise(oracle_mod, act, fmt):
+    """Every finite BF16 value as the activation's input a (runs of 32 in bit order), each run
+    against a row of random linear inputs b, rowwise against the oracle.  |b| < 1 keeps every
+    product finite (the activations of finite inputs are finite, squared ReLU below 2^64)."""
+    a_code = mx.binding.ACTIVATIONS[act]
+    a = RUNS.copy()
+    if a_code == 2:
+        a[(a & 0x7F80) >= ((127 + 64) << 7)] = 0
+    rng = np.random.Generator(np.random.PCG64(fmt + 10 * a_code))
+    mag = rng.uniform(0.5, 1.0, a.shape) * np.exp2(-rng.integers(1, 8, a.shape))
+    b = wl.to_bf16_bits(mag * rng.choice([-1.0, 1.0], a.shape))
+    x = np.ascontiguousarray(np.concatenate([a, b], axis=1))
+    r = mx.quantize_gated(dev(x), fmt, act, rowwise=True, colwise=False)
+    torch.cuda.synchronize()
+    y32 = oracle_mod.gate(x, a_code)
+    o = oracle_mod.quantize_f32(y32, fmt, True, False)
+    y64, w = (None, None) if a_code in (1, 2) else gated_window(oracle_mod, x, a_code)
     check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, y64, w, fmt, False)
