@@ -90,6 +90,8 @@ def _load():
             lib.mxo_quantize_f32.argtypes = [f32p, i64, i64, ctypes.c_int, u8p, u8p, u8p, u8p, f32p]
             lib.mxo_activate.restype = None
             lib.mxo_activate.argtypes = [u16p, i64, ctypes.c_int, f32p]
+            lib.mxo_dgate.restype = None
+            lib.mxo_dgate.argtypes = [u16p, u16p, i64, i64, ctypes.c_int, f32p, f32p]
             lib.mxo_gate.restype = None
             lib.mxo_gate.argtypes = [u16p, i64, i64, ctypes.c_int, f32p]
             _lib = lib
@@ -253,6 +255,32 @@ def gate(x_bits: np.ndarray, act: int) -> np.ndarray:
 def quantize_gated(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True, colwise: bool = True):
     """The MXFP8 cast of act(a) * b for a gated input [M, 2N] (no dbias)."""
     return quantize_f32(gate(x_bits, act), fmt, rowwise, colwise)[:4]
+
+
+def dgate(g_bits: np.ndarray, x_bits: np.ndarray, act: int):
+    """fp32 (da, db) = (g * b * act'(a), g * act(a)) for g [M, N] and x = [a | b] [M, 2N] (mxo_dgate)."""
+    g = np.ascontiguousarray(g_bits, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, N = g.shape
+    if x.shape != (M, 2 * N):
+        raise ValueError("oracle: x must be [M, 2N] for a gradient g of [M, N]")
+    da = np.empty((M, N), np.float32)
+    db = np.empty((M, N), np.float32)
+    _load().mxo_dgate(_ptr(g, ctypes.c_uint16), _ptr(x, ctypes.c_uint16), M, N, act,
+                      _ptr(da, ctypes.c_float), _ptr(db, ctypes.c_float))
+    return da, db
+
+
+def quantize_dgated(g_bits: np.ndarray, x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True,
+                    colwise: bool = True):
+    """The MXFP8 cast of the gated input's gradient [da | db]: da and db are quantized as two
+    [M, N] tensors and laid side by side, codes [M, 2N], scale_row [M, 2 ceil(N/32)] (da's
+    blocks, then db's), scale_col [ceil(M/32), 2N]."""
+    da, db = dgate(g_bits, x_bits, act)
+    qa = quantize_f32(da, fmt, rowwise, colwise)
+    qb = quantize_f32(db, fmt, rowwise, colwise)
+    return tuple(None if u is None else np.ascontiguousarray(np.concatenate([u, v], axis=1))
+                 for u, v in zip(qa[:4], qb[:4]))
 
 
 def activation_f64(v: float, act: int) -> float:

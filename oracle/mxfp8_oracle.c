@@ -535,3 +535,23 @@ void mxo_dactivate(const uint16_t *dy, const uint16_t *x, int64_t n, int act, fl
     for (i = 0; i < n; i++)
         y[i] = (float)(mxo_bf16_to_double(dy[i]) * mxo_dactivation_f64(mxo_bf16_to_double(x[i]), act));
 }
+
+/*
+ * Backward of the gated activation (mxo_gate): for y = act(a) * b and the
+ * gradient g = dL/dy (BF16 [M, N]), the gradient of x = [a | b] is
+ *     da = g * b * act'(a),   db = g * act(a),
+ * each evaluated in double (act and act' as in mxo_activation_f64 /
+ * mxo_dactivation_f64) and rounded once to fp32.  da and db are [M, N] fp32.
+ */
+void mxo_dgate(const uint16_t *g, const uint16_t *x, int64_t M, int64_t N, int act, float *da, float *db)
+{
+    int64_t i, j;
+    for (i = 0; i < M; i++)
+        for (j = 0; j < N; j++) {
+            const double gv = mxo_bf16_to_double(g[i * N + j]);
+            const double a = mxo_bf16_to_double(x[i * 2 * N + j]);
+            const double b = mxo_bf16_to_double(x[i * 2 * N + N + j]);
+            da[i * N + j] = (float)(gv * b * mxo_dactivation_f64(a, act));
+            db[i * N + j] = (float)(gv * mxo_activation_f64(a, act));
+        }
+}

@@ -44,6 +44,8 @@ MUTATIONS = [
      "s0 += rows / MXO_BLOCK;"),
     ("gated halves swapped", "const double a = mxo_bf16_to_double(x[i * 2 * N + j]);",
      "const double a = mxo_bf16_to_double(x[i * 2 * N + N + j]);"),
+    ("gated backward's da without the derivative", "(float)(gv * b * mxo_dactivation_f64(a, act));",
+     "(float)(gv * b * mxo_activation_f64(a, act));"),
 ]
 
 

@@ -586,3 +586,58 @@ def test_quantize_gated_is_the_cast_of_the_gate(oracle_mod):
         r = oracle_mod.quantize_f32(oracle_mod.gate(x, act), 1)
         for u, v in zip(q, r[:4]):
             assert np.array_equal(u, v)
+
+
+@pytest.mark.parametrize("act", [1, 2, 3, 4, 5])
+def test_dgate_matches_torch_autograd(oracle_mod, act):
+    """(da, db) of y = act(a) * b against torch autograd in float64 (the library's own derivative)."""
+    import torch.nn.functional as F
+    N = 40
+    x = structured_input(32, 2 * N, seed=40 + act)
+    g = structured_input(32, N, seed=50 + act)
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    gv = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    a = xv[:, :N].clone().requires_grad_(True)
+    b = xv[:, N:].clone().requires_grad_(True)
+    if act == 1:
+        ya = torch.relu(a)
+    elif act == 2:
+        ya = torch.relu(a) ** 2
+    elif act == 3:
+        ya = F.gelu(a, approximate="tanh")
+    elif act == 4:
+        ya = F.silu(a)
+    else:
+        ya = a * torch.sigmoid(1.702 * a)
+    (ya * b).backward(gv)
+    da, db = oracle_mod.dgate(g, x, act)
+    # one fp32 rounding on the oracle's side; torch's tanh-form GeLU derivative cancels for a << 0,
+    # which the 1e-12 |g| (|b| + 1) slack covers (as in the derivative's own pin above)
+    slack = 1e-12 * np.abs(gv.numpy()) * (np.abs(xv[:, N:].numpy()) + 1) + 1e-38
+    for got, want in ((da, a.grad.numpy()), (db, b.grad.numpy())):
+        if act in (1, 2):
+            assert np.array_equal(got.astype(np.float64), want.astype(np.float32).astype(np.float64))
+        else:
+            assert np.all(np.abs(got.astype(np.float64) - want) <= 2 ** -23 * np.abs(want) + slack)
+
+
+def test_dgate_hand_worked_and_layout(oracle_mod):
+    # ReGLU: a = [-2, 3], b = [5, -4], g = [1, 2]: da = g b relu'(a) = [0, -8], db = g relu(a) = [0, 6]
+    x = wl.to_bf16_bits(np.array([[-2.0, 3.0, 5.0, -4.0]]))
+    g = wl.to_bf16_bits(np.array([[1.0, 2.0]]))
+    da, db = oracle_mod.dgate(g, x, 1)
+    assert da.tolist() == [[0.0, -8.0]] and db.tolist() == [[0.0, 6.0]]
+    # N a multiple of 32: [da | db] quantized as one [M, 2N] tensor; otherwise side by side
+    for N in (64, 40):
+        xs = structured_input(64, 2 * N, seed=N)
+        gs = structured_input(64, N, seed=N + 1)
+        q = oracle_mod.quantize_dgated(gs, xs, 1, 4)
+        da, db = oracle_mod.dgate(gs, xs, 4)
+        both = oracle_mod.quantize_f32(np.concatenate([da, db], axis=1), 1)
+        assert q[0].shape == (64, 2 * N) and q[1].shape == (64, 2 * -(-N // 32)) and q[3].shape == (2, 2 * N)
+        if N % 32 == 0:
+            for u, v in zip(q, both[:4]):
+                assert np.array_equal(u, v)
+        else:
+            qa = oracle_mod.quantize_f32(da, 1)
+            assert np.array_equal(q[1][:, :2], qa[1]) and np.array_equal(q[0][:, :N], qa[0])
