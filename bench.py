@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # Every source the kernels are built from: a committed ncu traffic figure is only reported
 # while these are unchanged since it was taken.
 KERNEL_SOURCES = [f"mxfp8_block_scaled_04_gb300/csrc/{f}"
-                  for f in ("api.cu", "dact.cuh", "dbias_reduce.cuh", "ptx.cuh", "quantize.cuh")]
+                  for f in ("api.cu", "dact.cuh", "dbias_reduce.cuh", "dgated.cuh", "ptx.cuh", "quantize.cuh")]
 
 
 def parse_args():
@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--glu", default="none",
                     help="gated activation act(a) * b before the cast: x = [a | b] with a = the workload and "
                          "b = N(0,1) of the same shape (relu, srelu, gelu, silu = SwiGLU, qgelu)")
+    ap.add_argument("--dglu", default="none",
+                    help="gated backward: quantize [g b act'(a) | g act(a)] with g = the workload and "
+                         "x = [a | b] two N(0,1) matrices of its shape (relu, srelu, gelu, silu, qgelu)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -120,10 +123,11 @@ def profile_name(args, M, N, workload_dbias):
     """Name of the committed ncu summary (profiles/<name>.md) for this run's kernel, workload and options."""
     name = args.workload if not args.shape else f"{args.workload.split('_')[0]}_{M}x{N}"
     family = ("quantize_dact" if args.dact.lower() != "none" else
-              "quantize_gated" if args.glu.lower() != "none" else "quantize")
+              "quantize_gated" if args.glu.lower() != "none" else
+              "quantize_dgated" if args.dglu.lower() != "none" else "quantize")
     opts = [o for o, on in (("swizzled", args.swizzled), ("amax", args.amax),
                             ("dbias", args.dbias and not workload_dbias)) if on]
-    opts += [a.lower() for a in (args.act, args.dact, args.glu) if a.lower() != "none"]
+    opts += [a.lower() for a in (args.act, args.dact, args.glu, args.dglu) if a.lower() != "none"]
     return "_".join([family, name] + opts)
 
 
@@ -362,11 +366,13 @@ def run_ours(args):
     M, N = x_bits.shape
     grouped = offsets is not None
     x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    out_row = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    dglu = mx.binding.ACTIVATIONS[args.dglu.lower()]
+    W = 2 if dglu else 1    # the gated backward writes [da | db]: outputs of width 2N
+    out_row = torch.empty((M, W * N), dtype=torch.uint8, device="cuda")
     layout = mx.SCALES_SWIZZLED if args.swizzled else mx.SCALES_PLAIN
-    scale_row = torch.empty((mx.mxfp8_scale_bytes(M, N // 32, layout),), dtype=torch.uint8, device="cuda")
-    out_col = torch.empty((M, N), dtype=torch.uint8, device="cuda")
-    scale_col = torch.empty((mx.mxfp8_scale_bytes(N, M // 32, layout),), dtype=torch.uint8, device="cuda")
+    scale_row = torch.empty((mx.mxfp8_scale_bytes(M, W * (N // 32), layout),), dtype=torch.uint8, device="cuda")
+    out_col = torch.empty((M, W * N), dtype=torch.uint8, device="cuda")
+    scale_col = torch.empty((mx.mxfp8_scale_bytes(W * N, M // 32, layout),), dtype=torch.uint8, device="cuda")
     amax = torch.empty((1,), dtype=torch.float32, device="cuda") if args.amax else None
     act = mx.binding.ACTIVATIONS[args.act.lower()]
     dact = mx.binding.ACTIVATIONS[args.dact.lower()]
@@ -376,6 +382,13 @@ def run_ours(args):
              if dact else None)
     glu = mx.binding.ACTIVATIONS[args.glu.lower()]
     x_in_bits = x_bits
+    x_gate = None
+    if dglu:
+        if act or dact or glu or args.swizzled or args.amax or grouped or with_dbias:
+            raise SystemExit("--dglu takes a flat workload without dbias or other options")
+        xg_bits = np.ascontiguousarray(np.concatenate([wl.normal_bf16(M, N, seed=1234),
+                                                       wl.normal_bf16(M, N, seed=4321)], axis=1))
+        x_gate = torch.from_numpy(xg_bits.view(np.int16)).view(torch.bfloat16).cuda()
     if glu:
         if act or dact or args.swizzled or args.amax or grouped or with_dbias:
             raise SystemExit("--glu takes a flat workload without dbias or other options")
@@ -405,6 +418,9 @@ def run_ours(args):
                                         dbias, ws, None, stream)
         elif glu:
             st = mx.mxfp8_quantize_gated(xin, M, N, fmt, glu, out_row, scale_row, out_col, scale_col, None, stream)
+        elif dglu:
+            st = mx.mxfp8_quantize_dgated(xin, x_gate, M, N, fmt, dglu, out_row, scale_row, out_col, scale_col,
+                                          None, stream)
         elif args.swizzled or args.amax or act:
             cfg = mx.make_config(xin, M, N, fmt, out_row, scale_row, out_col, scale_col, dbias, ws, None,
                                  layout, amax, act)
@@ -415,9 +431,10 @@ def run_ours(args):
         if st != 0:
             raise mx.MXFP8Error(st, "bench step")
 
-    algo_bytes = (BYTES_PER_ELEM + (2 if dact or glu else 0)) * M * N + (4 * N * max(G, 1) if with_dbias else 0)
+    algo_bytes = ((BYTES_PER_ELEM + (2 if dact or glu else 0)) * M * N if not dglu else
+                  (3 * 2 + 2 * (1 + 1 + 1 / 16)) * M * N) + (4 * N * max(G, 1) if with_dbias else 0)
     prof = profile_name(args, M, N, w["with_dbias"])
-    kernels = (["amax_init_kernel"] if args.amax else []) + ["quantize_dact_kernel" if dact or glu else "quantize_kernel"]
+    kernels = (["amax_init_kernel"] if args.amax else []) + ["quantize_dact_kernel" if dact or glu else "quantize_dgated_kernel" if dglu else "quantize_kernel"]
     if with_dbias:
         kernels.append("dbias_reduce_grouped_kernel" if grouped else "dbias_reduce_kernel")
     uuid = None
@@ -518,7 +535,7 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped or args.swizzled or args.amax or act or dact or glu:
+        if grouped or args.swizzled or args.amax or act or dact or glu or dglu:
             # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
             path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"
@@ -575,7 +592,7 @@ def run_ours(args):
             "config": {"workload": args.workload + (f"@{M}x{N}" if args.shape else ""), "M": M, "N": N, "fmt": "e4m3" if fmt == 0 else "e5m2",
                        "directions": "rowwise+colwise", "dbias": with_dbias, "grouped": grouped,
                        "scales": "swizzled" if args.swizzled else "plain", "amax": bool(args.amax),
-                       "activation": args.act.lower(), "dact": args.dact.lower(), "glu": args.glu.lower(),
+                       "activation": args.act.lower(), "dact": args.dact.lower(), "glu": args.glu.lower(), "dglu": args.dglu.lower(),
                        "bytes_per_step": algo_bytes,
                        "l2": (f"L2 flushed (256 MiB written) before each timed step; {M * N * 2 / 1e6:.0f} MB "
                               f"bf16 input; time = sum of the per-step event intervals" if flush else

@@ -326,6 +326,30 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
                                     const float *noop, void *stream);
 
 /*
+ * Backward of the gated activation (mxfp8_quantize_gated): for y = act(a) * b
+ * and its gradient g, the cast of the gradient of x = [a | b]:
+ *     da = g * b * act'(a),   db = g * act(a)     (fp32, act' as for
+ *                                                  mxfp8_quantize_dact)
+ * da and db are quantized as two [M, N] tensors laid side by side (this
+ * library's reading; the pages do not define the gated forms):
+ *   grad        device bf16 [M, N], 16-byte aligned.
+ *   x           device bf16 [M, 2N] = [a | b], 16-byte aligned.
+ *   out_row     uint8 [M, 2N]: da's codes in columns 0..N-1, db's in N..2N-1
+ *               (block = 1x32 along a row within one half).
+ *   scale_row   uint8 [M, 2 ceil(N/32)]: da's ceil(N/32) blocks, then db's.
+ *   out_col     uint8 [M, 2N], scale_col uint8 [ceil(M/32), 2N] (columns as
+ *               in out_col).
+ *   Either direction may be NULL; noop and stream as for mxfp8_quantize.
+ * With N a multiple of 32 the result is the cast of [da | db] as one [M, 2N]
+ * tensor.  M >= 0, N a multiple of 8 below 2^30.  Status codes as for
+ * mxfp8_quantize_dact.
+ */
+mxfp8_status_t mxfp8_quantize_dgated(const void *grad, const void *x, int64_t M, int64_t N, int fp8_fmt,
+                                     int activation, void *out_row, void *scale_row,
+                                     void *out_col, void *scale_col,
+                                     const float *noop, void *stream);
+
+/*
  * Workspace bytes for mxfp8_quantize_grouped_dbias: a header of
  * (num_groups + 1) int64 (each group's first row tile) padded to 256 bytes,
  * then one fp32 partial row per 128-row tile, tiles never spanning two

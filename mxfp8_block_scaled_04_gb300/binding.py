@@ -82,6 +82,8 @@ def lib():
             L.mxfp8_quantize_dact.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_gated.restype = i32
             L.mxfp8_quantize_gated.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_dgated.restype = i32
+            L.mxfp8_quantize_dgated.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
@@ -174,6 +176,16 @@ def mxfp8_quantize_gated(x, M, N, fp8_fmt, activation, out_row, scale_row, out_c
     return int(lib().mxfp8_quantize_gated(_addr(x), M, N, fp8_fmt, int(activation), _addr(out_row),
                                           _addr(scale_row), _addr(out_col), _addr(scale_col), _addr(noop),
                                           _stream(stream)))
+
+
+def mxfp8_quantize_dgated(grad, x, M, N, fp8_fmt, activation, out_row, scale_row, out_col, scale_col,
+                          noop=None, stream=None) -> int:
+    """The cast of [g b act'(a) | g act(a)] for x = [a | b]; see include/mxfp8.h."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_dgated(_addr(grad), _addr(x), M, N, fp8_fmt, int(activation), _addr(out_row),
+                                           _addr(scale_row), _addr(out_col), _addr(scale_col), _addr(noop),
+                                           _stream(stream)))
 
 
 def mxfp8_quantize_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
@@ -375,6 +387,31 @@ def quantize_gated(x: torch.Tensor, fmt=E4M3, activation="silu", rowwise: bool =
     st = mxfp8_quantize_gated(x, M, N, _fmt(fmt), activation, out_row, scale_row, out_col, scale_col, noop, stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_gated")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
+
+
+def quantize_dgated(grad: torch.Tensor, x: torch.Tensor, fmt=E5M2, activation="silu", rowwise: bool = True,
+                    colwise: bool = True, noop: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+    """The cast of the gradient of x = [a | b] for y = act(a) * b, given grad = dL/dy [M, N].
+
+    Returns codes [M, 2N] (da | db), scale_row [M, 2 ceil(N/32)] (da's blocks, then db's),
+    scale_col [ceil(M/32), 2N].
+    """
+    for t in (grad, x):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("grad and x must be contiguous 2-D torch.bfloat16 tensors")
+    M, N = grad.shape
+    if x.shape != (M, 2 * N):
+        raise ValueError("x must be [M, 2N] for grad of shape [M, N]")
+    u8 = dict(dtype=torch.uint8, device=grad.device)
+    out_row = torch.empty((M, 2 * N), **u8) if rowwise else None
+    scale_row = torch.empty((M, 2 * (-(-N // BLOCK))), **u8) if rowwise else None
+    out_col = torch.empty((M, 2 * N), **u8) if colwise else None
+    scale_col = torch.empty((-(-M // BLOCK), 2 * N), **u8) if colwise else None
+    st = mxfp8_quantize_dgated(grad, x, M, N, _fmt(fmt), activation, out_row, scale_row, out_col, scale_col,
+                               noop, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_dgated")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
 
 

@@ -17,6 +17,7 @@
 #include "../../include/mxfp8.h"
 #include "dact.cuh"
 #include "dbias_reduce.cuh"
+#include "dgated.cuh"
 #include "quantize.cuh"
 
 namespace {
@@ -56,6 +57,7 @@ struct DeviceInfo {
     int sm_count = 0;
     int ctas_per_sm[192] = {};  // indexed by kernel variant
     int dact_ctas_per_sm[48] = {};  // two-input kernels: FMT + 2 * DBIAS + 4 * ACT + 24 * GATED
+    int dgated_ctas_per_sm[12] = {};  // gated backward: FMT + 2 * ACT
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -273,6 +275,50 @@ mxfp8_status_t launch_gated(int fmt, int device, const CUtensorMap &map_b, const
 {
     return fmt == MXFP8_E4M3 ? launch_dact_fmt<0, false, ACT, true>(device, map_b, map_a, p, tiles, stream)
                              : launch_dact_fmt<1, false, ACT, true>(device, map_b, map_a, p, tiles, stream);
+}
+
+// The gated backward kernel: one-time set-up per (device, variant), then launch.
+template <int FMT, int ACT>
+mxfp8_status_t launch_dgated_fmt(int device, const CUtensorMap &map_g, const CUtensorMap &map_a,
+                                 const CUtensorMap &map_b, const QuantParams &p, int64_t tiles, cudaStream_t stream)
+{
+    int cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (device < 0 || device >= kMaxDevices)
+            return MXFP8_ERR_DEVICE;
+        DeviceInfo &d = g_dev[device];
+        if (!d.ready) {
+            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+                cudaGetLastError();
+                return MXFP8_ERR_DEVICE;
+            }
+            d.ready = true;
+        }
+        const int v = FMT + 2 * ACT;
+        if (d.dgated_ctas_per_sm[v] == 0) {
+            auto kern = quantize_dgated_kernel<FMT, ACT>;
+            int n = 0;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDgated) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDgated) != cudaSuccess ||
+                n < 1) {
+                cudaGetLastError();
+                return MXFP8_ERR_LAUNCH;
+            }
+            d.dgated_ctas_per_sm[v] = n;
+        }
+        cap = d.dgated_ctas_per_sm[v] * d.sm_count;
+    }
+    const int grid = static_cast<int>(tiles < cap ? tiles : cap);
+    return launch_pdl(quantize_dgated_kernel<FMT, ACT>, grid, kThreads, kSmemDgated, stream, map_g, map_a, map_b, p);
+}
+
+template <int ACT>
+mxfp8_status_t launch_dgated(int fmt, int device, const CUtensorMap &map_g, const CUtensorMap &map_a,
+                             const CUtensorMap &map_b, const QuantParams &p, int64_t tiles, cudaStream_t stream)
+{
+    return fmt == MXFP8_E4M3 ? launch_dgated_fmt<0, ACT>(device, map_g, map_a, map_b, p, tiles, stream)
+                             : launch_dgated_fmt<1, ACT>(device, map_g, map_a, map_b, p, tiles, stream);
 }
 
 // Activated (ACT != 0) variants: flat, no dbias; swizzle and amax as template switches.
@@ -709,6 +755,65 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
     case MXFP8_ACT_GELU: return launch_gated<3>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     case MXFP8_ACT_SILU: return launch_gated<4>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     default: return launch_gated<5>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    }
+}
+
+mxfp8_status_t mxfp8_quantize_dgated(const void *grad, const void *x, int64_t M, int64_t N, int fp8_fmt,
+                                     int activation, void *out_row, void *scale_row, void *out_col,
+                                     void *scale_col, const float *noop, void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (M < 0 || N < 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 30))
+        return MXFP8_ERR_SHAPE;
+    const bool empty = M == 0 || N == 0;
+    mxfp8_status_t st;
+    if (!empty) {
+        if (grad == nullptr || x == nullptr)
+            return MXFP8_ERR_NULL;
+        if ((st = check_outputs(out_row, scale_row, out_col, scale_col)) != MXFP8_OK)
+            return st;
+    }
+    if (!aligned(grad, 16) || !aligned(x, 16))
+        return MXFP8_ERR_ALIGN;
+    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kDBN - 1) / kDBN;
+    if (row_tiles * col_tiles >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(grad, device) || !on_device(x, device) || !on_device(out_row, device) ||
+        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
+        !on_device(noop, device))
+        return MXFP8_ERR_DEVICE;
+    if (empty)
+        return MXFP8_OK;
+    CUtensorMap map_g, map_a, map_b;
+    const void *b = static_cast<const uint16_t *>(x) + N;  // 16-byte aligned: N is a multiple of 8
+    if ((st = make_tensor_map(&map_g, grad, M, N)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_a, x, M, N, 2 * N)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_b, b, M, N, 2 * N)) != MXFP8_OK)
+        return st;
+    QuantParams p{};
+    p.out_row = static_cast<uint8_t *>(out_row);
+    p.scale_row = static_cast<uint8_t *>(scale_row);
+    p.out_col = static_cast<uint8_t *>(out_col);
+    p.scale_col = static_cast<uint8_t *>(scale_col);
+    p.noop = noop;
+    p.M = M;
+    p.N = N;
+    p.row_tiles = static_cast<int>(row_tiles);
+    p.col_tiles = static_cast<int>(col_tiles);
+    const int64_t tiles = row_tiles * col_tiles;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    switch (activation) {
+    case MXFP8_ACT_RELU: return launch_dgated<1>(fp8_fmt, device, map_g, map_a, map_b, p, tiles, stream);
+    case MXFP8_ACT_SRELU: return launch_dgated<2>(fp8_fmt, device, map_g, map_a, map_b, p, tiles, stream);
+    case MXFP8_ACT_GELU: return launch_dgated<3>(fp8_fmt, device, map_g, map_a, map_b, p, tiles, stream);
+    case MXFP8_ACT_SILU: return launch_dgated<4>(fp8_fmt, device, map_g, map_a, map_b, p, tiles, stream);
+    default: return launch_dgated<5>(fp8_fmt, device, map_g, map_a, map_b, p, tiles, stream);
     }
 }
 

@@ -232,6 +232,22 @@ def test_gated_host_checks(cuda_lib):
         mx.quantize_gated(torch.zeros(4, 6, dtype=torch.bfloat16)[:, :5].contiguous())
 
 
+def test_dgated_host_checks(cuda_lib):
+    def dg(**kw):
+        a = dict(g=A, x=A, M=64, N=64, fmt=1, act=4, orow=A, srow=A, ocol=A, scol=A)
+        a.update(kw)
+        return mx.mxfp8_quantize_dgated(a["g"], a["x"], a["M"], a["N"], a["fmt"], a["act"], a["orow"], a["srow"],
+                                        a["ocol"], a["scol"], None, 0)
+    assert dg(act=0) == FORMAT and dg(act=6) == FORMAT and dg(fmt=2) == FORMAT
+    assert dg(N=36) == SHAPE and dg(M=-1) == SHAPE and dg(N=1 << 30) == SHAPE
+    assert dg(g=None) == NULL and dg(x=None) == NULL and dg(scol=None) == NULL
+    assert dg(g=A + 8) == ALIGN and dg(x=A + 8) == ALIGN and dg(orow=A + 8) == ALIGN
+    assert dg() == DEVICE and dg(N=40) == DEVICE
+    import torch
+    with pytest.raises(ValueError):
+        mx.quantize_dgated(torch.zeros(4, 8, dtype=torch.bfloat16), torch.zeros(4, 8, dtype=torch.bfloat16))
+
+
 def test_selftest_bounded_wait_rejections(cuda_lib):
     assert mx.mxfp8_selftest_bounded_wait(1_000_000, None) == NULL
     assert mx.mxfp8_selftest_bounded_wait(0, A) == SHAPE

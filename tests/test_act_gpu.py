@@ -391,3 +391,59 @@ def test_gated_every_bf16_activation_input_rowwise(oracle_mod, act, fmt):
     o = oracle_mod.quantize_f32(y32, fmt, True, False)
     y64, w = (None, None) if a_code in (1, 2) else gated_window(oracle_mod, x, a_code)
     check_codes(oracle_mod, r.out_row.cpu().numpy(), o[0], r.scale_row.cpu().numpy(), o[1], y32, y64, w, fmt, False)
+
+
+# ---- gated backward: [g b act'(a) | g act(a)] --------------------------------------------
+
+def dgated_windows(oracle_mod, g_bits, x_bits, a):
+    """(exact da, window), (exact db, window): the derivative's and the activation's windows scaled
+    by |g b| and |g| (g b is exact in fp32), plus one fp32 rounding on each side."""
+    N = g_bits.shape[1]
+    gv, av, bv = x_values(g_bits), x_values(x_bits[:, :N]), x_values(x_bits[:, N:])
+    dact64 = np.vectorize(lambda v: oracle_mod.dactivation_f64(v, a))(av)
+    act64 = np.vectorize(lambda v: oracle_mod.activation_f64(v, a))(av)
+    da64, db64 = gv * bv * dact64, gv * act64
+    wa = np.abs(gv * bv) * (DELTA * derivative_terms(av, a) + SUB) + ROUND * np.abs(da64) + 2.0 ** -148
+    wb = np.abs(gv) * (DELTA * forward_cond(av, a) * np.abs(act64) + SUB) + ROUND * np.abs(db64) + 2.0 ** -148
+    return (da64, wa), (db64, wb)
+
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("fmt,shape", [(1, (544, 1056)), (0, (45, 80)), (1, (257, 1032)), (0, (70, 24))])
+def test_dgated_parity(oracle_mod, act, fmt, shape):
+    M, N = shape
+    a = mx.binding.ACTIVATIONS[act]
+    g_bits = wl.grad_bf16(M, N, seed=M + 7 * a)
+    x_bits = gated_input(M, N, seed=N + a + fmt)
+    r = mx.quantize_dgated(dev(g_bits), dev(x_bits), fmt, act)
+    torch.cuda.synchronize()
+    da32, db32 = oracle_mod.dgate(g_bits, x_bits, a)
+    Cn = -(-N // 32)
+    wins = (None, None) if a in (1, 2) else dgated_windows(oracle_mod, g_bits, x_bits, a)
+    for h, y32 in enumerate((da32, db32)):
+        o = oracle_mod.quantize_f32(y32, fmt)
+        y64, w = (None, None) if wins[0] is None else wins[h]
+        cs, ss = slice(h * N, (h + 1) * N), slice(h * Cn, (h + 1) * Cn)
+        check_codes(oracle_mod, r.out_row.cpu().numpy()[:, cs], o[0], r.scale_row.cpu().numpy()[:, ss], o[1],
+                    y32, y64, w, fmt, False)
+        check_codes(oracle_mod, r.out_col.cpu().numpy()[:, cs], o[2], r.scale_col.cpu().numpy()[:, cs], o[3],
+                    y32, y64, w, fmt, True)
+
+
+def test_dgated_matches_oracle_layout_and_noop(oracle_mod):
+    """ReGLU (exact): the whole [M, 2N] outputs against the oracle's side-by-side layout; noop = 1
+    writes nothing."""
+    M, N = 96, 72
+    g_bits = wl.grad_bf16(M, N, seed=3)
+    x_bits = gated_input(M, N, seed=4)
+    r = mx.quantize_dgated(dev(g_bits), dev(x_bits), 1, "relu")
+    torch.cuda.synchronize()
+    for got, want in zip(r[:4], oracle_mod.quantize_dgated(g_bits, x_bits, 1, 1)):
+        assert np.array_equal(got.cpu().numpy(), want)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    outs = [torch.full((M, 2 * N), 0x3C, **u8), torch.full((M, 6), 0x3C, **u8),
+            torch.full((M, 2 * N), 0x3C, **u8), torch.full((3, 2 * N), 0x3C, **u8)]
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert mx.mxfp8_quantize_dgated(dev(g_bits), dev(x_bits), M, N, 1, "silu", *outs, one, None) == 0
+    torch.cuda.synchronize()
+    assert all(bool((t == 0x3C).all()) for t in outs)

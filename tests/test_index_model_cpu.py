@@ -325,6 +325,54 @@ def test_backward_fusion_writes_every_byte_once(shape):
         model_dact(*shape, grid=304, reuse=reuse)
 
 
+def model_dgated(M, N, grid):
+    """quantize_dgated_kernel: da and db side by side in [M, 2N] codes, [M, 2 ceil(N/32)] row scales,
+    [ceil(M/32), 2N] column scales; the stage holds three boxes (g, a, b) of 16 KiB."""
+    rows16 = N % 16 == 0
+    N2, Cn = 2 * N, -(-N // 32)
+    out_row, out_col = Plane("out_row", M * N2), Plane("out_col", M * N2)
+    scale_row, scale_col = Plane("scale_row", M * 2 * Cn), Plane("scale_col", -(-M // 32) * N2)
+    row_tiles, col_tiles = -(-M // BM), -(-N // DBN)
+    tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN) for rt in range(row_tiles) for ct in range(col_tiles)]
+    tid = np.arange(THREADS)
+    rb1, c1 = tid >> 6, tid & 63
+    w2 = np.repeat(np.arange(8), 2 * 32)
+    k2 = np.tile(np.repeat(np.arange(2), 32), 8)
+    l2 = np.tile(LANES, 16)
+    rg2, rr2, sp2 = 2 * w2 + k2, l2 >> 2, l2 & 3
+    for b in range(grid):
+        for t in range(b, len(tiles), grid):
+            row0, row_end, col0 = tiles[t]
+            assert (col0 * 2) % 16 == 0 and col0 < N and row0 < M
+            # the a and b maps: bases x and x + 2N bytes, pitch 4N bytes, both 16-byte multiples
+            assert (2 * N) % 16 == 0 and (4 * N) % 16 == 0
+            grow, gcol = row0 + rb1 * 32, col0 + c1
+            sel = (grow < row_end) & (gcol < N)
+            for out in range(2):
+                scale_col.write((grow[sel] >> 5) * N2 + out * N + gcol[sel])
+            grow, gcol = row0 + rg2 * 8 + rr2, col0 + sp2 * 16
+            # phase 2 rows stay in the box; the b box is the last 16 KiB of the 48 KiB stage
+            assert np.all(rg2 * 8 + rr2 < 128) and np.all(2 * 16384 + (rg2 * 8 + rr2) * 128 + 127 < 3 * 16384)
+            ok = (row0 + rg2 * 8 < row_end) & (grow < row_end) & (gcol < N)
+            half_seg = gcol + 16 > N
+            full, part = ok & ~half_seg, ok & half_seg
+            for plane in (out_row, out_col):
+                for out in range(2):
+                    plane.write(grow[full] * N2 + out * N + gcol[full], 16, align=16 if rows16 else 8)
+                    plane.write(grow[part] * N2 + out * N + gcol[part], 8, align=8)
+            se = ok & (sp2 % 2 == 0)
+            for out in range(2):
+                scale_row.write(grow[se] * 2 * Cn + out * Cn + (gcol[se] >> 5))
+    for p in (out_row, out_col, scale_row, scale_col):
+        p.once()
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (70, 24), (257, 1032), (130, 144), (256, 64), (33, 8)])
+def test_gated_backward_writes_every_byte_once(shape):
+    model_dgated(*shape, grid=5)
+    model_dgated(*shape, grid=304)
+
+
 def grouped_reduce_reads(hdr, N):
     """dbias_reduce_grouped_kernel: the partial rows each (group, column) sums, for one CTA of 32
     columns, following its 16 contiguous warp ranges and the head / tail hand-over."""
