@@ -460,7 +460,7 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
         const unsigned blocks = static_cast<unsigned>((N + kReduceCols - 1) / kReduceCols);
         const float *partials = ws + grouped_header_floats(num_groups);
         const int64_t *hdr = reinterpret_cast<const int64_t *>(ws);
-        st = launch_pdl(dbias_reduce_grouped_kernel, blocks, kReduceCols * kReduceWarps, 0, stream, partials, hdr,
+        st = launch_pdl(dbias_reduce_grouped_kernel, blocks, kReduceCols * kGReduceWarps, 0, stream, partials, hdr,
                         num_groups, N, dbias, noop);
         if (st != MXFP8_OK)
             return st;

@@ -21,6 +21,14 @@ namespace mxfp8 {
 
 constexpr int kReduceCols = 32;
 constexpr int kReduceWarps = 16;
+#ifndef MXFP8_GREDUCE_WARPS
+#define MXFP8_GREDUCE_WARPS 16
+#endif
+#ifndef MXFP8_GREDUCE_INFLIGHT
+#define MXFP8_GREDUCE_INFLIGHT 16
+#endif
+constexpr int kGReduceWarps = MXFP8_GREDUCE_WARPS;        // grouped reduce: warps per 32-column CTA
+constexpr int kGReduceInflight = MXFP8_GREDUCE_INFLIGHT;  // grouped reduce: tile loads in flight per warp
 
 __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     dbias_reduce_kernel(const float *__restrict__ ws, int64_t row_tiles, int64_t N, float *__restrict__ dbias,
@@ -56,12 +64,13 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
 //
 // One CTA owns 32 columns of every group.  Its 16 warps split the T row tiles
 // into contiguous ranges [T w / 16, T (w + 1) / 16); a warp sums the tiles of
-// each group inside its range in tile order.  A group that lies wholly inside
+// each group inside its range in tile order, with 16 tiles' loads in flight
+// (8 measured 0.5% slower on the whole 64-expert call; 32 warps no better).  A group that lies wholly inside
 // one range is written by that warp; the partial sums of a group that crosses
 // ranges are left in shared memory, and the warp holding the group's last
 // tile adds them in warp order.  The order of every sum depends only on T and
 // hdr, so the result does not depend on scheduling.  Empty groups get zeros.
-__global__ void __launch_bounds__(kReduceCols * kReduceWarps)
+__global__ void __launch_bounds__(kReduceCols * kGReduceWarps)
     dbias_reduce_grouped_kernel(const float *__restrict__ ws, const int64_t *__restrict__ hdr, int num_groups,
                                 int64_t N, float *__restrict__ dbias, const float *noop)
 {
@@ -71,8 +80,8 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     if (hdr[0] < 0)
         return;
     __shared__ int64_t first[kMaxGroups + 1];
-    __shared__ float head[kReduceWarps][kReduceCols];  // partial of a group that began in an earlier range
-    __shared__ float tail[kReduceWarps][kReduceCols];  // partial of a group that goes on into a later range
+    __shared__ float head[kGReduceWarps][kReduceCols];  // partial of a group that began in an earlier range
+    __shared__ float tail[kGReduceWarps][kReduceCols];  // partial of a group that goes on into a later range
     const int G = num_groups;
     for (int i = threadIdx.x; i <= G; i += blockDim.x)
         first[i] = hdr[i];
@@ -80,9 +89,9 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kReduceCols + lane;
     const int64_t T = first[G];
-    const int64_t a = T * warp / kReduceWarps, b = T * (warp + 1) / kReduceWarps;
+    const int64_t a = T * warp / kGReduceWarps, b = T * (warp + 1) / kGReduceWarps;
 
-    for (int g = warp; g < G; g += kReduceWarps)
+    for (int g = warp; g < G; g += kGReduceWarps)
         if (first[g] == first[g + 1] && j < N)
             dbias[static_cast<int64_t>(g) * N + j] = 0.f;
 
@@ -110,14 +119,14 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
         int g = g0;
         int64_t gend = first[g + 1];
         float acc = 0.f;
-        // 8 tiles' loads in flight at a time, whatever the group boundaries
-        for (int64_t t0 = a; t0 < b; t0 += 8) {
-            float v[8];
+        // kGReduceInflight tiles' loads in flight at a time, whatever the group boundaries
+        for (int64_t t0 = a; t0 < b; t0 += kGReduceInflight) {
+            float v[kGReduceInflight];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < kGReduceInflight; ++k)
                 v[k] = (t0 + k < b && j < N) ? ws[(t0 + k) * N + j] : 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < kGReduceInflight; ++k) {
                 const int64_t t = t0 + k;
                 if (t < b) {
                     if (t == gend) {  // warp-uniform: tile t starts the next non-empty group
@@ -138,11 +147,11 @@ __global__ void __launch_bounds__(kReduceCols * kReduceWarps)
     // a group that began before this range and ends inside it: add the partials in warp order
     if (a < b && first[g0] < a && first[g0 + 1] <= b) {
         int w1 = warp - 1;  // the range holding the group's first tile
-        while (w1 > 0 && T * w1 / kReduceWarps > first[g0])
+        while (w1 > 0 && T * w1 / kGReduceWarps > first[g0])
             --w1;
         float s = tail[w1][lane];
         for (int w = w1 + 1; w < warp; ++w)
-            if (T * w / kReduceWarps < T * (w + 1) / kReduceWarps)
+            if (T * w / kGReduceWarps < T * (w + 1) / kGReduceWarps)
                 s += head[w][lane];
         s += head[warp][lane];
         if (j < N)
