@@ -82,3 +82,25 @@ def test_graph_grouped(oracle_mod):
               x, new)
     for g, w in zip(o, oracle_mod.quantize_grouped(new, off_np, mx.E4M3)):
         assert np.array_equal(g.cpu().numpy(), w)
+
+
+def test_graph_gated_and_its_backward(oracle_mod):
+    M, N = 160, 96
+    x = bf16(np.concatenate([wl.normal_bf16(M, N, seed=5), wl.normal_bf16(M, N, seed=6)], axis=1)).cuda()
+    g = bf16(wl.grad_bf16(M, N, seed=7)).cuda()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    o = [torch.empty((M, N), **u8), torch.empty((M, N // 32), **u8), torch.empty((M, N), **u8),
+         torch.empty((M // 32, N), **u8)]
+    od = [torch.empty((M, 2 * N), **u8), torch.empty((M, 2 * N // 32), **u8), torch.empty((M, 2 * N), **u8),
+          torch.empty((M // 32, 2 * N), **u8)]
+    new = np.concatenate([wl.normal_bf16(M, N, seed=8), wl.normal_bf16(M, N, seed=9)], axis=1)
+
+    def both(s):   # ReGLU and its backward: exact, so bytes must match the oracle
+        st = mx.mxfp8_quantize_gated(x, M, N, mx.E4M3, "relu", *o, None, s)
+        return st or mx.mxfp8_quantize_dgated(g, x, M, N, mx.E5M2, "relu", *od, None, s)
+    run_graph(both, x, new)
+    for got, want in zip(o, oracle_mod.quantize_gated(new, mx.E4M3, 1)):
+        assert np.array_equal(got.cpu().numpy(), want)
+    g_bits = g.cpu().view(torch.int16).numpy().view(np.uint16)
+    for got, want in zip(od, oracle_mod.quantize_dgated(g_bits, new, mx.E5M2, 1)):
+        assert np.array_equal(got.cpu().numpy(), want)

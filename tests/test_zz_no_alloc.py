@@ -119,3 +119,28 @@ def test_noalloc_noop_writes_nothing():
     assert mx.mxfp8_quantize_dbias_noalloc(x, M, N, mx.E5M2, *o[:4], o[4], zero, None) == 0
     torch.cuda.synchronize()
     assert not all(bool((t == 0x11).all()) for t in o[:4]) and not bool((o[4] == 7.0).all())
+
+
+def test_noalloc_inside_a_captured_graph(oracle_mod):
+    """A first call outside capture, then the call captured and replayed on new input: the
+    replayed launches use the static workspace and the live buffers."""
+    M, N = 1056, 512
+    x = torch.from_numpy(wl.grad_bf16(M, N, seed=600).view(np.int16)).view(torch.bfloat16).cuda()
+    o = outputs(M, N)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert binding.mxfp8_quantize_dbias_noalloc(x, M, N, mx.E5M2, *o[:4], o[4], None, s) == 0
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        st = binding.mxfp8_quantize_dbias_noalloc(x, M, N, mx.E5M2, *o[:4], o[4], None, s)
+    assert st == 0
+    new = wl.grad_bf16(M, N, seed=601)
+    x.copy_(torch.from_numpy(new.view(np.int16)).view(torch.bfloat16).cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    want = oracle_slices.quantize(oracle_mod, new, mx.E5M2, with_dbias=True)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), o[:4], want[:4]):
+        assert np.array_equal(g.cpu().numpy(), w), name
+    tol = 1e-5 * np.abs(torch.from_numpy(new.view(np.int16)).view(torch.bfloat16).double().numpy()).sum(0)
+    assert bool((np.abs(o[4].double().cpu().numpy() - want[4]) <= tol).all())
