@@ -30,6 +30,8 @@ def name_for(argv, M=0, N=0, workload_dbias=False):
     (["--workload", "grad_16384x8192", "--dact", "gelu"], True, "quantize_dact_grad_16384x8192_gelu"),
     (["--act", "gelu"], False, "quantize_fc1_8192x28672_gelu"),
     (["--swizzled", "--amax"], False, "quantize_fc1_8192x28672_swizzled_amax"),
+    (["--glu", "silu"], False, "quantize_gated_fc1_8192x28672_silu"),
+    (["--dglu", "silu"], False, "quantize_dgated_fc1_8192x28672_silu"),
 ])
 def test_profile_name_follows_kernel_workload_and_options(argv, wd, want):
     assert name_for(argv, workload_dbias=wd) == want
@@ -59,3 +61,10 @@ def test_traffic_is_reported_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("quantize_x") == 123
     assert bench.profiled_traffic("quantize_y") is None
     assert bench.profiled_traffic("quantize_missing") is None
+
+
+def test_kernel_sources_cover_every_csrc_file():
+    """The sources hashed into kernel_source_sha are exactly the CUDA sources the library builds from."""
+    csrc = sorted(os.path.relpath(p, ROOT) for p in glob.glob(os.path.join(ROOT, "mxfp8_block_scaled_04_gb300",
+                                                                          "csrc", "*.cu*")))
+    assert sorted(bench.KERNEL_SOURCES) == csrc
