@@ -390,8 +390,8 @@ def run_ours(args):
                                                        wl.normal_bf16(M, N, seed=4321)], axis=1))
         x_gate = torch.from_numpy(xg_bits.view(np.int16)).view(torch.bfloat16).cuda()
     if glu:
-        if act or dact or args.swizzled or args.amax or grouped or with_dbias:
-            raise SystemExit("--glu takes a flat workload without dbias or other options")
+        if act or dact or args.swizzled or args.amax or with_dbias:
+            raise SystemExit("--glu takes a workload without dbias or other options")
         x_in_bits = np.ascontiguousarray(np.concatenate([x_bits, wl.normal_bf16(M, N, seed=4321)], axis=1))
         x = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).cuda()
     if (args.swizzled or args.amax or act) and offsets is not None:
@@ -407,7 +407,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step(xin=x):
-        if grouped and with_dbias:
+        if grouped and glu:
+            st = mx.mxfp8_quantize_gated_grouped(xin, M, N, G, off_dev, fmt, glu, out_row, scale_row, out_col,
+                                                 scale_col, None, None, stream)
+        elif grouped and with_dbias:
             st = mx.mxfp8_quantize_grouped_dbias(xin, M, N, G, off_dev, fmt, out_row, scale_row, out_col,
                                                  scale_col, dbias, ws, None, None, stream)
         elif grouped:

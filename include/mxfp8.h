@@ -326,6 +326,24 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
                                     const float *noop, void *stream);
 
 /*
+ * mxfp8_quantize_gated over ragged per-expert row groups in one launch (an MoE
+ * layer's gated activation before its second GEMM): rows
+ * [offsets[g], offsets[g+1]) of x = [a | b] (bf16 [total_rows, 2N]) are group g,
+ * each quantized as its own flat problem, laid out as by mxfp8_quantize_grouped:
+ * out_row, scale_row, out_col indexed by row ([total_rows, N],
+ * [total_rows, ceil(N/32)], [total_rows, N]); scale_col holds
+ * S = sum_g ceil(rows_g / 32) rows, group g's after those of the groups before
+ * it (total_rows / 32 rows when every offset is a multiple of 32).  offsets,
+ * num_groups, err_flag and their checks as for mxfp8_quantize_grouped; noop and
+ * stream as for mxfp8_quantize.  N a multiple of 8 below 2^30.
+ */
+mxfp8_status_t mxfp8_quantize_gated_grouped(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                            const int64_t *offsets, int fp8_fmt, int activation,
+                                            void *out_row, void *scale_row,
+                                            void *out_col, void *scale_col,
+                                            const float *noop, int *err_flag, void *stream);
+
+/*
  * Backward of the gated activation (mxfp8_quantize_gated): for y = act(a) * b
  * and its gradient g, the cast of the gradient of x = [a | b]:
  *     da = g * b * act'(a),   db = g * act(a)     (fp32, act' as for

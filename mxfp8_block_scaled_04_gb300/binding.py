@@ -82,6 +82,8 @@ def lib():
             L.mxfp8_quantize_dact.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_gated.restype = i32
             L.mxfp8_quantize_gated.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_gated_grouped.restype = i32
+            L.mxfp8_quantize_gated_grouped.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_dgated.restype = i32
             L.mxfp8_quantize_dgated.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_host_staging_bytes.restype = ctypes.c_size_t
@@ -176,6 +178,16 @@ def mxfp8_quantize_gated(x, M, N, fp8_fmt, activation, out_row, scale_row, out_c
     return int(lib().mxfp8_quantize_gated(_addr(x), M, N, fp8_fmt, int(activation), _addr(out_row),
                                           _addr(scale_row), _addr(out_col), _addr(scale_col), _addr(noop),
                                           _stream(stream)))
+
+
+def mxfp8_quantize_gated_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, activation, out_row, scale_row,
+                                 out_col, scale_col, noop=None, err_flag=None, stream=None) -> int:
+    """The gated cast over ragged row groups in one launch; see include/mxfp8.h."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_gated_grouped(_addr(x), total_rows, N, num_groups, _addr(offsets), fp8_fmt,
+                                                  int(activation), _addr(out_row), _addr(scale_row), _addr(out_col),
+                                                  _addr(scale_col), _addr(noop), _addr(err_flag), _stream(stream)))
 
 
 def mxfp8_quantize_dgated(grad, x, M, N, fp8_fmt, activation, out_row, scale_row, out_col, scale_col,
@@ -387,6 +399,30 @@ def quantize_gated(x: torch.Tensor, fmt=E4M3, activation="silu", rowwise: bool =
     st = mxfp8_quantize_gated(x, M, N, _fmt(fmt), activation, out_row, scale_row, out_col, scale_col, noop, stream)
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_gated")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
+
+
+def quantize_gated_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, activation="silu",
+                           rowwise: bool = True, colwise: bool = True, noop: Optional[torch.Tensor] = None,
+                           err_flag: Optional[torch.Tensor] = None, stream=None,
+                           scale_col_rows: Optional[int] = None) -> MXFP8Tensor:
+    """The gated cast of x = [a | b] (bf16 [total_rows, 2N]) over the row groups of ``offsets``
+    (a CUDA int64 prefix vector [G+1]); scale_col rows as for quantize_grouped."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
+    if x.shape[1] % 2:
+        raise ValueError("a gated input has an even number of columns")
+    if offsets.dtype != torch.int64 or offsets.dim() != 1 or not offsets.is_contiguous():
+        raise ValueError("offsets must be a contiguous 1-D torch.int64 tensor")
+    total, N = x.shape[0], x.shape[1] // 2
+    G = offsets.numel() - 1
+    if colwise and scale_col_rows is None:
+        scale_col_rows = grouped_scale_col_rows(offsets.cpu())
+    out_row, scale_row, out_col, scale_col = _alloc(x[:, :N], rowwise, colwise, scale_col_rows)
+    st = mxfp8_quantize_gated_grouped(x, total, N, G, offsets, _fmt(fmt), activation, out_row, scale_row, out_col,
+                                      scale_col, noop, err_flag, stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_gated_grouped")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
 
 

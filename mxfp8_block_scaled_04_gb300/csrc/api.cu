@@ -58,6 +58,7 @@ struct DeviceInfo {
     int ctas_per_sm[192] = {};  // indexed by kernel variant
     int dact_ctas_per_sm[48] = {};  // two-input kernels: FMT + 2 * DBIAS + 4 * ACT + 24 * GATED
     int dgated_ctas_per_sm[12] = {};  // gated backward: FMT + 2 * ACT
+    int ggated_ctas_per_sm[12] = {};  // grouped gated cast: FMT + 2 * ACT
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -223,10 +224,11 @@ __global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const 
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
 // The backward-fusion kernel (dY * act'(X)): one-time set-up per (device, variant), then launch.
-template <int FMT, bool DBIAS, int ACT, bool GATED = false>
+template <int FMT, bool DBIAS, int ACT, bool GATED = false, bool GROUPED = false>
 mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUtensorMap &map_x, const QuantParams &p,
                                int64_t tiles, cudaStream_t stream)
 {
+    constexpr int smem = GROUPED ? kSmemDactGrouped : kSmemDact;
     int cap = 0;
     {
         std::lock_guard<std::mutex> lock(g_dev_mu);
@@ -240,22 +242,23 @@ mxfp8_status_t launch_dact_fmt(int device, const CUtensorMap &map_g, const CUten
             }
             d.ready = true;
         }
-        const int v = FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT + (GATED ? 24 : 0);
-        if (d.dact_ctas_per_sm[v] == 0) {
-            auto kern = quantize_dact_kernel<FMT, DBIAS, ACT, GATED>;
+        int &slot = GROUPED ? d.ggated_ctas_per_sm[FMT + 2 * ACT]
+                            : d.dact_ctas_per_sm[FMT + 2 * (DBIAS ? 1 : 0) + 4 * ACT + (GATED ? 24 : 0)];
+        if (slot == 0) {
+            auto kern = quantize_dact_kernel<FMT, DBIAS, ACT, GATED, GROUPED>;
             int n = 0;
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDact) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDact) != cudaSuccess || n < 1) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1) {
                 cudaGetLastError();
                 return MXFP8_ERR_LAUNCH;
             }
-            d.dact_ctas_per_sm[v] = n;
+            slot = n;
         }
-        cap = d.dact_ctas_per_sm[v] * d.sm_count;
+        cap = slot * d.sm_count;
     }
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    return launch_pdl(quantize_dact_kernel<FMT, DBIAS, ACT, GATED>, grid, kThreads, kSmemDact, stream, map_g, map_x,
-                      p);
+    return launch_pdl(quantize_dact_kernel<FMT, DBIAS, ACT, GATED, GROUPED>, grid, kThreads, smem, stream, map_g,
+                      map_x, p);
 }
 
 template <int ACT>
@@ -269,12 +272,12 @@ mxfp8_status_t launch_dact(int fmt, bool dbias, int device, const CUtensorMap &m
                  : launch_dact_fmt<1, false, ACT>(device, map_g, map_x, p, tiles, stream);
 }
 
-template <int ACT>
+template <int ACT, bool GROUPED = false>
 mxfp8_status_t launch_gated(int fmt, int device, const CUtensorMap &map_b, const CUtensorMap &map_a,
                             const QuantParams &p, int64_t tiles, cudaStream_t stream)
 {
-    return fmt == MXFP8_E4M3 ? launch_dact_fmt<0, false, ACT, true>(device, map_b, map_a, p, tiles, stream)
-                             : launch_dact_fmt<1, false, ACT, true>(device, map_b, map_a, p, tiles, stream);
+    return fmt == MXFP8_E4M3 ? launch_dact_fmt<0, false, ACT, true, GROUPED>(device, map_b, map_a, p, tiles, stream)
+                             : launch_dact_fmt<1, false, ACT, true, GROUPED>(device, map_b, map_a, p, tiles, stream);
 }
 
 // The gated backward kernel: one-time set-up per (device, variant), then launch.
@@ -755,6 +758,68 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
     case MXFP8_ACT_GELU: return launch_gated<3>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     case MXFP8_ACT_SILU: return launch_gated<4>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     default: return launch_gated<5>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
+    }
+}
+
+mxfp8_status_t mxfp8_quantize_gated_grouped(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                            const int64_t *offsets, int fp8_fmt, int activation, void *out_row,
+                                            void *scale_row, void *out_col, void *scale_col, const float *noop,
+                                            int *err_flag, void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (total_rows < 0 || N < 0 || N % 8 || total_rows >= (int64_t{1} << 31) || N >= (int64_t{1} << 30))
+        return MXFP8_ERR_SHAPE;
+    if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || offsets == nullptr)
+        return MXFP8_ERR_GROUPS;
+    if (x == nullptr)
+        return MXFP8_ERR_NULL;
+    mxfp8_status_t st = check_outputs(out_row, scale_row, out_col, scale_col);
+    if (st != MXFP8_OK)
+        return st;
+    if (!aligned(x, 16) || !aligned(offsets, 8) || !aligned(err_flag, 4))
+        return MXFP8_ERR_ALIGN;
+    const int64_t col_tiles = (N + kDBN - 1) / kDBN;
+    // every non-empty group adds at most one partial row tile
+    const int64_t tile_bound = (total_rows / kBM + num_groups) * col_tiles;
+    if (tile_bound >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (!on_device(x, device) || !on_device(offsets, device) || !on_device(out_row, device) ||
+        !on_device(scale_row, device) || !on_device(out_col, device) || !on_device(scale_col, device) ||
+        !on_device(noop, device) || !on_device(err_flag, device))
+        return MXFP8_ERR_DEVICE;
+    if (total_rows == 0 || N == 0)
+        return MXFP8_OK;
+    CUtensorMap map_a, map_b;
+    const void *b = static_cast<const uint16_t *>(x) + N;  // 16-byte aligned: N is a multiple of 8
+    if ((st = make_tensor_map_pitch(&map_a, x, total_rows, N, 2 * N)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_b, b, total_rows, N, 2 * N)) != MXFP8_OK)
+        return st;
+    QuantParams p{};
+    p.out_row = static_cast<uint8_t *>(out_row);
+    p.scale_row = static_cast<uint8_t *>(scale_row);
+    p.out_col = static_cast<uint8_t *>(out_col);
+    p.scale_col = static_cast<uint8_t *>(scale_col);
+    p.noop = noop;
+    p.offsets = offsets;
+    p.err_flag = err_flag;
+    p.M = total_rows;
+    p.N = N;
+    p.num_groups = num_groups;
+    p.col_tiles = static_cast<int>(col_tiles);
+    p.row_tiles = static_cast<int>((total_rows + kBM - 1) / kBM);  // the flat schedule (aligned groups)
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    switch (activation) {
+    case MXFP8_ACT_RELU: return launch_gated<1, true>(fp8_fmt, device, map_b, map_a, p, tile_bound, stream);
+    case MXFP8_ACT_SRELU: return launch_gated<2, true>(fp8_fmt, device, map_b, map_a, p, tile_bound, stream);
+    case MXFP8_ACT_GELU: return launch_gated<3, true>(fp8_fmt, device, map_b, map_a, p, tile_bound, stream);
+    case MXFP8_ACT_SILU: return launch_gated<4, true>(fp8_fmt, device, map_b, map_a, p, tile_bound, stream);
+    default: return launch_gated<5, true>(fp8_fmt, device, map_b, map_a, p, tile_bound, stream);
     }
 }
 

@@ -24,7 +24,11 @@
 // GATED: the same kernel casts a gated activation act(a) * b (ReGLU, squared-ReLU
 // GLU, GeGLU, SwiGLU, QGeGLU) of an input x = [a | b], BF16 [M, 2N]: the dY slot
 // holds the box of b (columns N.. of x), the X slot the box of a, and the forward
-// activation takes the derivative's place.  No dbias.
+// activation takes the derivative's place.  No dbias.  GROUPED (gated only): the
+// rows form groups, each quantized as its own flat problem, scheduled as in the
+// grouped cast (no tile straddles two groups; a group's columnwise scale rows follow
+// the previous group's); a partial last block leaves out the rows the tile loads
+// past its group's end.
 #pragma once
 
 #include <cstdint>
@@ -43,6 +47,12 @@ constexpr int kDOffPartD = kDOffPartF + 2 * 4 * kDBN * 4;  // float [2][4][64]
 constexpr int kDOffBars = kDOffPartD + 2 * 4 * kDBN * 4;   // uint64 [kStages]
 constexpr int kDOffCoord = kDOffBars + 8 * kStages;        // TileCoord [kStages]
 constexpr int kSmemDact = kDOffCoord + 32 * kStages + 1024;
+// grouped (gated cast only): the group schedule after the flat layout
+constexpr int kDOffScan = kDOffCoord + 32 * kStages;                 // int64 [kThreads / 32]
+constexpr int kDOffGOff = kDOffScan + 8 * (kThreads / 32);          // int64 [kMaxGroups + 1]
+constexpr int kDOffGPre = kDOffGOff + 8 * (kMaxGroups + 1);         // int [kMaxGroups + 1]
+constexpr int kDOffGSB = kDOffGPre + 4 * (kMaxGroups + 1);          // int [kMaxGroups + 1]
+constexpr int kSmemDactGrouped = kDOffGSB + 4 * (kMaxGroups + 1) + 1024;
 
 // Beyond |x| = 200 every derivative here is at its fp32 limit (1 for x > 0, -0 for
 // x < 0).  The factors that overflow for huge |x| (x^2 in dGeLU's t', 1.702 x in
@@ -110,7 +120,7 @@ __device__ __forceinline__ uint64_t dactivation2(uint64_t x)
     }
 }
 
-template <int FMT, bool DBIAS, int ACT, bool GATED = false>
+template <int FMT, bool DBIAS, int ACT, bool GATED = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 2)
     quantize_dact_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_x,
                          const QuantParams p)
@@ -128,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the transcendental derivatives keep each product for phase 2 (see the top)
     constexpr bool kKeep = ACT > 2;
     static_assert(!(GATED && DBIAS), "the gated cast has no dbias");
+    static_assert(!GROUPED || GATED, "the grouped two-input kernel is the gated cast");
     // act'(x) for the backward fusion, act(x) for the gated cast (two lanes)
     auto factor2 = [](uint64_t x) -> uint64_t {
         if constexpr (GATED)
@@ -140,7 +151,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t N = p.N;
-    const int num_tiles = p.row_tiles * p.col_tiles;
+    int64_t *goff = reinterpret_cast<int64_t *>(smem + kDOffGOff);
+    int *gpre = reinterpret_cast<int *>(smem + kDOffGPre);
+    int *gsb = reinterpret_cast<int *>(smem + kDOffGSB);
+    int num_tiles;
+    bool by_group = false;  // grouped schedule; with every offset a multiple of 32 the flat one
+    if constexpr (GROUPED) {
+        num_tiles = grouped_setup(p, goff, gpre, gsb, reinterpret_cast<int64_t *>(smem + kDOffScan));
+        if (num_tiles < 0) {
+            if (blockIdx.x == 0 && tid == 0 && p.err_flag != nullptr)
+                atomicOr(p.err_flag, 1);
+            return;
+        }
+        // With every group a whole number of 32-row blocks no block crosses a group and the
+        // flat call on the concatenated rows writes the same bytes (scale_col row = row / 32):
+        // flat 128-row tiles then skip the groups' partial last tiles.
+        int unaligned = 0;
+        for (int g = tid; g <= p.num_groups; g += kThreads)
+            unaligned |= (goff[g] & 31) != 0;
+        by_group = __syncthreads_or(unaligned) != 0;
+        if (!by_group)
+            num_tiles = p.row_tiles * p.col_tiles;
+    } else {
+        num_tiles = p.row_tiles * p.col_tiles;
+    }
     const int first = blockIdx.x, stride = gridDim.x;
     const int my_count = first < num_tiles ? (num_tiles - 1 - first) / stride + 1 : 0;
     if (my_count == 0)
@@ -158,12 +192,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     auto issue = [&](int slot, int t) {
-        const int rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
         TileCoord c;
-        c.row0 = static_cast<int64_t>(rt) * kBM;
-        c.row_end = min(c.row0 + kBM, p.M);
-        c.col0 = ct * kDBN;
-        c.rt = rt;
+        if (GROUPED && by_group) {
+            c = tile_coord<true, kDBN>(t, p, goff, gpre, gsb);
+        } else {
+            const int rt = t / p.col_tiles, ct = t - rt * p.col_tiles;
+            c.row0 = static_cast<int64_t>(rt) * kBM;
+            c.row_end = min(c.row0 + kBM, p.M);
+            c.col0 = ct * kDBN;
+            c.rt = rt;
+            c.sb = rt * (kBM / 32);
+        }
         coords[slot] = c;  // published to the consumers by the arrive below
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * kStageBytes);
@@ -189,12 +228,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int rb = warp >> 1, hh = warp & 1;
             const int cq = lane & 15, q = lane >> 4;
             const int r0 = rb * 32 + hh * 16 + q * 8;  // r0 & 7 == 0
+            // rows of this lane's 8 that belong to the tile's group (grouped schedule)
+            const int64_t left = tc.row_end - (tc.row0 + r0);
+            const int live = left < 8 ? static_cast<int>(left) : 8;
             float f[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
             uint64_t d01 = 0, d23 = 0;  // packed column sums (+0.0 in both lanes)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int off = (r0 + i) * 128 + (((cq >> 1) ^ i) << 4) + (cq & 1) * 8;
-                const uint2 g = lds64(gbox + off), xv = lds64(xbox + off);
+                uint2 g = lds64(gbox + off);
+                const uint2 xv = lds64(xbox + off);
+                if (GROUPED && i >= live) {
+                    g.x = 0u;  // a row after the group's end (the next group's): its products are +-0
+                    g.y = 0u;
+                }
                 const uint64_t y01 = f2_mul(f2_pack(bf16_lo(g.x), bf16_hi(g.x)),
                                             factor2(f2_pack(bf16_lo(xv.x), bf16_hi(xv.x))));
                 const uint64_t y23 = f2_mul(f2_pack(bf16_lo(g.y), bf16_hi(g.y)),
@@ -239,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 atomicOr(&g_fault_word, 1u);
+                if (GROUPED && p.err_flag != nullptr)
+                    atomicOr(p.err_flag, 2);
                 for (int j = it; j < my_count && j < it + kStages; ++j)
                     mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
                                       kDrainLimitNs);
@@ -252,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int e = block_exponent_f32<FMT>(__float_as_uint(amax));
             const int64_t grow = tc.row0 + rb * 32, gcol = tc.col0 + c;
             if (do_col && grow < tc.row_end && gcol < N)
-                p.scale_col[(grow >> 5) * N + gcol] = static_cast<uint8_t>(e);
+                p.scale_col[(GROUPED ? static_cast<int64_t>(tc.sb + rb) : grow >> 5) * N + gcol] =
+                    static_cast<uint8_t>(e);
             const int sp = c >> 4, qq = (c >> 2) & 3;  // rotated layout, as in the main kernel
             colmul[rb * kDBN + 4 * (4 * sp + ((qq + (sp >> 1)) & 3)) + (c & 3)] = scale_multiplier(e);
             if constexpr (DBIAS)

@@ -239,7 +239,8 @@ struct TileCoord {
 };
 static_assert(sizeof(TileCoord) <= 32, "coordinate slot");
 
-template <bool GROUPED>
+// Tile t's coordinates; BN is the tile's width in columns.
+template <bool GROUPED, int BN = kBN>
 __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, const int64_t *goff,
                                                 const int *gpre, const int *gsb)
 {
@@ -258,7 +259,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         const int ct = local - rtl * p.col_tiles;
         c.row0 = goff[lo] + static_cast<int64_t>(rtl) * kBM;
         c.row_end = min(c.row0 + kBM, goff[lo + 1]);
-        c.col0 = ct * kBN;
+        c.col0 = ct * BN;
         c.rt = gpre[lo] / p.col_tiles + rtl;  // global row-tile index (per-group dbias partial row)
         c.sb = gsb[lo] + rtl * (kBM / 32);     // the group's scale rows follow the groups before it
     } else {
@@ -266,7 +267,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         const int ct = t - rt * p.col_tiles;
         c.row0 = static_cast<int64_t>(rt) * kBM;
         c.row_end = min(c.row0 + kBM, p.M);
-        c.col0 = ct * kBN;
+        c.col0 = ct * BN;
         c.rt = rt;
         c.sb = rt * (kBM / 32);
     }

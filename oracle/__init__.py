@@ -257,6 +257,32 @@ def quantize_gated(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True,
     return quantize_f32(gate(x_bits, act), fmt, rowwise, colwise)[:4]
 
 
+def quantize_gated_grouped(x_bits: np.ndarray, offsets, fmt: int, act: int):
+    """The gated cast over row groups, each group its own flat problem (as quantize_grouped):
+    row-indexed outputs at the group's rows, the group's ceil(rows/32) columnwise scale rows after
+    those of the groups before it.  ValueError for offsets quantize_grouped rejects."""
+    off = np.asarray(offsets, dtype=np.int64)
+    total = x_bits.shape[0]
+    if off.size < 2 or off[0] != 0 or off[-1] != total or np.any(np.diff(off) < 0):
+        raise ValueError("oracle: invalid group offsets")
+    y = gate(x_bits, act)
+    N = y.shape[1]
+    out_row = np.zeros((total, N), np.uint8)
+    scale_row = np.zeros((total, -(-N // BLOCK)), np.uint8)
+    out_col = np.zeros((total, N), np.uint8)
+    scale_col = np.zeros((grouped_scale_col_rows(off), N), np.uint8)
+    s0 = 0
+    for g in range(off.size - 1):
+        a, b = int(off[g]), int(off[g + 1])
+        if a == b:
+            continue
+        o_r, s_r, o_c, s_c, _ = quantize_f32(y[a:b], fmt)
+        out_row[a:b], scale_row[a:b], out_col[a:b] = o_r, s_r, o_c
+        scale_col[s0:s0 + s_c.shape[0]] = s_c
+        s0 += s_c.shape[0]
+    return out_row, scale_row, out_col, scale_col
+
+
 def dgate(g_bits: np.ndarray, x_bits: np.ndarray, act: int):
     """fp32 (da, db) = (g * b * act'(a), g * act(a)) for g [M, N] and x = [a | b] [M, 2N] (mxo_dgate)."""
     g = np.ascontiguousarray(g_bits, dtype=np.uint16)

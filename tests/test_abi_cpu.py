@@ -232,6 +232,20 @@ def test_gated_host_checks(cuda_lib):
         mx.quantize_gated(torch.zeros(4, 6, dtype=torch.bfloat16)[:, :5].contiguous())
 
 
+def test_gated_grouped_host_checks(cuda_lib):
+    def gg(**kw):
+        a = dict(x=A, total=128, N=64, G=2, off=A, fmt=0, act=4, orow=A, srow=A, ocol=A, scol=A, err=None)
+        a.update(kw)
+        return mx.mxfp8_quantize_gated_grouped(a["x"], a["total"], a["N"], a["G"], a["off"], a["fmt"], a["act"],
+                                               a["orow"], a["srow"], a["ocol"], a["scol"], None, a["err"], 0)
+    assert gg(fmt=3) == FORMAT and gg(act=0) == FORMAT
+    assert gg(N=36) == SHAPE and gg(total=-1) == SHAPE
+    assert gg(G=0) == GROUPS and gg(G=mx.MAX_GROUPS + 1) == GROUPS and gg(off=None) == GROUPS
+    assert gg(x=None) == NULL and gg(orow=None) == NULL
+    assert gg(x=A + 8) == ALIGN and gg(off=A + 4) == ALIGN and gg(err=A + 2) == ALIGN
+    assert gg() == DEVICE and gg(total=45) == DEVICE
+
+
 def test_dgated_host_checks(cuda_lib):
     def dg(**kw):
         a = dict(g=A, x=A, M=64, N=64, fmt=1, act=4, orow=A, srow=A, ocol=A, scol=A)

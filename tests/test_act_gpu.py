@@ -447,3 +447,66 @@ def test_dgated_matches_oracle_layout_and_noop(oracle_mod):
     assert mx.mxfp8_quantize_dgated(dev(g_bits), dev(x_bits), M, N, 1, "silu", *outs, one, None) == 0
     torch.cuda.synchronize()
     assert all(bool((t == 0x3C).all()) for t in outs)
+
+
+# ---- the gated cast over ragged row groups -----------------------------------------------
+
+def run_gated_grouped(x_bits, offsets, fmt, act, prefill=0x3C, noop=None):
+    total, N2 = x_bits.shape
+    N = N2 // 2
+    off = torch.from_numpy(np.asarray(offsets, np.int64)).cuda()
+    srows = max(mx.grouped_scale_col_rows(np.maximum.accumulate(np.asarray(offsets, np.int64))), 1)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    outs = [torch.full((total, N), prefill, **u8), torch.full((total, -(-N // 32)), prefill, **u8),
+            torch.full((total, N), prefill, **u8), torch.full((srows, N), prefill, **u8)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = mx.mxfp8_quantize_gated_grouped(dev(x_bits), total, N, off.numel() - 1, off, fmt, act, *outs, noop, err,
+                                         None)
+    assert st == 0, mx.mxfp8_status_string(st)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in outs], int(err.item())
+
+
+GATED_GROUPS = [np.array([64, 0, 32, 416, 96], np.int64),                 # multiples of 32
+                np.array([45, 0, 1, 31, 33, 96, 70, 127, 129, 13], np.int64)]   # ragged
+
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("fmt,N", [(0, 96), (1, 1032)])
+def test_gated_grouped_parity(oracle_mod, act, case, fmt, N):
+    a = mx.binding.ACTIVATIONS[act]
+    sizes = GATED_GROUPS[case]
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = gated_input(int(off[-1]), N, seed=N + 5 * a + case)
+    got, err = run_gated_grouped(x_bits, off, fmt, act)
+    assert err == 0
+    want = oracle_mod.quantize_gated_grouped(x_bits, off, fmt, a)
+    if a in (1, 2):
+        for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got, want):
+            assert np.array_equal(g, w), name
+        return
+    # transcendental: each group under the boundary rule, its own blocks
+    y32 = oracle_mod.gate(x_bits, a)
+    y64, w = gated_window(oracle_mod, x_bits, a)
+    s0 = 0
+    for g in range(len(sizes)):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if lo == hi:
+            continue
+        o = oracle_mod.quantize_f32(y32[lo:hi], fmt)
+        nb = o[3].shape[0]
+        check_codes(oracle_mod, got[0][lo:hi], o[0], got[1][lo:hi], o[1], y32[lo:hi], y64[lo:hi], w[lo:hi], fmt,
+                    False)
+        check_codes(oracle_mod, got[2][lo:hi], o[2], got[3][s0:s0 + nb], o[3], y32[lo:hi], y64[lo:hi], w[lo:hi],
+                    fmt, True)
+        s0 += nb
+
+
+def test_gated_grouped_bad_offsets_and_noop():
+    x_bits = gated_input(160, 64, seed=2)
+    got, err = run_gated_grouped(x_bits, [0, 100, 50, 160], 0, "silu")
+    assert err == 1 and all(np.all(t == 0x3C) for t in got)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    got, err = run_gated_grouped(x_bits, [0, 100, 160], 0, "silu", noop=one)
+    assert err == 0 and all(np.all(t == 0x3C) for t in got)

@@ -281,13 +281,30 @@ def test_grouped_unaligned_offsets_write_every_byte_once(sizes, N):
         assert sb == sum(-(-(off[h + 1] - off[h]) // 32) for h in range(g)) + (row0 - off[g]) // 32
 
 
-def model_dact(M, N, grid, dbias=True, reuse=False):
+def model_dact(M, N, grid, dbias=True, reuse=False, offsets=None):
+    """quantize_dact_kernel (the backward fusion, and with offsets the grouped gated cast)."""
     rows16 = N % 16 == 0
     out_row, out_col = Plane("out_row", M * N), Plane("out_col", M * N)
-    scale_row, scale_col = Plane("scale_row", M * -(-N // 32)), Plane("scale_col", -(-M // 32) * N)
+    scale_row, scale_col = Plane("scale_row", M * -(-N // 32)), Plane("scale_col", scale_col_rows(M, offsets) * N)
     row_tiles, col_tiles = -(-M // BM), -(-N // DBN)
     ws = Plane("ws", row_tiles * N, 4)
-    tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN, rt) for rt in range(row_tiles) for ct in range(col_tiles)]
+    if offsets is None or all(o % 32 == 0 for o in offsets):
+        # flat tiles; also the grouped gated cast's when every offset is a multiple of 32
+        tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN, rt, rt * 4) for rt in range(row_tiles)
+                 for ct in range(col_tiles)]
+    else:   # the grouped schedule with 64-column tiles: tile_list's rows, DBN's columns
+        tiles = []
+        G = len(offsets) - 1
+        gpre, gsb = [0], [0]
+        for g in range(G):
+            gpre.append(gpre[-1] + -(-(offsets[g + 1] - offsets[g]) // BM) * col_tiles)
+            gsb.append(gsb[-1] + -(-(offsets[g + 1] - offsets[g]) // 32))
+        for t in range(gpre[G]):
+            lo = max(g for g in range(G) if gpre[g] <= t and gpre[g + 1] > gpre[g])
+            local = t - gpre[lo]
+            rtl, ct = local // col_tiles, local % col_tiles
+            r0 = offsets[lo] + rtl * BM
+            tiles.append((r0, min(r0 + BM, offsets[lo + 1]), ct * DBN, gpre[lo] // col_tiles + rtl, gsb[lo] + rtl * 4))
     tid = np.arange(THREADS)
     rb1, c1 = tid >> 6, tid & 63                       # one thread per (32-row block, column)
     w2 = np.repeat(np.arange(8), 2 * 32)
@@ -297,11 +314,11 @@ def model_dact(M, N, grid, dbias=True, reuse=False):
     rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
-            row0, row_end, col0, rt = tiles[t]
+            row0, row_end, col0, rt, sb = tiles[t]
             assert (col0 * 2) % 16 == 0 and col0 < N and row0 < M
             grow, gcol = row0 + rb1 * 32, col0 + c1
             sel = (grow < row_end) & (gcol < N)
-            scale_col.write((grow[sel] >> 5) * N + gcol[sel])
+            scale_col.write((sb + rb1[sel]) * N + gcol[sel])
             if dbias:
                 gc = col0 + np.arange(DBN)
                 ws.write(rt * N + gc[gc < N], 1, align=4)
@@ -314,8 +331,16 @@ def model_dact(M, N, grid, dbias=True, reuse=False):
                 plane.write(grow[part] * N + gcol[part], 8, align=8)
             se = ok & (sp2 % 2 == 0)
             scale_row.write(grow[se] * -(-N // 32) + (gcol[se] >> 5))
-    for p in (out_row, out_col, scale_row, scale_col, ws):
+    for p in (out_row, out_col, scale_row, scale_col) + ((ws,) if dbias else ()):
         p.once()
+
+
+@pytest.mark.parametrize("sizes", [[45, 0, 1, 31, 33, 96, 70, 127, 129, 0, 13], [64, 0, 32, 416, 96], [17, 15]])
+@pytest.mark.parametrize("N", [24, 96, 1032])
+def test_grouped_gated_cast_writes_every_byte_once(sizes, N):
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    model_dact(off[-1], N, 7, dbias=False, reuse=True, offsets=off)
+    model_dact(off[-1], N, 304, dbias=False, reuse=True, offsets=off)
 
 
 @pytest.mark.parametrize("shape", [(45, 80), (70, 24), (257, 1032), (130, 144), (256, 64)])

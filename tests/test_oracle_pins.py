@@ -641,3 +641,28 @@ def test_dgate_hand_worked_and_layout(oracle_mod):
         else:
             qa = oracle_mod.quantize_f32(da, 1)
             assert np.array_equal(q[1][:, :2], qa[1]) and np.array_equal(q[0][:, :N], qa[0])
+
+
+def test_gated_grouped_is_per_group_gated_cast(oracle_mod):
+    """The grouped gated cast: with 32-row-multiple groups it equals the gated cast of all rows
+    (no block crosses a group); with ragged groups each group equals the gated cast of its rows."""
+    N = 40
+    for sizes, flat_equal in (([64, 0, 32, 96], True), ([45, 1, 0, 83, 31], False)):
+        off = wl.offsets_from_sizes(np.array(sizes, np.int64))
+        x = structured_input(int(off[-1]), 2 * N, seed=len(sizes))
+        q = oracle_mod.quantize_gated_grouped(x, off, 1, 4)
+        if flat_equal:
+            for u, v in zip(q, oracle_mod.quantize_gated(x, 1, 4)):
+                assert np.array_equal(u, v)
+        s0 = 0
+        for g in range(len(sizes)):
+            a, b = off[g], off[g + 1]
+            if a == b:
+                continue
+            f = oracle_mod.quantize_gated(x[a:b], 1, 4)
+            assert np.array_equal(q[0][a:b], f[0]) and np.array_equal(q[1][a:b], f[1])
+            assert np.array_equal(q[2][a:b], f[2]) and np.array_equal(q[3][s0:s0 + f[3].shape[0]], f[3])
+            s0 += f[3].shape[0]
+        assert s0 == q[3].shape[0]
+    with pytest.raises(ValueError):
+        oracle_mod.quantize_gated_grouped(x, np.array([0, 100, 50, 160]), 1, 4)
