@@ -9,15 +9,15 @@
 //   - phase 1: warp w takes rows 32*(w>>1) + 16*(w&1) .. +15 of the tile; a
 //     lane takes 4 columns x 8 rows; the two 16-row halves of a 32-row block
 //     meet in shared memory, where one thread per (row block, column) forms
-//     the column's scale, multiplier and dbias partial.  For dGeLU, dSiLU and
-//     dQGeLU each fp32 product is written back over its own two inputs (low
-//     half in the dY slot, high half in the X slot: the same 4 bytes per
-//     element);
+//     the column's scale, multiplier and dbias partial.  Each fp32 product is
+//     written back over its own two inputs (low half in the dY slot, high half
+//     in the X slot: the same 4 bytes per element);
 //   - phase 2: warp w takes the 8-row groups 2w and 2w + 1 (one 32-row block,
 //     whose column multipliers it loads once per tile; dReLU: w and w + 8); a
 //     lane takes 16 columns of one row, as in the main kernel, reading those
 //     products back (one byte permute per element instead of a second
-//     evaluation; dReLU and dSReLU are cheaper to evaluate again).
+//     evaluation: measured faster for every activation, the ReLU family
+//     included).
 // The derivative is evaluated in fp32 with the same ex2 / rcp approximations
 // as the forward activations; dReLU and dSReLU are exact.
 //
@@ -135,8 +135,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDOffBars);
     TileCoord *coords = reinterpret_cast<TileCoord *>(smem + kDOffCoord);
 
-    // the transcendental derivatives keep each product for phase 2 (see the top)
-    constexpr bool kKeep = ACT > 2;
     static_assert(!(GATED && DBIAS), "the gated cast has no dbias");
     static_assert(!GROUPED || GATED, "the grouped two-input kernel is the gated cast");
     // act'(x) for the backward fusion, act(x) for the gated cast (two lanes)
@@ -257,15 +255,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     d01 = f2_add(d01, y01);
                     d23 = f2_add(d23, y23);
                 }
-                if constexpr (kKeep) {
+                {  // keep the products for phase 2 (see the top)
                     const uint32_t b0 = __float_as_uint(y0), b1 = __float_as_uint(y1);
                     const uint32_t b2 = __float_as_uint(y2), b3 = __float_as_uint(y3);
                     sts64(gbox + off, __byte_perm(b0, b1, 0x5410), __byte_perm(b2, b3, 0x5410));
                     sts64(xbox + off, __byte_perm(b0, b1, 0x7632), __byte_perm(b2, b3, 0x7632));
                 }
             }
-            if constexpr (kKeep)
-                fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
+            fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
             if constexpr (DBIAS) {
                 f2_unpack(d01, d[0], d[1]);
                 f2_unpack(d23, d[2], d[3]);
@@ -346,25 +343,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float y[16];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    if constexpr (kKeep) {  // the products phase 1 left in the two slots
-                        y[2 * j] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x5410));
-                        y[2 * j + 1] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x7632));
-                    } else if constexpr (GATED) {  // ReGLU, squared-ReLU GLU: exact, evaluated again
-                        y[2 * j] = bf16_lo(gw[j]) * relu_family<ACT>(bf16_lo(xw[j]));
-                        y[2 * j + 1] = bf16_hi(gw[j]) * relu_family<ACT>(bf16_hi(xw[j]));
-                    } else {                // dReLU, dSReLU: cheaper to evaluate again
-                        y[2 * j] = bf16_lo(gw[j]) * dactivation<ACT>(bf16_lo(xw[j]));
-                        y[2 * j + 1] = bf16_hi(gw[j]) * dactivation<ACT>(bf16_hi(xw[j]));
-                    }
+                    // the products phase 1 left in the two slots
+                    y[2 * j] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x5410));
+                    y[2 * j + 1] = __uint_as_float(__byte_perm(gw[j], xw[j], 0x7632));
                 }
                 const int64_t grow = tc.row0 + r, gcol = tc.col0 + sp * 16;
                 const bool in = grow < tc.row_end && gcol < N;
-                // two codes from two values and their multipliers (f32x2 for the transcendental ones)
+                // two codes from two values and their multipliers (one f32x2 multiply)
                 auto cvt_pair = [](float a, float b, float ma, float mb) -> uint32_t {
-                    if constexpr (kKeep)
-                        return cvt_fp8x2_scaled<FMT>(a, b, f2_pack(ma, mb));
-                    else
-                        return cvt_fp8x2<FMT>(a * ma, b * mb);
+                    return cvt_fp8x2_scaled<FMT>(a, b, f2_pack(ma, mb));
                 };
                 if (do_row) {
                     float fm = 0.f;
