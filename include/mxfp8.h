@@ -28,8 +28,11 @@
  *     dbias      fp32  [N]        column sums of x (unquantized)
  *
  * Conventions shared by every call:
- *   - The library allocates nothing.  It keeps per-device cached attributes
- *     and a launch counter, nothing else.
+ *   - The library allocates no device memory for a call: every buffer is the
+ *     caller's.  It keeps per-device cached kernel attributes, a launch
+ *     counter, a fault word, the internal streams and events of
+ *     mxfp8_quantize_host (created on its first call on a device) and the
+ *     static 8 MiB scratch array of mxfp8_quantize_dbias_noalloc.
  *   - All validation happens on the host before any launch; every rejection
  *     is a status code, nothing throws or aborts across this boundary.
  *   - Work is stream-ordered on `stream` (a cudaStream_t; NULL = the legacy
@@ -66,7 +69,7 @@ typedef enum {
     MXFP8_ERR_NULL = 1,      /* required pointer NULL, a data/scale pair half set, or no direction */
     MXFP8_ERR_SHAPE = 2,     /* M or N negative, N not a multiple of 8, or too large */
     MXFP8_ERR_ALIGN = 3,     /* x/out/workspace not 16-byte aligned, scale_col/dbias not 4-byte */
-    MXFP8_ERR_FORMAT = 4,    /* fp8_fmt not MXFP8_E4M3 / MXFP8_E5M2 */
+    MXFP8_ERR_FORMAT = 4,    /* fp8_fmt not MXFP8_E4M3 / MXFP8_E5M2, or an unknown option value */
     MXFP8_ERR_WORKSPACE = 5, /* dbias requested and workspace NULL */
     MXFP8_ERR_DEVICE = 6,    /* no usable CUDA device, or a buffer not on the current device */
     MXFP8_ERR_LAUNCH = 7,    /* a CUDA call of this library failed (driver/launch error) */
