@@ -328,7 +328,7 @@ def gated_window(oracle_mod, x_bits, a):
 
 @pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
 @pytest.mark.parametrize("fmt,shape", [(0, (544, 1056)), (1, (544, 1056)), (0, (45, 80)), (1, (257, 4112)),
-                                       (0, (70, 24))])
+                                       (0, (70, 24)), (1, (1, 8)), (0, (33, 8))])
 def test_gated_parity(oracle_mod, act, fmt, shape):
     M, N = shape
     a = mx.binding.ACTIVATIONS[act]
@@ -409,7 +409,8 @@ def dgated_windows(oracle_mod, g_bits, x_bits, a):
 
 
 @pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
-@pytest.mark.parametrize("fmt,shape", [(1, (544, 1056)), (0, (45, 80)), (1, (257, 1032)), (0, (70, 24))])
+@pytest.mark.parametrize("fmt,shape", [(1, (544, 1056)), (0, (45, 80)), (1, (257, 1032)), (0, (70, 24)),
+                                       (1, (1, 8)), (0, (33, 8))])
 def test_dgated_parity(oracle_mod, act, fmt, shape):
     M, N = shape
     a = mx.binding.ACTIVATIONS[act]
@@ -510,3 +511,12 @@ def test_gated_grouped_bad_offsets_and_noop():
     one = torch.ones(1, dtype=torch.float32, device="cuda")
     got, err = run_gated_grouped(x_bits, [0, 100, 160], 0, "silu", noop=one)
     assert err == 0 and all(np.all(t == 0x3C) for t in got)
+
+
+def test_gated_and_dgated_empty_shapes():
+    """M == 0 or N == 0: nothing to do, status OK, no launch."""
+    before = mx.mxfp8_kernel_launch_count()
+    assert mx.mxfp8_quantize_gated(None, 0, 64, 0, "silu", None, None, None, None, None, None) == 0
+    assert mx.mxfp8_quantize_gated(None, 64, 0, 0, "silu", None, None, None, None, None, None) == 0
+    assert mx.mxfp8_quantize_dgated(None, None, 0, 64, 1, "silu", None, None, None, None, None, None) == 0
+    assert mx.mxfp8_kernel_launch_count() == before
