@@ -394,8 +394,8 @@ def run_ours(args):
             raise SystemExit("--glu takes a workload without dbias or other options")
         x_in_bits = np.ascontiguousarray(np.concatenate([x_bits, wl.normal_bf16(M, N, seed=4321)], axis=1))
         x = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    if (args.swizzled or args.amax or act) and offsets is not None:
-        raise SystemExit("--swizzled / --amax / --act apply to the flat workloads")
+    if (args.swizzled or args.amax) and offsets is not None:
+        raise SystemExit("--swizzled / --amax apply to the flat workloads")
     if act and with_dbias:
         raise SystemExit("--act does not combine with the dbias workload")
     G = offsets.size - 1 if grouped else 0
@@ -410,6 +410,9 @@ def run_ours(args):
         if grouped and glu:
             st = mx.mxfp8_quantize_gated_grouped(xin, M, N, G, off_dev, fmt, glu, out_row, scale_row, out_col,
                                                  scale_col, None, None, stream)
+        elif grouped and act:
+            st = mx.mxfp8_quantize_grouped_activated(xin, M, N, G, off_dev, fmt, act, out_row, scale_row, out_col,
+                                                     scale_col, None, None, stream)
         elif grouped and with_dbias:
             st = mx.mxfp8_quantize_grouped_dbias(xin, M, N, G, off_dev, fmt, out_row, scale_row, out_col,
                                                  scale_col, dbias, ws, None, None, stream)

@@ -329,6 +329,19 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
                                     const float *noop, void *stream);
 
 /*
+ * mxfp8_quantize_grouped with an activation applied before the cast
+ * (MXFP8_ACT_RELU .. MXFP8_ACT_QGELU, evaluated as for mxfp8_activation_t):
+ * each group is its own flat problem of act(x) values, laid out as by
+ * mxfp8_quantize_grouped.  No dbias.  Status codes as for
+ * mxfp8_quantize_grouped, plus MXFP8_ERR_FORMAT for an unknown activation.
+ */
+mxfp8_status_t mxfp8_quantize_grouped_activated(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                                const int64_t *offsets, int fp8_fmt, int activation,
+                                                void *out_row, void *scale_row,
+                                                void *out_col, void *scale_col,
+                                                const float *noop, int *err_flag, void *stream);
+
+/*
  * mxfp8_quantize_gated over ragged per-expert row groups in one launch (an MoE
  * layer's gated activation before its second GEMM): rows
  * [offsets[g], offsets[g+1]) of x = [a | b] (bf16 [total_rows, 2N]) are group g,

@@ -82,6 +82,9 @@ def lib():
             L.mxfp8_quantize_dact.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_gated.restype = i32
             L.mxfp8_quantize_gated.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_quantize_grouped_activated.restype = i32
+            L.mxfp8_quantize_grouped_activated.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                           vp]
             L.mxfp8_quantize_gated_grouped.restype = i32
             L.mxfp8_quantize_gated_grouped.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_dgated.restype = i32
@@ -178,6 +181,17 @@ def mxfp8_quantize_gated(x, M, N, fp8_fmt, activation, out_row, scale_row, out_c
     return int(lib().mxfp8_quantize_gated(_addr(x), M, N, fp8_fmt, int(activation), _addr(out_row),
                                           _addr(scale_row), _addr(out_col), _addr(scale_col), _addr(noop),
                                           _stream(stream)))
+
+
+def mxfp8_quantize_grouped_activated(x, total_rows, N, num_groups, offsets, fp8_fmt, activation, out_row,
+                                     scale_row, out_col, scale_col, noop=None, err_flag=None, stream=None) -> int:
+    """The grouped cast of act(x); see include/mxfp8.h."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_grouped_activated(_addr(x), total_rows, N, num_groups, _addr(offsets), fp8_fmt,
+                                                      int(activation), _addr(out_row), _addr(scale_row),
+                                                      _addr(out_col), _addr(scale_col), _addr(noop), _addr(err_flag),
+                                                      _stream(stream)))
 
 
 def mxfp8_quantize_gated_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, activation, out_row, scale_row,
@@ -454,14 +468,15 @@ def quantize_dgated(grad: torch.Tensor, x: torch.Tensor, fmt=E5M2, activation="s
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,
                      colwise: bool = True, noop: Optional[torch.Tensor] = None,
                      err_flag: Optional[torch.Tensor] = None, stream=None, with_dbias: bool = False,
-                     scale_col_rows: Optional[int] = None) -> MXFP8Tensor:
+                     scale_col_rows: Optional[int] = None, activation="none") -> MXFP8Tensor:
     """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device).
 
     Every group is quantized as its own flat problem; ``scale_col`` has
     ``grouped_scale_col_rows(offsets)`` rows, group g's after those of the groups before it.
     Pass ``scale_col_rows`` when it is known on the host; otherwise it is computed from a
     host copy of ``offsets`` (one device-to-host read).  ``with_dbias`` also returns the
-    per-group column sums as float32 [G, N].
+    per-group column sums as float32 [G, N]; ``activation`` ("relu", "srelu", "gelu", "silu",
+    "qgelu") casts act(x) instead (no dbias then).
     """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
@@ -472,7 +487,14 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: 
     if colwise and scale_col_rows is None:
         scale_col_rows = grouped_scale_col_rows(offsets.cpu())
     out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise, scale_col_rows)
-    if with_dbias:
+    act = ACTIVATIONS[activation.lower()] if isinstance(activation, str) else int(activation)
+    if act and with_dbias:
+        raise ValueError("an activation does not combine with dbias")
+    if act:
+        dbias = None
+        st = mxfp8_quantize_grouped_activated(x, total, N, G, offsets, _fmt(fmt), act, out_row, scale_row, out_col,
+                                              scale_col, noop, err_flag, stream)
+    elif with_dbias:
         dbias = torch.empty((G, N), dtype=torch.float32, device=x.device)
         ws = torch.empty((max(mxfp8_quantize_grouped_dbias_workspace_bytes(total, N, G), 16),), dtype=torch.uint8,
                          device=x.device)

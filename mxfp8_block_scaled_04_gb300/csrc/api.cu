@@ -407,9 +407,12 @@ int64_t grouped_header_floats(int num_groups)
 // The grouped call, with or without per-group dbias (ws and dbias both set).
 mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int num_groups, const int64_t *offsets,
                             int fp8_fmt, void *out_row, void *scale_row, void *out_col, void *scale_col,
-                            float *dbias, float *ws, const float *noop, int *err_flag, cudaStream_t stream)
+                            float *dbias, float *ws, const float *noop, int *err_flag, cudaStream_t stream,
+                            int act = MXFP8_ACT_NONE)
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (act < MXFP8_ACT_NONE || act > MXFP8_ACT_QGELU || (act != MXFP8_ACT_NONE && dbias != nullptr))
         return MXFP8_ERR_FORMAT;
     if (total_rows < 0 || N < 0 || N % 8 || total_rows >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
@@ -454,8 +457,22 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
         p.N = N;
         p.num_groups = num_groups;
         p.col_tiles = static_cast<int>(col_tiles);
-        st = dbias != nullptr ? launch_quantize<true, true>(fp8_fmt, device, map, p, tile_bound, stream)
-                              : launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, stream);
+        p.row_tiles = static_cast<int>((total_rows + kBM - 1) / kBM);  // the flat schedule (aligned groups)
+        switch (act) {
+        case MXFP8_ACT_RELU: st = launch_quantize<false, true, false, false, 1>(fp8_fmt, device, map, p, tile_bound,
+                                                                              stream); break;
+        case MXFP8_ACT_SRELU: st = launch_quantize<false, true, false, false, 2>(fp8_fmt, device, map, p, tile_bound,
+                                                                               stream); break;
+        case MXFP8_ACT_GELU: st = launch_quantize<false, true, false, false, 3>(fp8_fmt, device, map, p, tile_bound,
+                                                                              stream); break;
+        case MXFP8_ACT_SILU: st = launch_quantize<false, true, false, false, 4>(fp8_fmt, device, map, p, tile_bound,
+                                                                              stream); break;
+        case MXFP8_ACT_QGELU: st = launch_quantize<false, true, false, false, 5>(fp8_fmt, device, map, p, tile_bound,
+                                                                               stream); break;
+        default:
+            st = dbias != nullptr ? launch_quantize<true, true>(fp8_fmt, device, map, p, tile_bound, stream)
+                                  : launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, stream);
+        }
         if (st != MXFP8_OK)
             return st;
     }
@@ -759,6 +776,17 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
     case MXFP8_ACT_SILU: return launch_gated<4>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     default: return launch_gated<5>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     }
+}
+
+mxfp8_status_t mxfp8_quantize_grouped_activated(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                                const int64_t *offsets, int fp8_fmt, int activation, void *out_row,
+                                                void *scale_row, void *out_col, void *scale_col, const float *noop,
+                                                int *err_flag, void *stream_)
+{
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    return grouped_impl(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                        nullptr, nullptr, noop, err_flag, static_cast<cudaStream_t>(stream_), activation);
 }
 
 mxfp8_status_t mxfp8_quantize_gated_grouped(const void *x, int64_t total_rows, int64_t N, int num_groups,

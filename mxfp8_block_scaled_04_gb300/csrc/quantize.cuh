@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     int64_t *goff = reinterpret_cast<int64_t *>(smem + kOffGOff);
     int *gpre = reinterpret_cast<int *>(smem + kOffGPre);
     int *gsb = reinterpret_cast<int *>(smem + kOffGSB);
-    unsigned *stage_done = reinterpret_cast<unsigned *>(smem + kOffScan);  // warp-local: [kStages] warps done
+    // warp-local: [kStages] warps done with a stage (in the scan's space, which the grouped
+    // set-up has finished with before the counters are reset)
+    unsigned *stage_done = reinterpret_cast<unsigned *>(smem + kOffScan);
 
     constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
     // With a transcendental activation (bound on the SM side) a warp's phase-2 tasks are the
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // faster there.  Without one (bound by memory) the tasks step through the row blocks and
     // CTA barriers pace the tile: the order of the stores that measured fastest.
     constexpr bool kWarpLocal = ACT > 2;
-    static_assert(!(kWarpLocal && (GROUPED || DBIAS)), "warp-local phases: flat casts without dbias");
+    static_assert(!(kWarpLocal && DBIAS), "warp-local phases: casts without dbias");
     pdl_wait_and_release();
     if (p.noop != nullptr && *p.noop == 1.0f)
         return;
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t N = p.N;
 
     int num_tiles;
+    bool by_group = GROUPED;  // the grouped schedule (else the flat one)
     if constexpr (GROUPED) {
         num_tiles = grouped_setup(p, goff, gpre, gsb, scan);
         if (num_tiles < 0) {
@@ -394,6 +397,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             // each group's first row tile in the partials (and the total), for the dbias reduce
             for (int g = tid; g <= p.num_groups; g += kThreads)
                 p.ws_hdr[g] = gpre[g] / p.col_tiles;
+        }
+        if constexpr (ACT != 0) {
+            // With every group a whole number of 32-row blocks the flat cast of the
+            // concatenated rows writes the same bytes: flat tiles then skip the groups'
+            // partial last tiles (measured faster for the activated casts only).
+            int unaligned = 0;
+            for (int g = tid; g <= p.num_groups; g += kThreads)
+                unaligned |= (goff[g] & 31) != 0;
+            if (!__syncthreads_or(unaligned)) {
+                by_group = false;
+                num_tiles = p.row_tiles * p.col_tiles;
+            }
         }
     } else {
         num_tiles = p.row_tiles * p.col_tiles;
@@ -419,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     auto issue = [&](int slot, int t) {
-        const TileCoord c = tile_coord<GROUPED>(t, p, goff, gpre, gsb);
+        const TileCoord c = by_group ? tile_coord<true>(t, p, goff, gpre, gsb) : tile_coord<false>(t, p, goff, gpre, gsb);
         coords[slot] = c;  // published to the consumers by the arrive below
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * kStageBytes);
@@ -728,6 +743,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!ok) {
                 if (lane == 0) {
                     atomicOr(&g_fault_word, 1u);
+                    if (GROUPED && p.err_flag != nullptr)
+                        atomicOr(p.err_flag, 2);
                     for (int j = it; j < my_count && j < it + kStages; ++j)
                         mbar_wait_bounded(smem_u32(&bars[j % kStages]), static_cast<uint32_t>(j / kStages) & 1u,
                                           kDrainLimitNs);

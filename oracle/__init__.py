@@ -257,16 +257,12 @@ def quantize_gated(x_bits: np.ndarray, fmt: int, act: int, rowwise: bool = True,
     return quantize_f32(gate(x_bits, act), fmt, rowwise, colwise)[:4]
 
 
-def quantize_gated_grouped(x_bits: np.ndarray, offsets, fmt: int, act: int):
-    """The gated cast over row groups, each group its own flat problem (as quantize_grouped):
-    row-indexed outputs at the group's rows, the group's ceil(rows/32) columnwise scale rows after
-    those of the groups before it.  ValueError for offsets quantize_grouped rejects."""
+def _grouped_f32(y: np.ndarray, offsets, fmt: int):
+    """quantize_f32 of each group's rows of y, laid out as quantize_grouped lays out its groups."""
     off = np.asarray(offsets, dtype=np.int64)
-    total = x_bits.shape[0]
+    total, N = y.shape
     if off.size < 2 or off[0] != 0 or off[-1] != total or np.any(np.diff(off) < 0):
         raise ValueError("oracle: invalid group offsets")
-    y = gate(x_bits, act)
-    N = y.shape[1]
     out_row = np.zeros((total, N), np.uint8)
     scale_row = np.zeros((total, -(-N // BLOCK)), np.uint8)
     out_col = np.zeros((total, N), np.uint8)
@@ -281,6 +277,23 @@ def quantize_gated_grouped(x_bits: np.ndarray, offsets, fmt: int, act: int):
         scale_col[s0:s0 + s_c.shape[0]] = s_c
         s0 += s_c.shape[0]
     return out_row, scale_row, out_col, scale_col
+
+
+def quantize_gated_grouped(x_bits: np.ndarray, offsets, fmt: int, act: int):
+    """The gated cast over row groups, each group its own flat problem (as quantize_grouped):
+    row-indexed outputs at the group's rows, the group's ceil(rows/32) columnwise scale rows after
+    those of the groups before it.  ValueError for offsets quantize_grouped rejects."""
+    if x_bits.shape[1] % 2:
+        raise ValueError("oracle: a gated input has an even number of columns")
+    off = np.asarray(offsets, dtype=np.int64)
+    if off.size < 2 or off[-1] != x_bits.shape[0]:
+        raise ValueError("oracle: invalid group offsets")
+    return _grouped_f32(gate(x_bits, act), off, fmt)
+
+
+def quantize_grouped_act(x_bits: np.ndarray, offsets, fmt: int, act: int):
+    """The grouped cast of the fp32 activations act(x) (see activate), each group its own flat problem."""
+    return _grouped_f32(activate(x_bits, act), offsets, fmt)
 
 
 def dgate(g_bits: np.ndarray, x_bits: np.ndarray, act: int):

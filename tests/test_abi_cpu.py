@@ -232,6 +232,17 @@ def test_gated_host_checks(cuda_lib):
         mx.quantize_gated(torch.zeros(4, 6, dtype=torch.bfloat16)[:, :5].contiguous())
 
 
+def test_grouped_activated_host_checks(cuda_lib):
+    def ga(**kw):
+        a = dict(x=A, total=128, N=64, G=2, off=A, fmt=0, act=3)
+        a.update(kw)
+        return mx.mxfp8_quantize_grouped_activated(a["x"], a["total"], a["N"], a["G"], a["off"], a["fmt"], a["act"],
+                                                   A, A, A, A, None, None, 0)
+    assert ga(act=0) == FORMAT and ga(act=6) == FORMAT and ga(fmt=2) == FORMAT
+    assert ga(N=36) == SHAPE and ga(G=0) == GROUPS and ga(x=None) == NULL and ga(x=A + 8) == ALIGN
+    assert ga() == DEVICE and ga(total=45) == DEVICE
+
+
 def test_gated_grouped_host_checks(cuda_lib):
     def gg(**kw):
         a = dict(x=A, total=128, N=64, G=2, off=A, fmt=0, act=4, orow=A, srow=A, ocol=A, scol=A, err=None)

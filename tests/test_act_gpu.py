@@ -520,3 +520,53 @@ def test_gated_and_dgated_empty_shapes():
     assert mx.mxfp8_quantize_gated(None, 64, 0, 0, "silu", None, None, None, None, None, None) == 0
     assert mx.mxfp8_quantize_dgated(None, None, 0, 64, 1, "silu", None, None, None, None, None, None) == 0
     assert mx.mxfp8_kernel_launch_count() == before
+
+
+# ---- the grouped cast with an activation ---------------------------------------------------
+
+@pytest.mark.parametrize("act", ["relu", "srelu", "gelu", "silu", "qgelu"])
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("fmt,N", [(0, 96), (1, 1032)])
+def test_grouped_activated_parity(oracle_mod, act, case, fmt, N):
+    a = mx.binding.ACTIVATIONS[act]
+    sizes = GATED_GROUPS[case]
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = act_input(int(off[-1]), N, seed=N + 3 * a + case)
+    srows = mx.grouped_scale_col_rows(off)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mx.quantize_grouped(dev(x_bits), torch.from_numpy(off).cuda(), fmt, activation=act, err_flag=err,
+                            scale_col_rows=srows)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = [t.cpu().numpy() for t in r[:4]]
+    if a in (1, 2):
+        for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got,
+                              oracle_mod.quantize_grouped_act(x_bits, off, fmt, a)):
+            assert np.array_equal(g, w), name
+        return
+    y32 = oracle_mod.activate(x_bits, a)
+    y64, w = forward_window(oracle_mod, x_bits, a)
+    s0 = 0
+    for g in range(len(sizes)):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if lo == hi:
+            continue
+        o = oracle_mod.quantize_f32(y32[lo:hi], fmt)
+        nb = o[3].shape[0]
+        check_codes(oracle_mod, got[0][lo:hi], o[0], got[1][lo:hi], o[1], y32[lo:hi], y64[lo:hi], w[lo:hi], fmt,
+                    False)
+        check_codes(oracle_mod, got[2][lo:hi], o[2], got[3][s0:s0 + nb], o[3], y32[lo:hi], y64[lo:hi], w[lo:hi],
+                    fmt, True)
+        s0 += nb
+
+
+def test_grouped_activated_rejects_dbias_and_unknown_activation():
+    x = dev(act_input(64, 64, seed=1))
+    off = torch.tensor([0, 32, 64], dtype=torch.int64, device="cuda")
+    with pytest.raises(ValueError):
+        mx.quantize_grouped(x, off, 0, activation="gelu", with_dbias=True)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    o = [torch.empty((64, 64), **u8), torch.empty((64, 2), **u8), torch.empty((64, 64), **u8),
+         torch.empty((2, 64), **u8)]
+    assert mx.mxfp8_quantize_grouped_activated(x, 64, 64, 2, off, 0, 9, *o, None, None, None) == 4
+    assert mx.mxfp8_quantize_grouped_activated(x, 64, 64, 2, off, 0, 0, *o, None, None, None) == 4

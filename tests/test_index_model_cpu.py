@@ -258,6 +258,16 @@ def test_grouped_cast_writes_every_byte_once(N, grid):
         assert row_end <= off[g + 1]
 
 
+@pytest.mark.parametrize("sizes", [[45, 0, 1, 31, 33, 96, 70, 127, 129, 0, 13], [64, 0, 32, 416, 96]])
+def test_grouped_activated_cast_task_map_writes_every_byte_once(sizes):
+    """The grouped cast with a transcendental activation: warp-local task map; grouped tiles, or
+    with every offset a multiple of 32 the flat tiles (the same bytes)."""
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    sched = None if all(o % 32 == 0 for o in off) else off
+    for N in (40, 160):
+        check_quantize(off[-1], N, 7, offsets=sched, reuse=True)
+
+
 def test_grouped_many_groups_and_empty_ones():
     rng = np.random.Generator(np.random.PCG64(5))
     sizes = (32 * rng.choice([0, 1, 3, 4, 5, 17], size=200)).tolist()

@@ -666,3 +666,25 @@ def test_gated_grouped_is_per_group_gated_cast(oracle_mod):
         assert s0 == q[3].shape[0]
     with pytest.raises(ValueError):
         oracle_mod.quantize_gated_grouped(x, np.array([0, 100, 50, 160]), 1, 4)
+
+
+def test_grouped_activated_is_per_group_activated_cast(oracle_mod):
+    """act(x) cast per group: aligned groups give the flat activated cast of all rows; ragged
+    groups give each group's own activated cast."""
+    N = 40
+    for sizes, flat_equal in (([64, 0, 32, 96], True), ([45, 1, 0, 83, 31], False)):
+        off = wl.offsets_from_sizes(np.array(sizes, np.int64))
+        x = structured_input(int(off[-1]), N, seed=7 + len(sizes))
+        q = oracle_mod.quantize_grouped_act(x, off, 0, 3)
+        if flat_equal:
+            for u, v in zip(q, oracle_mod.quantize_act(x, 0, 3)[:4]):
+                assert np.array_equal(u, v)
+        s0 = 0
+        for g in range(len(sizes)):
+            a, b = off[g], off[g + 1]
+            if a == b:
+                continue
+            f = oracle_mod.quantize_act(x[a:b], 0, 3)
+            assert np.array_equal(q[0][a:b], f[0]) and np.array_equal(q[2][a:b], f[2])
+            assert np.array_equal(q[3][s0:s0 + f[3].shape[0]], f[3])
+            s0 += f[3].shape[0]
