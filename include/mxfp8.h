@@ -342,6 +342,36 @@ mxfp8_status_t mxfp8_quantize_grouped_activated(const void *x, int64_t total_row
                                                 const float *noop, int *err_flag, void *stream);
 
 /*
+ * mxfp8_quantize_grouped (activation MXFP8_ACT_NONE, or an activation as for
+ * mxfp8_quantize_grouped_activated) with each group's scale planes in the
+ * GEMM-ready layout of MXFP8_SCALES_SWIZZLED, the layout a grouped
+ * block-scaled GEMM reads per expert (this library's reading for the grouped
+ * call; the pages define the swizzled bit for one tensor):
+ *   scale_row  group g's own [rows_g, ceil(N/32)] plane, padded to 128-row x
+ *              4-column tiles (padding zero), after the planes of the groups
+ *              before it (at byte sum_{h<g} ceil(rows_h/128) * 128 *
+ *              ceil(ceil(N/32)/4)*4);
+ *   scale_col  group g's columnwise scales as the transposed operand's
+ *              [N, ceil(rows_g/32)] plane in the same layout, after the planes
+ *              of the groups before it (at byte sum_{h<g} ceil(rows_h/128) * 4 *
+ *              ceil(N/128)*128).
+ * Plane sizes: mxfp8_grouped_swizzled_scale_bytes.  out_row / out_col, offsets,
+ * err_flag, noop and the checks as for mxfp8_quantize_grouped; no dbias.
+ */
+mxfp8_status_t mxfp8_quantize_grouped_swizzled(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                               const int64_t *offsets, int fp8_fmt, int activation,
+                                               void *out_row, void *scale_row,
+                                               void *out_col, void *scale_col,
+                                               const float *noop, int *err_flag, void *stream);
+
+/*
+ * Bytes of one GEMM-ready scale plane of mxfp8_quantize_grouped_swizzled
+ * (colwise = 0: scale_row, 1: scale_col) for host_offsets (a host copy of the
+ * call's offsets, num_groups + 1 entries).  0 for invalid arguments.
+ */
+size_t mxfp8_grouped_swizzled_scale_bytes(const int64_t *host_offsets, int num_groups, int64_t N, int colwise);
+
+/*
  * mxfp8_quantize_gated over ragged per-expert row groups in one launch (an MoE
  * layer's gated activation before its second GEMM): rows
  * [offsets[g], offsets[g+1]) of x = [a | b] (bf16 [total_rows, 2N]) are group g,

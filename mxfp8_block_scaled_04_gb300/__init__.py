@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     mxfp8_quantize_workspace_bytes, mxfp8_status_string, quantize, quantize_grouped, grouped_scale_col_rows,
     mxfp8_quantize_grouped_dbias, mxfp8_quantize_grouped_dbias_workspace_bytes,
     mxfp8_quantize_dact, quantize_dact, mxfp8_quantize_gated, quantize_gated, mxfp8_quantize_dgated,
-    quantize_dgated, mxfp8_quantize_gated_grouped, quantize_gated_grouped, mxfp8_quantize_grouped_activated, mxfp8_selftest_bounded_wait, mxfp8_activation_values,
+    quantize_dgated, mxfp8_quantize_gated_grouped, quantize_gated_grouped, mxfp8_quantize_grouped_activated,
+    mxfp8_quantize_grouped_swizzled, mxfp8_grouped_swizzled_scale_bytes, mxfp8_selftest_bounded_wait, mxfp8_activation_values,
     QuantizeConfig, SCALES_PLAIN, SCALES_SWIZZLED, make_config, mxfp8_quantize_ex, mxfp8_scale_bytes,
 )

@@ -85,6 +85,10 @@ def lib():
             L.mxfp8_quantize_grouped_activated.restype = i32
             L.mxfp8_quantize_grouped_activated.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp,
                                                            vp]
+            L.mxfp8_quantize_grouped_swizzled.restype = i32
+            L.mxfp8_quantize_grouped_swizzled.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+            L.mxfp8_grouped_swizzled_scale_bytes.restype = ctypes.c_size_t
+            L.mxfp8_grouped_swizzled_scale_bytes.argtypes = [ctypes.POINTER(ctypes.c_int64), i32, i64, i32]
             L.mxfp8_quantize_gated_grouped.restype = i32
             L.mxfp8_quantize_gated_grouped.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.mxfp8_quantize_dgated.restype = i32
@@ -194,6 +198,24 @@ def mxfp8_quantize_grouped_activated(x, total_rows, N, num_groups, offsets, fp8_
                                                       _stream(stream)))
 
 
+def mxfp8_quantize_grouped_swizzled(x, total_rows, N, num_groups, offsets, fp8_fmt, activation, out_row, scale_row,
+                                    out_col, scale_col, noop=None, err_flag=None, stream=None) -> int:
+    """The grouped cast with per-group GEMM-ready scale planes; see include/mxfp8.h."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_grouped_swizzled(_addr(x), total_rows, N, num_groups, _addr(offsets), fp8_fmt,
+                                                     int(activation), _addr(out_row), _addr(scale_row),
+                                                     _addr(out_col), _addr(scale_col), _addr(noop), _addr(err_flag),
+                                                     _stream(stream)))
+
+
+def mxfp8_grouped_swizzled_scale_bytes(host_offsets, N: int, colwise: bool) -> int:
+    """Bytes of one per-group GEMM-ready scale plane for host offsets [G+1]."""
+    off = torch.as_tensor(host_offsets, dtype=torch.int64, device="cpu").contiguous()
+    ptr = ctypes.cast(off.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+    return int(lib().mxfp8_grouped_swizzled_scale_bytes(ptr, off.numel() - 1, N, int(bool(colwise))))
+
+
 def mxfp8_quantize_gated_grouped(x, total_rows, N, num_groups, offsets, fp8_fmt, activation, out_row, scale_row,
                                  out_col, scale_col, noop=None, err_flag=None, stream=None) -> int:
     """The gated cast over ragged row groups in one launch; see include/mxfp8.h."""
@@ -290,15 +312,17 @@ def _fmt(fmt) -> int:
     return int(fmt)
 
 
-def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool, scale_col_rows: Optional[int] = None):
+def _alloc(x: torch.Tensor, rowwise: bool, colwise: bool, scale_col_rows: Optional[int] = None,
+           scales: bool = True):
+    """FP8 planes and (with ``scales``) plain scale planes for x [M, N]."""
     M, N = x.shape
     dev = x.device
     u8 = torch.uint8
     sc = -(-M // BLOCK) if scale_col_rows is None else scale_col_rows
     return (torch.empty((M, N), dtype=u8, device=dev) if rowwise else None,
-            torch.empty((M, -(-N // BLOCK)), dtype=u8, device=dev) if rowwise else None,
+            torch.empty((M, -(-N // BLOCK)), dtype=u8, device=dev) if rowwise and scales else None,
             torch.empty((M, N), dtype=u8, device=dev) if colwise else None,
-            torch.empty((sc, N), dtype=u8, device=dev) if colwise else None)
+            torch.empty((sc, N), dtype=u8, device=dev) if colwise and scales else None)
 
 
 def grouped_scale_col_rows(offsets) -> int:
@@ -468,7 +492,8 @@ def quantize_dgated(grad: torch.Tensor, x: torch.Tensor, fmt=E5M2, activation="s
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: bool = True,
                      colwise: bool = True, noop: Optional[torch.Tensor] = None,
                      err_flag: Optional[torch.Tensor] = None, stream=None, with_dbias: bool = False,
-                     scale_col_rows: Optional[int] = None, activation="none") -> MXFP8Tensor:
+                     scale_col_rows: Optional[int] = None, activation="none",
+                     swizzled: bool = False) -> MXFP8Tensor:
     """Grouped quantize; ``offsets`` is a CUDA int64 prefix vector [G+1] (kept on the device).
 
     Every group is quantized as its own flat problem; ``scale_col`` has
@@ -476,7 +501,9 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: 
     Pass ``scale_col_rows`` when it is known on the host; otherwise it is computed from a
     host copy of ``offsets`` (one device-to-host read).  ``with_dbias`` also returns the
     per-group column sums as float32 [G, N]; ``activation`` ("relu", "srelu", "gelu", "silu",
-    "qgelu") casts act(x) instead (no dbias then).
+    "qgelu") casts act(x) instead (no dbias then).  ``swizzled`` writes each group's scale planes
+    in the GEMM-ready layout (1-D uint8 tensors; see include/mxfp8.h; no dbias), which reads a host
+    copy of ``offsets``.
     """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 tensor")
@@ -484,13 +511,25 @@ def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, rowwise: 
         raise ValueError("offsets must be a contiguous 1-D torch.int64 tensor")
     total, N = x.shape
     G = offsets.numel() - 1
-    if colwise and scale_col_rows is None:
-        scale_col_rows = grouped_scale_col_rows(offsets.cpu())
-    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise, scale_col_rows)
     act = ACTIVATIONS[activation.lower()] if isinstance(activation, str) else int(activation)
     if act and with_dbias:
         raise ValueError("an activation does not combine with dbias")
-    if act:
+    if swizzled and with_dbias:
+        raise ValueError("the swizzled grouped call has no dbias")
+    if colwise and scale_col_rows is None and not swizzled:
+        scale_col_rows = grouped_scale_col_rows(offsets.cpu())
+    out_row, scale_row, out_col, scale_col = _alloc(x, rowwise, colwise, scale_col_rows or 0, scales=not swizzled)
+    if swizzled:
+        host_off = offsets.cpu()
+        u8 = dict(dtype=torch.uint8, device=x.device)
+        if rowwise:
+            scale_row = torch.empty((max(mxfp8_grouped_swizzled_scale_bytes(host_off, N, False), 1),), **u8)
+        if colwise:
+            scale_col = torch.empty((max(mxfp8_grouped_swizzled_scale_bytes(host_off, N, True), 1),), **u8)
+        dbias = None
+        st = mxfp8_quantize_grouped_swizzled(x, total, N, G, offsets, _fmt(fmt), act, out_row, scale_row, out_col,
+                                             scale_col, noop, err_flag, stream)
+    elif act:
         dbias = None
         st = mxfp8_quantize_grouped_activated(x, total, N, G, offsets, _fmt(fmt), act, out_row, scale_row, out_col,
                                               scale_col, noop, err_flag, stream)

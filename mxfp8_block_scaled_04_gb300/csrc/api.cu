@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -220,6 +221,54 @@ __global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const 
     }
 }
 
+// The same for a grouped call's planes, one group per CTA: group g's plane (rowwise:
+// rows_g x ceil(N/32); columnwise: N x ceil(rows_g/32)) starts after the planes of the
+// groups before it (see the quantize kernel's swz_row_offset / swz_col_offset).  Offsets
+// the grouped kernel rejects make this kernel write nothing too.
+__global__ void grouped_swizzle_pad_kernel(uint8_t *scales, const int64_t *offsets, int num_groups, int64_t total_rows,
+                                           int64_t N, int colwise, const float *noop)
+{
+    if (noop != nullptr && *noop == 1.0f)
+        return;
+    __shared__ int bad;
+    __shared__ int64_t before;  // sum of ceil(rows_h / 128) over h < g
+    const int g = blockIdx.x;
+    if (threadIdx.x == 0) {
+        bad = offsets[0] != 0 || offsets[num_groups] != total_rows;
+        before = 0;
+    }
+    __syncthreads();
+    int64_t part = 0;
+    for (int h = threadIdx.x; h < num_groups; h += blockDim.x) {
+        const int64_t a = offsets[h], b = offsets[h + 1];
+        if (b < a)
+            atomicOr(&bad, 1);
+        else if (h < g)
+            part += (b - a + 127) / 128;
+    }
+    atomicAdd(reinterpret_cast<unsigned long long *>(&before), static_cast<unsigned long long>(part));
+    __syncthreads();
+    const int64_t rows_g = offsets[g + 1] - offsets[g];
+    if (bad || rows_g <= 0)
+        return;
+    const int64_t Cn = (N + 31) / 32;
+    const int64_t R = colwise ? N : rows_g, C = colwise ? (rows_g + 31) / 32 : Cn;
+    uint8_t *plane = scales + (colwise ? before * 4 * ((N + 127) / 128 * 128) : before * 128 * ((Cn + 3) / 4 * 4));
+    if (R % 128 == 0 && C % 4 == 0)
+        return;
+    const int64_t col_tiles = (C + 3) / 4, row_tiles = (R + 127) / 128;
+    const int64_t ntiles = col_tiles + row_tiles - 1;
+    for (int64_t t = 0; t < ntiles; ++t) {
+        const int64_t rt = t < col_tiles ? row_tiles - 1 : t - col_tiles;
+        const int64_t ct = t < col_tiles ? t : col_tiles - 1;
+        for (int w = threadIdx.x; w < 512; w += blockDim.x) {
+            const int64_t r = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), c = ct * 4 + (w & 3);
+            if (r >= R || c >= C)
+                plane[((rt * col_tiles + ct) << 9) + w] = 0;
+        }
+    }
+}
+
 // Enqueue the flat quantize kernel (no validation: the caller has checked every
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
@@ -408,11 +457,12 @@ int64_t grouped_header_floats(int num_groups)
 mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int num_groups, const int64_t *offsets,
                             int fp8_fmt, void *out_row, void *scale_row, void *out_col, void *scale_col,
                             float *dbias, float *ws, const float *noop, int *err_flag, cudaStream_t stream,
-                            int act = MXFP8_ACT_NONE)
+                            int act = MXFP8_ACT_NONE, bool swizzled = false)
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
-    if (act < MXFP8_ACT_NONE || act > MXFP8_ACT_QGELU || (act != MXFP8_ACT_NONE && dbias != nullptr))
+    if (act < MXFP8_ACT_NONE || act > MXFP8_ACT_QGELU || (act != MXFP8_ACT_NONE && dbias != nullptr) ||
+        (swizzled && dbias != nullptr))
         return MXFP8_ERR_FORMAT;
     if (total_rows < 0 || N < 0 || N % 8 || total_rows >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
@@ -458,21 +508,42 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
         p.num_groups = num_groups;
         p.col_tiles = static_cast<int>(col_tiles);
         p.row_tiles = static_cast<int>((total_rows + kBM - 1) / kBM);  // the flat schedule (aligned groups)
-        switch (act) {
-        case MXFP8_ACT_RELU: st = launch_quantize<false, true, false, false, 1>(fp8_fmt, device, map, p, tile_bound,
-                                                                              stream); break;
-        case MXFP8_ACT_SRELU: st = launch_quantize<false, true, false, false, 2>(fp8_fmt, device, map, p, tile_bound,
-                                                                               stream); break;
-        case MXFP8_ACT_GELU: st = launch_quantize<false, true, false, false, 3>(fp8_fmt, device, map, p, tile_bound,
-                                                                              stream); break;
-        case MXFP8_ACT_SILU: st = launch_quantize<false, true, false, false, 4>(fp8_fmt, device, map, p, tile_bound,
-                                                                              stream); break;
-        case MXFP8_ACT_QGELU: st = launch_quantize<false, true, false, false, 5>(fp8_fmt, device, map, p, tile_bound,
-                                                                               stream); break;
-        default:
-            st = dbias != nullptr ? launch_quantize<true, true>(fp8_fmt, device, map, p, tile_bound, stream)
-                                  : launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, stream);
+        if (swizzled) {
+            // each group's GEMM-ready planes have their own padding entries (zeroed here)
+            for (int colwise = 0; colwise < 2; ++colwise) {
+                void *plane = colwise ? scale_col : scale_row;
+                if (plane == nullptr)
+                    continue;
+                grouped_swizzle_pad_kernel<<<num_groups, 256, 0, stream>>>(static_cast<uint8_t *>(plane), offsets,
+                                                                          num_groups, total_rows, N, colwise, noop);
+                g_launches.fetch_add(1, std::memory_order_relaxed);
+            }
+            if (cudaGetLastError() != cudaSuccess)
+                return MXFP8_ERR_LAUNCH;
         }
+        auto launch_act = [&](auto swz_tag) -> mxfp8_status_t {
+            constexpr bool S = decltype(swz_tag)::value;
+            switch (act) {
+            case MXFP8_ACT_RELU: return launch_quantize<false, true, S, false, 1>(fp8_fmt, device, map, p, tile_bound,
+                                                                                 stream);
+            case MXFP8_ACT_SRELU: return launch_quantize<false, true, S, false, 2>(fp8_fmt, device, map, p, tile_bound,
+                                                                                  stream);
+            case MXFP8_ACT_GELU: return launch_quantize<false, true, S, false, 3>(fp8_fmt, device, map, p, tile_bound,
+                                                                                 stream);
+            case MXFP8_ACT_SILU: return launch_quantize<false, true, S, false, 4>(fp8_fmt, device, map, p, tile_bound,
+                                                                                 stream);
+            case MXFP8_ACT_QGELU: return launch_quantize<false, true, S, false, 5>(fp8_fmt, device, map, p,
+                                                                                  tile_bound, stream);
+            default:
+                if constexpr (S)
+                    return launch_quantize<false, true, true, false>(fp8_fmt, device, map, p, tile_bound, stream);
+                else
+                    return dbias != nullptr
+                               ? launch_quantize<true, true>(fp8_fmt, device, map, p, tile_bound, stream)
+                               : launch_quantize<false, true>(fp8_fmt, device, map, p, tile_bound, stream);
+            }
+        };
+        st = swizzled ? launch_act(std::true_type{}) : launch_act(std::false_type{});
         if (st != MXFP8_OK)
             return st;
     }
@@ -776,6 +847,32 @@ mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8
     case MXFP8_ACT_SILU: return launch_gated<4>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     default: return launch_gated<5>(fp8_fmt, device, map_b, map_a, p, tiles, stream);
     }
+}
+
+mxfp8_status_t mxfp8_quantize_grouped_swizzled(const void *x, int64_t total_rows, int64_t N, int num_groups,
+                                               const int64_t *offsets, int fp8_fmt, int activation, void *out_row,
+                                               void *scale_row, void *out_col, void *scale_col, const float *noop,
+                                               int *err_flag, void *stream_)
+{
+    return grouped_impl(x, total_rows, N, num_groups, offsets, fp8_fmt, out_row, scale_row, out_col, scale_col,
+                        nullptr, nullptr, noop, err_flag, static_cast<cudaStream_t>(stream_), activation, true);
+}
+
+size_t mxfp8_grouped_swizzled_scale_bytes(const int64_t *host_offsets, int num_groups, int64_t N, int colwise)
+{
+    if (host_offsets == nullptr || num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || N < 0 || N % 8 ||
+        host_offsets[0] != 0)
+        return 0;
+    int64_t tiles = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        const int64_t rows = host_offsets[g + 1] - host_offsets[g];
+        if (rows < 0)
+            return 0;
+        tiles += (rows + kBM - 1) / kBM;
+    }
+    const int64_t Cn = (N + 31) / 32;
+    const int64_t per_tile = colwise ? 4 * ((N + 127) / 128 * 128) : 128 * ((Cn + 3) / 4 * 4);
+    return static_cast<size_t>(tiles) * static_cast<size_t>(per_tile);
 }
 
 mxfp8_status_t mxfp8_quantize_grouped_activated(const void *x, int64_t total_rows, int64_t N, int num_groups,

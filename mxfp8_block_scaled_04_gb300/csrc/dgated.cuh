@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         c.col0 = ct * kDBN;
         c.rt = rt;
         c.sb = rt * (kBM / 32);
+        c.g = 0;
         coords[slot] = c;  // published to the consumers by the arrive below
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(smem + slot * kGStageBytes);

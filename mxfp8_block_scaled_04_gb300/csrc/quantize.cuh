@@ -236,6 +236,7 @@ struct TileCoord {
     int col0;
     int rt;           // flat row-tile index (dbias partial row)
     int sb;           // columnwise scale row of the tile's first 32-row block
+    int g;            // the tile's group (0 for a flat call)
 };
 static_assert(sizeof(TileCoord) <= 32, "coordinate slot");
 
@@ -262,6 +263,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         c.col0 = ct * BN;
         c.rt = gpre[lo] / p.col_tiles + rtl;  // global row-tile index (per-group dbias partial row)
         c.sb = gsb[lo] + rtl * (kBM / 32);     // the group's scale rows follow the groups before it
+        c.g = lo;
     } else {
         const int rt = t / p.col_tiles;
         const int ct = t - rt * p.col_tiles;
@@ -270,6 +272,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const QuantParams &p, con
         c.col0 = ct * BN;
         c.rt = rt;
         c.sb = rt * (kBM / 32);
+        c.g = 0;
     }
     return c;
 }
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int g = tid; g <= p.num_groups; g += kThreads)
                 p.ws_hdr[g] = gpre[g] / p.col_tiles;
         }
-        if constexpr (ACT != 0) {
+        if constexpr (ACT != 0 && !SWZ) {
             // With every group a whole number of 32-row blocks the flat cast of the
             // concatenated rows writes the same bytes: flat tiles then skip the groups'
             // partial last tiles (measured faster for the activated casts only).
@@ -451,6 +454,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     uint32_t amax_acc = 0;  // running max |value| as fp32 bits (amax output only)
+    // GEMM-ready scale planes.  A flat call's planes are one swizzled matrix each; a grouped
+    // call's are one per group, each swizzled on its own (padded to 128-row x 4-column tiles)
+    // and laid out after the previous group's: group g's rowwise plane starts after
+    // sum_{h<g} ceil(rows_h/128) tile rows of ceil(ceil(N/32)/4) tiles, its columnwise plane
+    // (N rows x ceil(rows_g/32) scale columns) after sum_{h<g} ceil(rows_h/128) tile columns of
+    // ceil(N/128) tiles: both prefixes are the groups' row-tile prefix.
+    const int64_t Cn = (N + 31) >> 5;
+    auto swz_row_offset = [&](const TileCoord &tc, int64_t grow, int64_t sc) -> int64_t {
+        if constexpr (GROUPED) {
+            const int64_t tiles_before = gpre[tc.g] / p.col_tiles;
+            return tiles_before * 128 * ((Cn + 3) & ~int64_t{3}) + swizzled_offset(grow - goff[tc.g], sc, Cn);
+        } else {
+            return swizzled_offset(grow, sc, Cn);
+        }
+    };
+    auto swz_col_offset = [&](const TileCoord &tc, int64_t gcol, int64_t grow) -> int64_t {
+        if constexpr (GROUPED) {
+            const int64_t tiles_before = gpre[tc.g] / p.col_tiles;
+            const int64_t rows_g = goff[tc.g + 1] - goff[tc.g];
+            return tiles_before * 4 * ((N + 127) & ~int64_t{127}) +
+                   swizzled_offset(gcol, (grow - goff[tc.g]) >> 5, (rows_g + 31) >> 5);
+        } else {
+            return swizzled_offset(gcol, grow >> 5, (p.M + 31) >> 5);
+        }
+    };
     for (int it = 0; it < my_count; ++it) {
         const int slot = it % kStages;
         const uint32_t parity = static_cast<uint32_t>(it / kStages) & 1u;
@@ -584,11 +612,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                             (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
                     } else {
                         // the columnwise operand's scales, seen as N rows x ceil(M/32) scale columns
-                        const int64_t C = (p.M + 31) >> 5, c = grow >> 5;
-                        p.scale_col[swizzled_offset(gcol, c, C)] = static_cast<uint8_t>(e0);
-                        p.scale_col[swizzled_offset(gcol + 1, c, C)] = static_cast<uint8_t>(e1);
-                        p.scale_col[swizzled_offset(gcol + 2, c, C)] = static_cast<uint8_t>(e2);
-                        p.scale_col[swizzled_offset(gcol + 3, c, C)] = static_cast<uint8_t>(e3);
+                        p.scale_col[swz_col_offset(tc, gcol, grow)] = static_cast<uint8_t>(e0);
+                        p.scale_col[swz_col_offset(tc, gcol + 1, grow)] = static_cast<uint8_t>(e1);
+                        p.scale_col[swz_col_offset(tc, gcol + 2, grow)] = static_cast<uint8_t>(e2);
+                        p.scale_col[swz_col_offset(tc, gcol + 3, grow)] = static_cast<uint8_t>(e3);
                     }
                 }
                 if constexpr (DBIAS)
@@ -713,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (in) {
                         store_codes(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                         if ((sp & 1) == 0)
-                            p.scale_row[SWZ ? swizzled_offset(grow, gcol >> 5, (N + 31) >> 5)
-                                            : grow * ((N + 31) >> 5) + (gcol >> 5)] = static_cast<uint8_t>(er);
+                            p.scale_row[SWZ ? swz_row_offset(tc, grow, gcol >> 5)
+                                            : grow * Cn + (gcol >> 5)] = static_cast<uint8_t>(er);
                         if (AMAX && !do_col)
                             amax_acc = max(amax_acc, row_amax_bits);
                     }

@@ -279,6 +279,29 @@ def _grouped_f32(y: np.ndarray, offsets, fmt: int):
     return out_row, scale_row, out_col, scale_col
 
 
+def quantize_grouped_swizzled(x_bits: np.ndarray, offsets, fmt: int, act: int = 0):
+    """The grouped cast (of act(x) when act != 0) with each group's scale planes in the GEMM-ready
+    layout: group g's rowwise plane is swizzle_scales of its [rows_g, ceil(N/32)] scales, its
+    columnwise plane swizzle_scales of the transposed [N, ceil(rows_g/32)] scales; the planes of the
+    groups are concatenated in group order.  Returns (out_row, scale_row, out_col, scale_col)."""
+    off = np.asarray(offsets, dtype=np.int64)
+    y = activate(x_bits, act) if act else None
+    if act:
+        o_r, _, o_c, _ = _grouped_f32(y, off, fmt)
+    else:
+        o_r, _, o_c, _ = quantize_grouped(x_bits, off, fmt)
+    rows_planes, col_planes = [], []
+    for g in range(off.size - 1):
+        a, b = int(off[g]), int(off[g + 1])
+        if a == b:
+            continue
+        q = quantize_f32(y[a:b], fmt) if act else quantize(x_bits[a:b], fmt)
+        rows_planes.append(swizzle_scales(q[1]))
+        col_planes.append(swizzle_scales(np.ascontiguousarray(q[3].T)))
+    cat = lambda ps: np.concatenate(ps) if ps else np.zeros(0, np.uint8)
+    return o_r, cat(rows_planes), o_c, cat(col_planes)
+
+
 def quantize_gated_grouped(x_bits: np.ndarray, offsets, fmt: int, act: int):
     """The gated cast over row groups, each group its own flat problem (as quantize_grouped):
     row-indexed outputs at the group's rows, the group's ceil(rows/32) columnwise scale rows after

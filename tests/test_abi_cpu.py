@@ -243,6 +243,27 @@ def test_grouped_activated_host_checks(cuda_lib):
     assert ga() == DEVICE and ga(total=45) == DEVICE
 
 
+def test_grouped_swizzled_host_checks(cuda_lib):
+    def gs(**kw):
+        a = dict(x=A, total=128, N=64, G=2, off=A, fmt=0, act=0, srow=A, scol=A)
+        a.update(kw)
+        return mx.mxfp8_quantize_grouped_swizzled(a["x"], a["total"], a["N"], a["G"], a["off"], a["fmt"], a["act"],
+                                                  A, a["srow"], A, a["scol"], None, None, 0)
+    assert gs(act=6) == FORMAT and gs(act=-1) == FORMAT and gs(fmt=2) == FORMAT
+    assert gs(N=36) == SHAPE and gs(G=0) == GROUPS and gs(off=None) == GROUPS
+    assert gs(x=None) == NULL and gs(x=A + 8) == ALIGN
+    assert gs() == DEVICE and gs(total=45) == DEVICE and gs(act=3) == DEVICE
+    # plane sizes: ceil(rows_g / 128) tiles per group, 128 x ceil(ceil(N/32)/4)*4 (rowwise) or
+    # ceil(N/128)*128 x 4 (columnwise) bytes per tile
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 45, 45, 300], 96, False) == 3 * 128 * 4
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 45, 45, 300], 96, True) == 3 * 128 * 4
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 129], 1032, False) == 2 * 128 * 36
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 129], 1032, True) == 2 * 1152 * 4
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 50, 40], 64, False) == 0      # decreasing
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([1, 50], 64, False) == 0          # not starting at 0
+    assert mx.mxfp8_grouped_swizzled_scale_bytes([0, 50], 36, False) == 0          # N % 8
+
+
 def test_gated_grouped_host_checks(cuda_lib):
     def gg(**kw):
         a = dict(x=A, total=128, N=64, G=2, off=A, fmt=0, act=4, orow=A, srow=A, ocol=A, scol=A, err=None)

@@ -570,3 +570,94 @@ def test_grouped_activated_rejects_dbias_and_unknown_activation():
          torch.empty((2, 64), **u8)]
     assert mx.mxfp8_quantize_grouped_activated(x, 64, 64, 2, off, 0, 9, *o, None, None, None) == 4
     assert mx.mxfp8_quantize_grouped_activated(x, 64, 64, 2, off, 0, 0, *o, None, None, None) == 4
+
+
+# ---- the grouped cast with per-group GEMM-ready scale planes ---------------------------------
+
+def run_grouped_swizzled(x_bits, offsets, fmt, act, prefill=0x3C, noop=None):
+    total, N = x_bits.shape
+    off_np = np.asarray(offsets, np.int64)
+    off = torch.from_numpy(off_np).cuda()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    rb = mx.mxfp8_grouped_swizzled_scale_bytes(np.maximum.accumulate(off_np), N, False)
+    cb = mx.mxfp8_grouped_swizzled_scale_bytes(np.maximum.accumulate(off_np), N, True)
+    outs = [torch.full((total, N), prefill, **u8), torch.full((max(rb, 1),), prefill, **u8),
+            torch.full((total, N), prefill, **u8), torch.full((max(cb, 1),), prefill, **u8)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = mx.mxfp8_quantize_grouped_swizzled(dev(x_bits), total, N, len(off_np) - 1, off, fmt, act, *outs, noop, err,
+                                            None)
+    assert st == 0, mx.mxfp8_status_string(st)
+    torch.cuda.synchronize()
+    got = [t.cpu().numpy() for t in outs]
+    got[1], got[3] = got[1][:rb], got[3][:cb]
+    return got, int(err.item())
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "srelu"])
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("fmt,N", [(0, 96), (1, 1032)])
+def test_grouped_swizzled_parity(oracle_mod, act, case, fmt, N):
+    a = mx.binding.ACTIVATIONS[act]
+    sizes = GATED_GROUPS[case]
+    off = wl.offsets_from_sizes(sizes)
+    x_bits = act_input(int(off[-1]), N, seed=N + 7 * a + case)
+    got, err = run_grouped_swizzled(x_bits, off, fmt, act)
+    assert err == 0
+    want = oracle_mod.quantize_grouped_swizzled(x_bits, off, fmt, a)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got, want):
+        assert g.shape == w.shape and np.array_equal(g, w), name
+
+
+def _unswizzle(oracle_mod, plane, R, C):
+    idx = np.array([[oracle_mod.swizzle_offset(r, c, C) for c in range(C)] for r in range(R)], np.int64)
+    return plane[idx]
+
+
+def test_grouped_swizzled_gelu_codes(oracle_mod):
+    """A transcendental activation with per-group GEMM-ready planes: each group's planes read back
+    through the oracle's layout function, its codes under the boundary rule."""
+    sizes = np.array([45, 0, 83, 130], np.int64)
+    off = wl.offsets_from_sizes(sizes)
+    N, fmt, a = 72, 0, 3
+    x_bits = act_input(int(off[-1]), N, seed=17)
+    got, err = run_grouped_swizzled(x_bits, off, fmt, a)
+    assert err == 0
+    y32 = oracle_mod.activate(x_bits, a)
+    y64, w = forward_window(oracle_mod, x_bits, a)
+    Cn = -(-N // 32)
+    rbase = cbase = 0
+    for g in range(len(sizes)):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if lo == hi:
+            continue
+        rows = hi - lo
+        o = oracle_mod.quantize_f32(y32[lo:hi], fmt)
+        rsz = -(-rows // 128) * 128 * (-(-Cn // 4) * 4)
+        csz = -(-N // 128) * 128 * (-(-(-(-rows // 32)) // 4) * 4)
+        srow = _unswizzle(oracle_mod, got[1][rbase:rbase + rsz], rows, Cn)
+        scol = _unswizzle(oracle_mod, got[3][cbase:cbase + csz], N, -(-rows // 32)).T
+        check_codes(oracle_mod, got[0][lo:hi], o[0], srow, o[1], y32[lo:hi], y64[lo:hi], w[lo:hi], fmt, False)
+        check_codes(oracle_mod, got[2][lo:hi], o[2], np.ascontiguousarray(scol), o[3], y32[lo:hi], y64[lo:hi],
+                    w[lo:hi], fmt, True)
+        rbase += rsz
+        cbase += csz
+    assert rbase == got[1].size and cbase == got[3].size
+
+
+def test_grouped_swizzled_noop_and_bad_offsets():
+    x_bits = act_input(160, 64, seed=5)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    got, err = run_grouped_swizzled(x_bits, [0, 100, 160], 0, 0, noop=one)
+    assert err == 0 and all(np.all(t == 0x3C) for t in got)
+    got, err = run_grouped_swizzled(x_bits, [0, 100, 50, 160], 0, 0)
+    assert err == 1 and all(np.all(t == 0x3C) for t in got)
+
+
+def test_grouped_swizzled_through_the_binding(oracle_mod):
+    off = wl.offsets_from_sizes(np.array([45, 0, 83, 130], np.int64))
+    x_bits = act_input(int(off[-1]), 96, seed=29)
+    t = mx.quantize_grouped(dev(x_bits), torch.from_numpy(off).cuda(), fmt=1, activation="relu", swizzled=True)
+    want = oracle_mod.quantize_grouped_swizzled(x_bits, off, 1, 1)
+    got = [t.out_row, t.scale_row, t.out_col, t.scale_col]
+    for g, w in zip(got, want):
+        assert np.array_equal(g.cpu().numpy(), w)

@@ -64,12 +64,12 @@ def swizzled_bytes(R, C):
 
 
 def tile_list(M, N, offsets):
-    """The kernel's tiles in order: (row0, row_end, col0, rt, sb) per tile index; sb is the
-    columnwise scale row of the tile's first 32-row block."""
+    """The kernel's tiles in order: (row0, row_end, col0, rt, sb, g) per tile index; sb is the
+    columnwise scale row of the tile's first 32-row block, g the tile's group (0 when flat)."""
     col_tiles = -(-N // BN)
     if offsets is None:
         row_tiles = -(-M // BM)
-        return [(rt * BM, min(rt * BM + BM, M), ct * BN, rt, rt * (BM // 32))
+        return [(rt * BM, min(rt * BM + BM, M), ct * BN, rt, rt * (BM // 32), 0)
                 for rt in range(row_tiles) for ct in range(col_tiles)]
     G = len(offsets) - 1
     gpre, gsb = [0], [0]
@@ -89,7 +89,7 @@ def tile_list(M, N, offsets):
         rtl, ct = local // col_tiles, local % col_tiles
         row0 = offsets[lo] + rtl * BM
         tiles.append((row0, min(row0 + BM, offsets[lo + 1]), ct * BN, gpre[lo] // col_tiles + rtl,
-                      gsb[lo] + rtl * (BM // 32)))
+                      gsb[lo] + rtl * (BM // 32), lo))
     return tiles
 
 
@@ -104,7 +104,11 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
     Cr = -(-N // 32)
     out_row = Plane("out_row", M * N)
     out_col = Plane("out_col", M * N)
-    if swz:
+    if swz and offsets is not None:     # one GEMM-ready plane per group, in group order
+        tiles_g = sum(-(-(offsets[g + 1] - offsets[g]) // BM) for g in range(len(offsets) - 1))
+        scale_row = Plane("scale_row", tiles_g * 128 * ((Cr + 3) // 4 * 4))
+        scale_col = Plane("scale_col", tiles_g * 4 * ((N + 127) // 128 * 128))
+    elif swz:
         scale_row = Plane("scale_row", swizzled_bytes(M, Cr))
         scale_col = Plane("scale_col", swizzled_bytes(N, -(-M // 32)))
     else:
@@ -129,7 +133,7 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
     rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
-            row0, row_end, col0, rt, sb = tiles[t]
+            row0, row_end, col0, rt, sb, g = tiles[t]
             for box in range(2):            # TMA box origins (x must be 16-byte aligned)
                 x = col0 + box * BOX
                 if x < N:
@@ -155,7 +159,13 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                         assert len(chunks) == len(set(chunks)) == (32 - live) * 8
             grow, gcol = row0 + rb1 * 32, col0 + box1 * BOX + cq1 * 4
             sel = (grow < row_end) & (half1 == 0) & (gcol < N) & do_col
-            if swz:
+            if swz and offsets is not None:
+                before = rt - (row0 - offsets[g]) // BM          # the kernel's gpre[g] / col_tiles
+                C = -(-(offsets[g + 1] - offsets[g]) // 32)
+                for j in range(4):
+                    scale_col.write(before * 4 * ((N + 127) // 128 * 128) +
+                                    swizzled_offset(gcol[sel] + j, (grow[sel] - offsets[g]) >> 5, C))
+            elif swz:
                 C = -(-M // 32)
                 for j in range(4):
                     scale_col.write(swizzled_offset(gcol[sel] + j, grow[sel] >> 5, C))
@@ -176,9 +186,41 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                     plane.write(grow[part] * N + gcol[part], 8, align=8)
             if do_row:
                 se = ok & (sp2 % 2 == 0)
-                scale_row.write(swizzled_offset(grow[se], gcol[se] >> 5, Cr) if swz else grow[se] * Cr + (gcol[se] >> 5))
+                if swz and offsets is not None:
+                    before = rt - (row0 - offsets[g]) // BM
+                    scale_row.write(before * 128 * ((Cr + 3) // 4 * 4) +
+                                    swizzled_offset(grow[se] - offsets[g], gcol[se] >> 5, Cr))
+                else:
+                    scale_row.write(swizzled_offset(grow[se], gcol[se] >> 5, Cr) if swz
+                                    else grow[se] * Cr + (gcol[se] >> 5))
     return dict(out_row=out_row, out_col=out_col, scale_row=scale_row, scale_col=scale_col, ws=ws,
                 ws_rows=ws_rows, tiles=tiles)
+
+
+class PlaneAt:
+    """A view of a Plane from byte `base` on (a group's plane inside the concatenated planes)."""
+
+    def __init__(self, plane, base):
+        self.plane, self.base = plane, base
+
+    def write(self, idx, nbytes=1, align=1):
+        self.plane.write(np.asarray(idx, np.int64) + self.base, nbytes, align)
+
+
+def model_grouped_swizzle_pad(offsets, N, scale_row, scale_col):
+    """grouped_swizzle_pad_kernel, one CTA per group and one launch per plane: the group's plane
+    starts at its row-tile prefix (sum of ceil(rows_h / 128) over h < g) times the bytes of one
+    128-row tile of that plane; zero its padding entries as the flat pad kernel does."""
+    Cn = -(-N // 32)
+    for colwise, plane in ((False, scale_row), (True, scale_col)):
+        for g in range(len(offsets) - 1):
+            before = sum(-(-(offsets[h + 1] - offsets[h]) // 128) for h in range(g))
+            rows_g = offsets[g + 1] - offsets[g]
+            if rows_g <= 0:
+                continue
+            R, C = (N, -(-rows_g // 32)) if colwise else (rows_g, Cn)
+            base = before * 4 * ((N + 127) // 128 * 128) if colwise else before * 128 * ((Cn + 3) // 4 * 4)
+            model_swizzle_pad(R, C, PlaneAt(plane, base))
 
 
 def model_swizzle_pad(R, C, plane):
@@ -202,7 +244,11 @@ def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
             m[name].once()
         else:
             assert not m[name].count.any()
-    if swz:
+    if swz and offsets is not None:
+        model_grouped_swizzle_pad(offsets, N, m["scale_row"], m["scale_col"])
+        m["scale_row"].once()
+        m["scale_col"].once()
+    elif swz:
         Cr = -(-N // 32)
         if do_row:
             model_swizzle_pad(M, Cr, m["scale_row"])
@@ -253,7 +299,7 @@ def test_grouped_cast_writes_every_byte_once(N, grid):
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
     m = check_quantize(off[-1], N, grid, offsets=off, dbias=True)
     # no tile straddles two groups; each group's tiles are contiguous in the partial-sum rows
-    for row0, row_end, col0, rt, sb in m["tiles"]:
+    for row0, row_end, col0, rt, sb, g_tile in m["tiles"]:
         g = max(i for i in range(len(off) - 1) if off[i] <= row0)
         assert row_end <= off[g + 1]
 
@@ -285,10 +331,20 @@ def test_grouped_unaligned_offsets_write_every_byte_once(sizes, N):
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
     m = check_quantize(off[-1], N, 7, offsets=off, dbias=True)
     assert m["scale_col"].count.size == scale_col_rows(off[-1], off) * N
-    for row0, row_end, col0, rt, sb in m["tiles"]:
+    for row0, row_end, col0, rt, sb, g_tile in m["tiles"]:
         g = max(i for i in range(len(off) - 1) if off[i] <= row0 and off[i + 1] > off[i])
         assert off[g] <= row0 < row_end <= off[g + 1]
         assert sb == sum(-(-(off[h + 1] - off[h]) // 32) for h in range(g)) + (row0 - off[g]) // 32
+
+
+@pytest.mark.parametrize("sizes", [[45, 0, 1, 31, 33, 96, 70, 127, 129, 0, 13], [64, 0, 32, 416, 96], [300]])
+@pytest.mark.parametrize("N", [24, 72, 1032])
+@pytest.mark.parametrize("reuse", [False, True])
+def test_grouped_swizzled_planes_written_once(sizes, N, reuse):
+    """The grouped cast with one GEMM-ready scale plane per group: the cast's scale writes and the
+    pad kernel's zeros together cover every byte of both concatenated planes exactly once."""
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
+    check_quantize(off[-1], N, 5, offsets=off, swz=True, reuse=reuse)
 
 
 def model_dact(M, N, grid, dbias=True, reuse=False, offsets=None):
@@ -300,7 +356,7 @@ def model_dact(M, N, grid, dbias=True, reuse=False, offsets=None):
     ws = Plane("ws", row_tiles * N, 4)
     if offsets is None or all(o % 32 == 0 for o in offsets):
         # flat tiles; also the grouped gated cast's when every offset is a multiple of 32
-        tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN, rt, rt * 4) for rt in range(row_tiles)
+        tiles = [(rt * BM, min(rt * BM + BM, M), ct * DBN, rt, rt * 4, 0) for rt in range(row_tiles)
                  for ct in range(col_tiles)]
     else:   # the grouped schedule with 64-column tiles: tile_list's rows, DBN's columns
         tiles = []
@@ -314,7 +370,8 @@ def model_dact(M, N, grid, dbias=True, reuse=False, offsets=None):
             local = t - gpre[lo]
             rtl, ct = local // col_tiles, local % col_tiles
             r0 = offsets[lo] + rtl * BM
-            tiles.append((r0, min(r0 + BM, offsets[lo + 1]), ct * DBN, gpre[lo] // col_tiles + rtl, gsb[lo] + rtl * 4))
+            tiles.append((r0, min(r0 + BM, offsets[lo + 1]), ct * DBN, gpre[lo] // col_tiles + rtl, gsb[lo] + rtl * 4,
+                          lo))
     tid = np.arange(THREADS)
     rb1, c1 = tid >> 6, tid & 63                       # one thread per (32-row block, column)
     w2 = np.repeat(np.arange(8), 2 * 32)
@@ -324,7 +381,7 @@ def model_dact(M, N, grid, dbias=True, reuse=False, offsets=None):
     rr2, sp2 = l2 >> 2, l2 & 3
     for b in range(grid):
         for t in range(b, len(tiles), grid):
-            row0, row_end, col0, rt, sb = tiles[t]
+            row0, row_end, col0, rt, sb, g = tiles[t]
             assert (col0 * 2) % 16 == 0 and col0 < N and row0 < M
             grow, gcol = row0 + rb1 * 32, col0 + c1
             sel = (grow < row_end) & (gcol < N)

@@ -688,3 +688,24 @@ def test_grouped_activated_is_per_group_activated_cast(oracle_mod):
             assert np.array_equal(q[0][a:b], f[0]) and np.array_equal(q[2][a:b], f[2])
             assert np.array_equal(q[3][s0:s0 + f[3].shape[0]], f[3])
             s0 += f[3].shape[0]
+
+
+def test_grouped_swizzled_planes(oracle_mod):
+    """Per-group GEMM-ready planes: one group gives the flat call's swizzled planes; groups of
+    128-row multiples give the flat rowwise plane (row tiles in order); ragged groups give each
+    group's own swizzled planes, padded and concatenated."""
+    N = 96
+    x = structured_input(384, N, seed=31)
+    flat = oracle_mod.quantize(x, 0)
+    one = oracle_mod.quantize_grouped_swizzled(x, np.array([0, 384]), 0)
+    assert np.array_equal(one[1], oracle_mod.swizzle_scales(flat[1]))
+    assert np.array_equal(one[3], oracle_mod.swizzle_scales(np.ascontiguousarray(flat[3].T)))
+    three = oracle_mod.quantize_grouped_swizzled(x, np.array([0, 128, 128, 384]), 0)
+    assert np.array_equal(three[1], oracle_mod.swizzle_scales(flat[1]))
+    ragged = oracle_mod.quantize_grouped_swizzled(x, np.array([0, 45, 45, 300, 384]), 0)
+    # sizes: ceil(45/128) + ceil(255/128) + ceil(84/128) = 4 tiles of 128 x 4 (rowwise) and 4 x 128 (colwise)
+    assert ragged[1].size == 4 * 128 * 4 and ragged[3].size == 4 * 4 * 128
+    g1 = oracle_mod.quantize(x[45:300], 0)
+    assert np.array_equal(ragged[1][512:512 + 1024], oracle_mod.swizzle_scales(g1[1]))
+    assert np.array_equal(ragged[3][512:512 + 1024], oracle_mod.swizzle_scales(np.ascontiguousarray(g1[3].T)))
+    assert np.array_equal(ragged[0], oracle_mod.quantize_grouped(x, np.array([0, 45, 45, 300, 384]), 0)[0])
