@@ -370,9 +370,15 @@ def run_ours(args):
     W = 2 if dglu else 1    # the gated backward writes [da | db]: outputs of width 2N
     out_row = torch.empty((M, W * N), dtype=torch.uint8, device="cuda")
     layout = mx.SCALES_SWIZZLED if args.swizzled else mx.SCALES_PLAIN
-    scale_row = torch.empty((mx.mxfp8_scale_bytes(M, W * (N // 32), layout),), dtype=torch.uint8, device="cuda")
+    if grouped and args.swizzled:   # one GEMM-ready plane per group
+        row_bytes = mx.mxfp8_grouped_swizzled_scale_bytes(offsets, N, False)
+        col_bytes = mx.mxfp8_grouped_swizzled_scale_bytes(offsets, N, True)
+    else:
+        row_bytes = mx.mxfp8_scale_bytes(M, W * (N // 32), layout)
+        col_bytes = mx.mxfp8_scale_bytes(W * N, M // 32, layout)
+    scale_row = torch.empty((row_bytes,), dtype=torch.uint8, device="cuda")
     out_col = torch.empty((M, W * N), dtype=torch.uint8, device="cuda")
-    scale_col = torch.empty((mx.mxfp8_scale_bytes(W * N, M // 32, layout),), dtype=torch.uint8, device="cuda")
+    scale_col = torch.empty((col_bytes,), dtype=torch.uint8, device="cuda")
     amax = torch.empty((1,), dtype=torch.float32, device="cuda") if args.amax else None
     act = mx.binding.ACTIVATIONS[args.act.lower()]
     dact = mx.binding.ACTIVATIONS[args.dact.lower()]
@@ -394,8 +400,10 @@ def run_ours(args):
             raise SystemExit("--glu takes a workload without dbias or other options")
         x_in_bits = np.ascontiguousarray(np.concatenate([x_bits, wl.normal_bf16(M, N, seed=4321)], axis=1))
         x = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    if (args.swizzled or args.amax) and offsets is not None:
-        raise SystemExit("--swizzled / --amax apply to the flat workloads")
+    if args.amax and offsets is not None:
+        raise SystemExit("--amax applies to the flat workloads")
+    if args.swizzled and grouped and (glu or with_dbias):
+        raise SystemExit("--swizzled on the grouped workload takes no --glu / --dbias")
     if act and with_dbias:
         raise SystemExit("--act does not combine with the dbias workload")
     G = offsets.size - 1 if grouped else 0
@@ -407,7 +415,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step(xin=x):
-        if grouped and glu:
+        if grouped and args.swizzled:
+            st = mx.mxfp8_quantize_grouped_swizzled(xin, M, N, G, off_dev, fmt, act, out_row, scale_row, out_col,
+                                                    scale_col, None, None, stream)
+        elif grouped and glu:
             st = mx.mxfp8_quantize_gated_grouped(xin, M, N, G, off_dev, fmt, glu, out_row, scale_row, out_col,
                                                  scale_col, None, None, stream)
         elif grouped and act:

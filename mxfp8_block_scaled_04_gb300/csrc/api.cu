@@ -201,74 +201,6 @@ __global__ void amax_init_kernel(float *amax, const float *noop)
     *amax = 0.0f;
 }
 
-// Zero the padding entries of a GEMM-ready scale plane of R x C real entries
-// (unless noop): the tiles of the last row tile and of the last column tile.
-__global__ void swizzle_pad_kernel(uint8_t *scales, int64_t R, int64_t C, const float *noop)
-{
-    if (noop != nullptr && *noop == 1.0f)
-        return;
-    const int64_t col_tiles = (C + 3) / 4, row_tiles = (R + 127) / 128;
-    // tile list: row tile row_tiles-1 (all column tiles), then column tile col_tiles-1 of the others
-    const int64_t ntiles = col_tiles + row_tiles - 1;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int64_t rt = t < col_tiles ? row_tiles - 1 : t - col_tiles;
-        const int64_t ct = t < col_tiles ? t : col_tiles - 1;
-        for (int w = threadIdx.x; w < 512; w += blockDim.x) {
-            const int64_t r = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), c = ct * 4 + (w & 3);
-            if (r >= R || c >= C)
-                scales[((rt * col_tiles + ct) << 9) + w] = 0;
-        }
-    }
-}
-
-// The same for a grouped call's planes, one group per CTA: group g's plane (rowwise:
-// rows_g x ceil(N/32); columnwise: N x ceil(rows_g/32)) starts after the planes of the
-// groups before it (see the quantize kernel's swz_row_offset / swz_col_offset).  Offsets
-// the grouped kernel rejects make this kernel write nothing too.
-__global__ void grouped_swizzle_pad_kernel(uint8_t *scales, const int64_t *offsets, int num_groups, int64_t total_rows,
-                                           int64_t N, int colwise, const float *noop)
-{
-    if (noop != nullptr && *noop == 1.0f)
-        return;
-    __shared__ int bad;
-    __shared__ int64_t before;  // sum of ceil(rows_h / 128) over h < g
-    const int g = blockIdx.x;
-    if (threadIdx.x == 0) {
-        bad = offsets[0] != 0 || offsets[num_groups] != total_rows;
-        before = 0;
-    }
-    __syncthreads();
-    int64_t part = 0;
-    for (int h = threadIdx.x; h < num_groups; h += blockDim.x) {
-        const int64_t a = offsets[h], b = offsets[h + 1];
-        if (b < a)
-            atomicOr(&bad, 1);
-        else if (h < g)
-            part += (b - a + 127) / 128;
-    }
-    atomicAdd(reinterpret_cast<unsigned long long *>(&before), static_cast<unsigned long long>(part));
-    __syncthreads();
-    const int64_t rows_g = offsets[g + 1] - offsets[g];
-    if (bad || rows_g <= 0)
-        return;
-    const int64_t Cn = (N + 31) / 32;
-    const int64_t R = colwise ? N : rows_g, C = colwise ? (rows_g + 31) / 32 : Cn;
-    uint8_t *plane = scales + (colwise ? before * 4 * ((N + 127) / 128 * 128) : before * 128 * ((Cn + 3) / 4 * 4));
-    if (R % 128 == 0 && C % 4 == 0)
-        return;
-    const int64_t col_tiles = (C + 3) / 4, row_tiles = (R + 127) / 128;
-    const int64_t ntiles = col_tiles + row_tiles - 1;
-    for (int64_t t = 0; t < ntiles; ++t) {
-        const int64_t rt = t < col_tiles ? row_tiles - 1 : t - col_tiles;
-        const int64_t ct = t < col_tiles ? t : col_tiles - 1;
-        for (int w = threadIdx.x; w < 512; w += blockDim.x) {
-            const int64_t r = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), c = ct * 4 + (w & 3);
-            if (r >= R || c >= C)
-                plane[((rt * col_tiles + ct) << 9) + w] = 0;
-        }
-    }
-}
-
 // Enqueue the flat quantize kernel (no validation: the caller has checked every
 // argument).  ws != nullptr selects the dbias variant, which writes one fp32
 // partial column sum per 128-row tile of this call to ws[tile][N].
@@ -508,19 +440,6 @@ mxfp8_status_t grouped_impl(const void *x, int64_t total_rows, int64_t N, int nu
         p.num_groups = num_groups;
         p.col_tiles = static_cast<int>(col_tiles);
         p.row_tiles = static_cast<int>((total_rows + kBM - 1) / kBM);  // the flat schedule (aligned groups)
-        if (swizzled) {
-            // each group's GEMM-ready planes have their own padding entries (zeroed here)
-            for (int colwise = 0; colwise < 2; ++colwise) {
-                void *plane = colwise ? scale_col : scale_row;
-                if (plane == nullptr)
-                    continue;
-                grouped_swizzle_pad_kernel<<<num_groups, 256, 0, stream>>>(static_cast<uint8_t *>(plane), offsets,
-                                                                          num_groups, total_rows, N, colwise, noop);
-                g_launches.fetch_add(1, std::memory_order_relaxed);
-            }
-            if (cudaGetLastError() != cudaSuccess)
-                return MXFP8_ERR_LAUNCH;
-        }
         auto launch_act = [&](auto swz_tag) -> mxfp8_status_t {
             constexpr bool S = decltype(swz_tag)::value;
             switch (act) {
@@ -685,17 +604,6 @@ mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *strea
     if (cfg->amax != nullptr) {
         amax_init_kernel<<<1, 1, 0, stream>>>(cfg->amax, cfg->noop);
         g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
-    if (swz && !empty) {
-        // padding exists when a scale plane's rows or columns are not tile multiples
-        auto pad = [&](void *plane, int64_t R, int64_t C) {
-            if (plane != nullptr && (R % 128 != 0 || C % 4 != 0)) {
-                swizzle_pad_kernel<<<64, 128, 0, stream>>>(static_cast<uint8_t *>(plane), R, C, cfg->noop);
-                g_launches.fetch_add(1, std::memory_order_relaxed);
-            }
-        };
-        pad(cfg->scale_row, M, (N + 31) / 32);
-        pad(cfg->scale_col, N, (M + 31) / 32);
     }
     if (cudaGetLastError() != cudaSuccess)
         return MXFP8_ERR_LAUNCH;

@@ -84,13 +84,12 @@ struct QuantParams {
     int64_t *ws_hdr;         // grouped dbias: [num_groups + 1] first row tile of each group (-1: bad offsets)
 };
 
-// Byte offset of scale (r, c) of an R x C scale matrix (C scale columns) in the
-// GEMM-ready layout: 128-row x 4-column tiles of 512 bytes, row-tile major,
-// entry (r, c) of a tile at 16 * (r % 32) + 4 * (r / 32) + c.
-__device__ __forceinline__ int64_t swizzled_offset(int64_t r, int64_t c, int64_t C)
+// GEMM-ready layout: a scale matrix stored as 128-row x 4-column tiles of 512 bytes,
+// row-tile major, entry (r, c) of a tile at 16 * (r % 32) + 4 * (r / 32) + c.  The
+// byte of entry (r, c) within its tile (0 <= r < 128, 0 <= c < 4):
+__device__ __forceinline__ int swizzled_in_tile(int r, int c)
 {
-    const int64_t col_tiles = (C + 3) >> 2;
-    return (((r >> 7) * col_tiles + (c >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3);
+    return ((r & 31) << 4) | (((r >> 5) & 3) << 2) | c;
 }
 
 // Library-wide device fault word (bit 0: a bounded wait expired).
@@ -456,27 +455,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t amax_acc = 0;  // running max |value| as fp32 bits (amax output only)
     // GEMM-ready scale planes.  A flat call's planes are one swizzled matrix each; a grouped
     // call's are one per group, each swizzled on its own (padded to 128-row x 4-column tiles)
-    // and laid out after the previous group's: group g's rowwise plane starts after
-    // sum_{h<g} ceil(rows_h/128) tile rows of ceil(ceil(N/32)/4) tiles, its columnwise plane
-    // (N rows x ceil(rows_g/32) scale columns) after sum_{h<g} ceil(rows_h/128) tile columns of
-    // ceil(N/128) tiles: both prefixes are the groups' row-tile prefix.
-    const int64_t Cn = (N + 31) >> 5;
-    auto swz_row_offset = [&](const TileCoord &tc, int64_t grow, int64_t sc) -> int64_t {
-        if constexpr (GROUPED) {
-            const int64_t tiles_before = gpre[tc.g] / p.col_tiles;
-            return tiles_before * 128 * ((Cn + 3) & ~int64_t{3}) + swizzled_offset(grow - goff[tc.g], sc, Cn);
-        } else {
-            return swizzled_offset(grow, sc, Cn);
-        }
+    // and laid out after the previous group's.  A 128 x 128 cast tile's scales fill exactly one
+    // 512-byte tile of each plane: rowwise, its 128 rows x 4 row blocks; columnwise (the plane
+    // of the transposed operand, N rows), its 128 columns x 4 column blocks.
+    //  - rowwise plane tile (rt, ct), tiles of ceil(N/128) per tile row: index rt * col_tiles + ct.
+    //    A grouped tile's rt counts the row tiles of the groups before it too (their planes come
+    //    first), so the same index holds.
+    //  - columnwise plane tile (ct, rt): flat, index ct * row_tiles + rt; grouped, group g's plane
+    //    has N rows and ceil(rows_g/128) tile columns and starts after before * col_tiles tiles
+    //    (before = the row tiles of the groups before g = rt - the tile's row tile in its group):
+    //    index before * col_tiles + ct * ceil(rows_g/128) + (rt - before).
+    static_assert(kBM == 128 && kBN == 128, "one plane tile per cast tile");
+    const int64_t Cn = (N + 31) >> 5;  // scale columns of the plain rowwise plane
+    auto swz_row_tile = [&](const TileCoord &tc) -> uint8_t * {
+        return p.scale_row + (static_cast<int64_t>(tc.rt) * p.col_tiles + (tc.col0 >> 7)) * 512;
     };
-    auto swz_col_offset = [&](const TileCoord &tc, int64_t gcol, int64_t grow) -> int64_t {
+    auto swz_col_tile = [&](const TileCoord &tc) -> uint8_t * {
+        const int ct = tc.col0 >> 7;
         if constexpr (GROUPED) {
-            const int64_t tiles_before = gpre[tc.g] / p.col_tiles;
-            const int64_t rows_g = goff[tc.g + 1] - goff[tc.g];
-            return tiles_before * 4 * ((N + 127) & ~int64_t{127}) +
-                   swizzled_offset(gcol, (grow - goff[tc.g]) >> 5, (rows_g + 31) >> 5);
+            const int64_t first = goff[tc.g];
+            const int rtl = static_cast<int>((tc.row0 - first) >> 7);
+            const int tiles_g = static_cast<int>((goff[tc.g + 1] - first + 127) >> 7);
+            return p.scale_col + (static_cast<int64_t>(tc.rt - rtl) * p.col_tiles + static_cast<int64_t>(ct) * tiles_g +
+                                  rtl) * 512;
         } else {
-            return swizzled_offset(gcol, grow >> 5, (p.M + 31) >> 5);
+            return p.scale_col + (static_cast<int64_t>(ct) * p.row_tiles + tc.rt) * 512;
         }
     };
     for (int it = 0; it < my_count; ++it) {
@@ -611,11 +614,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                             static_cast<uint32_t>(e0) | (static_cast<uint32_t>(e1) << 8) |
                             (static_cast<uint32_t>(e2) << 16) | (static_cast<uint32_t>(e3) << 24);
                     } else {
-                        // the columnwise operand's scales, seen as N rows x ceil(M/32) scale columns
-                        p.scale_col[swz_col_offset(tc, gcol, grow)] = static_cast<uint8_t>(e0);
-                        p.scale_col[swz_col_offset(tc, gcol + 1, grow)] = static_cast<uint8_t>(e1);
-                        p.scale_col[swz_col_offset(tc, gcol + 2, grow)] = static_cast<uint8_t>(e2);
-                        p.scale_col[swz_col_offset(tc, gcol + 3, grow)] = static_cast<uint8_t>(e3);
+                        // the columnwise operand's scales: plane row = this column, plane column =
+                        // the row block; the next three columns are the plane's next rows in the
+                        // same 32-row group (box * 64 + cq * 4 is a multiple of 4): 16 bytes apart
+                        uint8_t *sc = swz_col_tile(tc) + swizzled_in_tile(box * kBoxCols + cq * 4, rb);
+                        sc[0] = static_cast<uint8_t>(e0);
+                        sc[16] = static_cast<uint8_t>(e1);
+                        sc[32] = static_cast<uint8_t>(e2);
+                        sc[48] = static_cast<uint8_t>(e3);
                     }
                 }
                 if constexpr (DBIAS)
@@ -629,6 +635,36 @@ __global__ void __launch_bounds__(kThreads, 2)
                 *reinterpret_cast<float4 *>(colmul + rb * kBN + box * kBoxCols + chunk * 4) =
                     make_float4(scale_multiplier(e0), scale_multiplier(e1), scale_multiplier(e2),
                                 scale_multiplier(e3));
+            }
+        }
+        // GEMM-ready planes: the tile owns one 512-byte tile of each plane (the rowwise plane's
+        // 128 rows x 4 scale columns, the columnwise plane's 128 rows (this tile's columns) x 4
+        // scale columns (its 32-row blocks)).  The entries of those that hold no scale (rows past
+        // the tile's end, columns past N) are zeroed here, so no separate padding pass is needed:
+        // warp (rb, box) zeroes those of its 32 rows x 2 row blocks and of its 64 columns x 1
+        // column block.  Every other entry is written by the phase that forms its scale.
+        if constexpr (SWZ) {
+            if (ok) {
+                const int rb = warp >> 1, box = warp & 1;
+                const int64_t grow = tc.row0 + rb * 32;
+                if (do_row) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int64_t bc = tc.col0 + box * kBoxCols + j * 32;  // the block's first column
+                        if (grow + lane >= tc.row_end || bc >= N)
+                            swz_row_tile(tc)[swizzled_in_tile(rb * 32 + lane, box * 2 + j)] = 0;
+                    }
+                }
+                if (do_col && lane < 16) {
+                    const int64_t gcol = tc.col0 + box * kBoxCols + lane * 4;
+                    if (grow >= tc.row_end || gcol >= N) {
+                        uint8_t *sc = swz_col_tile(tc) + swizzled_in_tile(box * kBoxCols + lane * 4, rb);
+                        sc[0] = 0;
+                        sc[16] = 0;
+                        sc[32] = 0;
+                        sc[48] = 0;
+                    }
+                }
             }
         }
         // a bounded wait that expired: record it, drain this CTA's own copies, return
@@ -739,9 +775,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                     if (in) {
                         store_codes(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
-                        if ((sp & 1) == 0)
-                            p.scale_row[SWZ ? swz_row_offset(tc, grow, gcol >> 5)
-                                            : grow * Cn + (gcol >> 5)] = static_cast<uint8_t>(er);
+                        if ((sp & 1) == 0) {
+                            if constexpr (SWZ)
+                                swz_row_tile(tc)[swizzled_in_tile(r, box * 2 + (sp >> 1))] = static_cast<uint8_t>(er);
+                            else
+                                p.scale_row[grow * Cn + (gcol >> 5)] = static_cast<uint8_t>(er);
+                        }
                         if (AMAX && !do_col)
                             amax_acc = max(amax_acc, row_amax_bits);
                     }

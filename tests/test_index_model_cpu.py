@@ -4,7 +4,7 @@ compute-sanitizer is not available on the test machines, so the kernels'
 memory accesses are checked here instead: this file restates, for every thread
 of every CTA of one launch, the global addresses quantize_kernel (flat and
 grouped, with and without dbias, plain and GEMM-ready scales),
-quantize_dact_kernel, swizzle_pad_kernel and the dbias reduces compute, with
+quantize_dact_kernel and the dbias reduces compute, with
 the same expressions as csrc/quantize.cuh, csrc/dact.cuh, csrc/dbias_reduce.cuh
 and csrc/api.cu (persistent tile loop, per-group tile prefix, phase-1 and
 phase-2 lane maps, 16- and 8-byte stores, scale and partial-sum rows).  Each
@@ -117,6 +117,37 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
     tiles = tile_list(M, N, offsets)
     ws_rows = max([t[3] for t in tiles], default=-1) + 1
     ws = Plane("ws", ws_rows * N, 4)
+
+    # GEMM-ready planes: the kernel addresses one 512-byte plane tile per cast tile (swz_row_tile /
+    # swz_col_tile) plus the entry's byte within it; each is checked against the layout's
+    # definition on the whole plane (swizzled_offset, after the planes of the groups before)
+    def in_tile(r, c):
+        return ((r & 31) << 4) | (((r >> 5) & 3) << 2) | c
+
+    def swz_row(tile, r, sc):
+        row0, _, col0, rt, _, g = tile
+        got = (rt * -(-N // BN) + (col0 >> 7)) * 512 + in_tile(r - row0, sc - (col0 >> 5))
+        first = 0 if offsets is None else offsets[g]
+        before = rt - (row0 - first) // BM
+        want = before * 128 * ((Cr + 3) // 4 * 4) + swizzled_offset(r - first, sc, Cr)
+        assert np.array_equal(got, want)
+        return got
+
+    def swz_col(tile, gcol, grow):
+        row0, _, col0, rt, _, g = tile
+        ct, rb = col0 >> 7, (grow - row0) >> 5
+        if offsets is None:
+            got = (ct * -(-M // BM) + rt) * 512 + in_tile(gcol - col0, rb)
+            want = swizzled_offset(gcol, grow >> 5, -(-M // 32))
+        else:
+            first = offsets[g]
+            rtl, tiles_g = (row0 - first) >> 7, -(-(offsets[g + 1] - first) // BM)
+            got = ((rt - rtl) * -(-N // BN) + ct * tiles_g + rtl) * 512 + in_tile(gcol - col0, rb)
+            want = ((rt - rtl) * 4 * ((N + 127) // 128 * 128) +
+                    swizzled_offset(gcol, (grow - first) >> 5, -(-(offsets[g + 1] - first) // 32)))
+        assert np.array_equal(got, want)
+        return got
+
     # phase-1 lane map: warp -> (32-row block, box); lane -> (4-column group, 16-row half)
     w1, l1 = np.repeat(np.arange(8), 32), np.tile(LANES, 8)
     rb1, box1, cq1, half1 = w1 >> 1, w1 & 1, l1 & 15, l1 >> 4
@@ -157,18 +188,29 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                         zeroed_rows = sorted({first + c // 8 for c in chunks})
                         assert zeroed_rows == list(range(first + live, first + 32))
                         assert len(chunks) == len(set(chunks)) == (32 - live) * 8
+            tile = tiles[t]
             grow, gcol = row0 + rb1 * 32, col0 + box1 * BOX + cq1 * 4
             sel = (grow < row_end) & (half1 == 0) & (gcol < N) & do_col
-            if swz and offsets is not None:
-                before = rt - (row0 - offsets[g]) // BM          # the kernel's gpre[g] / col_tiles
-                C = -(-(offsets[g + 1] - offsets[g]) // 32)
+            if swz:
+                # one offset per lane, the next three plane rows 16 bytes on (gcol % 4 == 0)
+                o = swz_col(tile, gcol[sel], grow[sel])
                 for j in range(4):
-                    scale_col.write(before * 4 * ((N + 127) // 128 * 128) +
-                                    swizzled_offset(gcol[sel] + j, (grow[sel] - offsets[g]) >> 5, C))
-            elif swz:
-                C = -(-M // 32)
-                for j in range(4):
-                    scale_col.write(swizzled_offset(gcol[sel] + j, grow[sel] >> 5, C))
+                    assert np.array_equal(o + 16 * j, swz_col(tile, gcol[sel] + j, grow[sel]))
+                    scale_col.write(o + 16 * j)
+                # the tile's own plane tiles' padding: warp (rb, box) zeroes the entries of its
+                # 32 rows x 2 row blocks past the tile's end or N (all lanes, one row each), and
+                # of its 64 columns x 1 column block (lanes < 16, four plane rows each)
+                if do_row:
+                    r = row0 + rb1 * 32 + l1
+                    for j in range(2):
+                        bc = col0 + box1 * BOX + j * 32
+                        pad = (r >= row_end) | (bc >= N)
+                        scale_row.write(swz_row(tile, r[pad], bc[pad] >> 5))
+                if do_col:
+                    pad = (l1 < 16) & ((grow >= row_end) | (gcol >= N))
+                    o = swz_col(tile, gcol[pad], grow[pad])
+                    for j in range(4):
+                        scale_col.write(o + 16 * j)
             else:
                 scale_col.write((sb + rb1[sel]) * N + gcol[sel], 4, align=4)
             if dbias:
@@ -186,55 +228,9 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                     plane.write(grow[part] * N + gcol[part], 8, align=8)
             if do_row:
                 se = ok & (sp2 % 2 == 0)
-                if swz and offsets is not None:
-                    before = rt - (row0 - offsets[g]) // BM
-                    scale_row.write(before * 128 * ((Cr + 3) // 4 * 4) +
-                                    swizzled_offset(grow[se] - offsets[g], gcol[se] >> 5, Cr))
-                else:
-                    scale_row.write(swizzled_offset(grow[se], gcol[se] >> 5, Cr) if swz
-                                    else grow[se] * Cr + (gcol[se] >> 5))
+                scale_row.write(swz_row(tile, grow[se], gcol[se] >> 5) if swz else grow[se] * Cr + (gcol[se] >> 5))
     return dict(out_row=out_row, out_col=out_col, scale_row=scale_row, scale_col=scale_col, ws=ws,
                 ws_rows=ws_rows, tiles=tiles)
-
-
-class PlaneAt:
-    """A view of a Plane from byte `base` on (a group's plane inside the concatenated planes)."""
-
-    def __init__(self, plane, base):
-        self.plane, self.base = plane, base
-
-    def write(self, idx, nbytes=1, align=1):
-        self.plane.write(np.asarray(idx, np.int64) + self.base, nbytes, align)
-
-
-def model_grouped_swizzle_pad(offsets, N, scale_row, scale_col):
-    """grouped_swizzle_pad_kernel, one CTA per group and one launch per plane: the group's plane
-    starts at its row-tile prefix (sum of ceil(rows_h / 128) over h < g) times the bytes of one
-    128-row tile of that plane; zero its padding entries as the flat pad kernel does."""
-    Cn = -(-N // 32)
-    for colwise, plane in ((False, scale_row), (True, scale_col)):
-        for g in range(len(offsets) - 1):
-            before = sum(-(-(offsets[h + 1] - offsets[h]) // 128) for h in range(g))
-            rows_g = offsets[g + 1] - offsets[g]
-            if rows_g <= 0:
-                continue
-            R, C = (N, -(-rows_g // 32)) if colwise else (rows_g, Cn)
-            base = before * 4 * ((N + 127) // 128 * 128) if colwise else before * 128 * ((Cn + 3) // 4 * 4)
-            model_swizzle_pad(R, C, PlaneAt(plane, base))
-
-
-def model_swizzle_pad(R, C, plane):
-    """swizzle_pad_kernel: zero the padding entries of the last row tile and the last column tile."""
-    col_tiles, row_tiles = (C + 3) // 4, (R + 127) // 128
-    if R % 128 == 0 and C % 4 == 0:
-        return
-    for t in range(col_tiles + row_tiles - 1):
-        rt = row_tiles - 1 if t < col_tiles else t - col_tiles
-        ct = t if t < col_tiles else col_tiles - 1
-        for w in range(512):
-            r, c = rt * 128 + ((w >> 2) & 3) * 32 + (w >> 4), ct * 4 + (w & 3)
-            if r >= R or c >= C:
-                plane.write(((rt * col_tiles + ct) << 9) + w)
 
 
 def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True, do_col=True, reuse=False):
@@ -244,23 +240,12 @@ def check_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
             m[name].once()
         else:
             assert not m[name].count.any()
-    if swz and offsets is not None:
-        model_grouped_swizzle_pad(offsets, N, m["scale_row"], m["scale_col"])
-        m["scale_row"].once()
-        m["scale_col"].once()
-    elif swz:
-        Cr = -(-N // 32)
-        if do_row:
-            model_swizzle_pad(M, Cr, m["scale_row"])
-            m["scale_row"].once()
-        if do_col:
-            model_swizzle_pad(N, -(-M // 32), m["scale_col"])
-            m["scale_col"].once()
-    else:
-        if do_row:
-            m["scale_row"].once()
-        if do_col:
-            m["scale_col"].once()
+    # every scale byte once; a GEMM-ready plane's padding entries included (written by the tiles)
+    for name, on in (("scale_row", do_row), ("scale_col", do_col)):
+        if on:
+            m[name].once()
+        else:
+            assert not m[name].count.any()
     if dbias:
         # the reduce reads ws[t * N + j] for every tile row t < ws_rows and column j < N
         m["ws"].once()
