@@ -60,7 +60,8 @@ constexpr int kOffDSum = kOffColMul + 4 * kBN * 4;     // float [4][128]
 constexpr int kOffBars = kOffDSum + 4 * kBN * 4;       // uint64 [kStages]
 constexpr int kOffCoord = kOffBars + 8 * kStages;      // TileCoord [kStages]
 constexpr int kOffScan = kOffCoord + 32 * kStages;     // int64 [kThreads / 32]
-constexpr int kOffGOff = kOffScan + 8 * (kThreads / 32);   // int64 [kMaxGroups + 1]
+constexpr int kOffRowSc = kOffScan + 8 * (kThreads / 32);  // uint32 [kBM]: a tile's row scales
+constexpr int kOffGOff = kOffRowSc + 4 * kBM;              // int64 [kMaxGroups + 1]
 constexpr int kOffGPre = kOffGOff + 8 * (kMaxGroups + 1);  // int [kMaxGroups + 1]
 constexpr int kOffGSB = kOffGPre + 4 * (kMaxGroups + 1);   // int [kMaxGroups + 1]
 constexpr int kSmemFlat = kOffGOff + 1024;                 // + alignment slack
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // warp-local: [kStages] warps done with a stage (in the scan's space, which the grouped
     // set-up has finished with before the counters are reset)
     unsigned *stage_done = reinterpret_cast<unsigned *>(smem + kOffScan);
+    uint32_t *rowsc = reinterpret_cast<uint32_t *>(smem + kOffRowSc);
 
     constexpr bool kXS = GROUPED || DBIAS;  // form of the BF16 |x| maximum (absmax_step)
     // With a transcendental activation (bound on the SM side) a warp's phase-2 tasks are the
@@ -480,6 +482,33 @@ __global__ void __launch_bounds__(kThreads, 2)
                                   rtl) * 512;
         } else {
             return p.scale_col + (static_cast<int64_t>(ct) * p.row_tiles + tc.rt) * 512;
+        }
+    };
+    // A row's four 32-column blocks of a tile have their scales in four contiguous bytes (plain:
+    // scale columns col0/32 .. +3 of the row; GEMM-ready: the row's entries of its plane tile).
+    // Outside the warp-local phases, phase 2 collects them in shared memory and the tile's end
+    // stores each row's four with one store (one L2 request per row, not one per lane pair):
+    // v holds block b in byte b.  Blocks at or past N are not stored (plain), or stored as the
+    // plane's zero padding (GEMM-ready).  A 32-bit store where the destination allows it
+    // (scale_row needs no alignment), bytes otherwise.
+    const bool row_scales_aligned = (reinterpret_cast<uintptr_t>(p.scale_row) & 3) == 0 && (SWZ || (Cn & 3) == 0);
+    auto store_row_scales = [&](const TileCoord &tc, int r, int64_t grow, uint32_t v) {
+        const int64_t left = (N - tc.col0 + 31) >> 5;
+        const int nb = left < 4 ? static_cast<int>(left) : 4;  // blocks of the row in this tile
+        uint8_t *dst;
+        if constexpr (SWZ) {
+            dst = swz_row_tile(tc) + swizzled_in_tile(r, 0);
+            if (nb < 4)
+                v &= (1u << (8 * nb)) - 1u;
+        } else {
+            dst = p.scale_row + grow * Cn + (tc.col0 >> 5);
+        }
+        if (row_scales_aligned && (SWZ || nb == 4)) {
+            *reinterpret_cast<uint32_t *>(dst) = v;
+        } else {
+            const int nw = SWZ ? 4 : nb;
+            for (int b = 0; b < nw; ++b)
+                dst[b] = static_cast<uint8_t>(v >> (8 * b));
         }
     };
     for (int it = 0; it < my_count; ++it) {
@@ -651,7 +680,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int64_t bc = tc.col0 + box * kBoxCols + j * 32;  // the block's first column
-                        if (grow + lane >= tc.row_end || bc >= N)
+                        // (a live row's blocks past N are written with its other scales outside
+                        // the warp-local phases)
+                        if (grow + lane >= tc.row_end || (kWarpLocal && bc >= N))
                             swz_row_tile(tc)[swizzled_in_tile(rb * 32 + lane, box * 2 + j)] = 0;
                     }
                 }
@@ -776,7 +807,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (in) {
                         store_codes(p.out_row + grow * N + gcol, o[0], o[1], o[2], o[3], rows16, gcol + 16 > N);
                         if ((sp & 1) == 0) {
-                            if constexpr (SWZ)
+                            if constexpr (!kWarpLocal)
+                                reinterpret_cast<uint8_t *>(rowsc)[r * 4 + box * 2 + (sp >> 1)] = static_cast<uint8_t>(er);
+                            else if constexpr (SWZ)
                                 swz_row_tile(tc)[swizzled_in_tile(r, box * 2 + (sp >> 1))] = static_cast<uint8_t>(er);
                             else
                                 p.scale_row[grow * Cn + (gcol >> 5)] = static_cast<uint8_t>(er);
@@ -834,7 +867,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             continue;
         } else {
-            __syncthreads();  // stage `slot` and colmul are free again
+            __syncthreads();  // stage `slot` and colmul are free again; the tile's row scales are in rowsc
+            if (do_row && tid < kBM && tc.row0 + tid < tc.row_end)
+                store_row_scales(tc, tid, tc.row0 + tid, rowsc[tid]);
         }
 
         if (tid == 0 && it + kStages < my_count) {

@@ -204,7 +204,7 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                     r = row0 + rb1 * 32 + l1
                     for j in range(2):
                         bc = col0 + box1 * BOX + j * 32
-                        pad = (r >= row_end) | (bc >= N)
+                        pad = (r >= row_end) | (reuse & (bc >= N))
                         scale_row.write(swz_row(tile, r[pad], bc[pad] >> 5))
                 if do_col:
                     pad = (l1 < 16) & ((grow >= row_end) | (gcol >= N))
@@ -226,9 +226,25 @@ def model_quantize(M, N, grid, offsets=None, dbias=False, swz=False, do_row=True
                 if on:
                     plane.write(grow[full] * N + gcol[full], 16, align=16 if rows16 else 8)
                     plane.write(grow[part] * N + gcol[part], 8, align=8)
-            if do_row:
-                se = ok & (sp2 % 2 == 0)
+            se = ok & (sp2 % 2 == 0)
+            if do_row and reuse:    # one byte per (row, block): lanes sp = 0, 2
                 scale_row.write(swz_row(tile, grow[se], gcol[se] >> 5) if swz else grow[se] * Cr + (gcol[se] >> 5))
+            elif do_row:
+                # phase 2 puts row r's block b scale at byte 4r + b of the shared rowsc; after the
+                # tile's barrier thread tid < 128 stores row tid's four bytes (blocks past N: not
+                # stored, or zero padding of the GEMM-ready plane), one 32-bit store where aligned
+                staged = (grow[se] - row0) * 4 + box2[se] * 2 + (sp2[se] >> 1)
+                assert len(set(staged.tolist())) == staged.size and staged.max(initial=0) < 4 * BM
+                nb = min(4, -(-(N - col0) // 32))
+                live = np.arange(row0, row_end)
+                want = {4 * (r - row0) + b for r in live for b in range(nb)}
+                assert want == set(staged.tolist())         # every stored byte was formed by this tile
+                if swz:
+                    scale_row.write(swz_row(tile, live, np.full(live.size, col0 >> 5)), 4, align=4)
+                elif nb == 4 and Cr % 4 == 0:
+                    scale_row.write(live * Cr + (col0 >> 5), 4, align=4)
+                else:
+                    scale_row.write(live * Cr + (col0 >> 5), nb)
     return dict(out_row=out_row, out_col=out_col, scale_row=scale_row, scale_col=scale_col, ws=ws,
                 ws_rows=ws_rows, tiles=tiles)
 
