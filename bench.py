@@ -552,7 +552,19 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
-        if grouped or args.swizzled or args.amax or act or dact or glu or dglu:
+        if grouped and not (with_dbias or args.swizzled or glu):
+            staging = torch.empty(mx.mxfp8_quantize_grouped_host_staging_bytes(M, N, G), dtype=torch.uint8,
+                                  device="cuda")
+            off_host = torch.from_numpy(offsets.astype(np.int64))
+            path = ("mxfp8_quantize_grouped_host: pinned host buffers in and out, host offsets, H2D / kernel / "
+                    "D2H pipelined over row chunks inside the library")
+
+            def e2e_step():
+                st = mx.mxfp8_quantize_grouped_host(x_host, M, N, G, off_host, fmt, act, *outs_host[:4], staging,
+                                                    staging.numel(), stream)
+                if st != 0:
+                    raise mx.MXFP8Error(st, "bench e2e step")
+        elif grouped or args.swizzled or args.amax or act or dact or glu or dglu:
             # no host-buffer call for these options: copy in, device call, copy every output out
             x_stage = torch.empty_like(x)
             path = "pinned host -> device copy, C-ABI call, device -> pinned host copies (one stream)"

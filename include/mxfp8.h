@@ -205,6 +205,55 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
                                    float *dbias_host, void *staging, size_t staging_bytes,
                                    void *stream);
 
+/*
+ * Device staging bytes mxfp8_quantize_grouped_host needs: three chunk slots
+ * (a chunk of x, its outputs, its columnwise scale rows and its group
+ * offsets).  0 for invalid shapes or group counts.
+ */
+size_t mxfp8_quantize_grouped_host_staging_bytes(int64_t total_rows, int64_t N, int num_groups);
+
+/*
+ * The grouped cast (mxfp8_quantize_grouped; with an activation,
+ * mxfp8_quantize_grouped_activated) with x, the offsets and every output in
+ * HOST memory, pipelined over row chunks like mxfp8_quantize_host.  Results
+ * are identical to the device call on the same data: a chunk boundary that
+ * falls inside a group is moved down to a row a multiple of 32 rows after the
+ * group's first row, so a group cut in two keeps its own 32-row blocks, and
+ * the columnwise scale rows of the pieces are contiguous.
+ *
+ *   x_host        host bf16 [total_rows, N].
+ *   host_offsets  host int64 [num_groups + 1], the layout of
+ *                 mxfp8_quantize_grouped; checked here (offsets[0] == 0,
+ *                 non-decreasing, offsets[num_groups] == total_rows), else
+ *                 MXFP8_ERR_GROUPS before any work.  Read during the call
+ *                 only.
+ *   activation    MXFP8_ACT_NONE or one of the activations.
+ *   out_*_host    host buffers in the device call's layouts (scale_col with
+ *                 sum_g ceil(rows_g / 32) rows); a direction is skipped by
+ *                 passing both of its pointers NULL.  Pinned memory lets the
+ *                 copies overlap.
+ *   staging       device buffer, 256-byte aligned, at least
+ *                 mxfp8_quantize_grouped_host_staging_bytes(...) bytes.
+ *   stream        as mxfp8_quantize_host.
+ * No dbias, noop or err_flag.  total_rows > 0.
+ */
+mxfp8_status_t mxfp8_quantize_grouped_host(const void *x_host, int64_t total_rows, int64_t N,
+                                           int num_groups, const int64_t *host_offsets,
+                                           int fp8_fmt, int activation,
+                                           void *out_row_host, void *scale_row_host,
+                                           void *out_col_host, void *scale_col_host,
+                                           void *staging, size_t staging_bytes, void *stream);
+
+/*
+ * Diagnostic (no counterpart on the pages): the row boundaries
+ * 0 = b[0] < ... < b[k] = total_rows of the chunks mxfp8_quantize_grouped_host
+ * uses for these offsets and N.  Writes min(k + 1, max_bounds) of them to
+ * bounds (may be NULL) and returns k + 1, or -1 for invalid arguments.
+ * Host only: it touches no device.
+ */
+int64_t mxfp8_grouped_host_chunks(const int64_t *host_offsets, int num_groups, int64_t total_rows,
+                                  int64_t N, int64_t *bounds, int64_t max_bounds);
+
 /* Layout of the E8M0 scale planes (the `swizzled` field of the PR #3137 config key). */
 typedef enum {
     MXFP8_SCALES_PLAIN = 0,    /* scale_row [M, N/32], scale_col [M/32, N], row-major */

@@ -16,5 +16,7 @@ from .binding import (  # noqa: F401
     mxfp8_quantize_dact, quantize_dact, mxfp8_quantize_gated, quantize_gated, mxfp8_quantize_dgated,
     quantize_dgated, mxfp8_quantize_gated_grouped, quantize_gated_grouped, mxfp8_quantize_grouped_activated,
     mxfp8_quantize_grouped_swizzled, mxfp8_grouped_swizzled_scale_bytes, mxfp8_selftest_bounded_wait, mxfp8_activation_values,
+    mxfp8_quantize_grouped_host, mxfp8_quantize_grouped_host_staging_bytes, mxfp8_grouped_host_chunks,
+    quantize_grouped_host,
     QuantizeConfig, SCALES_PLAIN, SCALES_SWIZZLED, make_config, mxfp8_quantize_ex, mxfp8_scale_bytes,
 )

@@ -97,6 +97,13 @@ def lib():
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
             L.mxfp8_quantize_host.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.mxfp8_quantize_grouped_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_grouped_host_staging_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_grouped_host.restype = i32
+            L.mxfp8_quantize_grouped_host.argtypes = [vp, i64, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp,
+                                                      ctypes.c_size_t, vp]
+            L.mxfp8_grouped_host_chunks.restype = i64
+            L.mxfp8_grouped_host_chunks.argtypes = [vp, i32, i64, i64, vp, i64]
             L.mxfp8_scale_bytes.restype = ctypes.c_size_t
             L.mxfp8_scale_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_ex.restype = i32
@@ -245,6 +252,34 @@ def mxfp8_quantize_host(x_host, M, N, fp8_fmt, out_row_host, scale_row_host, out
     return int(lib().mxfp8_quantize_host(_addr(x_host), M, N, fp8_fmt, _addr(out_row_host), _addr(scale_row_host),
                                          _addr(out_col_host), _addr(scale_col_host), _addr(dbias_host),
                                          _addr(staging), int(staging_bytes), _stream(stream)))
+
+
+def mxfp8_quantize_grouped_host_staging_bytes(total_rows: int, N: int, num_groups: int) -> int:
+    return int(lib().mxfp8_quantize_grouped_host_staging_bytes(total_rows, N, num_groups))
+
+
+def mxfp8_quantize_grouped_host(x_host, total_rows, N, num_groups, host_offsets, fp8_fmt, activation, out_row_host,
+                                scale_row_host, out_col_host, scale_col_host, staging, staging_bytes,
+                                stream=None) -> int:
+    """The grouped cast with host buffers; ``host_offsets`` a CPU int64 tensor or address."""
+    if isinstance(activation, str):
+        activation = ACTIVATIONS[activation.lower()]
+    return int(lib().mxfp8_quantize_grouped_host(_addr(x_host), total_rows, N, num_groups, _addr(host_offsets),
+                                                 fp8_fmt, int(activation), _addr(out_row_host),
+                                                 _addr(scale_row_host), _addr(out_col_host), _addr(scale_col_host),
+                                                 _addr(staging), int(staging_bytes), _stream(stream)))
+
+
+def mxfp8_grouped_host_chunks(host_offsets, total_rows: int, N: int) -> list:
+    """Chunk boundaries the grouped host call uses for these host offsets (a list of rows)."""
+    off = torch.as_tensor(host_offsets, dtype=torch.int64, device="cpu").contiguous()
+    G = off.numel() - 1
+    n = int(lib().mxfp8_grouped_host_chunks(off.data_ptr(), G, total_rows, N, None, 0))
+    if n < 0:
+        raise ValueError("invalid offsets or shape")
+    out = torch.empty((n,), dtype=torch.int64)
+    lib().mxfp8_grouped_host_chunks(off.data_ptr(), G, total_rows, N, out.data_ptr(), n)
+    return out.tolist()
 
 
 def mxfp8_scale_bytes(rows: int, scale_cols: int, scale_layout: int = SCALES_PLAIN) -> int:
@@ -398,6 +433,32 @@ def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_host")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+
+
+def quantize_grouped_host(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, activation="none",
+                          rowwise: bool = True, colwise: bool = True, staging: Optional[torch.Tensor] = None,
+                          stream=None) -> MXFP8Tensor:
+    """The grouped cast of a host (CPU, ideally pinned) bf16 tensor with host int64 offsets [G+1];
+    outputs are pinned host tensors, ready once ``stream`` has been synchronised."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous() or x.is_cuda:
+        raise ValueError("x must be a contiguous 2-D torch.bfloat16 host tensor")
+    off = torch.as_tensor(offsets, dtype=torch.int64, device="cpu").contiguous()
+    total, N = x.shape
+    G = off.numel() - 1
+    pin = dict(pin_memory=True)
+    u8 = torch.uint8
+    out_row = torch.empty((total, N), dtype=u8, **pin) if rowwise else None
+    scale_row = torch.empty((total, -(-N // BLOCK)), dtype=u8, **pin) if rowwise else None
+    out_col = torch.empty((total, N), dtype=u8, **pin) if colwise else None
+    scale_col = torch.empty((grouped_scale_col_rows(off), N), dtype=u8, **pin) if colwise else None
+    need = mxfp8_quantize_grouped_host_staging_bytes(total, N, G)
+    if staging is None:
+        staging = torch.empty((max(need, 256),), dtype=u8, device="cuda")
+    st = mxfp8_quantize_grouped_host(x, total, N, G, off, _fmt(fmt), activation, out_row, scale_row, out_col,
+                                     scale_col, staging, staging.numel(), stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_grouped_host")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
 
 
 def quantize_dact(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activation="gelu",

@@ -1289,6 +1289,66 @@ bool cuda_ok(cudaError_t e)
     return false;
 }
 
+// Chunk boundaries of a grouped host call: the flat plan's, each interior one moved down to the
+// nearest row a multiple of 32 rows after the start of the group that contains it.  A group cut
+// by a boundary is then quantized as two pieces whose 32-row blocks are the group's own, so the
+// chunks together give the one-shot call's bytes (each group is its own flat problem).  The flat
+// plan's interior boundaries are at least 128 rows apart and move by less than 32, so they stay
+// increasing, and a chunk holds at most R + 31 rows.  host_offsets are checked by the caller.
+std::vector<int64_t> grouped_chunk_plan(const int64_t *off, int G, int64_t M, int64_t R)
+{
+    std::vector<int64_t> b = chunk_plan(M, R);
+    int g = 0;
+    for (size_t i = 1; i + 1 < b.size(); ++i) {
+        while (g < G && off[g + 1] <= b[i])
+            ++g;  // now off[g] <= b[i] < off[g + 1]
+        b[i] = off[g] + (b[i] - off[g]) / 32 * 32;
+    }
+    return b;
+}
+
+// Device staging of one chunk of a grouped host call: up to Rcap rows of x and its outputs, the
+// chunk's columnwise scale rows (at most Rcap/32 + G: each group piece rounds up once) and the
+// chunk's group offsets.
+struct GroupedSlotLayout {
+    size_t x, out_row, out_col, scale_row, scale_col, off, bytes;
+};
+
+GroupedSlotLayout grouped_slot_layout(int64_t Rcap, int64_t N, int G)
+{
+    GroupedSlotLayout L;
+    size_t o = 0;
+    L.x = o;
+    o += align256(static_cast<size_t>(Rcap * N * 2));
+    L.out_row = o;
+    o += align256(static_cast<size_t>(Rcap * N));
+    L.out_col = o;
+    o += align256(static_cast<size_t>(Rcap * N));
+    L.scale_row = o;
+    o += align256(static_cast<size_t>(Rcap * ((N + 31) / 32)));
+    L.scale_col = o;
+    o += align256(static_cast<size_t>((Rcap / 32 + G) * N));
+    L.off = o;
+    o += align256(static_cast<size_t>(G + 1) * 8);
+    L.bytes = o;
+    return L;
+}
+
+int64_t grouped_host_rcap(int64_t M, int64_t N) { return host_chunk_rows(M, N) + 32; }
+
+// A chunk's group offsets, passed by value to a one-CTA kernel on the upload stream (so the
+// upload needs no host staging buffer that must outlive the call).
+constexpr int kOffsetPack = 257;
+struct OffsetPack {
+    int64_t v[kOffsetPack];
+};
+
+__global__ void fill_offsets_kernel(int64_t *dst, OffsetPack pack, int n)
+{
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        dst[i] = pack.v[i];
+}
+
 }  // namespace
 
 extern "C" {
@@ -1406,6 +1466,149 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
             return MXFP8_ERR_LAUNCH;
     }
     // the caller's stream resumes once the last copy to the host is done
+    if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
+        return MXFP8_ERR_LAUNCH;
+    return MXFP8_OK;
+}
+
+size_t mxfp8_quantize_grouped_host_staging_bytes(int64_t total_rows, int64_t N, int num_groups)
+{
+    if (total_rows <= 0 || N <= 0 || N % 8 || num_groups < 1 || num_groups > MXFP8_MAX_GROUPS)
+        return 0;
+    return kHostSlots * grouped_slot_layout(grouped_host_rcap(total_rows, N), N, num_groups).bytes;
+}
+
+int64_t mxfp8_grouped_host_chunks(const int64_t *host_offsets, int num_groups, int64_t total_rows, int64_t N,
+                                  int64_t *bounds, int64_t max_bounds)
+{
+    if (host_offsets == nullptr || num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || total_rows <= 0 || N <= 0 ||
+        N % 8 || host_offsets[0] != 0 || host_offsets[num_groups] != total_rows)
+        return -1;
+    for (int g = 0; g < num_groups; ++g)
+        if (host_offsets[g + 1] < host_offsets[g])
+            return -1;
+    const std::vector<int64_t> b =
+        grouped_chunk_plan(host_offsets, num_groups, total_rows, host_chunk_rows(total_rows, N));
+    for (size_t i = 0; i < b.size() && static_cast<int64_t>(i) < max_bounds && bounds != nullptr; ++i)
+        bounds[i] = b[i];
+    return static_cast<int64_t>(b.size());
+}
+
+mxfp8_status_t mxfp8_quantize_grouped_host(const void *x_host, int64_t total_rows, int64_t N, int num_groups,
+                                           const int64_t *host_offsets, int fp8_fmt, int activation,
+                                           void *out_row_host, void *scale_row_host, void *out_col_host,
+                                           void *scale_col_host, void *staging, size_t staging_bytes,
+                                           void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_NONE || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (total_rows <= 0 || N <= 0 || N % 8 || total_rows >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (num_groups < 1 || num_groups > MXFP8_MAX_GROUPS || host_offsets == nullptr)
+        return MXFP8_ERR_GROUPS;
+    // the offsets are on the host here, so a bad vector is rejected before any work
+    if (host_offsets[0] != 0 || host_offsets[num_groups] != total_rows)
+        return MXFP8_ERR_GROUPS;
+    for (int g = 0; g < num_groups; ++g)
+        if (host_offsets[g + 1] < host_offsets[g])
+            return MXFP8_ERR_GROUPS;
+    if (x_host == nullptr || staging == nullptr)
+        return MXFP8_ERR_NULL;
+    if ((out_row_host == nullptr) != (scale_row_host == nullptr) ||
+        (out_col_host == nullptr) != (scale_col_host == nullptr) ||
+        (out_row_host == nullptr && out_col_host == nullptr))
+        return MXFP8_ERR_NULL;
+    if (!aligned(staging, 256))
+        return MXFP8_ERR_ALIGN;
+    if (staging_bytes < mxfp8_quantize_grouped_host_staging_bytes(total_rows, N, num_groups))
+        return MXFP8_ERR_WORKSPACE;
+
+    int device = 0;
+    mxfp8_status_t st = current_device(&device);
+    if (st != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(device, &hp)) != MXFP8_OK)
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const GroupedSlotLayout L = grouped_slot_layout(grouped_host_rcap(total_rows, N), N, num_groups);
+    unsigned char *base = static_cast<unsigned char *>(staging);
+    const unsigned char *xh = static_cast<const unsigned char *>(x_host);
+    const bool row = out_row_host != nullptr, col = out_col_host != nullptr;
+    const int64_t Cn = (N + 31) / 32;
+
+    if (!cuda_ok(cudaEventRecord(hp->start, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+        !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+        return MXFP8_ERR_LAUNCH;
+    const std::vector<int64_t> plan =
+        grouped_chunk_plan(host_offsets, num_groups, total_rows, host_chunk_rows(total_rows, N));
+    const int64_t chunks = static_cast<int64_t>(plan.size()) - 1;
+    int64_t s0 = 0;  // the chunk's first columnwise scale row
+    OffsetPack pack;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int k = static_cast<int>(c % kHostSlots);
+        const int64_t r0 = plan[c], r1 = plan[c + 1], rows = r1 - r0;
+        unsigned char *slot = base + k * L.bytes;
+        int64_t *off_dev = reinterpret_cast<int64_t *>(slot + L.off);
+        // the slot is free once its previous outputs have left
+        if (c >= kHostSlots && !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->d2h_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // the chunk's offsets: every group's rows clipped to [r0, r1), relative to r0
+        int64_t scale_rows = 0;
+        for (int g0 = 0; g0 <= num_groups; g0 += kOffsetPack) {
+            const int n = num_groups + 1 - g0 < kOffsetPack ? num_groups + 1 - g0 : kOffsetPack;
+            for (int i = 0; i < n; ++i) {
+                const int64_t o = host_offsets[g0 + i];
+                pack.v[i] = (o < r0 ? r0 : o > r1 ? r1 : o) - r0;
+            }
+            fill_offsets_kernel<<<1, 256, 0, hp->h2d>>>(off_dev + g0, pack, n);
+            g_launches.fetch_add(1, std::memory_order_relaxed);
+        }
+        for (int g = 0; g < num_groups; ++g) {
+            const int64_t a = host_offsets[g] < r0 ? r0 : host_offsets[g] > r1 ? r1 : host_offsets[g];
+            const int64_t e = host_offsets[g + 1] < r0 ? r0 : host_offsets[g + 1] > r1 ? r1 : host_offsets[g + 1];
+            scale_rows += (e - a + 31) / 32;
+        }
+        if (!cuda_ok(cudaGetLastError()) ||
+            !cuda_ok(cudaMemcpyAsync(slot + L.x, xh + r0 * N * 2, static_cast<size_t>(rows * N * 2),
+                                     cudaMemcpyHostToDevice, hp->h2d)) ||
+            !cuda_ok(cudaEventRecord(hp->h2d_done[k], hp->h2d)) ||
+            !cuda_ok(cudaStreamWaitEvent(stream, hp->h2d_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // the grouped cast of the chunk on the caller's stream
+        st = grouped_impl(slot + L.x, rows, N, num_groups, off_dev, fp8_fmt, row ? slot + L.out_row : nullptr,
+                          row ? slot + L.scale_row : nullptr, col ? slot + L.out_col : nullptr,
+                          col ? slot + L.scale_col : nullptr, nullptr, nullptr, nullptr, nullptr, stream, activation);
+        if (st != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->comp_done[k], stream)) ||
+            !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->comp_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        bool ok = true;
+        if (row) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + r0 * N, slot + L.out_row,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + r0 * Cn,
+                                               slot + L.scale_row, static_cast<size_t>(rows * Cn),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (col) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + r0 * N, slot + L.out_col,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + s0 * N,
+                                               slot + L.scale_col, static_cast<size_t>(scale_rows * N),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+        s0 += scale_rows;
+    }
     if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
         return MXFP8_ERR_LAUNCH;
     return MXFP8_OK;

@@ -312,3 +312,66 @@ def test_noalloc_status_order_matches_quantize(cuda_lib):
     assert binding.mxfp8_quantize_dbias_noalloc(A, 1 << 31, 64, 0, A, A, A, A, A, None, None) == 2      # SHAPE
     assert binding.mxfp8_quantize_dbias_noalloc(A, 64, 64, 0, A, A, A, A, None, None, None) == 1        # NULL dbias
     assert binding.mxfp8_quantize_dbias_noalloc(A, 32768, 16384, 0, A, A, A, A, A, None, None) == 2     # beyond 8 MiB
+
+
+def test_grouped_host_rejections(cuda_lib):
+    import torch
+    good = torch.tensor([0, 45, 45, 128], dtype=torch.int64)
+
+    def gh(x=A, total=128, N=64, off=good, G=3, fmt=0, act=0, orow=A, srow=A, ocol=A, scol=A, staging=A,
+           nbytes=1 << 30):
+        return mx.mxfp8_quantize_grouped_host(x, total, N, G, off, fmt, act, orow, srow, ocol, scol, staging,
+                                              nbytes, 0)
+    assert gh(fmt=2) == FORMAT and gh(act=6) == FORMAT and gh(act=-1) == FORMAT
+    assert gh(total=0) == SHAPE and gh(N=36) == SHAPE
+    assert gh(G=0) == GROUPS and gh(off=None) == GROUPS and gh(G=mx.MAX_GROUPS + 1) == GROUPS
+    # the offsets are read on the host: a bad vector is rejected before any device work
+    assert gh(off=torch.tensor([0, 50, 40, 128])) == GROUPS
+    assert gh(off=torch.tensor([1, 50, 60, 128])) == GROUPS
+    assert gh(off=torch.tensor([0, 50, 60, 127])) == GROUPS
+    assert gh(x=None) == NULL and gh(staging=None) == NULL and gh(orow=None) == NULL
+    assert gh(orow=None, srow=None, ocol=None, scol=None) == NULL
+    assert gh(staging=A + 16) == ALIGN and gh(nbytes=1024) == WORKSPACE
+    assert gh() == DEVICE and gh(act=3) == DEVICE and gh(orow=None, srow=None) == DEVICE
+
+
+def _plan_checks(off, total, N):
+    b = mx.mxfp8_grouped_host_chunks(off, total, N)
+    R = max(128, (32 << 20) // (2 * N) // 128 * 128)
+    assert b[0] == 0 and b[-1] == total and all(x < y for x, y in zip(b, b[1:]))
+    for x in b[1:-1]:
+        g = max(i for i in range(len(off) - 1) if off[i] <= x < off[i + 1])
+        assert (x - off[g]) % 32 == 0                     # a cut group keeps its own 32-row blocks
+    assert all(y - x <= R + 31 for x, y in zip(b, b[1:]))  # fits a staging slot of R + 32 rows
+    # the pieces' columnwise scale rows add up to the group's: sum_g ceil(rows_g / 32)
+    pieces = 0
+    for x, y in zip(b, b[1:]):
+        for g in range(len(off) - 1):
+            a, e = min(max(off[g], x), y), min(max(off[g + 1], x), y)
+            pieces += -(-(e - a) // 32)
+    assert pieces == mx.grouped_scale_col_rows(off)
+    return b
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_host_chunk_plan(cuda_lib, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    N = int(rng.choice([64, 1032, 7168, 16384]))
+    G = int(rng.integers(1, 200))
+    sizes = rng.integers(0, 3000, G)
+    sizes[rng.random(G) < 0.2] = 0
+    sizes[0] += 1
+    off = [0] + np.cumsum(sizes).tolist()
+    b = _plan_checks(off, off[-1], N)
+    assert len(b) >= 2
+
+
+def test_grouped_host_chunk_plan_edges(cuda_lib):
+    _plan_checks([0, 1], 1, 64)                              # one row
+    _plan_checks([0, 100000], 100000, 7168)                  # one group cut many times
+    _plan_checks([0, 45, 45, 3000, 3001, 9000, 16384], 16384, 7168)
+    _plan_checks([0] + [37 * i for i in range(1, 513)], 37 * 512, 4096)   # 512 groups, none 32-aligned
+    assert mx.lib().mxfp8_grouped_host_chunks(None, 1, 10, 64, None, 0) == -1
+    with pytest.raises(ValueError):
+        mx.mxfp8_grouped_host_chunks([0, 5, 3], 3, 64)

@@ -81,3 +81,64 @@ def test_host_pipeline_single_direction_and_staging_reuse():
         torch.cuda.synchronize()
         assert got.out_row is None
         assert torch.equal(got.out_col, want[2]) and torch.equal(got.scale_col, want[3])
+
+
+# ---- the grouped cast with host buffers ---------------------------------------------------------
+
+GROUPED_HOST_CASES = [
+    # (rows, N, offsets): N = 16384 gives 1024-row chunks, so every case spans several chunks and
+    # boundaries fall inside groups that do not start on a multiple of 32
+    (5000, 16384, [0, 45, 45, 1500, 1533, 4001, 4700, 5000]),
+    (4097, 16384, [0, 4097]),                                   # one group cut into every chunk
+    (3000, 16384, [0] + [10 * i for i in range(1, 300)] + [3000]),  # 300 groups, most 10 rows
+    (6144, 7168, [0, 1024, 1024, 2048, 4096, 6144]),            # 32-row-multiple groups, 2304-row chunks
+]
+
+
+def _grouped_host_input(rows, N, seed):
+    return wl.grad_bf16(rows, N, seed=seed)
+
+
+@pytest.mark.parametrize("case", range(len(GROUPED_HOST_CASES)))
+@pytest.mark.parametrize("act", ["none", "relu", "gelu"])
+def test_grouped_host_matches_device_path(case, act):
+    rows, N, off = GROUPED_HOST_CASES[case]
+    assert len(mx.mxfp8_grouped_host_chunks(off, rows, N)) > 3
+    x_bits = _grouped_host_input(rows, N, seed=rows + case)
+    off_t = torch.tensor(off, dtype=torch.int64)
+    x_dev = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    want = mx.quantize_grouped(x_dev, off_t.cuda(), mx.E4M3, activation=act)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    before = mx.mxfp8_kernel_launch_count()
+    got = mx.quantize_grouped_host(x_host, off_t, mx.E4M3, activation=act)
+    torch.cuda.synchronize()
+    assert mx.mxfp8_kernel_launch_count() > before
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got[:4], want[:4]):
+        assert torch.equal(g, w.cpu()), name
+
+
+def test_grouped_host_matches_oracle(oracle_mod):
+    rows, N, off = GROUPED_HOST_CASES[0]
+    x_bits = _grouped_host_input(rows, N, seed=99)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    got = mx.quantize_grouped_host(x_host, torch.tensor(off), mx.E5M2)
+    torch.cuda.synchronize()
+    want = oracle_mod.quantize_grouped(x_bits, np.array(off, np.int64), mx.E5M2)
+    for name, g, w in zip(("out_row", "scale_row", "out_col", "scale_col"), got[:4], want[:4]):
+        assert np.array_equal(g.numpy(), w), name
+
+
+def test_grouped_host_pageable_single_direction_and_staging_reuse():
+    rows, N, off = GROUPED_HOST_CASES[1]
+    x_bits = _grouped_host_input(rows, N, seed=5)
+    off_t = torch.tensor(off, dtype=torch.int64)
+    x_dev = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    want = mx.quantize_grouped(x_dev, off_t.cuda(), mx.E4M3, rowwise=False, colwise=True)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).clone()     # pageable
+    staging = torch.empty(mx.mxfp8_quantize_grouped_host_staging_bytes(rows, N, 1), dtype=torch.uint8,
+                          device="cuda")
+    for _ in range(2):
+        got = mx.quantize_grouped_host(x_host, off_t, mx.E4M3, rowwise=False, colwise=True, staging=staging)
+        torch.cuda.synchronize()
+        assert got.out_row is None and got.scale_row is None
+        assert torch.equal(got.out_col, want.out_col.cpu()) and torch.equal(got.scale_col, want.scale_col.cpu())
