@@ -342,8 +342,8 @@ def test_grouped_unaligned_offsets_write_every_byte_once(sizes, N):
 @pytest.mark.parametrize("N", [24, 72, 1032])
 @pytest.mark.parametrize("reuse", [False, True])
 def test_grouped_swizzled_planes_written_once(sizes, N, reuse):
-    """The grouped cast with one GEMM-ready scale plane per group: the cast's scale writes and the
-    pad kernel's zeros together cover every byte of both concatenated planes exactly once."""
+    """The grouped cast with one GEMM-ready scale plane per group: the tiles' scale writes and their
+    padding zeros together cover every byte of both concatenated planes exactly once."""
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(int).tolist()
     check_quantize(off[-1], N, 5, offsets=off, swz=True, reuse=reuse)
 
