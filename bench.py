@@ -548,7 +548,8 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         x_host = torch.from_numpy(x_in_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-        outs_dev = [out_row, scale_row, out_col, scale_col] + ([dbias] if with_dbias else [])
+        outs_dev = [out_row, scale_row, out_col, scale_col] + ([dbias] if with_dbias else []) + \
+            ([amax] if amax is not None else [])
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
@@ -562,6 +563,19 @@ def run_ours(args):
             def e2e_step():
                 st = mx.mxfp8_quantize_grouped_host(x_host, M, N, G, off_host, fmt, act, *outs_host[:4], staging,
                                                     staging.numel(), stream)
+                if st != 0:
+                    raise mx.MXFP8Error(st, "bench e2e step")
+        elif (args.swizzled or args.amax or act) and not (grouped or dact or glu or dglu):
+            amax_host = outs_host[-1] if amax is not None else None
+            cfg_host = mx.make_config(x_host, M, N, fmt, *outs_host[:4], outs_host[4] if with_dbias else None, None,
+                                      None, layout, amax_host, act)
+            staging = torch.empty(mx.mxfp8_quantize_ex_host_staging_bytes(cfg_host), dtype=torch.uint8,
+                                  device="cuda")
+            path = ("mxfp8_quantize_ex_host: pinned host buffers in and out, H2D / kernel / D2H pipelined over "
+                    "row chunks inside the library")
+
+            def e2e_step():
+                st = mx.mxfp8_quantize_ex_host(cfg_host, staging, staging.numel(), stream)
                 if st != 0:
                     raise mx.MXFP8Error(st, "bench e2e step")
         elif grouped or args.swizzled or args.amax or act or dact or glu or dglu:

@@ -334,6 +334,35 @@ typedef struct mxfp8_quantize_config {
 mxfp8_status_t mxfp8_quantize_ex(const mxfp8_quantize_config_t *cfg, void *stream);
 
 /*
+ * Device staging bytes mxfp8_quantize_ex_host needs for cfg (its M, N, dbias,
+ * scale_layout and amax fields): three chunk slots sized for the layout, then
+ * the dbias workspace and vector, then the amax.  0 for cfg == NULL or
+ * invalid shapes.
+ */
+size_t mxfp8_quantize_ex_host_staging_bytes(const mxfp8_quantize_config_t *cfg);
+
+/*
+ * mxfp8_quantize_ex with x, every output, dbias and amax in HOST memory,
+ * pipelined over row chunks as mxfp8_quantize_host (which is this call
+ * without the layout, amax and activation options).  Results are identical to
+ * mxfp8_quantize_ex on the same data: every chunk but the last is a whole
+ * number of 128-row tiles, so a chunk's GEMM-ready rowwise plane is whole tile
+ * rows of the matrix's plane and its columnwise plane a band of tile columns
+ * (copied out with one strided copy); the amax is reduced on the device
+ * across the chunks and copied out once.
+ *   cfg->workspace and cfg->noop must be NULL (MXFP8_ERR_FORMAT otherwise):
+ *   the workspace lives in the staging buffer, and a skipped call would still
+ *   copy stale staging bytes out.
+ *   staging   device buffer, 256-byte aligned, at least
+ *             mxfp8_quantize_ex_host_staging_bytes(cfg) bytes.
+ *   stream    as mxfp8_quantize_host.
+ * M > 0, N > 0 a multiple of 8; otherwise the status codes of
+ * mxfp8_quantize_host and of mxfp8_quantize_ex.
+ */
+mxfp8_status_t mxfp8_quantize_ex_host(const mxfp8_quantize_config_t *cfg, void *staging,
+                                      size_t staging_bytes, void *stream);
+
+/*
  * Backward fusion (the `with_dact` field of the PR #3137 config key): the
  * cast of y = dY * act'(X), with dbias (optional) = column sums of y.
  *   grad        device bf16 [M, N]: dY, 16-byte aligned.

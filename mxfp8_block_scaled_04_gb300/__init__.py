@@ -17,6 +17,6 @@ from .binding import (  # noqa: F401
     quantize_dgated, mxfp8_quantize_gated_grouped, quantize_gated_grouped, mxfp8_quantize_grouped_activated,
     mxfp8_quantize_grouped_swizzled, mxfp8_grouped_swizzled_scale_bytes, mxfp8_selftest_bounded_wait, mxfp8_activation_values,
     mxfp8_quantize_grouped_host, mxfp8_quantize_grouped_host_staging_bytes, mxfp8_grouped_host_chunks,
-    quantize_grouped_host,
+    quantize_grouped_host, mxfp8_quantize_ex_host, mxfp8_quantize_ex_host_staging_bytes,
     QuantizeConfig, SCALES_PLAIN, SCALES_SWIZZLED, make_config, mxfp8_quantize_ex, mxfp8_scale_bytes,
 )

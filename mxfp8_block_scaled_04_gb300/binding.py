@@ -97,6 +97,10 @@ def lib():
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
             L.mxfp8_quantize_host.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.mxfp8_quantize_ex_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_ex_host_staging_bytes.argtypes = [ctypes.POINTER(QuantizeConfig)]
+            L.mxfp8_quantize_ex_host.restype = i32
+            L.mxfp8_quantize_ex_host.argtypes = [ctypes.POINTER(QuantizeConfig), vp, ctypes.c_size_t, vp]
             L.mxfp8_quantize_grouped_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_grouped_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_grouped_host.restype = i32
@@ -254,6 +258,16 @@ def mxfp8_quantize_host(x_host, M, N, fp8_fmt, out_row_host, scale_row_host, out
                                          _addr(staging), int(staging_bytes), _stream(stream)))
 
 
+def mxfp8_quantize_ex_host_staging_bytes(cfg: QuantizeConfig) -> int:
+    return int(lib().mxfp8_quantize_ex_host_staging_bytes(ctypes.byref(cfg) if cfg is not None else None))
+
+
+def mxfp8_quantize_ex_host(cfg: QuantizeConfig, staging, staging_bytes, stream=None) -> int:
+    """mxfp8_quantize_ex with host buffers (the config's pointers are host addresses)."""
+    return int(lib().mxfp8_quantize_ex_host(ctypes.byref(cfg) if cfg is not None else None, _addr(staging),
+                                            int(staging_bytes), _stream(stream)))
+
+
 def mxfp8_quantize_grouped_host_staging_bytes(total_rows: int, N: int, num_groups: int) -> int:
     return int(lib().mxfp8_quantize_grouped_host_staging_bytes(total_rows, N, num_groups))
 
@@ -409,30 +423,49 @@ def quantize(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = Tr
 
 
 def quantize_host(x: torch.Tensor, fmt=E4M3, rowwise: bool = True, colwise: bool = True,
-                  with_dbias: bool = False, staging: Optional[torch.Tensor] = None, stream=None) -> MXFP8Tensor:
+                  with_dbias: bool = False, staging: Optional[torch.Tensor] = None, stream=None,
+                  swizzled: bool = False, with_amax: bool = False, activation="none") -> MXFP8Tensor:
     """Quantize a host (CPU, ideally pinned) bf16 tensor; outputs are pinned host tensors.
 
     The copies and kernels are pipelined by the library.  The outputs are ready
     once ``stream`` (default: the current CUDA stream) has been synchronised.
+    ``swizzled``, ``with_amax`` and ``activation`` are the options of ``quantize``.
     """
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous() or x.is_cuda:
         raise ValueError("x must be a contiguous 2-D torch.bfloat16 host tensor")
     M, N = x.shape
     pin = dict(pin_memory=True)
     u8 = torch.uint8
+    layout = SCALES_SWIZZLED if swizzled else SCALES_PLAIN
     out_row = torch.empty((M, N), dtype=u8, **pin) if rowwise else None
-    scale_row = torch.empty((M, -(-N // BLOCK)), dtype=u8, **pin) if rowwise else None
     out_col = torch.empty((M, N), dtype=u8, **pin) if colwise else None
-    scale_col = torch.empty((-(-M // BLOCK), N), dtype=u8, **pin) if colwise else None
+    if swizzled:
+        scale_row = torch.empty((mxfp8_scale_bytes(M, -(-N // BLOCK), layout),), dtype=u8, **pin) if rowwise else None
+        scale_col = torch.empty((mxfp8_scale_bytes(N, -(-M // BLOCK), layout),), dtype=u8, **pin) if colwise else None
+    else:
+        scale_row = torch.empty((M, -(-N // BLOCK)), dtype=u8, **pin) if rowwise else None
+        scale_col = torch.empty((-(-M // BLOCK), N), dtype=u8, **pin) if colwise else None
     dbias = torch.empty((N,), dtype=torch.float32, **pin) if with_dbias else None
-    need = mxfp8_quantize_host_staging_bytes(M, N, with_dbias)
+    amax = torch.empty((1,), dtype=torch.float32, **pin) if with_amax else None
+    act = ACTIVATIONS[activation.lower()] if isinstance(activation, str) else int(activation)
+    if not (swizzled or with_amax or act):
+        need = mxfp8_quantize_host_staging_bytes(M, N, with_dbias)
+        if staging is None:
+            staging = torch.empty((max(need, 256),), dtype=u8, device="cuda")
+        st = mxfp8_quantize_host(x, M, N, _fmt(fmt), out_row, scale_row, out_col, scale_col, dbias,
+                                 staging, staging.numel(), stream)
+        if st != 0:
+            raise MXFP8Error(st, "mxfp8_quantize_host")
+        return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+    cfg = make_config(x, M, N, _fmt(fmt), out_row, scale_row, out_col, scale_col, dbias, None, None, layout,
+                      amax, act)
+    need = mxfp8_quantize_ex_host_staging_bytes(cfg)
     if staging is None:
         staging = torch.empty((max(need, 256),), dtype=u8, device="cuda")
-    st = mxfp8_quantize_host(x, M, N, _fmt(fmt), out_row, scale_row, out_col, scale_col, dbias,
-                             staging, staging.numel(), stream)
+    st = mxfp8_quantize_ex_host(cfg, staging, staging.numel(), stream)
     if st != 0:
-        raise MXFP8Error(st, "mxfp8_quantize_host")
-    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias)
+        raise MXFP8Error(st, "mxfp8_quantize_ex_host")
+    return MXFP8Tensor(out_row, scale_row, out_col, scale_col, dbias, amax)
 
 
 def quantize_grouped_host(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, activation="none",

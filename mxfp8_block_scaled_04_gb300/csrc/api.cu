@@ -1212,7 +1212,9 @@ struct SlotLayout {
     size_t x, out_row, out_col, scale_row, scale_col, bytes;
 };
 
-SlotLayout slot_layout(int64_t R, int64_t N)
+// One chunk slot of R rows (a multiple of 128); with swz, the scale planes in the GEMM-ready
+// layout (R rows x ceil(N/32) padded to 4 columns; ceil(N/128)*128 rows x R/32 columns).
+SlotLayout slot_layout(int64_t R, int64_t N, bool swz = false)
 {
     SlotLayout L;
     size_t o = 0;
@@ -1223,9 +1225,10 @@ SlotLayout slot_layout(int64_t R, int64_t N)
     L.out_col = o;
     o += align256(static_cast<size_t>(R * N));
     L.scale_row = o;
-    o += align256(static_cast<size_t>(R * ((N + 31) / 32)));
+    const int64_t Cn = (N + 31) / 32;
+    o += align256(static_cast<size_t>(swz ? R * ((Cn + 3) / 4 * 4) : R * Cn));
     L.scale_col = o;
-    o += align256(static_cast<size_t>(R / 32 * N));
+    o += align256(static_cast<size_t>(swz ? (N + 127) / 128 * 128 * (R / 32) : R / 32 * N));
     L.bytes = o;
     return L;
 }
@@ -1287,6 +1290,160 @@ bool cuda_ok(cudaError_t e)
         return true;
     cudaGetLastError();
     return false;
+}
+
+// Device staging bytes of the flat host pipeline: three chunk slots, then (with dbias) the
+// workspace of the whole matrix and an fp32 [N] vector, then (with amax) one fp32.
+size_t host_staging_bytes(int64_t M, int64_t N, bool dbias, bool swz, bool amax)
+{
+    if (M <= 0 || N <= 0 || N % 8)
+        return 0;
+    size_t b = kHostSlots * slot_layout(host_chunk_rows(M, N), N, swz).bytes;
+    if (dbias)
+        b += align256(mxfp8_quantize_workspace_bytes(M, N, 1)) + align256(static_cast<size_t>(N) * 4);
+    if (amax)
+        b += 256;
+    return b;
+}
+
+// The flat host pipeline (mxfp8_quantize_host, mxfp8_quantize_ex_host): x and the outputs in host
+// memory, chunks of rows through three device slots.  act, swz and amax_host are the options of
+// the config call; with swz the rowwise plane of a chunk is a contiguous run of whole tile rows of
+// the matrix's plane, and the columnwise one a column band of it (one strided copy).
+mxfp8_status_t host_pipeline(const void *x_host, int64_t M, int64_t N, int fp8_fmt, int act, bool swz,
+                             void *out_row_host, void *scale_row_host, void *out_col_host, void *scale_col_host,
+                             float *dbias_host, float *amax_host, void *staging, size_t staging_bytes,
+                             void *stream_)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (M <= 0 || N <= 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    if (x_host == nullptr || staging == nullptr)
+        return MXFP8_ERR_NULL;
+    mxfp8_status_t st = MXFP8_OK;
+    if ((out_row_host == nullptr) != (scale_row_host == nullptr) ||
+        (out_col_host == nullptr) != (scale_col_host == nullptr) ||
+        (out_row_host == nullptr && out_col_host == nullptr))
+        return MXFP8_ERR_NULL;
+    if (!aligned(staging, 256))
+        return MXFP8_ERR_ALIGN;
+    if (staging_bytes < host_staging_bytes(M, N, dbias_host != nullptr, swz, amax_host != nullptr))
+        return MXFP8_ERR_WORKSPACE;
+    if ((M + kBM - 1) / kBM * ((N + kBN - 1) / kBN) >= (int64_t{1} << 31))
+        return MXFP8_ERR_SHAPE;
+    const int64_t row_tiles = (M + kBM - 1) / kBM;
+
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(device, &hp)) != MXFP8_OK)
+        return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t R = host_chunk_rows(M, N);
+    const SlotLayout L = slot_layout(R, N, swz);
+    unsigned char *base = static_cast<unsigned char *>(staging);
+    float *ws = nullptr, *dbias_dev = nullptr;
+    size_t tail = kHostSlots * L.bytes;  // after the slots: dbias workspace and vector, amax
+    if (dbias_host != nullptr) {
+        ws = reinterpret_cast<float *>(base + tail);
+        tail += align256(mxfp8_quantize_workspace_bytes(M, N, 1));
+        dbias_dev = reinterpret_cast<float *>(base + tail);
+        tail += align256(static_cast<size_t>(N) * 4);
+    }
+    float *amax_dev = amax_host != nullptr ? reinterpret_cast<float *>(base + tail) : nullptr;
+    const int64_t col_tiles = (N + kBN - 1) / kBN;  // GEMM-ready planes: tiles of 128 rows (or columns)
+    const unsigned char *xh = static_cast<const unsigned char *>(x_host);
+
+    if (!cuda_ok(cudaEventRecord(hp->start, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+        !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+        return MXFP8_ERR_LAUNCH;
+    if (amax_dev != nullptr) {
+        amax_init_kernel<<<1, 1, 0, stream>>>(amax_dev, nullptr);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (cudaGetLastError() != cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+    }
+    const std::vector<int64_t> plan = chunk_plan(M, R);
+    const int64_t chunks = static_cast<int64_t>(plan.size()) - 1;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int k = static_cast<int>(c % kHostSlots);
+        const int64_t row0 = plan[c], rows = plan[c + 1] - plan[c];
+        unsigned char *slot = base + k * L.bytes;
+        // host -> device, once the slot's previous outputs have left
+        if (c >= kHostSlots && !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->d2h_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        if (!cuda_ok(cudaMemcpyAsync(slot + L.x, xh + row0 * N * 2, static_cast<size_t>(rows * N * 2),
+                                     cudaMemcpyHostToDevice, hp->h2d)) ||
+            !cuda_ok(cudaEventRecord(hp->h2d_done[k], hp->h2d)) ||
+            !cuda_ok(cudaStreamWaitEvent(stream, hp->h2d_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // quantize the chunk on the caller's stream
+        const bool row = out_row_host != nullptr, col = out_col_host != nullptr;
+        st = enqueue_flat(device, fp8_fmt, slot + L.x, rows, N, row ? slot + L.out_row : nullptr,
+                          row ? slot + L.scale_row : nullptr, col ? slot + L.out_col : nullptr,
+                          col ? slot + L.scale_col : nullptr, ws != nullptr ? ws + (row0 / kBM) * N : nullptr,
+                          nullptr, stream, swz, amax_dev, act);
+        if (st != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->comp_done[k], stream)) ||
+            !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->comp_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        // device -> host of every requested output of the chunk
+        bool ok = true;
+        const int64_t rt0 = row0 / kBM, crt = (rows + kBM - 1) / kBM;  // the chunk's tile rows
+        if (row) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + row0 * N, slot + L.out_row,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            const int64_t cr = (N + 31) / 32;
+            if (swz)  // whole tile rows of the plane: col_tiles tiles of 512 bytes each
+                ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + rt0 * col_tiles * 512,
+                                                   slot + L.scale_row, static_cast<size_t>(crt * col_tiles * 512),
+                                                   cudaMemcpyDeviceToHost, hp->d2h));
+            else
+                ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * cr,
+                                                   slot + L.scale_row, static_cast<size_t>(rows * cr),
+                                                   cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (col) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + row0 * N, slot + L.out_col,
+                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
+            if (swz)  // tile columns rt0 .. rt0 + crt of each of the plane's col_tiles tile rows
+                ok = ok && cuda_ok(cudaMemcpy2DAsync(static_cast<unsigned char *>(scale_col_host) + rt0 * 512,
+                                                     static_cast<size_t>(row_tiles * 512), slot + L.scale_col,
+                                                     static_cast<size_t>(crt * 512), static_cast<size_t>(crt * 512),
+                                                     static_cast<size_t>(col_tiles), cudaMemcpyDeviceToHost,
+                                                     hp->d2h));
+            else
+                ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + (row0 / 32) * N,
+                                                   slot + L.scale_col, static_cast<size_t>(((rows + 31) / 32) * N),
+                                                   cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    if (dbias_host != nullptr) {
+        if ((st = enqueue_reduce(ws, row_tiles, N, dbias_dev, nullptr, stream)) != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->reduced, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->reduced, 0)) ||
+            !cuda_ok(cudaMemcpyAsync(dbias_host, dbias_dev, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
+                                     hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    if (amax_dev != nullptr) {
+        if (!cuda_ok(cudaEventRecord(hp->reduced, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->reduced, 0)) ||
+            !cuda_ok(cudaMemcpyAsync(amax_host, amax_dev, 4, cudaMemcpyDeviceToHost, hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    // the caller's stream resumes once the last copy to the host is done
+    if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
+        return MXFP8_ERR_LAUNCH;
+    return MXFP8_OK;
 }
 
 // Chunk boundaries of a grouped host call: the flat plan's, each interior one moved down to the
@@ -1355,120 +1512,44 @@ extern "C" {
 
 size_t mxfp8_quantize_host_staging_bytes(int64_t M, int64_t N, int with_dbias)
 {
-    if (M <= 0 || N <= 0 || N % 8)
-        return 0;
-    const SlotLayout L = slot_layout(host_chunk_rows(M, N), N);
-    size_t b = kHostSlots * L.bytes;
-    if (with_dbias)
-        b += align256(mxfp8_quantize_workspace_bytes(M, N, 1)) + align256(static_cast<size_t>(N) * 4);
-    return b;
+    return host_staging_bytes(M, N, with_dbias != 0, false, false);
 }
 
 mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int fp8_fmt, void *out_row_host,
                                    void *scale_row_host, void *out_col_host, void *scale_col_host,
                                    float *dbias_host, void *staging, size_t staging_bytes, void *stream_)
 {
-    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+    return host_pipeline(x_host, M, N, fp8_fmt, MXFP8_ACT_NONE, false, out_row_host, scale_row_host, out_col_host,
+                         scale_col_host, dbias_host, nullptr, staging, staging_bytes, stream_);
+}
+
+size_t mxfp8_quantize_ex_host_staging_bytes(const mxfp8_quantize_config_t *cfg)
+{
+    if (cfg == nullptr)
+        return 0;
+    return host_staging_bytes(cfg->M, cfg->N, cfg->dbias != nullptr, cfg->scale_layout == MXFP8_SCALES_SWIZZLED,
+                              cfg->amax != nullptr);
+}
+
+mxfp8_status_t mxfp8_quantize_ex_host(const mxfp8_quantize_config_t *cfg, void *staging, size_t staging_bytes,
+                                      void *stream_)
+{
+    if (cfg == nullptr)
+        return MXFP8_ERR_NULL;
+    for (int r : cfg->reserved)
+        if (r != 0)
+            return MXFP8_ERR_FORMAT;
+    if (cfg->scale_layout != MXFP8_SCALES_PLAIN && cfg->scale_layout != MXFP8_SCALES_SWIZZLED)
         return MXFP8_ERR_FORMAT;
-    if (M <= 0 || N <= 0 || N % 8 || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31))
-        return MXFP8_ERR_SHAPE;
-    if (x_host == nullptr || staging == nullptr)
-        return MXFP8_ERR_NULL;
-    mxfp8_status_t st = MXFP8_OK;
-    if ((out_row_host == nullptr) != (scale_row_host == nullptr) ||
-        (out_col_host == nullptr) != (scale_col_host == nullptr) ||
-        (out_row_host == nullptr && out_col_host == nullptr))
-        return MXFP8_ERR_NULL;
-    if (!aligned(staging, 256))
-        return MXFP8_ERR_ALIGN;
-    if (staging_bytes < mxfp8_quantize_host_staging_bytes(M, N, dbias_host != nullptr))
-        return MXFP8_ERR_WORKSPACE;
-    const int64_t col_tiles = (N + kBN - 1) / kBN, row_tiles = (M + kBM - 1) / kBM;
-    if (row_tiles * col_tiles >= (int64_t{1} << 31))
-        return MXFP8_ERR_SHAPE;
-
-    int device = 0;
-    if ((st = current_device(&device)) != MXFP8_OK)
-        return st;
-    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
-        return MXFP8_ERR_DEVICE;
-
-    std::lock_guard<std::mutex> lock(g_pipe_mu);
-    HostPipe *hp = nullptr;
-    if ((st = host_pipe(device, &hp)) != MXFP8_OK)
-        return st;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    const int64_t R = host_chunk_rows(M, N);
-    const SlotLayout L = slot_layout(R, N);
-    unsigned char *base = static_cast<unsigned char *>(staging);
-    float *ws = nullptr, *dbias_dev = nullptr;
-    if (dbias_host != nullptr) {
-        ws = reinterpret_cast<float *>(base + kHostSlots * L.bytes);
-        dbias_dev = reinterpret_cast<float *>(base + kHostSlots * L.bytes +
-                                              align256(mxfp8_quantize_workspace_bytes(M, N, 1)));
-    }
-    const unsigned char *xh = static_cast<const unsigned char *>(x_host);
-
-    if (!cuda_ok(cudaEventRecord(hp->start, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
-        !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
-        return MXFP8_ERR_LAUNCH;
-    const std::vector<int64_t> plan = chunk_plan(M, R);
-    const int64_t chunks = static_cast<int64_t>(plan.size()) - 1;
-    for (int64_t c = 0; c < chunks; ++c) {
-        const int k = static_cast<int>(c % kHostSlots);
-        const int64_t row0 = plan[c], rows = plan[c + 1] - plan[c];
-        unsigned char *slot = base + k * L.bytes;
-        // host -> device, once the slot's previous outputs have left
-        if (c >= kHostSlots && !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->d2h_done[k], 0)))
-            return MXFP8_ERR_LAUNCH;
-        if (!cuda_ok(cudaMemcpyAsync(slot + L.x, xh + row0 * N * 2, static_cast<size_t>(rows * N * 2),
-                                     cudaMemcpyHostToDevice, hp->h2d)) ||
-            !cuda_ok(cudaEventRecord(hp->h2d_done[k], hp->h2d)) ||
-            !cuda_ok(cudaStreamWaitEvent(stream, hp->h2d_done[k], 0)))
-            return MXFP8_ERR_LAUNCH;
-        // quantize the chunk on the caller's stream
-        const bool row = out_row_host != nullptr, col = out_col_host != nullptr;
-        st = enqueue_flat(device, fp8_fmt, slot + L.x, rows, N, row ? slot + L.out_row : nullptr,
-                          row ? slot + L.scale_row : nullptr, col ? slot + L.out_col : nullptr,
-                          col ? slot + L.scale_col : nullptr, ws != nullptr ? ws + (row0 / kBM) * N : nullptr,
-                          nullptr, stream);
-        if (st != MXFP8_OK)
-            return st;
-        if (!cuda_ok(cudaEventRecord(hp->comp_done[k], stream)) ||
-            !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->comp_done[k], 0)))
-            return MXFP8_ERR_LAUNCH;
-        // device -> host of every requested output of the chunk
-        bool ok = true;
-        if (row) {
-            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + row0 * N, slot + L.out_row,
-                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
-            const int64_t cr = (N + 31) / 32;
-            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * cr,
-                                               slot + L.scale_row, static_cast<size_t>(rows * cr),
-                                               cudaMemcpyDeviceToHost, hp->d2h));
-        }
-        if (col) {
-            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + row0 * N, slot + L.out_col,
-                                               static_cast<size_t>(rows * N), cudaMemcpyDeviceToHost, hp->d2h));
-            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + (row0 / 32) * N,
-                                               slot + L.scale_col, static_cast<size_t>(((rows + 31) / 32) * N),
-                                               cudaMemcpyDeviceToHost, hp->d2h));
-        }
-        if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))
-            return MXFP8_ERR_LAUNCH;
-    }
-    if (dbias_host != nullptr) {
-        if ((st = enqueue_reduce(ws, row_tiles, N, dbias_dev, nullptr, stream)) != MXFP8_OK)
-            return st;
-        if (!cuda_ok(cudaEventRecord(hp->reduced, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->reduced, 0)) ||
-            !cuda_ok(cudaMemcpyAsync(dbias_host, dbias_dev, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
-                                     hp->d2h)))
-            return MXFP8_ERR_LAUNCH;
-    }
-    // the caller's stream resumes once the last copy to the host is done
-    if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
-        return MXFP8_ERR_LAUNCH;
-    return MXFP8_OK;
+    if (cfg->activation < MXFP8_ACT_NONE || cfg->activation > MXFP8_ACT_QGELU ||
+        (cfg->activation != MXFP8_ACT_NONE && cfg->dbias != nullptr))
+        return MXFP8_ERR_FORMAT;
+    // the workspace lives in the staging buffer; a skipped call would still copy stale bytes out
+    if (cfg->workspace != nullptr || cfg->noop != nullptr)
+        return MXFP8_ERR_FORMAT;
+    return host_pipeline(cfg->x, cfg->M, cfg->N, cfg->fp8_fmt, cfg->activation,
+                         cfg->scale_layout == MXFP8_SCALES_SWIZZLED, cfg->out_row, cfg->scale_row, cfg->out_col,
+                         cfg->scale_col, cfg->dbias, cfg->amax, staging, staging_bytes, stream_);
 }
 
 size_t mxfp8_quantize_grouped_host_staging_bytes(int64_t total_rows, int64_t N, int num_groups)

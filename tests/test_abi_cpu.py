@@ -375,3 +375,31 @@ def test_grouped_host_chunk_plan_edges(cuda_lib):
     assert mx.lib().mxfp8_grouped_host_chunks(None, 1, 10, 64, None, 0) == -1
     with pytest.raises(ValueError):
         mx.mxfp8_grouped_host_chunks([0, 5, 3], 3, 64)
+
+
+def test_ex_host_rejections(cuda_lib):
+    def cfg(**kw):
+        a = dict(x=A, M=64, N=64, fmt=0, orow=A, srow=A, ocol=A, scol=A, dbias=None, ws=None, noop=None,
+                 layout=mx.SCALES_SWIZZLED, amax=A, act=3)
+        a.update(kw)
+        return mx.make_config(a["x"], a["M"], a["N"], a["fmt"], a["orow"], a["srow"], a["ocol"], a["scol"],
+                              a["dbias"], a["ws"], a["noop"], a["layout"], a["amax"], a["act"])
+
+    def eh(staging=A, nbytes=1 << 30, **kw):
+        return mx.mxfp8_quantize_ex_host(cfg(**kw), staging, nbytes, 0)
+    assert mx.lib().mxfp8_quantize_ex_host(None, A, 1 << 30, None) == NULL
+    c = cfg()
+    c.reserved[2] = 1
+    assert mx.mxfp8_quantize_ex_host(c, A, 1 << 30, 0) == FORMAT
+    assert eh(layout=2) == FORMAT and eh(act=6) == FORMAT and eh(act=1, dbias=A) == FORMAT
+    assert eh(ws=A) == FORMAT and eh(noop=A) == FORMAT          # no workspace or noop with host buffers
+    assert eh(fmt=2) == FORMAT and eh(M=0) == SHAPE and eh(N=36) == SHAPE
+    assert eh(x=None) == NULL and eh(staging=None) == NULL and eh(orow=None) == NULL
+    assert eh(staging=A + 16) == ALIGN and eh(nbytes=1024) == WORKSPACE
+    assert eh() == DEVICE and eh(act=0, amax=None) == DEVICE
+    # staging: GEMM-ready slots are at least the plain ones; amax adds one 256-byte line
+    plain = mx.mxfp8_quantize_ex_host_staging_bytes(cfg(layout=mx.SCALES_PLAIN, amax=None))
+    assert plain == mx.mxfp8_quantize_host_staging_bytes(64, 64, 0)
+    assert mx.mxfp8_quantize_ex_host_staging_bytes(cfg(layout=mx.SCALES_PLAIN)) == plain + 256
+    assert mx.mxfp8_quantize_ex_host_staging_bytes(cfg(amax=None)) >= plain
+    assert mx.mxfp8_quantize_ex_host_staging_bytes(None) == 0

@@ -142,3 +142,30 @@ def test_grouped_host_pageable_single_direction_and_staging_reuse():
         torch.cuda.synchronize()
         assert got.out_row is None and got.scale_row is None
         assert torch.equal(got.out_col, want.out_col.cpu()) and torch.equal(got.scale_col, want.scale_col.cpu())
+
+
+# ---- the config call's options with host buffers ------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(4195, 16384), (1056, 28672), (300, 1032)])
+@pytest.mark.parametrize("opts", [dict(swizzled=True), dict(with_amax=True), dict(activation="gelu"),
+                                  dict(swizzled=True, with_amax=True, activation="relu"),
+                                  dict(swizzled=True, activation="silu", colwise=False)])
+def test_ex_host_matches_device_path(shape, opts):
+    M, N = shape
+    x_bits = wl.fc1_bf16(M, N, seed=M + 3 * N)
+    kw = dict(opts)
+    colwise = kw.pop("colwise", True)
+    want = mx.quantize(torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda(), mx.E4M3,
+                       colwise=colwise, **kw)
+    torch.cuda.synchronize()
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    before = mx.mxfp8_kernel_launch_count()
+    got = mx.quantize_host(x_host, mx.E4M3, colwise=colwise, **kw)
+    torch.cuda.synchronize()
+    assert mx.mxfp8_kernel_launch_count() > before
+    for name in ("out_row", "scale_row", "out_col", "scale_col", "amax"):
+        g, w = getattr(got, name), getattr(want, name)
+        if w is None:
+            assert g is None, name
+            continue
+        assert torch.equal(g, w.cpu()), name

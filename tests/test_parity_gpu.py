@@ -547,6 +547,36 @@ def test_parity_moe_64x65536x7168_unaligned_full(oracle_mod):
     torch.cuda.empty_cache()
 
 
+def test_parity_moe_64x65536x7168_unaligned_swizzled_full(oracle_mod):
+    """The ragged MoE shape with one GEMM-ready plane pair per expert: every code against the
+    oracle's grouped call, and each expert's slice of both concatenated planes against the
+    oracle's swizzle of that expert's own scales (padding zero); expert g's planes follow the
+    sum_{h<g} ceil(rows_h/128) tile rows of the experts before it."""
+    sizes = wl.moe_group_sizes(64, 65536, seed=11, unit=1)
+    off = wl.offsets_from_sizes(sizes)
+    N = 7168
+    x_bits = wl.moe_bf16(sizes, N, seed=11)
+    r = mx.quantize_grouped(dev_bf16(x_bits), torch.from_numpy(off).cuda(), E4M3, swizzled=True)
+    torch.cuda.synchronize()
+    got = [t.cpu().numpy() for t in r[:4]]
+    want = oracle_slices.quantize_grouped(oracle_mod, x_bits, off, E4M3)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[2], want[2])
+    Cn, rb, cb, s0 = -(-N // 32), 0, 0, 0
+    for g in range(len(off) - 1):
+        rows = int(off[g + 1] - off[g])
+        if rows == 0:
+            continue
+        srow = oracle_mod.swizzle_scales(want[1][off[g]:off[g + 1]])
+        sc = -(-rows // 32)
+        scol = oracle_mod.swizzle_scales(np.ascontiguousarray(want[3][s0:s0 + sc].T))
+        assert np.array_equal(got[1][rb:rb + srow.size], srow), g
+        assert np.array_equal(got[3][cb:cb + scol.size], scol), g
+        rb, cb, s0 = rb + srow.size, cb + scol.size, s0 + sc
+    assert rb == got[1].size and cb == got[3].size
+    del r
+    torch.cuda.empty_cache()
+
+
 def test_grouped_dbias_moe_64x65536x7168_full(oracle_mod):
     w = wl.make("moe_64x65536x7168")
     x_bits, off = w["x"], w["offsets"]
