@@ -456,10 +456,10 @@ void mxo_gate(const uint16_t *x, int64_t M, int64_t N, int act, float *y)
 }
 
 /*
- * Per-expert dbias of a grouped call (the survey's "grouped-call dbias per
- * expert"): dbias[g][j] = sum of x[i][j] over the rows i of group g, in
- * double, rounded once to fp32; an empty group gets zeros.  Returns -1 for
- * offsets the grouped call rejects.
+ * Per-expert dbias of a grouped call (each expert's bias gradient, the
+ * column sums of its own rows): dbias[g][j] = sum of x[i][j] over the rows i
+ * of group g, in double, rounded once to fp32; an empty group gets zeros.
+ * Returns -1 for offsets the grouped call rejects.
  */
 int mxo_grouped_dbias(const uint16_t *x, int64_t total_rows, int64_t N, int num_groups,
                       const int64_t *offsets, float *dbias)
