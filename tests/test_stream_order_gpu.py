@@ -67,3 +67,42 @@ def test_alternating_grouped_dbias_same_workspace(oracle_mod):
     got = dbias.cpu().numpy().astype(np.float64)
     for g in range(G):
         assert np.all(np.abs(got[g] - want[g]) <= 1e-5 * xv[off_a[g]:off_a[g + 1]].sum(0)), g
+
+
+def test_concurrent_host_threads_on_their_own_streams():
+    """Several host threads enqueue calls at once, each on its own stream and buffers, the first
+    call of some variants among them (the per-variant set-up runs under a lock): every thread's
+    outputs equal a single-threaded call's."""
+    import threading
+    M, N = 2048, 4096
+    inputs = [wl.normal_bf16(M, N, seed=40 + t) for t in range(4)]
+    variants = [dict(), dict(swizzled=True), dict(activation="silu"), dict(with_amax=True, activation="relu")]
+    ref = []
+    for t, bits in enumerate(inputs):
+        r = mx.quantize(dev(bits), mx.E4M3, **variants[t])
+        torch.cuda.synchronize()
+        ref.append([v.cpu() if v is not None else None for v in r])
+    results, errors = [None] * 4, []
+
+    def work(t):
+        try:
+            s = torch.cuda.Stream()
+            x = dev(inputs[t])
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    r = mx.quantize(x, mx.E4M3, stream=s, **variants[t])
+            s.synchronize()
+            results[t] = [v.cpu() if v is not None else None for v in r]
+        except Exception as e:  # reported on the main thread
+            errors.append((t, e))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(4):
+        for g, w in zip(results[t], ref[t]):
+            assert (g is None and w is None) or torch.equal(g, w), t
