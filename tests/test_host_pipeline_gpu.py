@@ -149,7 +149,8 @@ def test_grouped_host_pageable_single_direction_and_staging_reuse():
 @pytest.mark.parametrize("shape", [(4195, 16384), (1056, 28672), (300, 1032)])
 @pytest.mark.parametrize("opts", [dict(swizzled=True), dict(with_amax=True), dict(activation="gelu"),
                                   dict(swizzled=True, with_amax=True, activation="relu"),
-                                  dict(swizzled=True, activation="silu", colwise=False)])
+                                  dict(swizzled=True, activation="silu", colwise=False),
+                                  dict(swizzled=True, with_dbias=True), dict(with_amax=True, with_dbias=True)])
 def test_ex_host_matches_device_path(shape, opts):
     M, N = shape
     x_bits = wl.fc1_bf16(M, N, seed=M + 3 * N)
@@ -163,9 +164,9 @@ def test_ex_host_matches_device_path(shape, opts):
     got = mx.quantize_host(x_host, mx.E4M3, colwise=colwise, **kw)
     torch.cuda.synchronize()
     assert mx.mxfp8_kernel_launch_count() > before
-    for name in ("out_row", "scale_row", "out_col", "scale_col", "amax"):
+    for name in ("out_row", "scale_row", "out_col", "scale_col", "dbias", "amax"):
         g, w = getattr(got, name), getattr(want, name)
         if w is None:
             assert g is None, name
             continue
-        assert torch.equal(g, w.cpu()), name
+        assert torch.equal(g, w.cpu()), name      # dbias too: the same partials and the same reduce
