@@ -135,15 +135,17 @@ mxfp8_status_t prepare(int device, int *grid_cap)
     return MXFP8_OK;
 }
 
-// TMA map of a BF16 matrix [rows, N] whose rows are `pitch` elements apart (pitch >= N).
-mxfp8_status_t make_tensor_map_pitch(CUtensorMap *map, const void *x, int64_t rows, int64_t N, int64_t pitch)
+// TMA map of a BF16 matrix [rows, N] whose rows are `pitch` elements apart (pitch >= N), in boxes
+// of box_rows rows x 64 columns.
+mxfp8_status_t make_tensor_map_pitch(CUtensorMap *map, const void *x, int64_t rows, int64_t N, int64_t pitch,
+                                     int box_rows = kBM)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr)
         return MXFP8_ERR_DEVICE;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
-    cuuint32_t box[2] = {kBoxCols, kBM};
+    cuuint32_t box[2] = {kBoxCols, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -261,6 +263,10 @@ mxfp8_status_t launch_gated(int fmt, int device, const CUtensorMap &map_b, const
                              : launch_dact_fmt<1, false, ACT, true, GROUPED>(device, map_b, map_a, p, tiles, stream);
 }
 
+// GeGLU, SwiGLU and QGeGLU backward: the kernel that evaluates each product once (64-row tiles).
+template <int ACT>
+constexpr bool kKeepDgated = ACT >= MXFP8_ACT_GELU;
+
 // The gated backward kernel: one-time set-up per (device, variant), then launch.
 template <int FMT, int ACT>
 mxfp8_status_t launch_dgated_fmt(int device, const CUtensorMap &map_g, const CUtensorMap &map_a,
@@ -281,11 +287,16 @@ mxfp8_status_t launch_dgated_fmt(int device, const CUtensorMap &map_g, const CUt
         }
         const int v = FMT + 2 * ACT;
         if (d.dgated_ctas_per_sm[v] == 0) {
-            auto kern = quantize_dgated_kernel<FMT, ACT>;
+            auto kern = [] {
+                if constexpr (kKeepDgated<ACT>)
+                    return quantize_dgated_keep_kernel<FMT, ACT>;
+                else
+                    return quantize_dgated_kernel<FMT, ACT>;
+            }();
+            const int smem = kKeepDgated<ACT> ? kSmemDgatedKeep : kSmemDgated;
             int n = 0;
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemDgated) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, kSmemDgated) != cudaSuccess ||
-                n < 1) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess || n < 1) {
                 cudaGetLastError();
                 return MXFP8_ERR_LAUNCH;
             }
@@ -294,7 +305,12 @@ mxfp8_status_t launch_dgated_fmt(int device, const CUtensorMap &map_g, const CUt
         cap = d.dgated_ctas_per_sm[v] * d.sm_count;
     }
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    return launch_pdl(quantize_dgated_kernel<FMT, ACT>, grid, kThreads, kSmemDgated, stream, map_g, map_a, map_b, p);
+    if constexpr (kKeepDgated<ACT>)
+        return launch_pdl(quantize_dgated_keep_kernel<FMT, ACT>, grid, kThreads, kSmemDgatedKeep, stream, map_g, map_a,
+                          map_b, p);
+    else
+        return launch_pdl(quantize_dgated_kernel<FMT, ACT>, grid, kThreads, kSmemDgated, stream, map_g, map_a, map_b,
+                          p);
 }
 
 template <int ACT>
@@ -876,7 +892,8 @@ mxfp8_status_t mxfp8_quantize_dgated(const void *grad, const void *x, int64_t M,
     }
     if (!aligned(grad, 16) || !aligned(x, 16))
         return MXFP8_ERR_ALIGN;
-    const int64_t row_tiles = (M + kBM - 1) / kBM, col_tiles = (N + kDBN - 1) / kDBN;
+    const int tile_rows = activation >= MXFP8_ACT_GELU ? kKRows : kBM;  // see kKeepDgated
+    const int64_t row_tiles = (M + tile_rows - 1) / tile_rows, col_tiles = (N + kDBN - 1) / kDBN;
     if (row_tiles * col_tiles >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;
     int device = 0;
@@ -890,9 +907,9 @@ mxfp8_status_t mxfp8_quantize_dgated(const void *grad, const void *x, int64_t M,
         return MXFP8_OK;
     CUtensorMap map_g, map_a, map_b;
     const void *b = static_cast<const uint16_t *>(x) + N;  // 16-byte aligned: N is a multiple of 8
-    if ((st = make_tensor_map(&map_g, grad, M, N)) != MXFP8_OK ||
-        (st = make_tensor_map_pitch(&map_a, x, M, N, 2 * N)) != MXFP8_OK ||
-        (st = make_tensor_map_pitch(&map_b, b, M, N, 2 * N)) != MXFP8_OK)
+    if ((st = make_tensor_map_pitch(&map_g, grad, M, N, N, tile_rows)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_a, x, M, N, 2 * N, tile_rows)) != MXFP8_OK ||
+        (st = make_tensor_map_pitch(&map_b, b, M, N, 2 * N, tile_rows)) != MXFP8_OK)
         return st;
     QuantParams p{};
     p.out_row = static_cast<uint8_t *>(out_row);

@@ -466,6 +466,80 @@ def test_gated_backward_writes_every_byte_once(shape):
     model_dgated(*shape, grid=304)
 
 
+def keep_chunk(c, r):
+    return c ^ ((c >> 3) << 1) ^ (r & 1)
+
+
+def model_dgated_keep(M, N, grid):
+    """quantize_dgated_keep_kernel (GeGLU, SwiGLU, QGeGLU backward): 64-row x 64-column tiles, da and
+    db kept in fp32 in a [2][64][64] area between the phases; the same side-by-side outputs."""
+    KR = 64
+    rows16 = N % 16 == 0
+    N2, Cn = 2 * N, -(-N // 32)
+    out_row, out_col = Plane("out_row", M * N2), Plane("out_col", M * N2)
+    scale_row, scale_col = Plane("scale_row", M * 2 * Cn), Plane("scale_col", -(-M // 32) * N2)
+    row_tiles, col_tiles = -(-M // KR), -(-N // DBN)
+    tiles = [(rt * KR, min(rt * KR + KR, M), ct * DBN) for rt in range(row_tiles) for ct in range(col_tiles)]
+    # phase 1: warp w, lane l -> rows 32 (w >> 2) + 8 (w & 3) + 4 (l >> 4) + i, column quad l & 15
+    w1, l1 = np.repeat(np.arange(8), 32), np.tile(LANES, 8)
+    r01 = 32 * (w1 >> 2) + 8 * (w1 & 3) + 4 * (l1 >> 4)
+    stage_reads = []
+    keep_w = []
+    for i in range(4):
+        r = r01 + i
+        stage_reads.append(r * 128 + ((((l1 & 15) >> 1) ^ (r & 7)) << 4) + (l1 & 1) * 8)
+        kc = keep_chunk(l1 & 15, r)
+        for out in range(2):
+            keep_w.append((out * KR + r) * 16 + kc)
+        # 128-bit keep stores: each quarter warp (8 lanes) meets 8 distinct 16-byte bank groups
+        for qw in range(0, 256, 8):
+            assert len(set((kc[qw:qw + 8] % 8).tolist())) == 8
+    stage_reads = np.concatenate(stage_reads)
+    assert stage_reads.size == len(set(stage_reads.tolist())) == KR * 128 // 8 and stage_reads.max() + 8 <= 8192
+    keep_w = np.concatenate(keep_w)
+    assert keep_w.size == len(set(keep_w.tolist())) == 2 * KR * 16          # every kept chunk once
+    # phase 2: warp w -> rows 8w + (l >> 2), segment l & 3: chunks 4 sp + j of its row
+    w2, l2 = np.repeat(np.arange(8), 32), np.tile(LANES, 8)
+    r2, sp2 = 8 * w2 + (l2 >> 2), l2 & 3
+    keep_r = []
+    for j in range(4):
+        kc = keep_chunk(4 * sp2 + j, r2)
+        for qw in range(0, 256, 8):
+            assert len(set((kc[qw:qw + 8] % 8).tolist())) == 8
+        for out in range(2):
+            keep_r.append((out * KR + r2) * 16 + kc)
+    assert set(np.concatenate(keep_r).tolist()) == set(keep_w.tolist())  # phase 2 reads what phase 1 kept
+    # the scale step: thread t -> (output t >> 7, row block (t >> 6) & 1, column t & 63)
+    t = np.arange(THREADS)
+    so, srb, sc = t >> 7, (t >> 6) & 1, t & 63
+    assert len({(int(a), int(b), int(c)) for a, b, c in zip(so, srb, sc)}) == 256
+    for b in range(grid):
+        for ti in range(b, len(tiles), grid):
+            row0, row_end, col0 = tiles[ti]
+            assert (col0 * 2) % 16 == 0 and col0 < N and row0 < M
+            grow, gcol = row0 + srb * 32, col0 + sc
+            sel = (grow < row_end) & (gcol < N)
+            scale_col.write((grow[sel] >> 5) * N2 + so[sel] * N + gcol[sel])
+            grow, gcol = row0 + r2, col0 + sp2 * 16
+            ok = (row0 + 8 * w2 < row_end) & (grow < row_end) & (gcol < N)
+            half_seg = gcol + 16 > N
+            full, part = ok & ~half_seg, ok & half_seg
+            for out in range(2):
+                for plane in (out_row, out_col):
+                    plane.write(grow[full] * N2 + out * N + gcol[full], 16, align=16 if rows16 else 8)
+                    plane.write(grow[part] * N2 + out * N + gcol[part], 8, align=8)
+                se = ok & (sp2 % 2 == 0)
+                scale_row.write(grow[se] * 2 * Cn + out * Cn + (gcol[se] >> 5))
+    for p_ in (out_row, out_col, scale_row, scale_col):
+        p_.once()
+
+
+@pytest.mark.parametrize("shape", [(45, 80), (70, 24), (257, 1032), (130, 144), (256, 64), (33, 8), (64, 8)])
+def test_gated_backward_keep_kernel_writes_every_byte_once(shape):
+    model_dgated_keep(*shape, grid=5)
+    model_dgated_keep(*shape, grid=304)
+
+
 def grouped_reduce_reads(hdr, N):
     """dbias_reduce_grouped_kernel: the partial rows each (group, column) sums, for one CTA of 32
     columns, following its 16 contiguous warp ranges and the head / tail hand-over."""
