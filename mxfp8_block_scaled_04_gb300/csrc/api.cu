@@ -263,9 +263,10 @@ mxfp8_status_t launch_gated(int fmt, int device, const CUtensorMap &map_b, const
                              : launch_dact_fmt<1, false, ACT, true, GROUPED>(device, map_b, map_a, p, tiles, stream);
 }
 
-// GeGLU, SwiGLU and QGeGLU backward: the kernel that evaluates each product once (64-row tiles).
+// The gated backward kernel that evaluates each product once (64-row tiles): for ReGLU, GeGLU,
+// SwiGLU and QGeGLU (measured 2-10% faster); squared-ReLU GLU runs 9% faster with the 128-row one.
 template <int ACT>
-constexpr bool kKeepDgated = ACT >= MXFP8_ACT_GELU;
+constexpr bool kKeepDgated = ACT != MXFP8_ACT_SRELU;
 
 // The gated backward kernel: one-time set-up per (device, variant), then launch.
 template <int FMT, int ACT>
@@ -892,7 +893,7 @@ mxfp8_status_t mxfp8_quantize_dgated(const void *grad, const void *x, int64_t M,
     }
     if (!aligned(grad, 16) || !aligned(x, 16))
         return MXFP8_ERR_ALIGN;
-    const int tile_rows = activation >= MXFP8_ACT_GELU ? kKRows : kBM;  // see kKeepDgated
+    const int tile_rows = activation != MXFP8_ACT_SRELU ? kKRows : kBM;  // see kKeepDgated
     const int64_t row_tiles = (M + tile_rows - 1) / tile_rows, col_tiles = (N + kDBN - 1) / kDBN;
     if (row_tiles * col_tiles >= (int64_t{1} << 31))
         return MXFP8_ERR_SHAPE;

@@ -6,7 +6,8 @@
 // buffers (codes; scale_row [M, 2 ceil(N/32)], da's blocks first;
 // scale_col [ceil(M/32), 2N]).
 //
-// Three BF16 inputs per element (g, a, b), so a stage holds three 128-row x
+// Two kernels.  The first (squared-ReLU GLU, measured faster there): three
+// BF16 inputs per element (g, a, b), so a stage holds three 128-row x
 // 64-column boxes (48 KiB) and the kernel keeps two stages per CTA, two CTAs
 // per SM (four tiles in flight per SM).  The phases follow the backward
 // fusion's kernel:
@@ -257,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 namespace mxfp8 {
 
-// The gated backward for GeGLU, SwiGLU and QGeGLU with each product evaluated once.  Their
-// activation and derivative dominate the kernel above, which evaluates them in both phases
-// because its 48 KiB stage cannot hold both fp32 products.  Here a tile is 64 rows x 64 columns
+// The gated backward with each product evaluated once (ReGLU, GeGLU, SwiGLU, QGeGLU).  For the
+// transcendental activations their evaluation dominates the kernel above, which evaluates them in
+// both phases because its 48 KiB stage cannot hold both fp32 products.  Here a tile is 64 rows x 64 columns
 // (three 8 KiB boxes, three stages), and phase 1 writes da and db in fp32 to a 32 KiB keep area
 // of the CTA; phase 2 reads them back, and the stage is refilled as soon as phase 1 is done.
 //   - phase 1: warp w takes the 8 rows 32*(w>>2) + 8*(w&3) .. +7 of the tile, a lane 4 columns
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     quantize_dgated_keep_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b, const QuantParams p)
 {
-    static_assert(ACT >= 3, "the kept-product kernel serves the activations with a transcendental");
+    static_assert(ACT != 2, "squared-ReLU GLU uses the 128-row kernel");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
