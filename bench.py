@@ -553,6 +553,10 @@ def run_ours(args):
         outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_dev]
         h2d = x_host.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_host)
+        second = x_act if dact else x_gate if dglu else None   # the two-input calls' other input
+        second_host = second.cpu().pin_memory() if second is not None else None
+        if second_host is not None:
+            h2d += second_host.numel() * 2
         if grouped and not (with_dbias or args.swizzled or glu):
             staging = torch.empty(mx.mxfp8_quantize_grouped_host_staging_bytes(M, N, G), dtype=torch.uint8,
                                   device="cuda")
@@ -563,6 +567,33 @@ def run_ours(args):
             def e2e_step():
                 st = mx.mxfp8_quantize_grouped_host(x_host, M, N, G, off_host, fmt, act, *outs_host[:4], staging,
                                                     staging.numel(), stream)
+                if st != 0:
+                    raise mx.MXFP8Error(st, "bench e2e step")
+        elif (dact or glu or dglu) and not grouped:
+            if dact:
+                nbytes = mx.mxfp8_quantize_dact_host_staging_bytes(M, N, with_dbias)
+                name = "mxfp8_quantize_dact_host"
+            elif glu:
+                nbytes = mx.mxfp8_quantize_gated_host_staging_bytes(M, N)
+                name = "mxfp8_quantize_gated_host"
+            else:
+                nbytes = mx.mxfp8_quantize_dgated_host_staging_bytes(M, N)
+                name = "mxfp8_quantize_dgated_host"
+            staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+            path = (f"{name}: pinned host buffers in and out (every input), H2D / kernel / D2H pipelined over "
+                    "row chunks inside the library")
+
+            def e2e_step():
+                if dact:
+                    st = mx.mxfp8_quantize_dact_host(x_host, second_host, M, N, fmt, dact, *outs_host[:4],
+                                                     outs_host[4] if with_dbias else None, staging, staging.numel(),
+                                                     stream)
+                elif glu:
+                    st = mx.mxfp8_quantize_gated_host(x_host, M, N, fmt, glu, *outs_host[:4], staging,
+                                                      staging.numel(), stream)
+                else:
+                    st = mx.mxfp8_quantize_dgated_host(x_host, second_host, M, N, fmt, dglu, *outs_host[:4], staging,
+                                                       staging.numel(), stream)
                 if st != 0:
                     raise mx.MXFP8Error(st, "bench e2e step")
         elif (args.swizzled or args.amax or act) and not (grouped or dact or glu or dglu):

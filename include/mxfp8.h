@@ -206,6 +206,37 @@ mxfp8_status_t mxfp8_quantize_host(const void *x_host, int64_t M, int64_t N, int
                                    void *stream);
 
 /*
+ * The backward fusion, the gated cast and its backward with every input and
+ * output in HOST memory, pipelined over row chunks (whole 128-row tiles,
+ * about 32 MiB of input each) like mxfp8_quantize_host: the same arguments
+ * as mxfp8_quantize_dact / mxfp8_quantize_gated / mxfp8_quantize_dgated,
+ * host buffers in their layouts, a device staging buffer (256-byte aligned,
+ * at least the matching *_host_staging_bytes) instead of the workspace, and
+ * no noop.  Results are identical to the device calls on the same data (the
+ * backward fusion's dbias too: every chunk writes its tile partials into one
+ * workspace in the staging buffer and one reduce follows).  M > 0.  The
+ * staging-bytes functions return 0 for invalid shapes.
+ */
+size_t mxfp8_quantize_dact_host_staging_bytes(int64_t M, int64_t N, int with_dbias);
+mxfp8_status_t mxfp8_quantize_dact_host(const void *grad_host, const void *act_input_host,
+                                        int64_t M, int64_t N, int fp8_fmt, int activation,
+                                        void *out_row_host, void *scale_row_host,
+                                        void *out_col_host, void *scale_col_host,
+                                        float *dbias_host, void *staging, size_t staging_bytes,
+                                        void *stream);
+size_t mxfp8_quantize_gated_host_staging_bytes(int64_t M, int64_t N);
+mxfp8_status_t mxfp8_quantize_gated_host(const void *x_host, int64_t M, int64_t N, int fp8_fmt,
+                                         int activation, void *out_row_host, void *scale_row_host,
+                                         void *out_col_host, void *scale_col_host, void *staging,
+                                         size_t staging_bytes, void *stream);
+size_t mxfp8_quantize_dgated_host_staging_bytes(int64_t M, int64_t N);
+mxfp8_status_t mxfp8_quantize_dgated_host(const void *grad_host, const void *x_host, int64_t M,
+                                          int64_t N, int fp8_fmt, int activation,
+                                          void *out_row_host, void *scale_row_host,
+                                          void *out_col_host, void *scale_col_host, void *staging,
+                                          size_t staging_bytes, void *stream);
+
+/*
  * Device staging bytes mxfp8_quantize_grouped_host needs: three chunk slots
  * (a chunk of x, its outputs, its columnwise scale rows and its group
  * offsets).  0 for invalid shapes or group counts.

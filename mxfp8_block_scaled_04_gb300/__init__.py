@@ -18,5 +18,8 @@ from .binding import (  # noqa: F401
     mxfp8_quantize_grouped_swizzled, mxfp8_grouped_swizzled_scale_bytes, mxfp8_selftest_bounded_wait, mxfp8_activation_values,
     mxfp8_quantize_grouped_host, mxfp8_quantize_grouped_host_staging_bytes, mxfp8_grouped_host_chunks,
     quantize_grouped_host, mxfp8_quantize_ex_host, mxfp8_quantize_ex_host_staging_bytes,
+    mxfp8_quantize_dact_host, mxfp8_quantize_dact_host_staging_bytes, quantize_dact_host,
+    mxfp8_quantize_gated_host, mxfp8_quantize_gated_host_staging_bytes, quantize_gated_host,
+    mxfp8_quantize_dgated_host, mxfp8_quantize_dgated_host_staging_bytes, quantize_dgated_host,
     QuantizeConfig, SCALES_PLAIN, SCALES_SWIZZLED, make_config, mxfp8_quantize_ex, mxfp8_scale_bytes,
 )

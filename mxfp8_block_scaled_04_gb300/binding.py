@@ -97,6 +97,20 @@ def lib():
             L.mxfp8_quantize_host_staging_bytes.argtypes = [i64, i64, i32]
             L.mxfp8_quantize_host.restype = i32
             L.mxfp8_quantize_host.argtypes = [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.mxfp8_quantize_dact_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_dact_host_staging_bytes.argtypes = [i64, i64, i32]
+            L.mxfp8_quantize_dact_host.restype = i32
+            L.mxfp8_quantize_dact_host.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                   ctypes.c_size_t, vp]
+            L.mxfp8_quantize_gated_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_gated_host_staging_bytes.argtypes = [i64, i64]
+            L.mxfp8_quantize_gated_host.restype = i32
+            L.mxfp8_quantize_gated_host.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.mxfp8_quantize_dgated_host_staging_bytes.restype = ctypes.c_size_t
+            L.mxfp8_quantize_dgated_host_staging_bytes.argtypes = [i64, i64]
+            L.mxfp8_quantize_dgated_host.restype = i32
+            L.mxfp8_quantize_dgated_host.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, vp,
+                                                     ctypes.c_size_t, vp]
             L.mxfp8_quantize_ex_host_staging_bytes.restype = ctypes.c_size_t
             L.mxfp8_quantize_ex_host_staging_bytes.argtypes = [ctypes.POINTER(QuantizeConfig)]
             L.mxfp8_quantize_ex_host.restype = i32
@@ -256,6 +270,45 @@ def mxfp8_quantize_host(x_host, M, N, fp8_fmt, out_row_host, scale_row_host, out
     return int(lib().mxfp8_quantize_host(_addr(x_host), M, N, fp8_fmt, _addr(out_row_host), _addr(scale_row_host),
                                          _addr(out_col_host), _addr(scale_col_host), _addr(dbias_host),
                                          _addr(staging), int(staging_bytes), _stream(stream)))
+
+
+def _act(activation) -> int:
+    return ACTIVATIONS[activation.lower()] if isinstance(activation, str) else int(activation)
+
+
+def mxfp8_quantize_dact_host_staging_bytes(M: int, N: int, with_dbias: bool) -> int:
+    return int(lib().mxfp8_quantize_dact_host_staging_bytes(M, N, int(bool(with_dbias))))
+
+
+def mxfp8_quantize_dact_host(grad_host, act_input_host, M, N, fp8_fmt, activation, out_row_host, scale_row_host,
+                             out_col_host, scale_col_host, dbias_host, staging, staging_bytes, stream=None) -> int:
+    return int(lib().mxfp8_quantize_dact_host(_addr(grad_host), _addr(act_input_host), M, N, fp8_fmt,
+                                              _act(activation), _addr(out_row_host), _addr(scale_row_host),
+                                              _addr(out_col_host), _addr(scale_col_host), _addr(dbias_host),
+                                              _addr(staging), int(staging_bytes), _stream(stream)))
+
+
+def mxfp8_quantize_gated_host_staging_bytes(M: int, N: int) -> int:
+    return int(lib().mxfp8_quantize_gated_host_staging_bytes(M, N))
+
+
+def mxfp8_quantize_gated_host(x_host, M, N, fp8_fmt, activation, out_row_host, scale_row_host, out_col_host,
+                              scale_col_host, staging, staging_bytes, stream=None) -> int:
+    return int(lib().mxfp8_quantize_gated_host(_addr(x_host), M, N, fp8_fmt, _act(activation), _addr(out_row_host),
+                                               _addr(scale_row_host), _addr(out_col_host), _addr(scale_col_host),
+                                               _addr(staging), int(staging_bytes), _stream(stream)))
+
+
+def mxfp8_quantize_dgated_host_staging_bytes(M: int, N: int) -> int:
+    return int(lib().mxfp8_quantize_dgated_host_staging_bytes(M, N))
+
+
+def mxfp8_quantize_dgated_host(grad_host, x_host, M, N, fp8_fmt, activation, out_row_host, scale_row_host,
+                               out_col_host, scale_col_host, staging, staging_bytes, stream=None) -> int:
+    return int(lib().mxfp8_quantize_dgated_host(_addr(grad_host), _addr(x_host), M, N, fp8_fmt, _act(activation),
+                                                _addr(out_row_host), _addr(scale_row_host), _addr(out_col_host),
+                                                _addr(scale_col_host), _addr(staging), int(staging_bytes),
+                                                _stream(stream)))
 
 
 def mxfp8_quantize_ex_host_staging_bytes(cfg: QuantizeConfig) -> int:
@@ -492,6 +545,71 @@ def quantize_grouped_host(x: torch.Tensor, offsets: torch.Tensor, fmt=E4M3, acti
     if st != 0:
         raise MXFP8Error(st, "mxfp8_quantize_grouped_host")
     return MXFP8Tensor(out_row, scale_row, out_col, scale_col, None)
+
+
+def _host_bf16(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous() or t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous 2-D torch.bfloat16 host tensor")
+
+
+def _host_outputs(M: int, W: int, SR: int, rowwise: bool, colwise: bool):
+    pin = dict(dtype=torch.uint8, pin_memory=True)
+    return (torch.empty((M, W), **pin) if rowwise else None, torch.empty((M, SR), **pin) if rowwise else None,
+            torch.empty((M, W), **pin) if colwise else None, torch.empty((-(-M // BLOCK), W), **pin) if colwise else None)
+
+
+def quantize_dact_host(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activation="gelu",
+                       rowwise: bool = True, colwise: bool = True, with_dbias: bool = False, stream=None) -> MXFP8Tensor:
+    """quantize_dact with host (CPU, ideally pinned) inputs; pinned host outputs, ready once ``stream``
+    has been synchronised."""
+    _host_bf16(grad, "grad")
+    _host_bf16(act_input, "act_input")
+    if grad.shape != act_input.shape:
+        raise ValueError("grad and act_input must have the same shape")
+    M, N = grad.shape
+    outs = _host_outputs(M, N, -(-N // BLOCK), rowwise, colwise)
+    dbias = torch.empty((N,), dtype=torch.float32, pin_memory=True) if with_dbias else None
+    need = mxfp8_quantize_dact_host_staging_bytes(M, N, with_dbias)
+    staging = torch.empty((max(need, 256),), dtype=torch.uint8, device="cuda")
+    st = mxfp8_quantize_dact_host(grad, act_input, M, N, _fmt(fmt), activation, *outs, dbias, staging,
+                                  staging.numel(), stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_dact_host")
+    return MXFP8Tensor(*outs, dbias)
+
+
+def quantize_gated_host(x: torch.Tensor, fmt=E4M3, activation="silu", rowwise: bool = True, colwise: bool = True,
+                        stream=None) -> MXFP8Tensor:
+    """quantize_gated with a host [M, 2N] input; pinned host outputs."""
+    _host_bf16(x, "x")
+    M, N2 = x.shape
+    if N2 % 2:
+        raise ValueError("a gated input has an even number of columns")
+    N = N2 // 2
+    outs = _host_outputs(M, N, -(-N // BLOCK), rowwise, colwise)
+    need = mxfp8_quantize_gated_host_staging_bytes(M, N)
+    staging = torch.empty((max(need, 256),), dtype=torch.uint8, device="cuda")
+    st = mxfp8_quantize_gated_host(x, M, N, _fmt(fmt), activation, *outs, staging, staging.numel(), stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_gated_host")
+    return MXFP8Tensor(*outs, None)
+
+
+def quantize_dgated_host(grad: torch.Tensor, x: torch.Tensor, fmt=E5M2, activation="silu", rowwise: bool = True,
+                         colwise: bool = True, stream=None) -> MXFP8Tensor:
+    """quantize_dgated with host inputs (grad [M, N], x [M, 2N]); pinned host outputs [M, 2N]."""
+    _host_bf16(grad, "grad")
+    _host_bf16(x, "x")
+    M, N = grad.shape
+    if x.shape != (M, 2 * N):
+        raise ValueError("x must be [M, 2N] for grad [M, N]")
+    outs = _host_outputs(M, 2 * N, 2 * -(-N // BLOCK), rowwise, colwise)
+    need = mxfp8_quantize_dgated_host_staging_bytes(M, N)
+    staging = torch.empty((max(need, 256),), dtype=torch.uint8, device="cuda")
+    st = mxfp8_quantize_dgated_host(grad, x, M, N, _fmt(fmt), activation, *outs, staging, staging.numel(), stream)
+    if st != 0:
+        raise MXFP8Error(st, "mxfp8_quantize_dgated_host")
+    return MXFP8Tensor(*outs, None)
 
 
 def quantize_dact(grad: torch.Tensor, act_input: torch.Tensor, fmt=E4M3, activation="gelu",

@@ -650,9 +650,15 @@ mxfp8_status_t mxfp8_quantize_grouped(const void *x, int64_t total_rows, int64_t
                         nullptr, nullptr, noop, err_flag, static_cast<cudaStream_t>(stream_));
 }
 
-mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int64_t M, int64_t N, int fp8_fmt,
-                                   int activation, void *out_row, void *scale_row, void *out_col, void *scale_col,
-                                   float *dbias, void *workspace, const float *noop, void *stream_)
+}  // extern "C"
+
+namespace {
+
+// The backward fusion's host checks and launches; with reduce false the dbias variant writes only
+// its per-tile partial sums into workspace (the host pipeline reduces them once at its end).
+mxfp8_status_t dact_impl(const void *grad, const void *act_input, int64_t M, int64_t N, int fp8_fmt, int activation,
+                         void *out_row, void *scale_row, void *out_col, void *scale_col, float *dbias, void *workspace,
+                         const float *noop, void *stream_, bool reduce)
 {
     if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
         return MXFP8_ERR_FORMAT;
@@ -711,9 +717,21 @@ mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int6
         if (st != MXFP8_OK)
             return st;
     }
-    if (dbias != nullptr && N > 0)
+    if (reduce && dbias != nullptr && N > 0)
         return enqueue_reduce(static_cast<const float *>(workspace), M > 0 ? row_tiles : 0, N, dbias, noop, stream);
     return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp8_status_t mxfp8_quantize_dact(const void *grad, const void *act_input, int64_t M, int64_t N, int fp8_fmt,
+                                   int activation, void *out_row, void *scale_row, void *out_col, void *scale_col,
+                                   float *dbias, void *workspace, const float *noop, void *stream_)
+{
+    return dact_impl(grad, act_input, M, N, fp8_fmt, activation, out_row, scale_row, out_col, scale_col, dbias,
+                     workspace, noop, stream_, true);
 }
 
 mxfp8_status_t mxfp8_quantize_gated(const void *x, int64_t M, int64_t N, int fp8_fmt, int activation, void *out_row,
@@ -1207,7 +1225,7 @@ std::vector<int64_t> chunk_plan(int64_t M, int64_t R)
         ramp_rows += r;
     std::vector<int64_t> b{0};
     const int64_t M128 = M / kBM * kBM;  // the last chunk also takes the final M - M128 rows
-    if (M128 <= 2 * ramp_rows + R) {
+    if (ramp.empty() || M128 <= 2 * ramp_rows + R) {  // no ramp (R < 256 rows) or too few rows for one
         for (int64_t r = R; r < M; r += R)
             b.push_back(r);
     } else {
@@ -1464,6 +1482,144 @@ mxfp8_status_t host_pipeline(const void *x_host, int64_t M, int64_t N, int fp8_f
     return MXFP8_OK;
 }
 
+// The host pipeline of the two- and three-input calls (backward fusion, gated cast and its
+// backward): up to two host inputs of b0 and b1 bytes per row, outputs of W bytes per row (the
+// FP8 codes of each direction), SR bytes per row (row scales) and W bytes per 32 rows (column
+// scales), all in the device calls' layouts.  Chunks of R rows (a multiple of 128) go through
+// three slots as in the flat pipeline; enqueue(in0, in1, row0, rows, out_row, scale_row,
+// out_col, scale_col) quantizes one chunk on the caller's stream.
+struct RowsLayout {
+    size_t in0, in1, out_row, out_col, scale_row, scale_col, bytes;
+};
+
+RowsLayout rows_layout(int64_t R, int64_t b0, int64_t b1, int64_t W, int64_t SR)
+{
+    RowsLayout L;
+    size_t o = 0;
+    L.in0 = o;
+    o += align256(static_cast<size_t>(R * b0));
+    L.in1 = o;
+    o += align256(static_cast<size_t>(R * b1));
+    L.out_row = o;
+    o += align256(static_cast<size_t>(R * W));
+    L.out_col = o;
+    o += align256(static_cast<size_t>(R * W));
+    L.scale_row = o;
+    o += align256(static_cast<size_t>(R * SR));
+    L.scale_col = o;
+    o += align256(static_cast<size_t>(R / 32 * W));
+    L.bytes = o;
+    return L;
+}
+
+// Rows per chunk: about kHostChunkBytes of input, whole 128-row tiles.
+int64_t rows_chunk(int64_t M, int64_t in_bytes_per_row)
+{
+    int64_t r = (kHostChunkBytes / in_bytes_per_row) / kBM * kBM;
+    if (r < kBM)
+        r = kBM;
+    const int64_t m_up = (M + kBM - 1) / kBM * kBM;
+    return r < m_up ? r : m_up;
+}
+
+template <class Enqueue>
+mxfp8_status_t rows_pipeline(int device, cudaStream_t stream, const void *in0_host, int64_t b0, const void *in1_host,
+                             int64_t b1, int64_t M, int64_t W, int64_t SR, void *out_row_host, void *scale_row_host,
+                             void *out_col_host, void *scale_col_host, unsigned char *base, Enqueue &&enqueue)
+{
+    HostPipe *hp = nullptr;
+    mxfp8_status_t st = host_pipe(device, &hp);
+    if (st != MXFP8_OK)
+        return st;
+    const int64_t R = rows_chunk(M, b0 + b1);
+    const RowsLayout L = rows_layout(R, b0, b1, W, SR);
+    const unsigned char *h0 = static_cast<const unsigned char *>(in0_host);
+    const unsigned char *h1 = static_cast<const unsigned char *>(in1_host);
+    const bool row = out_row_host != nullptr, col = out_col_host != nullptr;
+    if (!cuda_ok(cudaEventRecord(hp->start, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->start, 0)) ||
+        !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->start, 0)))
+        return MXFP8_ERR_LAUNCH;
+    const std::vector<int64_t> plan = chunk_plan(M, R);
+    const int64_t chunks = static_cast<int64_t>(plan.size()) - 1;
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int k = static_cast<int>(c % kHostSlots);
+        const int64_t row0 = plan[c], rows = plan[c + 1] - plan[c];
+        unsigned char *slot = base + k * L.bytes;
+        if (c >= kHostSlots && !cuda_ok(cudaStreamWaitEvent(hp->h2d, hp->d2h_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        if (!cuda_ok(cudaMemcpyAsync(slot + L.in0, h0 + row0 * b0, static_cast<size_t>(rows * b0),
+                                     cudaMemcpyHostToDevice, hp->h2d)) ||
+            (b1 > 0 && !cuda_ok(cudaMemcpyAsync(slot + L.in1, h1 + row0 * b1, static_cast<size_t>(rows * b1),
+                                                cudaMemcpyHostToDevice, hp->h2d))) ||
+            !cuda_ok(cudaEventRecord(hp->h2d_done[k], hp->h2d)) ||
+            !cuda_ok(cudaStreamWaitEvent(stream, hp->h2d_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        st = enqueue(slot + L.in0, slot + L.in1, row0, rows, row ? slot + L.out_row : nullptr,
+                     row ? slot + L.scale_row : nullptr, col ? slot + L.out_col : nullptr,
+                     col ? slot + L.scale_col : nullptr);
+        if (st != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->comp_done[k], stream)) ||
+            !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->comp_done[k], 0)))
+            return MXFP8_ERR_LAUNCH;
+        bool ok = true;
+        if (row) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_row_host) + row0 * W, slot + L.out_row,
+                                               static_cast<size_t>(rows * W), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_row_host) + row0 * SR,
+                                               slot + L.scale_row, static_cast<size_t>(rows * SR),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (col) {
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(out_col_host) + row0 * W, slot + L.out_col,
+                                               static_cast<size_t>(rows * W), cudaMemcpyDeviceToHost, hp->d2h));
+            ok = ok && cuda_ok(cudaMemcpyAsync(static_cast<unsigned char *>(scale_col_host) + (row0 / 32) * W,
+                                               slot + L.scale_col, static_cast<size_t>(((rows + 31) / 32) * W),
+                                               cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        if (!ok || !cuda_ok(cudaEventRecord(hp->d2h_done[k], hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    return MXFP8_OK;
+}
+
+// The caller's stream resumes once the last copy to the host is done.
+mxfp8_status_t rows_pipeline_end(int device, cudaStream_t stream)
+{
+    HostPipe *hp = nullptr;
+    mxfp8_status_t st = host_pipe(device, &hp);
+    if (st != MXFP8_OK)
+        return st;
+    if (!cuda_ok(cudaEventRecord(hp->end, hp->d2h)) || !cuda_ok(cudaStreamWaitEvent(stream, hp->end, 0)))
+        return MXFP8_ERR_LAUNCH;
+    return MXFP8_OK;
+}
+
+// Host checks shared by the three calls; `pointers` are the inputs, the staging buffer and the
+// outputs as in the device calls.
+mxfp8_status_t rows_host_checks(int fp8_fmt, int activation, int64_t M, int64_t N, int64_t n_limit, bool inputs_ok,
+                                void *staging, void *out_row_host, void *scale_row_host, void *out_col_host,
+                                void *scale_col_host, size_t staging_bytes, size_t need)
+{
+    if (fp8_fmt != MXFP8_E4M3 && fp8_fmt != MXFP8_E5M2)
+        return MXFP8_ERR_FORMAT;
+    if (activation < MXFP8_ACT_RELU || activation > MXFP8_ACT_QGELU)
+        return MXFP8_ERR_FORMAT;
+    if (M <= 0 || N <= 0 || N % 8 || M >= (int64_t{1} << 31) || N >= n_limit)
+        return MXFP8_ERR_SHAPE;
+    if (!inputs_ok || staging == nullptr)
+        return MXFP8_ERR_NULL;
+    if ((out_row_host == nullptr) != (scale_row_host == nullptr) ||
+        (out_col_host == nullptr) != (scale_col_host == nullptr) ||
+        (out_row_host == nullptr && out_col_host == nullptr))
+        return MXFP8_ERR_NULL;
+    if (!aligned(staging, 256))
+        return MXFP8_ERR_ALIGN;
+    if (staging_bytes < need)
+        return MXFP8_ERR_WORKSPACE;
+    return MXFP8_OK;
+}
+
 // Chunk boundaries of a grouped host call: the flat plan's, each interior one moved down to the
 // nearest row a multiple of 32 rows after the start of the group that contains it.  A group cut
 // by a boundary is then quantized as two pieces whose 32-row blocks are the group's own, so the
@@ -1591,6 +1747,135 @@ int64_t mxfp8_grouped_host_chunks(const int64_t *host_offsets, int num_groups, i
     for (size_t i = 0; i < b.size() && static_cast<int64_t>(i) < max_bounds && bounds != nullptr; ++i)
         bounds[i] = b[i];
     return static_cast<int64_t>(b.size());
+}
+
+size_t mxfp8_quantize_dact_host_staging_bytes(int64_t M, int64_t N, int with_dbias)
+{
+    if (M <= 0 || N <= 0 || N % 8)
+        return 0;
+    const int64_t Cn = (N + 31) / 32;
+    size_t b = kHostSlots * rows_layout(rows_chunk(M, 4 * N), 2 * N, 2 * N, N, Cn).bytes;
+    if (with_dbias)
+        b += align256(mxfp8_quantize_workspace_bytes(M, N, 1)) + align256(static_cast<size_t>(N) * 4);
+    return b;
+}
+
+mxfp8_status_t mxfp8_quantize_dact_host(const void *grad_host, const void *act_input_host, int64_t M, int64_t N,
+                                        int fp8_fmt, int activation, void *out_row_host, void *scale_row_host,
+                                        void *out_col_host, void *scale_col_host, float *dbias_host, void *staging,
+                                        size_t staging_bytes, void *stream_)
+{
+    mxfp8_status_t st = rows_host_checks(
+        fp8_fmt, activation, M, N, int64_t{1} << 31, grad_host != nullptr && act_input_host != nullptr, staging,
+        out_row_host, scale_row_host, out_col_host, scale_col_host, staging_bytes,
+        mxfp8_quantize_dact_host_staging_bytes(M, N, dbias_host != nullptr));
+    if (st != MXFP8_OK)
+        return st;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t Cn = (N + 31) / 32;
+    unsigned char *base = static_cast<unsigned char *>(staging);
+    const size_t slots = kHostSlots * rows_layout(rows_chunk(M, 4 * N), 2 * N, 2 * N, N, Cn).bytes;
+    float *ws = nullptr, *dbias_dev = nullptr;
+    if (dbias_host != nullptr) {
+        ws = reinterpret_cast<float *>(base + slots);
+        dbias_dev = reinterpret_cast<float *>(base + slots + align256(mxfp8_quantize_workspace_bytes(M, N, 1)));
+    }
+    st = rows_pipeline(device, stream, grad_host, 2 * N, act_input_host, 2 * N, M, N, Cn, out_row_host,
+                       scale_row_host, out_col_host, scale_col_host, base,
+                       [&](unsigned char *g, unsigned char *x, int64_t row0, int64_t rows, void *orow, void *srow,
+                           void *ocol, void *scol) {
+                           // the dbias variant writes the chunk's tile partials; one reduce follows
+                           return dact_impl(g, x, rows, N, fp8_fmt, activation, orow, srow, ocol, scol, dbias_dev,
+                                            ws != nullptr ? ws + (row0 / kBM) * N : nullptr, nullptr, stream, false);
+                       });
+    if (st != MXFP8_OK)
+        return st;
+    if (dbias_host != nullptr) {
+        HostPipe *hp = nullptr;
+        if ((st = host_pipe(device, &hp)) != MXFP8_OK)
+            return st;
+        if ((st = enqueue_reduce(ws, (M + kBM - 1) / kBM, N, dbias_dev, nullptr, stream)) != MXFP8_OK)
+            return st;
+        if (!cuda_ok(cudaEventRecord(hp->reduced, stream)) || !cuda_ok(cudaStreamWaitEvent(hp->d2h, hp->reduced, 0)) ||
+            !cuda_ok(cudaMemcpyAsync(dbias_host, dbias_dev, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
+                                     hp->d2h)))
+            return MXFP8_ERR_LAUNCH;
+    }
+    return rows_pipeline_end(device, stream);
+}
+
+size_t mxfp8_quantize_gated_host_staging_bytes(int64_t M, int64_t N)
+{
+    if (M <= 0 || N <= 0 || N % 8)
+        return 0;
+    return kHostSlots * rows_layout(rows_chunk(M, 4 * N), 4 * N, 0, N, (N + 31) / 32).bytes;
+}
+
+mxfp8_status_t mxfp8_quantize_gated_host(const void *x_host, int64_t M, int64_t N, int fp8_fmt, int activation,
+                                         void *out_row_host, void *scale_row_host, void *out_col_host,
+                                         void *scale_col_host, void *staging, size_t staging_bytes, void *stream_)
+{
+    mxfp8_status_t st = rows_host_checks(fp8_fmt, activation, M, N, int64_t{1} << 30, x_host != nullptr, staging,
+                                         out_row_host, scale_row_host, out_col_host, scale_col_host, staging_bytes,
+                                         mxfp8_quantize_gated_host_staging_bytes(M, N));
+    if (st != MXFP8_OK)
+        return st;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    st = rows_pipeline(device, stream, x_host, 4 * N, nullptr, 0, M, N, (N + 31) / 32, out_row_host, scale_row_host,
+                       out_col_host, scale_col_host, static_cast<unsigned char *>(staging),
+                       [&](unsigned char *x, unsigned char *, int64_t, int64_t rows, void *orow, void *srow,
+                           void *ocol, void *scol) {
+                           return mxfp8_quantize_gated(x, rows, N, fp8_fmt, activation, orow, srow, ocol, scol,
+                                                       nullptr, stream);
+                       });
+    return st != MXFP8_OK ? st : rows_pipeline_end(device, stream);
+}
+
+size_t mxfp8_quantize_dgated_host_staging_bytes(int64_t M, int64_t N)
+{
+    if (M <= 0 || N <= 0 || N % 8)
+        return 0;
+    return kHostSlots * rows_layout(rows_chunk(M, 6 * N), 2 * N, 4 * N, 2 * N, 2 * ((N + 31) / 32)).bytes;
+}
+
+mxfp8_status_t mxfp8_quantize_dgated_host(const void *grad_host, const void *x_host, int64_t M, int64_t N,
+                                          int fp8_fmt, int activation, void *out_row_host, void *scale_row_host,
+                                          void *out_col_host, void *scale_col_host, void *staging,
+                                          size_t staging_bytes, void *stream_)
+{
+    mxfp8_status_t st = rows_host_checks(fp8_fmt, activation, M, N, int64_t{1} << 30,
+                                         grad_host != nullptr && x_host != nullptr, staging, out_row_host,
+                                         scale_row_host, out_col_host, scale_col_host, staging_bytes,
+                                         mxfp8_quantize_dgated_host_staging_bytes(M, N));
+    if (st != MXFP8_OK)
+        return st;
+    int device = 0;
+    if ((st = current_device(&device)) != MXFP8_OK)
+        return st;
+    if (device < 0 || device >= kMaxDevices || !on_device(staging, device))
+        return MXFP8_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    st = rows_pipeline(device, stream, grad_host, 2 * N, x_host, 4 * N, M, 2 * N, 2 * ((N + 31) / 32), out_row_host,
+                       scale_row_host, out_col_host, scale_col_host, static_cast<unsigned char *>(staging),
+                       [&](unsigned char *g, unsigned char *x, int64_t, int64_t rows, void *orow, void *srow,
+                           void *ocol, void *scol) {
+                           return mxfp8_quantize_dgated(g, x, rows, N, fp8_fmt, activation, orow, srow, ocol, scol,
+                                                        nullptr, stream);
+                       });
+    return st != MXFP8_OK ? st : rows_pipeline_end(device, stream);
 }
 
 mxfp8_status_t mxfp8_quantize_grouped_host(const void *x_host, int64_t total_rows, int64_t N, int num_groups,

@@ -372,6 +372,10 @@ def test_grouped_host_chunk_plan_edges(cuda_lib):
     _plan_checks([0, 100000], 100000, 7168)                  # one group cut many times
     _plan_checks([0, 45, 45, 3000, 3001, 9000, 16384], 16384, 7168)
     _plan_checks([0] + [37 * i for i in range(1, 513)], 37 * 512, 4096)   # 512 groups, none 32-aligned
+    # rows wider than 128 KiB: chunks of 128 rows and no ramp at either end
+    assert _plan_checks([0, 5000], 5000, 200000) == list(range(0, 5000, 128)) + [5000]
+    _plan_checks([0, 45, 3000, 9000], 9000, 300000)
+    _plan_checks([0, 128], 128, 300000)
     assert mx.lib().mxfp8_grouped_host_chunks(None, 1, 10, 64, None, 0) == -1
     with pytest.raises(ValueError):
         mx.mxfp8_grouped_host_chunks([0, 5, 3], 3, 64)
@@ -403,3 +407,25 @@ def test_ex_host_rejections(cuda_lib):
     assert mx.mxfp8_quantize_ex_host_staging_bytes(cfg(layout=mx.SCALES_PLAIN)) == plain + 256
     assert mx.mxfp8_quantize_ex_host_staging_bytes(cfg(amax=None)) >= plain
     assert mx.mxfp8_quantize_ex_host_staging_bytes(None) == 0
+
+
+@pytest.mark.parametrize("which", ["dact", "gated", "dgated"])
+def test_two_input_host_rejections(cuda_lib, which):
+    def call(inp=A, M=64, N=64, fmt=0, act=3, orow=A, srow=A, ocol=A, scol=A, staging=A, nbytes=1 << 30):
+        if which == "dact":
+            return mx.mxfp8_quantize_dact_host(inp, A, M, N, fmt, act, orow, srow, ocol, scol, None, staging,
+                                               nbytes, 0)
+        if which == "gated":
+            return mx.mxfp8_quantize_gated_host(inp, M, N, fmt, act, orow, srow, ocol, scol, staging, nbytes, 0)
+        return mx.mxfp8_quantize_dgated_host(inp, A, M, N, fmt, act, orow, srow, ocol, scol, staging, nbytes, 0)
+    assert call(fmt=2) == FORMAT and call(act=0) == FORMAT and call(act=6) == FORMAT
+    assert call(M=0) == SHAPE and call(N=36) == SHAPE
+    assert call(inp=None) == NULL and call(staging=None) == NULL and call(orow=None) == NULL
+    assert call(orow=None, srow=None, ocol=None, scol=None) == NULL
+    assert call(staging=A + 16) == ALIGN and call(nbytes=1024) == WORKSPACE
+    assert call() == DEVICE and call(ocol=None, scol=None) == DEVICE
+    size = {"dact": lambda M, N: mx.mxfp8_quantize_dact_host_staging_bytes(M, N, False),
+            "gated": mx.mxfp8_quantize_gated_host_staging_bytes,
+            "dgated": mx.mxfp8_quantize_dgated_host_staging_bytes}[which]
+    assert size(0, 64) == 0 and size(64, 36) == 0 and size(64, 64) > 0
+    assert size(65536, 1024) > size(128, 1024)             # slots hold one chunk: at most ~32 MiB of input

@@ -170,3 +170,39 @@ def test_ex_host_matches_device_path(shape, opts):
             assert g is None, name
             continue
         assert torch.equal(g, w.cpu()), name      # dbias too: the same partials and the same reduce
+
+
+# ---- the two- and three-input calls with host buffers ------------------------------------------
+
+@pytest.mark.parametrize("shape", [(3000, 8192), (300, 1032), (400, 28672)])
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+def test_two_input_host_calls_match_device_paths(shape, act):
+    """Backward fusion (with dbias), gated cast and gated backward: host buffers give the device
+    calls' bytes; 3000 x 8192 spans several chunks with a ragged last one, and 400 x 28672 gives the
+    gated backward (6N bytes of input per row) chunks of 128 rows with no ramp."""
+    M, N = shape
+    g_bits = wl.grad_bf16(M, N, seed=M + N)
+    x_bits = wl.normal_bf16(M, N, seed=N + 1)
+    xg_bits = np.ascontiguousarray(np.concatenate([wl.normal_bf16(M, N, seed=5), wl.normal_bf16(M, N, seed=6)], 1))
+
+    def host(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    def cuda(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    pairs = [
+        (mx.quantize_dact(cuda(g_bits), cuda(x_bits), mx.E5M2, act, with_dbias=True),
+         mx.quantize_dact_host(host(g_bits), host(x_bits), mx.E5M2, act, with_dbias=True)),
+        (mx.quantize_gated(cuda(xg_bits), mx.E4M3, act), mx.quantize_gated_host(host(xg_bits), mx.E4M3, act)),
+        (mx.quantize_dgated(cuda(g_bits), cuda(xg_bits), mx.E5M2, act),
+         mx.quantize_dgated_host(host(g_bits), host(xg_bits), mx.E5M2, act)),
+    ]
+    torch.cuda.synchronize()
+    for k, (want, got) in enumerate(pairs):
+        for name in ("out_row", "scale_row", "out_col", "scale_col", "dbias"):
+            w, g = getattr(want, name), getattr(got, name)
+            if w is None:
+                assert g is None, (k, name)
+                continue
+            assert torch.equal(g, w.cpu()), (k, name)
