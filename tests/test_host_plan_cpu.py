@@ -106,3 +106,25 @@ def test_two_input_pipeline_copies_cover_the_host_buffers(M, N, which):
     cover(M * W, outs)
     cover(M * SR, srs)
     cover(-(-M // 32) * W, scs)
+
+
+@pytest.mark.parametrize("off,N", [([0, 45, 45, 1500, 1533, 4001, 4700, 5000], 16384), ([0, 4097], 16384),
+                                   ([0] + [10 * i for i in range(1, 300)] + [3000], 16384),
+                                   ([0, 1024, 1024, 2048, 4096, 6144], 7168), ([0, 37, 5000], 200000)])
+def test_grouped_pipeline_copies_cover_the_host_buffers(off, N):
+    """mxfp8_quantize_grouped_host: rows and the chunk's columnwise scale rows (sum over the groups
+    clipped to the chunk of ceil(rows / 32), placed after the previous chunks') tile the outputs."""
+    M = off[-1]
+    b = mx.mxfp8_grouped_host_chunks(off, M, N)
+    Cn = -(-N // 32)
+    rows_r, srow_r, scol_r, s0 = [], [], [], 0
+    for r0, r1 in zip(b, b[1:]):
+        rows_r.append((r0 * N, (r1 - r0) * N))
+        srow_r.append((r0 * Cn, (r1 - r0) * Cn))
+        sc = sum(-(-(min(max(e, r0), r1) - min(max(a, r0), r1)) // 32) for a, e in zip(off, off[1:]))
+        if sc:
+            scol_r.append((s0 * N, sc * N))
+        s0 += sc
+    cover(M * N, rows_r)
+    cover(M * Cn, srow_r)
+    cover(mx.grouped_scale_col_rows(off) * N, scol_r)
